@@ -1,0 +1,101 @@
+"""Seeded synthetic workloads for causal GQA attention.
+
+This module only draws inputs: it holds no attention arithmetic, and both the
+CUDA path's tests/benchmark and the CPU oracle's tests take their inputs from
+here.  Every tensor is drawn on the CPU from ``torch.Generator().manual_seed``
+in float32, then rounded to bf16, so the GPU and the oracle see identical
+bits.  Draw order: (variable-length: the sequence lengths first), then Q, K,
+V, dO.
+
+The five workloads are shaped after the models the pages train: a tiny GQA
+check, a Qwen3-0.6B-shaped layer, a GPT-2-small-shaped MHA layer, a long
+context GQA layer (T = 4096, D = 128) and a packed variable-length batch.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    Hq: int
+    Hkv: int
+    D: int
+    B: int = 0              # dense only
+    T: int = 0              # dense only
+    num_seqs: int = 0       # variable length only
+    min_len: int = 0
+    max_len: int = 0
+    q_std: float = 1.0
+    causal: bool = True
+    scale: float = field(default=0.0)
+
+    @property
+    def varlen(self) -> bool:
+        return self.num_seqs > 0
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale else 1.0 / math.sqrt(self.D)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", B=1, Hq=4, Hkv=2, T=128, D=64),
+    "qwen3_0p6b_layer": Workload("qwen3_0p6b_layer", B=4, Hq=16, Hkv=8, T=512, D=128),
+    "gpt2_small_mha": Workload("gpt2_small_mha", B=8, Hq=12, Hkv=12, T=1024, D=64),
+    "long_gqa_t4096": Workload("long_gqa_t4096", B=2, Hq=32, Hkv=8, T=4096, D=128),
+    "varlen16": Workload("varlen16", num_seqs=16, min_len=64, max_len=2048, Hq=16, Hkv=8, D=128, q_std=4.0),
+}
+
+HEADLINE = "long_gqa_t4096"
+
+
+def _randn(g, shape, std=1.0):
+    x = torch.randn(*shape, generator=g, dtype=torch.float32)
+    if std != 1.0:
+        x = x * std
+    return x.to(torch.bfloat16)
+
+
+def dense_inputs(B, Hq, Hkv, T, D, seed=0, q_std=1.0):
+    """Q,dO [B,Hq,T,D], K,V [B,Hkv,T,D], bf16, CPU."""
+    g = torch.Generator().manual_seed(seed)
+    q = _randn(g, (B, Hq, T, D), q_std)
+    k = _randn(g, (B, Hkv, T, D))
+    v = _randn(g, (B, Hkv, T, D))
+    do = _randn(g, (B, Hq, T, D))
+    return dict(q=q, k=k, v=v, do=do)
+
+
+def varlen_lengths(num_seqs, min_len, max_len, g):
+    return torch.randint(min_len, max_len + 1, (num_seqs,), generator=g, dtype=torch.int64)
+
+
+def varlen_inputs(lengths, Hq, Hkv, D, seed=0, q_std=1.0, g=None):
+    """Packed Q,dO [total,Hq,D], K,V [total,Hkv,D] bf16 and cu_seqlens int32 [N+1]."""
+    if g is None:
+        g = torch.Generator().manual_seed(seed)
+    lengths = torch.as_tensor(lengths, dtype=torch.int64)
+    cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+    if len(lengths):
+        cu[1:] = torch.cumsum(lengths, 0).to(torch.int32)
+    total = int(cu[-1])
+    q = _randn(g, (total, Hq, D), q_std)
+    k = _randn(g, (total, Hkv, D))
+    v = _randn(g, (total, Hkv, D))
+    do = _randn(g, (total, Hq, D))
+    return dict(q=q, k=k, v=v, do=do, cu_seqlens=cu, max_seqlen=int(lengths.max()) if len(lengths) else 0)
+
+
+def make_inputs(w: Workload, seed=0):
+    """Inputs of a named workload (dense or variable length)."""
+    if w.varlen:
+        g = torch.Generator().manual_seed(seed)
+        lengths = varlen_lengths(w.num_seqs, w.min_len, w.max_len, g)
+        return varlen_inputs(lengths, w.Hq, w.Hkv, w.D, q_std=w.q_std, g=g)
+    return dense_inputs(w.B, w.Hq, w.Hkv, w.T, w.D, seed=seed, q_std=w.q_std)
+

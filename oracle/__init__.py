@@ -1,0 +1,165 @@
+"""fp64 CPU oracle for causal grouped-query attention (forward and backward).
+
+TEST INFRASTRUCTURE ONLY: the test suite, the package smoke check and the
+benchmark's CPU-baseline leg use it; the product path never imports it.
+It shares no code with the CUDA library (``gqa_oracle.c`` is plain C, built by
+``build()`` with gcc and OpenMP).
+
+Every function takes float64 numpy arrays (callers up-cast the exact bf16
+inputs) and returns float64 arrays.  Layouts: dense Q/O/dO [B,Hq,T,D],
+K/V [B,Hkv,T,D], LSE/Delta [B,Hq,T]; packed variable length Q [total,Hq,D],
+K/V [total,Hkv,D], LSE/Delta [Hq,total].
+
+What is computed is stated in the header of ``gqa_oracle.c`` with its sources
+("Project Overview" of llm-from-scratch, section "Performance Layer: kernel/
+and parallel/" and the llm/transformer.py component list; the microLLM-rocm
+README, section "Why this project exists").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gqa_oracle.c")
+_LIB = os.path.join(_HERE, "libgqa_oracle.so")
+
+_lib = None
+
+
+def build(force: bool = False, extra_cflags=()) -> str:
+    """Compile gqa_oracle.c into libgqa_oracle.so next to it (gcc, OpenMP)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", *extra_cflags, _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def build_variant(out_path: str, extra_cflags) -> str:
+    """Compile a variant of the oracle (e.g. with a planted mistake) to ``out_path``."""
+    cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", *extra_cflags, _SRC, "-o", out_path, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out_path
+
+
+_D = ctypes.POINTER(ctypes.c_double)
+_I = ctypes.POINTER(ctypes.c_int)
+_L = ctypes.c_long
+
+
+def _bind(lib):
+    lib.oracle_fwd.argtypes = [_D, _D, _D, _D, _D, _L, _L, _L, _L, _L, ctypes.c_int, ctypes.c_double]
+    lib.oracle_bwd.argtypes = [_D] * 10 + [_L, _L, _L, _L, _L, ctypes.c_int, ctypes.c_double]
+    lib.oracle_varlen_fwd.argtypes = [_D, _D, _D, _D, _D, _I, _L, _L, _L, _L, _L, ctypes.c_int, ctypes.c_double]
+    lib.oracle_varlen_bwd.argtypes = [_D] * 10 + [_I, _L, _L, _L, _L, _L, ctypes.c_int, ctypes.c_double]
+    lib.oracle_set_threads.argtypes = [ctypes.c_int]
+    for f in (lib.oracle_fwd, lib.oracle_bwd, lib.oracle_varlen_fwd, lib.oracle_varlen_bwd,
+              lib.oracle_set_threads):
+        f.restype = ctypes.c_int
+    return lib
+
+
+def load(path: str | None = None):
+    """Load the oracle library (building it first if needed)."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        build()
+        _lib = _bind(ctypes.CDLL(_LIB))
+    return _lib
+
+
+def _p(a):
+    return a.ctypes.data_as(_D)
+
+
+def _c(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def set_threads(n: int = 0) -> int:
+    """Set the OpenMP thread count (0 keeps it); returns the count in use."""
+    return load().oracle_set_threads(int(n))
+
+
+def fwd(q, k, v, causal: bool = True, scale: float | None = None, lib=None):
+    """Dense forward.  Returns (O [B,Hq,T,D], LSE [B,Hq,T])."""
+    lib = lib or load()
+    q, k, v = _c(q), _c(k), _c(v)
+    B, Hq, T, D = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    o = np.zeros_like(q)
+    lse = np.zeros((B, Hq, T))
+    st = lib.oracle_fwd(_p(q), _p(k), _p(v), _p(o), _p(lse), B, Hq, Hkv, T, D, int(causal), scale)
+    if st:
+        raise ValueError(f"oracle_fwd status {st}")
+    return o, lse
+
+
+def bwd(q, k, v, dout, causal: bool = True, scale: float | None = None, lib=None):
+    """Dense backward of L = sum(dO * O).
+
+    Returns dict with dq, dk, dv and the forward's o, lse and the row term delta."""
+    lib = lib or load()
+    q, k, v, dout = _c(q), _c(k), _c(v), _c(dout)
+    B, Hq, T, D = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    o = np.zeros_like(q)
+    lse = np.zeros((B, Hq, T))
+    delta = np.zeros((B, Hq, T))
+    st = lib.oracle_bwd(_p(q), _p(k), _p(v), _p(dout), _p(dq), _p(dk), _p(dv), _p(o), _p(lse), _p(delta),
+                        B, Hq, Hkv, T, D, int(causal), scale)
+    if st:
+        raise ValueError(f"oracle_bwd status {st}")
+    return dict(dq=dq, dk=dk, dv=dv, o=o, lse=lse, delta=delta)
+
+
+def _cu(cu_seqlens):
+    return np.ascontiguousarray(np.asarray(cu_seqlens), dtype=np.int32)
+
+
+def varlen_fwd(q, k, v, cu_seqlens, causal: bool = True, scale: float | None = None, lib=None):
+    """Packed variable-length forward.  Returns (O [total,Hq,D], LSE [Hq,total])."""
+    lib = lib or load()
+    q, k, v = _c(q), _c(k), _c(v)
+    cu = _cu(cu_seqlens)
+    total, Hq, D = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    o = np.zeros_like(q)
+    lse = np.zeros((Hq, total))
+    st = lib.oracle_varlen_fwd(_p(q), _p(k), _p(v), _p(o), _p(lse), cu.ctypes.data_as(_I), len(cu) - 1,
+                               total, Hq, Hkv, D, int(causal), scale)
+    if st:
+        raise ValueError(f"oracle_varlen_fwd status {st}")
+    return o, lse
+
+
+def varlen_bwd(q, k, v, dout, cu_seqlens, causal: bool = True, scale: float | None = None, lib=None):
+    """Packed variable-length backward; returns the same dict as ``bwd``."""
+    lib = lib or load()
+    q, k, v, dout = _c(q), _c(k), _c(v), _c(dout)
+    cu = _cu(cu_seqlens)
+    total, Hq, D = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    o = np.zeros_like(q)
+    lse = np.zeros((Hq, total))
+    delta = np.zeros((Hq, total))
+    st = lib.oracle_varlen_bwd(_p(q), _p(k), _p(v), _p(dout), _p(dq), _p(dk), _p(dv), _p(o), _p(lse),
+                               _p(delta), cu.ctypes.data_as(_I), len(cu) - 1, total, Hq, Hkv, D,
+                               int(causal), scale)
+    if st:
+        raise ValueError(f"oracle_varlen_bwd status {st}")
+    return dict(dq=dq, dk=dk, dv=dv, o=o, lse=lse, delta=delta)

@@ -1,0 +1,240 @@
+"""Pins of the fp64 oracle to facts that do not come from the oracle itself.
+
+Each pin takes the loaded oracle library and raises AssertionError when the
+oracle disagrees with a closed form, an invariant, a hand-worked case, a
+library routine on a special case, or finite differences.  The same list is
+run against variants of the oracle with a planted mistake, each of which must
+fail at least one pin.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _ev(x):
+    if isinstance(x, list):
+        return [_ev(y) for y in x]
+    return float(eval(x, {"__builtins__": {}}, {"log": math.log}))
+
+
+def pin_hand_worked(lib):
+    """Two-token case worked by hand (tests/golden/hand_t2.json)."""
+    g = json.load(open(os.path.join(GOLDEN, "hand_t2.json")))
+    inp = {k: np.array(_ev(v)) for k, v in g["inputs"].items() if k != "scale"}
+    scale = _ev(g["inputs"]["scale"])
+    q, k, v, do = (inp[n][None, None] for n in ("q", "k", "v", "do"))
+    r = oracle.bwd(q, k, v, do, causal=True, scale=scale, lib=lib)
+    exp = {n: np.array(_ev(x)) for n, x in g["causal"].items()}
+    for n in ("o", "dq", "dk", "dv"):
+        np.testing.assert_allclose(r[n][0, 0], exp[n], atol=1e-14, err_msg=n)
+    np.testing.assert_allclose(r["lse"][0, 0], exp["lse"], atol=1e-14)
+    np.testing.assert_allclose(r["delta"][0, 0], exp["delta"], atol=1e-14)
+    o, lse = oracle.fwd(q, k, v, causal=False, scale=scale, lib=lib)
+    nc = g["noncausal_row0"]
+    np.testing.assert_allclose(o[0, 0, 0], _ev(nc["o"]), atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0, 0], _ev(nc["lse"]), atol=1e-14)
+
+
+def pin_rows_sum_to_one(lib):
+    """V = identity (D = T) makes O equal P: rows sum to 1, entries are
+    non-negative and the causal upper triangle is exactly zero; V = ones
+    gives O = 1."""
+    r = _rng(1)
+    T = 9
+    q = r.standard_normal((1, 2, T, T))
+    k = r.standard_normal((1, 1, T, T))
+    eye = np.broadcast_to(np.eye(T), (1, 1, T, T)).copy()
+    for causal in (True, False):
+        P, _ = oracle.fwd(q, k, eye, causal=causal, scale=0.7, lib=lib)
+        np.testing.assert_allclose(P.sum(-1), 1.0, atol=1e-13)
+        assert (P >= 0).all()
+        if causal:
+            assert np.all(np.triu(P[0, 0], 1) == 0) and np.all(np.triu(P[0, 1], 1) == 0)
+            assert np.all(np.diag(P[0, 0]) > 0)
+        else:
+            assert np.all(P > 0)
+    o, _ = oracle.fwd(q, k, np.ones((1, 1, T, T)), causal=True, scale=0.7, lib=lib)
+    np.testing.assert_allclose(o, 1.0, atol=1e-13)
+
+
+def pin_single_token(lib):
+    """T = 1: the only visible key is the query's own: O = V, LSE = scale q.k."""
+    r = _rng(2)
+    q = r.standard_normal((2, 4, 1, 8))
+    k = r.standard_normal((2, 2, 1, 8))
+    v = r.standard_normal((2, 2, 1, 8))
+    o, lse = oracle.fwd(q, k, v, causal=True, scale=0.3, lib=lib)
+    vrep = np.repeat(v, 2, axis=1)
+    krep = np.repeat(k, 2, axis=1)
+    np.testing.assert_allclose(o, vrep, atol=1e-14)
+    np.testing.assert_allclose(lse, 0.3 * (q * krep).sum(-1), atol=1e-13)
+
+
+def pin_constant_keys(lib):
+    """All key rows equal: scores are constant along a row, so P is uniform
+    over the visible keys: O_i = mean_{j<=i} V_j and LSE_i = s_i + ln(i+1).
+    Every dS row then sums to zero against the same key, so dQ = 0."""
+    r = _rng(3)
+    T, D = 13, 6
+    q = r.standard_normal((1, 2, T, D))
+    k = np.broadcast_to(r.standard_normal((1, 1, 1, D)), (1, 1, T, D)).copy()
+    v = r.standard_normal((1, 1, T, D))
+    do = r.standard_normal((1, 2, T, D))
+    res = oracle.bwd(q, k, v, do, causal=True, scale=0.5, lib=lib)
+    prefix_mean = np.cumsum(v[0, 0], 0) / np.arange(1, T + 1)[:, None]
+    for h in range(2):
+        np.testing.assert_allclose(res["o"][0, h], prefix_mean, atol=1e-13)
+        s = 0.5 * q[0, h] @ k[0, 0, 0]
+        np.testing.assert_allclose(res["lse"][0, h], s + np.log(np.arange(1, T + 1)), atol=1e-12)
+    np.testing.assert_allclose(res["dq"], 0.0, atol=1e-13)
+
+
+def pin_shift_invariance(lib):
+    """Adding u to every key shifts row i's scores by scale q_i.u, which the
+    row softmax cancels: O is unchanged and LSE_i shifts by exactly that."""
+    r = _rng(4)
+    T, D = 11, 5
+    q = r.standard_normal((1, 2, T, D))
+    k = r.standard_normal((1, 1, T, D))
+    v = r.standard_normal((1, 1, T, D))
+    u = r.standard_normal(D)
+    o1, l1 = oracle.fwd(q, k, v, causal=True, scale=0.8, lib=lib)
+    o2, l2 = oracle.fwd(q, k + u, v, causal=True, scale=0.8, lib=lib)
+    np.testing.assert_allclose(o2, o1, atol=1e-12)
+    np.testing.assert_allclose(l2 - l1, 0.8 * (q @ u), atol=1e-12)
+
+
+def pin_gqa_equals_repeated_mha(lib):
+    """GQA equals MHA with each K/V head repeated G times (query head h uses
+    key/value head h // G); dK, dV of GQA are the group sums of the MHA ones."""
+    r = _rng(5)
+    B, Hq, Hkv, T, D = 2, 6, 2, 10, 4
+    G = Hq // Hkv
+    q = r.standard_normal((B, Hq, T, D))
+    k = r.standard_normal((B, Hkv, T, D))
+    v = r.standard_normal((B, Hkv, T, D))
+    do = r.standard_normal((B, Hq, T, D))
+    g = oracle.bwd(q, k, v, do, causal=True, scale=0.4, lib=lib)
+    m = oracle.bwd(q, np.repeat(k, G, 1), np.repeat(v, G, 1), do, causal=True, scale=0.4, lib=lib)
+    for n in ("o", "lse", "dq"):
+        np.testing.assert_allclose(g[n], m[n], atol=1e-12, err_msg=n)
+    np.testing.assert_allclose(g["dk"], m["dk"].reshape(B, Hkv, G, T, D).sum(2), atol=1e-12)
+    np.testing.assert_allclose(g["dv"], m["dv"].reshape(B, Hkv, G, T, D).sum(2), atol=1e-12)
+    # MHA per head equals an independent single-head problem
+    for h in range(Hq):
+        o1, l1 = oracle.fwd(q[:, h:h + 1], k[:, h // G:h // G + 1], v[:, h // G:h // G + 1],
+                            causal=True, scale=0.4, lib=lib)
+        np.testing.assert_allclose(g["o"][:, h:h + 1], o1, atol=1e-12)
+
+
+def pin_torch_sdpa(lib):
+    """Special case that reduces to a library routine: PyTorch's
+    scaled_dot_product_attention (math path, float64, CPU) and its autograd,
+    with K/V repeated to full heads."""
+    r = _rng(6)
+    B, Hq, Hkv, T, D = 2, 4, 2, 17, 8
+    G = Hq // Hkv
+    q = r.standard_normal((B, Hq, T, D))
+    k = r.standard_normal((B, Hkv, T, D))
+    v = r.standard_normal((B, Hkv, T, D))
+    do = r.standard_normal((B, Hq, T, D))
+    for causal in (True, False):
+        res = oracle.bwd(q, k, v, do, causal=causal, scale=0.35, lib=lib)
+        tq = torch.tensor(q, requires_grad=True)
+        tk = torch.tensor(k, requires_grad=True)
+        tv = torch.tensor(v, requires_grad=True)
+        with torch.nn.attention.sdpa_kernel(torch.nn.attention.SDPBackend.MATH):
+            to = torch.nn.functional.scaled_dot_product_attention(
+                tq, tk.repeat_interleave(G, 1), tv.repeat_interleave(G, 1), is_causal=causal, scale=0.35)
+        to.backward(torch.tensor(do))
+        np.testing.assert_allclose(res["o"], to.detach().numpy(), atol=1e-12)
+        np.testing.assert_allclose(res["dq"], tq.grad.numpy(), atol=1e-12)
+        np.testing.assert_allclose(res["dk"], tk.grad.numpy(), atol=1e-12)
+        np.testing.assert_allclose(res["dv"], tv.grad.numpy(), atol=1e-12)
+
+
+def pin_finite_differences(lib):
+    """Central differences of L = sum(dO * O(Q,K,V)) in every element of Q, K
+    and V match the backward (h = 1e-6, relative error < 1e-6)."""
+    r = _rng(7)
+    B, Hq, Hkv, T, D = 1, 2, 1, 5, 3
+    q = r.standard_normal((B, Hq, T, D))
+    k = r.standard_normal((B, Hkv, T, D))
+    v = r.standard_normal((B, Hkv, T, D))
+    do = r.standard_normal((B, Hq, T, D))
+    scale = 0.6
+    res = oracle.bwd(q, k, v, do, causal=True, scale=scale, lib=lib)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle.fwd(q_, k_, v_, causal=True, scale=scale, lib=lib)
+        return float((o * do).sum())
+
+    h = 1e-6
+    for name, x, grad in (("q", q, res["dq"]), ("k", k, res["dk"]), ("v", v, res["dv"])):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp = x.copy(); xp[idx] += h
+            xm = x.copy(); xm[idx] -= h
+            args = {"q": q, "k": k, "v": v}
+            args[name] = xp
+            lp = loss(args["q"], args["k"], args["v"])
+            args[name] = xm
+            lm = loss(args["q"], args["k"], args["v"])
+            fd[idx] = (lp - lm) / (2 * h)
+        err = np.abs(fd - grad).max() / max(np.abs(grad).max(), 1e-12)
+        assert err < 1e-6, (name, err)
+
+
+def pin_delta_identity(lib):
+    """The backward's row term Delta_i = sum_j P_ij dP_ij equals sum_d dO_id O_id."""
+    r = _rng(8)
+    q = r.standard_normal((1, 2, 12, 6))
+    k = r.standard_normal((1, 1, 12, 6))
+    v = r.standard_normal((1, 1, 12, 6))
+    do = r.standard_normal((1, 2, 12, 6))
+    res = oracle.bwd(q, k, v, do, causal=True, scale=0.5, lib=lib)
+    np.testing.assert_allclose(res["delta"], (res["o"] * do).sum(-1), atol=1e-12)
+
+
+def pin_varlen_equals_slices(lib):
+    """Packed variable length equals independent dense runs on each slice,
+    including a length-1 and a zero-length sequence."""
+    r = _rng(9)
+    lens = [5, 1, 0, 9, 3]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total, Hq, Hkv, D = int(cu[-1]), 4, 2, 5
+    q = r.standard_normal((total, Hq, D))
+    k = r.standard_normal((total, Hkv, D))
+    v = r.standard_normal((total, Hkv, D))
+    do = r.standard_normal((total, Hq, D))
+    res = oracle.varlen_bwd(q, k, v, do, cu, causal=True, scale=0.45, lib=lib)
+    o2, lse2 = oracle.varlen_fwd(q, k, v, cu, causal=True, scale=0.45, lib=lib)
+    np.testing.assert_allclose(o2, res["o"], atol=1e-14)
+    np.testing.assert_allclose(lse2, res["lse"], atol=1e-14)
+    for s in range(len(lens)):
+        a, b = cu[s], cu[s + 1]
+        if a == b:
+            continue
+        sl = lambda x: np.ascontiguousarray(x[a:b].transpose(1, 0, 2)[None])
+        d = oracle.bwd(sl(q), sl(k), sl(v), sl(do), causal=True, scale=0.45, lib=lib)
+        for n in ("o", "dq", "dk", "dv"):
+            np.testing.assert_allclose(res[n][a:b], d[n][0].transpose(1, 0, 2), atol=1e-12, err_msg=n)
+        np.testing.assert_allclose(res["lse"][:, a:b], d["lse"][0], atol=1e-12)
+
+
+PINS = [pin_hand_worked, pin_rows_sum_to_one, pin_single_token, pin_constant_keys, pin_shift_invariance,
+        pin_gqa_equals_repeated_mha, pin_torch_sdpa, pin_finite_differences, pin_delta_identity,
+        pin_varlen_equals_slices]
