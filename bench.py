@@ -1,0 +1,383 @@
+"""Benchmark: causal GQA attention forward + backward on GB300.
+
+One step = one forward (attn_fwd) and one backward (attn_bwd) of the long
+context GQA layer (B=2, Hq=32, Hkv=8, T=4096, D=128, causal, bf16) over one
+batch of synthetic inputs already resident in HBM.  The L2 cache (129 MB) is
+flushed by a 256 MiB write before every timed step; the step itself is timed
+with CUDA events on the launching stream.  FLOPs follow the causal convention
+(half of dense): forward 4*D and backward 10*D per visible (query, key) pair,
+i.e. 2*B*Hq*T^2*D and 5*B*Hq*T^2*D.
+
+Prints one JSON line.  --impl reference times the fp64 CPU oracle (the only
+reference this method has) on a bounded sample of the same workload.
+Multi-GPU: each rank runs an independent replica (the path has no exchange
+step); value = all ranks' FLOPs / max over ranks of the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from causal_gqa_attention_fwd_gb300 import workloads as W  # noqa: E402
+
+METRIC = "causal GQA attention fwd+bwd TFLOP/s (bf16) and % of GB300 tensor peak"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def flops(w: W.Workload, cu=None):
+    """(fwd, bwd) algorithmic FLOPs, causal counted as half of dense."""
+    if w.varlen:
+        lens = (cu[1:] - cu[:-1]).to(torch.int64)
+        sq = int((lens * lens).sum())
+    else:
+        sq = w.B * w.T * w.T
+    pairs = w.Hq * sq / (2.0 if w.causal else 1.0)
+    return 4.0 * w.D * pairs, 10.0 * w.D * pairs
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"bf16_tflops": d["bf16_tflops"], "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == 0:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for t, line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                rows.append((t, float(f[2]), float(f[3]), f[5:10]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if self.t0 - 0.15 <= r[0] <= self.t1 + 0.15] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3][1:]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_sample(w: W.Workload, x, budget_s: float, t_prefix: int | None = None):
+    """Time the fp64 oracle on whole (batch, kv-head) groups of the workload
+    until about budget_s seconds of CPU work (at least one group).  With
+    t_prefix, each group is cut to its first t_prefix positions (a causal
+    prefix is itself a complete causal problem).  Returns (FLOP/s, sample
+    description, cores, seconds)."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    G = w.Hq // w.Hkv
+    T = min(w.T, t_prefix) if t_prefix else w.T
+    done_flops, elapsed, groups = 0.0, 0.0, 0
+    f = lambda t: t.float().numpy().astype(np.float64)
+    total_groups = w.B * w.Hkv
+    while groups == 0 or (elapsed < budget_s and groups < total_groups):
+        b, g = divmod(groups, w.Hkv)
+        q = f(x["q"][b:b + 1, g * G:(g + 1) * G, :T])
+        k = f(x["k"][b:b + 1, g:g + 1, :T])
+        v = f(x["v"][b:b + 1, g:g + 1, :T])
+        do = f(x["do"][b:b + 1, g * G:(g + 1) * G, :T])
+        t0 = time.perf_counter()
+        oracle.bwd(q, k, v, do, causal=w.causal, scale=w.softmax_scale)   # forward + backward
+        elapsed += time.perf_counter() - t0
+        groups += 1
+        ff, fb = flops(W.Workload("s", B=1, Hq=G, Hkv=1, T=T, D=w.D, causal=w.causal))
+        done_flops += ff + fb
+    where = f"first {T} of T={w.T} positions" if T < w.T else f"full T={w.T}"
+    desc = (f"{groups} of {total_groups} (batch, kv-head) groups of {w.name}, {where} "
+            f"(G={G} query heads each), forward + backward in fp64, {elapsed:.1f} s")
+    return done_flops / elapsed, desc, cores, elapsed
+
+
+# ------------------------------------------------------------------- main
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = W.WORKLOADS[args.workload]
+    x = W.make_inputs(w, seed=0)
+    rates, descs, secs = [], [], 0.0
+    cores = len(os.sched_getaffinity(0))
+    for _ in range(args.warmup + args.steps):
+        # one group per step, cut to a 1024-position causal prefix so that a
+        # run of many steps stays within minutes
+        r, d, cores, el = oracle_sample(w, x, budget_s=0.0, t_prefix=1024)
+        rates.append(r)
+        descs.append(d)
+        secs += el
+    timed = rates[args.warmup:]
+    value = statistics.mean(timed) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T, "D": w.D, "causal": w.causal,
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "each step: " + descs[-1]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import causal_gqa_attention_fwd_gb300 as gq
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[args.workload]
+    x = W.make_inputs(w, seed=rank)
+    stream = torch.cuda.current_stream()
+    varlen = w.varlen
+    cu = x.get("cu_seqlens")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    scale = w.softmax_scale
+    if varlen:
+        cud = cu.to(dev)
+        maxlen = x["max_seqlen"]
+        o, lse = gq.attn_varlen_fwd(q, k, v, cud, maxlen, scale=scale)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(gq.attn_varlen_bwd_workspace_size(len(cu) - 1, q.shape[0], w.Hq, w.Hkv, w.D) + 256,
+                         dtype=torch.uint8, device=dev)
+    else:
+        o, lse = gq.attn_fwd(q, k, v, scale=scale)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(gq.attn_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.T, w.D), dtype=torch.uint8, device=dev)
+
+    def step():
+        if varlen:
+            gq.attn_varlen_fwd(q, k, v, cud, maxlen, scale=scale, o=o, lse=lse)
+            gq.attn_varlen_bwd(q, k, v, o, lse, do, cud, maxlen, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+        else:
+            gq.attn_fwd(q, k, v, scale=scale, o=o, lse=lse)
+            gq.attn_bwd(q, k, v, o, lse, do, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    f_fwd, f_bwd = flops(w, cu)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    assert gq.get_device_status() == 0, "device status after warm-up"
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    gq.profile_reset()
+    gq.profile_enable(True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark(0)
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    clocks.mark(1)
+    gq.profile_enable(False)
+    prof = gq.profile_read()
+    clk = clocks.stop()
+    status = gq.get_device_status()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    local_ms = sum(step_ms)
+    total_ms = max_over_ranks(world, local_ms)
+    ms_per_step = total_ms / args.steps
+    value = world * (f_fwd + f_bwd) * args.steps / (total_ms / 1e3) / 1e12
+    n_fwd, t_fwd = prof["attn_fwd"]
+    n_main, t_main = prof["bwd_main"]
+    bwd_ms = sum(prof[k][1] for k in ("bwd_pre", "bwd_main", "bwd_post")) / args.steps
+    fwd_ms = t_fwd / max(n_fwd, 1)
+    pk = peaks()
+    gpu_launches = sum(prof[k][0] for k in prof)
+
+    # roofline of the dominant kernel (the backward main kernel)
+    main_ms = t_main / max(n_main, 1)
+    achieved = f_bwd / (main_ms / 1e3) / 1e12
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        tj = json.load(open(tp)).get(w.name, {}).get("bwd_main")
+        traffic = tj
+    roofline = {"kernel": "bwd_main", "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
+                "peak_source": pk["source"] + " (burst bf16)"}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.pin_memory() for t in (x["q"], x["k"], x["v"], x["do"]))
+        ho, hlse = torch.empty_like(hq).pin_memory(), torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        hdq, hdk, hdv = (torch.empty_like(t).pin_memory() for t in (hq, hk, hv))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) + (cu.numel() * 4 if varlen else 0)
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            do.copy_(hdo, non_blocking=True)
+            if varlen:
+                cud.copy_(cu, non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+            hdq.copy_(dq, non_blocking=True)
+            hdk.copy_(dk, non_blocking=True)
+            hdv.copy_(dv, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 20))
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_s = max_over_ranks(world, time.perf_counter() - t0)
+        e2e = {"value": world * (f_fwd + f_bwd) * n_e2e / e2e_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, desc, cores, el = oracle_sample(w, x, args.cpu_budget)
+        cpu = {"value": rate / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T, "D": w.D,
+                       "causal": w.causal, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "flushed before every timed step (256 MiB write)"},
+            "frac_of_peak": value / pk["bf16_tflops"],
+            "fwd_tflops": f_fwd / (fwd_ms / 1e3) / 1e12,
+            "bwd_tflops": f_bwd / (bwd_ms / 1e3) / 1e12,
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "kernel_ms": {k: (t / n if n else None) for k, (n, t) in prof.items()},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": gpu_launches,
+            "clocks": clk,
+            "device_status": status,
+            "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,29 @@
+"""Causal grouped-query attention (forward and backward) for GB300 (sm_103a).
+
+The public entry points mirror the C ABI of include/gqa_attn.h and take
+PyTorch CUDA tensors (PyTorch supplies device memory and the stream):
+
+    attn_fwd(q, k, v, causal=True, scale=None) -> (o, lse)
+    attn_bwd(q, k, v, o, lse, dout, causal=True, scale=None) -> (dq, dk, dv)
+    attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen, ...) -> (o, lse)
+    attn_varlen_bwd(q, k, v, o, lse, dout, cu_seqlens, max_seqlen, ...) -> (dq, dk, dv)
+
+All arithmetic runs in the library's hand-written sm_103a kernels; a call
+raises if the library is not built.
+"""
+from ._binding import (  # noqa: F401
+    LIB_PATH,
+    AttnError,
+    attn_bwd,
+    attn_bwd_workspace_size,
+    attn_fwd,
+    attn_varlen_bwd,
+    attn_varlen_bwd_workspace_size,
+    attn_varlen_fwd,
+    get_device_status,
+    lib,
+    profile_enable,
+    profile_read,
+    profile_reset,
+    status_string,
+)

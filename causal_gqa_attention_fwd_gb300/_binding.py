@@ -1,0 +1,207 @@
+"""ctypes binding of libgqa_attn.so (include/gqa_attn.h).
+
+Argument marshalling only: shape/dtype checks, output allocation with torch
+(device memory is PyTorch's), the current CUDA stream, and the C call.  Every
+step of the attention runs in the library's CUDA kernels; there is no other
+code path.  Importing this module does not load the library; the first call
+does, and raises if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgqa_attn.so")
+
+STATUS = {
+    0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_SHAPE", 3: "ATTN_ERR_HEADDIM", 4: "ATTN_ERR_ALIGN",
+    5: "ATTN_ERR_SEQLENS", 6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_ARCH", 8: "ATTN_ERR_CUDA",
+    9: "ATTN_ERR_TIMEOUT",
+}
+
+# name -> (restype, argtypes)
+_P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_bwd_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "attn_bwd": (_I, [_P] * 10 + [_Z, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_varlen_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_varlen_bwd_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "attn_varlen_bwd": (_I, [_P] * 10 + [_Z, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_status_string": (ctypes.c_char_p, [_I]),
+    "attn_get_device_status": (_I, [_P, ctypes.POINTER(_I), _I]),
+    "attn_profile_enable": (_I, [_I]),
+    "attn_profile_reset": (_I, []),
+    "attn_profile_read": (_I, [_I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)]),
+}
+
+PROFILE_KINDS = {"attn_fwd": 0, "bwd_pre": 1, "bwd_main": 2, "bwd_post": 3}
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({status_string(code) if _lib else ''})")
+
+
+def lib():
+    """The loaded ctypes library (raises if it is not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with causal_gqa_attention_fwd_gb300.build.build() "
+                "(nvcc, sm_103a). There is no fallback implementation.")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name, None)
+            if fn is None:      # reported by the export test; calls raise AttributeError
+                continue
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().attn_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise AttnError(code, where)
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=torch.bfloat16):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _scale(scale, D):
+    return float(scale) if scale is not None else 1.0 / float(D) ** 0.5
+
+
+def get_device_status(clear: bool = True, stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    out = ctypes.c_int(0)
+    _check(lib().attn_get_device_status(_stream(stream), ctypes.byref(out), int(clear)), "attn_get_device_status")
+    return out.value
+
+
+def profile_enable(on: bool = True):
+    """Record CUDA events around every kernel launch (see attn_profile_read)."""
+    _check(lib().attn_profile_enable(int(on)), "attn_profile_enable")
+
+
+def profile_reset():
+    _check(lib().attn_profile_reset(), "attn_profile_reset")
+
+
+def profile_read() -> dict:
+    """{kernel: (launches, total_ms)} since the last reset (synchronises)."""
+    out = {}
+    for name, kind in PROFILE_KINDS.items():
+        n = ctypes.c_int(0)
+        ms = ctypes.c_double(0.0)
+        _check(lib().attn_profile_read(kind, ctypes.byref(n), ctypes.byref(ms)), "attn_profile_read")
+        out[name] = (n.value, ms.value)
+    return out
+
+
+def attn_fwd(q, k, v, causal: bool = True, scale=None, o=None, lse=None, stream=None):
+    """Dense forward.  q [B,Hq,T,D], k/v [B,Hkv,T,D] bf16 -> (o bf16, lse f32 [B,Hq,T])."""
+    B, Hq, T, D = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, T, D) or v.shape != k.shape:
+        raise ValueError("k, v must be [B, Hkv, T, D] matching q")
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = lib().attn_fwd(_need(q, "q"), _need(k, "k"), _need(v, "v"), _need(o, "o"),
+                        _need(lse, "lse", torch.float32), B, Hq, Hkv, T, D, int(causal), _scale(scale, D),
+                        _stream(stream))
+    _check(st, "attn_fwd")
+    return o, lse
+
+
+def attn_bwd_workspace_size(B, Hq, Hkv, T, D) -> int:
+    return int(lib().attn_bwd_workspace_size(B, Hq, Hkv, T, D))
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool = True, scale=None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """Dense backward -> (dq, dk, dv) bf16."""
+    B, Hq, T, D = q.shape
+    Hkv = k.shape[1]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = attn_bwd_workspace_size(B, Hq, Hkv, T, D)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    st = lib().attn_bwd(_need(q, "q"), _need(k, "k"), _need(v, "v"), _need(o, "o"),
+                        _need(lse, "lse", torch.float32), _need(dout, "dout"), _need(dq, "dq"), _need(dk, "dk"),
+                        _need(dv, "dv"), _need(workspace, "workspace", torch.uint8), workspace.numel(),
+                        B, Hq, Hkv, T, D, int(causal), _scale(scale, D), _stream(stream))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = True, scale=None, o=None, lse=None,
+                    stream=None):
+    """Packed forward.  q [total,Hq,D], k/v [total,Hkv,D], cu_seqlens int32 (device) [N+1]
+    -> (o [total,Hq,D], lse [Hq,total])."""
+    total, Hq, D = q.shape
+    Hkv = k.shape[1]
+    n = cu_seqlens.numel() - 1
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((Hq, total), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = lib().attn_varlen_fwd(_need(q, "q"), _need(k, "k"), _need(v, "v"), _need(o, "o"),
+                               _need(lse, "lse", torch.float32), _need(cu_seqlens, "cu_seqlens", torch.int32),
+                               n, total, int(max_seqlen), Hq, Hkv, D, int(causal), _scale(scale, D),
+                               _stream(stream))
+    _check(st, "attn_varlen_fwd")
+    return o, lse
+
+
+def attn_varlen_bwd_workspace_size(num_seqs, total, Hq, Hkv, D) -> int:
+    return int(lib().attn_varlen_bwd_workspace_size(num_seqs, total, Hq, Hkv, D))
+
+
+def attn_varlen_bwd(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: bool = True, scale=None,
+                    dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Packed backward -> (dq, dk, dv)."""
+    total, Hq, D = q.shape
+    Hkv = k.shape[1]
+    n = cu_seqlens.numel() - 1
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = attn_varlen_bwd_workspace_size(n, total, Hq, Hkv, D)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    st = lib().attn_varlen_bwd(_need(q, "q"), _need(k, "k"), _need(v, "v"), _need(o, "o"),
+                               _need(lse, "lse", torch.float32), _need(dout, "dout"), _need(dq, "dq"),
+                               _need(dk, "dk"), _need(dv, "dv"), _need(workspace, "workspace", torch.uint8),
+                               workspace.numel(), _need(cu_seqlens, "cu_seqlens", torch.int32), n, total,
+                               int(max_seqlen), Hq, Hkv, D, int(causal), _scale(scale, D), _stream(stream))
+    _check(st, "attn_varlen_bwd")
+    return dq, dk, dv

@@ -1,0 +1,371 @@
+// api.cu -- the C ABI declared in include/gqa_attn.h: argument validation,
+// TMA tensor-map construction, workspace carving and kernel launches.
+// Every host-detectable error is returned before anything is launched.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <vector>
+
+#include "gqa_attn.h"
+#include "kernels.h"
+#include "tmap.h"
+
+namespace {
+
+using gqa::BwdArgs;
+using gqa::FwdArgs;
+
+// Per-device status word (first device-detected error since last cleared).
+__device__ int g_attn_status;
+
+constexpr int kMaxDevices = 64;
+
+int* status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  static int* cache[kMaxDevices] = {};
+  if (dev < kMaxDevices && cache[dev]) return cache[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_attn_status) != cudaSuccess) return nullptr;
+  if (dev < kMaxDevices) cache[dev] = static_cast<int*>(p);
+  return static_cast<int*>(p);
+}
+
+attn_status check_arch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  static signed char known[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 wrong arch
+  if (dev < kMaxDevices && known[dev]) return known[dev] > 0 ? ATTN_OK : ATTN_ERR_ARCH;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const bool ok = major == 10 && minor == 3;
+  if (dev < kMaxDevices) known[dev] = ok ? 1 : -1;
+  return ok ? ATTN_OK : ATTN_ERR_ARCH;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attn_status check_heads(int Hq, int Hkv, int D) {
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_SHAPE;
+  if (Hq > 65535 || Hkv > 65535) return ATTN_ERR_SHAPE;
+  if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  return ATTN_OK;
+}
+
+// Dense [N, T, D] bf16 tensor seen as 3-D (D, T, N); box_rows x 64-element boxes.
+bool map_dense(CUtensorMap* m, const void* base, int D, int T, long nheads, int box_rows = 128) {
+  const uint64_t dims[3] = {(uint64_t)D, (uint64_t)T, (uint64_t)nheads};
+  const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)T * D * 2};
+  const uint32_t box[3] = {64, (uint32_t)box_rows, 1};
+  return gqa::make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Packed [total, H, D] bf16 tensor seen as 3-D (D, H, total); boxes of 128 tokens.
+bool map_packed(CUtensorMap* m, const void* base, int D, int H, int total, int box_rows) {
+  const uint64_t dims[3] = {(uint64_t)D, (uint64_t)H, (uint64_t)total};
+  const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)H * D * 2};
+  const uint32_t box[3] = {64, 1, (uint32_t)box_rows};
+  return gqa::make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+attn_status launch_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+// f32 dQ accumulator [rows, D] seen as 2-D (D, rows); 32 x 128 boxes, 128-byte swizzle.
+bool map_accum(CUtensorMap* m, const float* base, int D, long rows) {
+  const uint64_t dims[2] = {(uint64_t)D, (uint64_t)rows};
+  const uint64_t strides[1] = {(uint64_t)D * 4};
+  const uint32_t box[2] = {32, 128};
+  return gqa::make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+// Backward workspace: Delta [rows], LSE*log2(e) [rows], f32 dQ [rows, D],
+// each section 256-byte aligned.  Dense rows: B*Hq*round_up(T, 128).
+// Packed rows: Hq * total_pad (every sequence gets a 4-aligned base and at
+// least 128 rows of slack before the next one).
+long varlen_total_pad(int num_seqs, int total) { return (long)round_up((size_t)total + 132L * num_seqs + 256, 128); }
+
+size_t ws_bytes(long rows, int D) { return round_up((size_t)rows * 4, 256) * 2 + (size_t)rows * D * 4; }
+
+attn_status bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, void* ws, const int* cu, int num_seqs,
+                       int T, int total, int max_seqlen, int Hq, int Hkv, int D, int causal, float scale,
+                       void* stream, bool varlen) {
+  int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
+  BwdArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.o = static_cast<const __nv_bfloat16*>(o);
+  a.dout = static_cast<const __nv_bfloat16*>(dout);
+  a.lse = lse;
+  a.dq = static_cast<__nv_bfloat16*>(dq);
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.cu_seqlens = cu;
+  a.status = status;
+  a.num_seqs = num_seqs;
+  a.T = varlen ? max_seqlen : T;
+  a.T_pad = varlen ? 0 : (int)round_up((size_t)T, 128);
+  a.total = total;
+  a.total_pad = varlen ? (int)varlen_total_pad(num_seqs, total) : 0;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = Hq / Hkv;
+  a.D = D;
+  a.causal = causal ? 1 : 0;
+  a.varlen = varlen ? 1 : 0;
+  a.n_items = (a.T + 127) / 128;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const long rows = varlen ? (long)Hq * a.total_pad : (long)num_seqs * Hq * a.T_pad;
+  char* w = static_cast<char*>(ws);
+  a.delta = reinterpret_cast<float*>(w);
+  a.lse_log2 = reinterpret_cast<float*>(w + round_up((size_t)rows * 4, 256));
+  a.dq_accum = reinterpret_cast<float*>(w + 2 * round_up((size_t)rows * 4, 256));
+  const long grid = (long)a.n_items * num_seqs * Hkv;
+  if (grid > 0x7fffffffL || rows > 0x7fffffffL || (long)a.num_seqs * Hq > 65535L * 65535L) return ATTN_ERR_SHAPE;
+  const int bm = gqa::bwd_query_block(D);
+  CUtensorMap tq, tk, tv, tdo, tacc;
+  bool ok;
+  if (varlen)
+    ok = map_packed(&tq, q, D, Hq, total, bm) && map_packed(&tdo, dout, D, Hq, total, bm) &&
+         map_packed(&tk, k, D, Hkv, total, 128) && map_packed(&tv, v, D, Hkv, total, 128);
+  else
+    ok = map_dense(&tq, q, D, T, (long)num_seqs * Hq, bm) && map_dense(&tdo, dout, D, T, (long)num_seqs * Hq, bm) &&
+         map_dense(&tk, k, D, T, (long)num_seqs * Hkv) && map_dense(&tv, v, D, T, (long)num_seqs * Hkv);
+  ok = ok && map_accum(&tacc, a.dq_accum, D, rows);
+  if (!ok) return ATTN_ERR_CUDA;
+  return launch_status(gqa::launch_attn_bwd(tq, tk, tv, tdo, tacc, a, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu,
+                       int num_seqs, int T, int total, int max_seqlen, int Hq, int Hkv, int D, int causal,
+                       float scale, void* stream, bool varlen) {
+  const int rows = varlen ? max_seqlen : T;
+  int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
+  FwdArgs a{};
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.cu_seqlens = cu;
+  a.status = status;
+  a.num_seqs = num_seqs;
+  a.T = T;
+  a.total = total;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = Hq / Hkv;
+  a.causal = causal ? 1 : 0;
+  a.varlen = varlen ? 1 : 0;
+  a.pair_heads = (a.G % 2 == 0) ? 1 : 0;
+  a.pairs_per_seq = a.pair_heads ? Hq / 2 : Hq;
+  const int mblocks = (rows + 127) / 128;
+  a.m_items = a.pair_heads ? mblocks : (mblocks + 1) / 2;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const long grid = (long)a.m_items * num_seqs * a.pairs_per_seq;
+  if (grid <= 0) return ATTN_OK;
+  if (grid > 0x7fffffffL) return ATTN_ERR_SHAPE;
+  CUtensorMap tq, tk, tv;
+  bool ok;
+  if (varlen)
+    ok = map_packed(&tq, q, D, Hq, total, 128) && map_packed(&tk, k, D, Hkv, total, 128) &&
+         map_packed(&tv, v, D, Hkv, total, 128);
+  else
+    ok = map_dense(&tq, q, D, T, (long)num_seqs * Hq) && map_dense(&tk, k, D, T, (long)num_seqs * Hkv) &&
+         map_dense(&tv, v, D, T, (long)num_seqs * Hkv);
+  if (!ok) return ATTN_ERR_CUDA;
+  return launch_status(gqa::launch_attn_fwd(tq, tk, tv, a, D, (int)grid, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+// ------------------------------------------------------- kernel timing
+namespace gqa {
+namespace {
+struct ProfRec {
+  int kind;
+  cudaEvent_t start, stop;
+};
+std::vector<ProfRec> g_prof;       // event pool; [0, g_prof_used) hold records
+size_t g_prof_used = 0;
+bool g_prof_on = false;
+bool g_prof_open = false;
+constexpr size_t kProfMax = 1u << 16;
+}  // namespace
+
+void prof_begin(int kind, cudaStream_t s) {
+  g_prof_open = false;
+  if (!g_prof_on || g_prof_used >= kProfMax) return;
+  if (g_prof_used == g_prof.size()) {
+    ProfRec r{};
+    if (cudaEventCreate(&r.start) != cudaSuccess) return;
+    if (cudaEventCreate(&r.stop) != cudaSuccess) {
+      cudaEventDestroy(r.start);
+      return;
+    }
+    g_prof.push_back(r);
+  }
+  g_prof[g_prof_used].kind = kind;
+  if (cudaEventRecord(g_prof[g_prof_used].start, s) == cudaSuccess) g_prof_open = true;
+}
+
+void prof_end(cudaStream_t s) {
+  if (!g_prof_open) return;
+  g_prof_open = false;
+  if (cudaEventRecord(g_prof[g_prof_used].stop, s) == cudaSuccess) ++g_prof_used;
+}
+}  // namespace gqa
+
+extern "C" {
+
+attn_status attn_profile_enable(int enable) {
+  gqa::g_prof_on = enable != 0;
+  return ATTN_OK;
+}
+
+attn_status attn_profile_reset(void) {
+  gqa::g_prof_used = 0;
+  return ATTN_OK;
+}
+
+attn_status attn_profile_read(int kind, int* launches, double* total_ms) {
+  if (!launches || !total_ms) return ATTN_ERR_NULL;
+  if (kind < 0 || kind >= gqa::kProfKinds) return ATTN_ERR_SHAPE;
+  int n = 0;
+  double ms = 0.0;
+  for (size_t i = 0; i < gqa::g_prof_used; ++i) {
+    const gqa::ProfRec& r = gqa::g_prof[i];
+    if (r.kind != kind) continue;
+    float t = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    ++n;
+    ms += t;
+  }
+  *launches = n;
+  *total_ms = ms;
+  return ATTN_OK;
+}
+
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int T, int D, int causal, float scale, void* stream) {
+  if (B < 0 || T < 0) return ATTN_ERR_SHAPE;
+  attn_status st = check_heads(Hq, Hkv, D);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || T == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_ALIGN;
+  if ((long)B * Hq > 0x7fffffffL || !isfinite(scale)) return ATTN_ERR_SHAPE;
+  if ((st = check_arch()) != ATTN_OK) return st;
+  return fwd_common(q, k, v, o, lse, nullptr, B, T, 0, 0, Hq, Hkv, D, causal, scale, stream, false);
+}
+
+attn_status attn_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen, int Hq,
+                            int Hkv, int D, int causal, float scale, void* stream) {
+  if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0) return ATTN_ERR_SHAPE;
+  attn_status st = check_heads(Hq, Hkv, D);
+  if (st != ATTN_OK) return st;
+  if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return ATTN_OK;
+  if (max_seqlen > total_tokens || !isfinite(scale)) return ATTN_ERR_SHAPE;
+  if (!q || !k || !v || !o || !lse || !cu_seqlens) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_ALIGN;
+  if ((st = check_arch()) != ATTN_OK) return st;
+  return fwd_common(q, k, v, o, lse, cu_seqlens, num_seqs, 0, total_tokens, max_seqlen, Hq, Hkv, D, causal,
+                    scale, stream, true);
+}
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int T, int D) {
+  if (B < 0 || T < 0 || check_heads(Hq, Hkv, D) != ATTN_OK) return 0;
+  return ws_bytes((long)B * Hq * (long)round_up((size_t)T, 128), D);
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                     int T, int D, int causal, float scale, void* stream) {
+  if (B < 0 || T < 0) return ATTN_ERR_SHAPE;
+  attn_status st = check_heads(Hq, Hkv, D);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || T == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return ATTN_ERR_ALIGN;
+  if (!isfinite(scale)) return ATTN_ERR_SHAPE;
+  if (!workspace || workspace_bytes < attn_bwd_workspace_size(B, Hq, Hkv, T, D) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_WORKSPACE;
+  if ((st = check_arch()) != ATTN_OK) return st;
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr, B, T, 0, 0, Hq, Hkv, D, causal, scale,
+                    stream, false);
+}
+
+size_t attn_varlen_bwd_workspace_size(int num_seqs, int total_tokens, int Hq, int Hkv, int D) {
+  if (num_seqs < 0 || total_tokens < 0 || check_heads(Hq, Hkv, D) != ATTN_OK) return 0;
+  return ws_bytes((long)Hq * varlen_total_pad(num_seqs, total_tokens), D);
+}
+
+attn_status attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                            const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen, int Hq, int Hkv,
+                            int D, int causal, float scale, void* stream) {
+  if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0) return ATTN_ERR_SHAPE;
+  attn_status st = check_heads(Hq, Hkv, D);
+  if (st != ATTN_OK) return st;
+  if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return ATTN_OK;
+  if (max_seqlen > total_tokens || !isfinite(scale)) return ATTN_ERR_SHAPE;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !cu_seqlens) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return ATTN_ERR_ALIGN;
+  if (!workspace || workspace_bytes < attn_varlen_bwd_workspace_size(num_seqs, total_tokens, Hq, Hkv, D) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_WORKSPACE;
+  if ((st = check_arch()) != ATTN_OK) return st;
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, cu_seqlens, num_seqs, 0, total_tokens,
+                    max_seqlen, Hq, Hkv, D, causal, scale, stream, true);
+}
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_NULL: return "a required pointer is NULL";
+    case ATTN_ERR_SHAPE: return "invalid sizes (negative, Hq % Hkv != 0, or too large)";
+    case ATTN_ERR_HEADDIM: return "head dimension must be 64 or 128";
+    case ATTN_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case ATTN_ERR_SEQLENS: return "cu_seqlens is invalid";
+    case ATTN_ERR_WORKSPACE: return "workspace is NULL or too small";
+    case ATTN_ERR_ARCH: return "the current device is not compute capability 10.3 (sm_103a)";
+    case ATTN_ERR_CUDA: return "a CUDA runtime call failed";
+    case ATTN_ERR_TIMEOUT: return "a bounded in-kernel wait expired";
+  }
+  return "unknown status";
+}
+
+attn_status attn_get_device_status(void* stream, int* out, int clear) {
+  if (!out) return ATTN_ERR_NULL;
+  int* w = status_word();
+  if (!w) return ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (clear && v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(w, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  *out = v;
+  return ATTN_OK;
+}
+
+}  // extern "C"

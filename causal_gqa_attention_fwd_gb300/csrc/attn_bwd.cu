@@ -1,0 +1,609 @@
+// attn_bwd.cu -- causal grouped-query attention backward for sm_103a.
+//
+// For L = sum(dO * O) with O = softmax(scale QK^T + mask) V (the causal GQA
+// backward of the microLLM-rocm README, section "Why this project exists"),
+// with P recomputed from the forward's LSE instead of stored:
+//   P  = exp(scale S - LSE),  dV = P^T dO,  dP = dO V^T,
+//   Delta_i = sum_d dO_id O_id,  dS = P * (dP - Delta),
+//   dQ = scale dS K,  dK = scale dS^T Q  (dK, dV summed over the G heads of a group).
+// Three kernels:
+//   1. bwd_pre   Delta, LSE*log2(e) into workspace rows; zero the f32 dQ
+//                accumulator (HBM-bound).
+//   2. bwd_main  key/value-stationary: one CTA per (sequence, K/V head, block
+//                of 128 keys) keeps K, V in shared memory and dK, dV in TMEM,
+//                and walks the G query heads of the group and every query
+//                block that sees its keys.  Per step, five tcgen05 MMAs:
+//                  S^T = K Q^T,  dP^T = V dO^T          (TMEM)
+//                  dV += P^T dO, dK += dS^T Q           (TMEM accumulators)
+//                  dQ partial = dS K                    (TMEM -> smem -> bulk
+//                                                        reduce-add into f32)
+//                dK and dV leave the CTA once, complete (no atomics).
+//   3. bwd_post  dQ = bf16(scale * accumulator).
+// Roles in bwd_main (384 threads): warp 0 TMA producer, warp 1 MMA issuer
+// (+TMEM owner), warps 4-7 compute P and dS (thread = key row), warps 8-11
+// drain dQ partials and write dK, dV.
+#include "sm103.cuh"
+#include "kernels.h"
+
+namespace gqa {
+
+namespace {
+
+constexpr int kBN = 128;  // keys per CTA
+
+// dst tensor (f32) += 128-byte-swizzled smem box at coordinates (x, y).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Workspace row of (sequence s, head h, position p).  Dense: s is the batch
+// index and every head owns T_pad rows.  Packed: every head owns total_pad
+// rows and sequence s starts at a 4-aligned base, 132 rows further apart than
+// the tokens before it, so a 128-row tile never reaches the next sequence.
+__device__ __forceinline__ long ws_row(const BwdArgs& a, int s, int tok0, int h, int p) {
+  if (a.varlen) return (long)h * a.total_pad + (long)(((tok0 + 3) & ~3) + 132 * s) + p;
+  return ((long)s * a.Hq + h) * a.T_pad + p;
+}
+
+__device__ __forceinline__ bool seq_bounds(const BwdArgs& a, int s, int& tok0, int& L) {
+  if (!a.varlen) {
+    tok0 = 0;
+    L = a.T;
+    return true;
+  }
+  tok0 = a.cu_seqlens[s];
+  const int tok1 = a.cu_seqlens[s + 1];
+  L = tok1 - tok0;
+  return tok0 >= 0 && L >= 0 && tok1 <= a.total;
+}
+
+// Element offset of row p of head h (of a tensor with H heads) in sequence s.
+__device__ __forceinline__ long row_off(const BwdArgs& a, int s, int tok0, int h, int H, int p, int D) {
+  if (a.varlen) return ((long)(tok0 + p) * H + h) * D;
+  return (((long)s * H + h) * a.T + p) * D;
+}
+
+}  // namespace
+
+// =========================================================== 1. preprocess
+// grid: (row blocks of 128, num_seqs * Hq); 256 threads, one warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
+  const int s = blockIdx.y / a.Hq, h = blockIdx.y % a.Hq;
+  int tok0, L;
+  if (!seq_bounds(a, s, tok0, L)) {
+    if (threadIdx.x == 0) atomicCAS(a.status, 0, kDevBadSeqlens);
+    return;
+  }
+  const int Lr = (L + 127) & ~127;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int rr = warp; rr < 128; rr += 8) {
+    const int p = blockIdx.x * 128 + rr;
+    if (p >= Lr) break;
+    const long w = ws_row(a, s, tok0, h, p);
+    float dl = 0.f, l2 = INFINITY;
+    if (p < L) {
+      const long off = row_off(a, s, tok0, h, a.Hq, p, D);
+      float acc = 0.f;
+      if (D == 128) {
+        const uint2 ov = *reinterpret_cast<const uint2*>(a.o + off + lane * 4);
+        const uint2 gv = *reinterpret_cast<const uint2*>(a.dout + off + lane * 4);
+        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float2 of = __bfloat1622float2(o2[i]), gf = __bfloat1622float2(g2[i]);
+          acc = fmaf(of.x, gf.x, acc);
+          acc = fmaf(of.y, gf.y, acc);
+        }
+      } else {
+        const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(a.o + off + lane * 2);
+        const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(a.dout + off + lane * 2);
+        const float2 of = __bfloat1622float2(o2), gf = __bfloat1622float2(g2);
+        acc = fmaf(of.x, gf.x, of.y * gf.y);
+      }
+#pragma unroll
+      for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+      dl = acc;
+      const long li = a.varlen ? (long)h * a.total + tok0 + p : ((long)s * a.Hq + h) * a.T + p;
+      l2 = a.lse[li] * 1.4426950408889634f;
+    }
+    if (lane == 0) {
+      a.delta[w] = dl;
+      a.lse_log2[w] = l2;
+    }
+    float* acc_row = a.dq_accum + w * D;
+    if (D == 128)
+      *reinterpret_cast<float4*>(acc_row + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    else
+      *reinterpret_cast<float2*>(acc_row + lane * 2) = make_float2(0.f, 0.f);
+  }
+}
+
+// ============================================================ 3. postprocess
+template <int D>
+__global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
+  const int s = blockIdx.y / a.Hq, h = blockIdx.y % a.Hq;
+  int tok0, L;
+  if (!seq_bounds(a, s, tok0, L)) return;
+  constexpr int kChunks = D / 8;
+  for (int idx = threadIdx.x; idx < 128 * kChunks; idx += 256) {
+    const int p = blockIdx.x * 128 + idx / kChunks, c = idx % kChunks;
+    if (p >= L) continue;
+    const float* src = a.dq_accum + ws_row(a, s, tok0, h, p) * D + c * 8;
+    const float4 x0 = *reinterpret_cast<const float4*>(src);
+    const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
+    uint4 out;
+    out.x = pack_bf16x2(x0.x * a.scale, x0.y * a.scale);
+    out.y = pack_bf16x2(x0.z * a.scale, x0.w * a.scale);
+    out.z = pack_bf16x2(x1.x * a.scale, x1.y * a.scale);
+    out.w = pack_bf16x2(x1.z * a.scale, x1.w * a.scale);
+    *reinterpret_cast<uint4*>(a.dq + row_off(a, s, tok0, h, a.Hq, p, D) + c * 8) = out;
+  }
+}
+
+// ============================================================== 2. main
+namespace {
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kBM = D == 128 ? 64 : 128;     // queries per step
+  static constexpr int kStages = 2;
+  static constexpr int kKVBytes = kBN * D * 2;         // K or V tile
+  static constexpr int kQBytes = kBM * D * 2;          // Q or dO tile
+  static constexpr int kQBoxBytes = kBM * 128;         // one 64-column box of a Q tile
+  static constexpr int kStatBytes = kBM * 4;
+  static constexpr int kStageBytes = 2 * kQBytes + 1024;   // Q, dO, LSE2 + Delta (padded)
+  static constexpr int kPBytes = kBN * kBM * 2;        // P^T or dS^T tile
+  static constexpr int kStgBytes = kBM * D * 4;        // f32 dQ staging
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kKVBytes;
+  static constexpr int kOffStage = kOffV + kKVBytes;
+  static constexpr int kOffP = kOffStage + kStages * kStageBytes;
+  static constexpr int kOffDS = kOffP + kPBytes;
+  static constexpr int kOffStg = kOffDS + kPBytes;
+  static constexpr int kSmemBytes = kOffStg + kStgBytes + 1024;
+  // TMEM columns
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColDP = kBM;
+  static constexpr uint32_t kColDQ = 2 * kBM;
+  static constexpr uint32_t kColDK = D == 128 ? 256 : 320;
+  static constexpr uint32_t kColDV = kColDK + D;
+  static constexpr uint32_t kIdescS = idesc_bf16(kBN, kBM, false, false);    // S^T, dP^T
+  static constexpr uint32_t kIdescKV = idesc_bf16(kBN, D, false, true);      // dV, dK
+  static constexpr uint32_t kIdescQ = idesc_bf16(128, 64, true, true);       // dQ^T (D=128) / dQ (D=64)
+};
+
+struct __align__(8) BwdBarriers {
+  uint64_t kv_full;
+  uint64_t st_full[2];
+  uint64_t st_empty[2];
+  uint64_t s_full, dp_full, p_full, ds_full;
+  uint64_t dq_full, dq_empty;
+  uint64_t stg_full, stg_free;
+  uint64_t dkdv_done, teardown;
+  uint32_t tmem_base;
+  int abort;
+};
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dqacc, const BwdArgs a) {
+  using C = BwdCfg<D>;
+  constexpr int BM = C::kBM;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ BwdBarriers bars;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Guard guard{&bars.abort, a.status};
+
+  // ------------------------------------------------------------- decode
+  int item = blockIdx.x;
+  const int hkv = item % a.Hkv;
+  item /= a.Hkv;
+  const int s = item % a.num_seqs;
+  const int nb = item / a.num_seqs;                    // key block; heaviest (0) first
+  int tok0, L;
+  if (!seq_bounds(a, s, tok0, L)) {
+    if (threadIdx.x == 0) atomicCAS(a.status, 0, kDevBadSeqlens);
+    return;
+  }
+  const int k0 = nb * kBN;
+  if (k0 >= L) return;
+  const int n_mb = (L + BM - 1) / BM;
+  const int mb0 = a.causal ? k0 / BM : 0;
+  const int per_head = n_mb - mb0;
+  const int n_it = a.G * per_head;
+
+  if (threadIdx.x == 0) {
+    bars.abort = 0;
+    mbar_init(&bars.kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.st_full[i], 1);
+      mbar_init(&bars.st_empty[i], 1);
+    }
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.p_full, 128);
+    mbar_init(&bars.ds_full, 128);
+    mbar_init(&bars.dq_full, 1);
+    mbar_init(&bars.dq_empty, 128);
+    mbar_init(&bars.stg_full, 128);
+    mbar_init(&bars.stg_free, 1);
+    mbar_init(&bars.dkdv_done, 1);
+    mbar_init(&bars.teardown, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
+  uint8_t* sP = smem + C::kOffP;
+  uint8_t* sDS = smem + C::kOffDS;
+  uint8_t* sStg = smem + C::kOffStg;
+  auto stage_q = [&](int st) { return smem + C::kOffStage + st * C::kStageBytes; };
+  auto stage_do = [&](int st) { return smem + C::kOffStage + st * C::kStageBytes + C::kQBytes; };
+  auto stage_lse = [&](int st) {
+    return reinterpret_cast<float*>(smem + C::kOffStage + st * C::kStageBytes + 2 * C::kQBytes);
+  };
+  auto stage_delta = [&](int st) {
+    return reinterpret_cast<float*>(smem + C::kOffStage + st * C::kStageBytes + 2 * C::kQBytes + 512);
+  };
+  // iteration -> (query head, query block)
+  auto it_head = [&](int i) { return hkv * a.G + i / per_head; };
+  auto it_mb = [&](int i) { return mb0 + i % per_head; };
+
+  if (warp == 0) {
+    // ======================================================== TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      int c1, c2;
+      if (a.varlen) { c1 = hkv; c2 = tok0 + k0; } else { c1 = k0; c2 = s * a.Hkv + hkv; }
+      mbar_expect_tx(&bars.kv_full, 2 * C::kKVBytes);
+      for (int b = 0; b < D / 64; ++b) {
+        tma_load_3d(sK + b * 16384, &tm_k, &bars.kv_full, b * 64, c1, c2);
+        tma_load_3d(sV + b * 16384, &tm_v, &bars.kv_full, b * 64, c1, c2);
+      }
+      int last_phase[2] = {-1, -1};
+      for (int i = 0; i < n_it; ++i) {
+        const int st = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        if (!mbar_wait(&bars.st_empty[st], ph ^ 1, guard)) break;
+        const int h = it_head(i), mb = it_mb(i);
+        if (a.varlen) { c1 = h; c2 = tok0 + mb * BM; } else { c1 = mb * BM; c2 = s * a.Hq + h; }
+        mbar_expect_tx(&bars.st_full[st], 2 * C::kQBytes + 2 * C::kStatBytes);
+        for (int b = 0; b < D / 64; ++b) {
+          tma_load_3d(stage_q(st) + b * C::kQBoxBytes, &tm_q, &bars.st_full[st], b * 64, c1, c2);
+          tma_load_3d(stage_do(st) + b * C::kQBoxBytes, &tm_do, &bars.st_full[st], b * 64, c1, c2);
+        }
+        const long w = ws_row(a, s, tok0, h, mb * BM);
+        bulk_load(stage_lse(st), a.lse_log2 + w, C::kStatBytes, &bars.st_full[st]);
+        bulk_load(stage_delta(st), a.delta + w, C::kStatBytes, &bars.st_full[st]);
+        last_phase[st] = (int)ph;
+      }
+      mbar_wait_drain(&bars.kv_full, 0);
+      for (int st = 0; st < 2; ++st)
+        if (last_phase[st] >= 0) mbar_wait_drain(&bars.st_full[st], (uint32_t)last_phase[st]);
+    }
+  } else if (warp == 1) {
+    // ========================================================= MMA issuer
+    if (lane == 0) {
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP), aDS = smem_u32(sDS);
+      // X^T = A B^T with A a [128 x D] K-major tile (K or V) and B a [BM x D]
+      // K-major stage tile (Q or dO).
+      auto mma_t = [&](uint32_t d, uint32_t a_base, uint32_t b_base) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(d, sdesc_sw128(a_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(b_base + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024), C::kIdescS, kk > 0);
+      };
+      // Acc += A^T-tile [128 x BM] (K-major, smem) * B [BM x D] (MN-major stage tile)
+      auto mma_acc = [&](uint32_t d, uint32_t a_base, uint32_t b_base, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          mma_ss(d, sdesc_sw128(a_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(b_base + kk * 2048, C::kQBoxBytes, 1024), C::kIdescKV, (acc || kk > 0) ? 1u : 0u);
+      };
+      // dQ^T = K^T dS^T (D = 128) or dQ = dS K (D = 64): both operands MN-major,
+      // contraction over the 128 keys.
+      auto mma_dq = [&]() {
+        const uint32_t qa = D == 128 ? aK : aDS, qb = D == 128 ? aDS : aK;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ss(tmem + C::kColDQ, sdesc_sw128(qa + kk * 2048, 16384, 1024), sdesc_sw128(qb + kk * 2048, 16384, 1024),
+                 C::kIdescQ, kk > 0);
+      };
+      bool ok = mbar_wait(&bars.kv_full, 0, guard);
+      if (ok && n_it > 0) {
+        ok = mbar_wait(&bars.st_full[0], 0, guard);
+        if (ok) {
+          tc_fence_after();
+          mma_t(tmem + C::kColS, aK, smem_u32(stage_q(0)));
+          tc_commit(&bars.s_full);
+          mma_t(tmem + C::kColDP, aV, smem_u32(stage_do(0)));
+          tc_commit(&bars.dp_full);
+        }
+      }
+      for (int i = 0; i < n_it && ok; ++i) {
+        const int st = i & 1;
+        const uint32_t par = i & 1;
+        if (!(ok = mbar_wait(&bars.p_full, par, guard))) break;
+        tc_fence_after();
+        mma_acc(tmem + C::kColDV, aP, smem_u32(stage_do(st)), i > 0);
+        if (i + 1 < n_it) {
+          const int st1 = (i + 1) & 1;
+          if (!(ok = mbar_wait(&bars.st_full[st1], ((i + 1) >> 1) & 1, guard))) break;
+          tc_fence_after();
+          mma_t(tmem + C::kColS, aK, smem_u32(stage_q(st1)));
+          tc_commit(&bars.s_full);
+        }
+        if (!(ok = mbar_wait(&bars.ds_full, par, guard))) break;
+        tc_fence_after();
+        mma_acc(tmem + C::kColDK, aDS, smem_u32(stage_q(st)), i > 0);
+        if (!(ok = mbar_wait(&bars.dq_empty, par ^ 1, guard))) break;
+        tc_fence_after();
+        mma_dq();
+        tc_commit(&bars.dq_full);
+        tc_commit(&bars.st_empty[st]);
+        if (i + 1 < n_it) {
+          mma_t(tmem + C::kColDP, aV, smem_u32(stage_do((i + 1) & 1)));
+          tc_commit(&bars.dp_full);
+        }
+      }
+      if (ok) tc_commit(&bars.dkdv_done);
+      tc_commit(&bars.teardown);
+      mbar_wait_drain(&bars.teardown, 0);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ================================================ compute P^T and dS^T
+    const int r = threadIdx.x & 127;                  // key row
+    const int key = k0 + r;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const float c = a.scale_log2;
+    const uint32_t rowP = smem_u32(sP) + r * 128, rowDS = smem_u32(sDS) + r * 128;
+    for (int i = 0; i < n_it; ++i) {
+      const int st = i & 1;
+      const uint32_t par = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars.st_full[st], (i >> 1) & 1, guard))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars.s_full, par, guard))) break;
+      tc_fence_after();
+      const float* lse2 = stage_lse(st);
+      const float* dl = stage_delta(st);
+      const int q0 = it_mb(i) * BM;
+      const bool need_mask = (a.causal && q0 <= k0 + kBN - 1) || (k0 + kBN > L) || (q0 + BM > L);
+      // visible iff key < L, query < L and (not causal or key <= query)
+      const int qmin = a.causal ? key : 0;     // smallest visible query index
+      uint32_t pv[BM];                          // S^T row, then P^T row (f32 bits)
+#pragma unroll
+      for (int q = 0; q < BM / 32; ++q) tmem_ld_x32(tmem + lane_base + C::kColS + q * 32, pv + q * 32);
+      tmem_ld_wait();
+      reg_fence<BM>(pv);
+      float* p = reinterpret_cast<float*>(pv);
+#pragma unroll
+      for (int j = 0; j < BM; ++j) p[j] = ex2_approx(fmaf(p[j], c, -lse2[j]));
+      if (need_mask) {
+        const bool krow_ok = key < L;
+#pragma unroll
+        for (int j = 0; j < BM; ++j) {
+          const int qi = q0 + j;
+          if (!krow_ok || qi >= L || qi < qmin) p[j] = 0.f;
+        }
+      }
+      // P^T row -> bf16 -> sP (128-byte swizzled K-major rows).  With 128
+      // query columns the bf16 copy is also what dS is formed from (register
+      // budget); with 64 the f32 values are kept.
+      constexpr bool kPackP = BM == 128;
+      uint32_t pk[BM / 2];
+#pragma unroll
+      for (int ch = 0; ch < BM / 8; ++ch) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pk[4 * ch + e] = pack_bf16x2(p[8 * ch + 2 * e], p[8 * ch + 2 * e + 1]);
+        const uint32_t addr = rowP + (ch >> 3) * 16384 + (((ch & 7) ^ (r & 7)) << 4);
+        st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars.p_full);
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars.dp_full, par, guard))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < BM / 32; ++q) {
+        uint32_t dv[32];
+        tmem_ld_x32(tmem + lane_base + C::kColDP + q * 32, dv);
+        tmem_ld_wait();
+        reg_fence<32>(dv);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int j0 = q * 32 + cc * 8;
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = j0 + 2 * e;
+            float p0, p1;
+            if (kPackP) {
+              const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[j / 2]));
+              p0 = pf.x;
+              p1 = pf.y;
+            } else {
+              p0 = p[j];
+              p1 = p[j + 1];
+            }
+            const float d0 = p0 * (__uint_as_float(dv[cc * 8 + 2 * e]) - dl[j]);
+            const float d1 = p1 * (__uint_as_float(dv[cc * 8 + 2 * e + 1]) - dl[j + 1]);
+            w[e] = pack_bf16x2(d0, d1);
+          }
+          const int ch = j0 / 8;
+          st_shared_v4(rowDS + (ch >> 3) * 16384 + (((ch & 7) ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars.ds_full);
+    }
+  } else if (warp >= 8) {
+    // ===================================== drain dQ partials; dK, dV epilogue
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const bool leader = (r == 0);
+    const uint32_t stg = smem_u32(sStg);
+    bool ok = true;
+    for (int i = 0; i < n_it; ++i) {
+      const uint32_t par = i & 1;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_full, par, guard)))) break;
+      tc_fence_after();
+      uint32_t v[64];
+      tmem_ld_x32(tmem + lane_base + C::kColDQ, v);
+      tmem_ld_x32(tmem + lane_base + C::kColDQ + 32, v + 32);
+      tmem_ld_wait();
+      reg_fence<64>(v);
+      tc_fence_before();
+      mbar_arrive(&bars.dq_empty);
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.stg_free, par ^ 1, guard)))) break;
+      if (D == 128) {
+        // lane = feature d, columns = 64 queries: staging [q][d]
+#pragma unroll
+        for (int q = 0; q < 64; ++q)
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(stg + (q * 128 + r) * 4), "r"(v[q]) : "memory");
+      } else {
+        // lane = query, columns = 64 features: two 128-byte-swizzled boxes of
+        // [128 queries][32 features] (the layout the tensor reduce reads)
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            st_shared_v4(stg + b * 16384 + r * 128 + ((ch ^ (r & 7)) << 4), v[32 * b + 4 * ch],
+                         v[32 * b + 4 * ch + 1], v[32 * b + 4 * ch + 2], v[32 * b + 4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars.stg_full);
+      if (leader) {
+        if (!mbar_wait(&bars.stg_full, par, guard)) { ok = false; }
+        if (ok) {
+          const long w = ws_row(a, s, tok0, it_head(i), it_mb(i) * BM);
+          if (D == 128) {
+            bulk_reduce_add_f32(a.dq_accum + w * D, sStg, C::kStgBytes);
+          } else {
+            tma_reduce_add_2d(&tm_dqacc, sStg, 0, (int)w);
+            tma_reduce_add_2d(&tm_dqacc, sStg + 16384, 32, (int)w);
+          }
+          bulk_commit();
+          bulk_wait_read0();
+        }
+        mbar_arrive(&bars.stg_free);
+      }
+      if (!__all_sync(0xffffffffu, ok)) break;
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.dkdv_done, 0, guard));
+    if (ok) {
+      tc_fence_after();
+      // dK (scaled) into sK, dV into sV (both dead now): row r, swizzled 16-byte chunks
+      for (int t = 0; t < 2; ++t) {
+        const uint32_t col = t == 0 ? C::kColDK : C::kColDV;
+        const float mul = t == 0 ? a.scale : 1.f;
+        const uint32_t srow = smem_u32(t == 0 ? sK : sV) + r * (D * 2);
+#pragma unroll 1
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t x[32];
+          tmem_ld_x32(tmem + lane_base + col + q * 32, x);
+          tmem_ld_wait();
+          reg_fence<32>(x);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int ch = q * 4 + cc;
+            st_shared_v4(srow + ((ch ^ (r & 7)) << 4),
+                         pack_bf16x2(__uint_as_float(x[8 * cc]) * mul, __uint_as_float(x[8 * cc + 1]) * mul),
+                         pack_bf16x2(__uint_as_float(x[8 * cc + 2]) * mul, __uint_as_float(x[8 * cc + 3]) * mul),
+                         pack_bf16x2(__uint_as_float(x[8 * cc + 4]) * mul, __uint_as_float(x[8 * cc + 5]) * mul),
+                         pack_bf16x2(__uint_as_float(x[8 * cc + 6]) * mul, __uint_as_float(x[8 * cc + 7]) * mul));
+          }
+        }
+      }
+      __syncwarp();
+      constexpr int kChunks = D * 2 / 16;
+      const int rows_valid = min(kBN, L - k0);
+      const int row0 = (warp & 3) * 32;
+      for (int t = 0; t < 2; ++t) {
+        __nv_bfloat16* dst = t == 0 ? a.dk : a.dv;
+        const uint32_t sb = smem_u32(t == 0 ? sK : sV);
+        for (int idx = lane; idx < 32 * kChunks; idx += 32) {
+          const int row = row0 + idx / kChunks, cch = idx % kChunks;
+          if (row < rows_valid) {
+            const uint4 val = ld_shared_v4(sb + row * (D * 2) + ((cch ^ (row & 7)) << 4));
+            *reinterpret_cast<uint4*>(dst + row_off(a, s, tok0, hkv, a.Hkv, k0 + row, D) + cch * 8) = val;
+          }
+        }
+      }
+    }
+    if (leader) bulk_wait0();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+template <int D>
+static cudaError_t launch_bwd_d(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                const CUtensorMap& dout, const CUtensorMap& dqacc, const BwdArgs& a,
+                                cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int rblocks = (a.T + 127) / 128;   // T: dense length, or the longest sequence
+  dim3 gpre(rblocks, a.num_seqs * a.Hq);
+  prof_begin(kProfBwdPre, stream);
+  bwd_pre_kernel<D><<<gpre, 256, 0, stream>>>(a);
+  prof_end(stream);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long grid = (long)a.n_items * a.num_seqs * a.Hkv;
+  prof_begin(kProfBwdMain, stream);
+  bwd_main_kernel<D><<<(unsigned)grid, 384, C::kSmemBytes, stream>>>(q, k, v, dout, dqacc, a);
+  prof_end(stream);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prof_begin(kProfBwdPost, stream);
+  bwd_post_kernel<D><<<gpre, 256, 0, stream>>>(a);
+  prof_end(stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& dout, const CUtensorMap& dqacc, const BwdArgs& a,
+                            cudaStream_t stream) {
+  if (a.D == 128) return launch_bwd_d<128>(q, k, v, dout, dqacc, a, stream);
+  return launch_bwd_d<64>(q, k, v, dout, dqacc, a, stream);
+}
+
+int bwd_query_block(int D) { return D == 128 ? BwdCfg<128>::kBM : BwdCfg<64>::kBM; }
+
+}  // namespace gqa

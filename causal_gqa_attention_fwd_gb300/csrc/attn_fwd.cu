@@ -1,0 +1,431 @@
+// attn_fwd.cu -- causal grouped-query attention forward for sm_103a.
+//
+// Computes, per query head h (key/value head h / G), O = softmax(scale*QK^T +
+// causal mask) V and the natural-log row log-sum-exp LSE, keeping the softmax
+// statistics block by block (running max and running sum) instead of
+// materialising the score matrix -- the blockwise scheme named in "Project
+// Overview" (llm-from-scratch), section "Performance Layer: kernel/ and
+// parallel/"; the operation itself is the ScaledDotProductAttention of its
+// llm/transformer.py list and the "Decoder-only MHA/GQA ... causal attention"
+// of the microLLM-rocm README, section "Why this project exists".
+//
+// One CTA owns two 128-row query tiles that read the same key/value blocks:
+// two query heads of one GQA group at the same rows (G even), or two
+// consecutive row blocks of one head (G odd).  Roles (384 threads):
+//   warp 0      TMA producer: Q tiles once, then K_j, V_j through a ring.
+//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM (SS form), then
+//               O += P V with P read from TMEM (TS form); allocates TMEM.
+//   warps 4-7   softmax for tile A, warps 8-11 for tile B; thread = row.
+// TMEM columns: S_A [0,128), S_B [128,256), O_A, O_B (D columns each).
+// P (bf16) overwrites the first 64 columns of its S block.
+// Tiles of key blocks past the diagonal are never visited; only the diagonal
+// block and a ragged last block are masked.
+#include "sm103.cuh"
+#include "kernels.h"
+
+namespace gqa {
+
+namespace {
+
+constexpr int kBM = 128;       // query rows per tile
+constexpr int kBN = 128;       // keys per block
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: lazy O rescale
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kTileBytes = kBM * D * 2;        // one Q / K / V tile
+  static constexpr int kBoxes = D / 64;                  // 64-element TMA boxes
+  static constexpr int kBoxBytes = kBM * 128;            // 16 KB
+  static constexpr int kStages = D == 128 ? 4 : 8;       // K/V ring depth
+  static constexpr int kSmemQ = 2 * kTileBytes;
+  static constexpr int kSmemRing = kStages * kTileBytes;
+  static constexpr int kSmemBytes = kSmemQ + kSmemRing + 1024;  // + alignment slack
+  __device__ static constexpr uint32_t col_s(int x) { return (uint32_t)x * 128u; }
+  __device__ static constexpr uint32_t col_o(int x) { return 256u + (uint32_t)x * D; }
+  static constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false, false);
+  static constexpr uint32_t kIdescPV = idesc_bf16(kBM, D, false, true);
+};
+
+struct __align__(8) FwdBarriers {
+  uint64_t q_full[2];
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t teardown;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct TileInfo {
+  int valid;
+  int hq;        // query head
+  int mb;        // row block within the sequence
+  int nkv;       // key blocks to visit
+};
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                      // 2 tiles
+  uint8_t* sRing = smem + C::kSmemQ;       // kStages tiles
+  __shared__ FwdBarriers bars;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  Guard guard{&bars.abort, args.status};
+
+  // ---------------------------------------------------------- work decode
+  // blockIdx.x -> (row-block item, sequence/batch, head pair); heaviest
+  // (largest row block) first.
+  int item = blockIdx.x;
+  const int pairs = args.pairs_per_seq;
+  const int pair = item % pairs;
+  item /= pairs;
+  const int seq = item % args.num_seqs;
+  const int mitem = args.m_items - 1 - item / args.num_seqs;
+
+  int tok0 = 0, L = args.T;
+  if (args.varlen) {
+    tok0 = args.cu_seqlens[seq];
+    const int tok1 = args.cu_seqlens[seq + 1];
+    L = tok1 - tok0;
+    if (L < 0 || tok0 < 0 || tok1 > args.total) {
+      if (threadIdx.x == 0) atomicCAS(args.status, 0, kDevBadSeqlens);
+      return;
+    }
+  }
+  const int nkv_all = (L + kBN - 1) / kBN;
+  TileInfo ti[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    if (args.pair_heads) {           // two heads of one group, same rows
+      ti[x].hq = 2 * pair + x;
+      ti[x].mb = mitem;
+    } else {                         // one head, two consecutive row blocks
+      ti[x].hq = pair;
+      ti[x].mb = 2 * mitem + x;
+    }
+    ti[x].valid = ti[x].mb * kBM < L;
+    ti[x].nkv = !ti[x].valid ? 0 : (args.causal ? min(ti[x].mb + 1, nkv_all) : nkv_all);
+  }
+  if (!ti[0].valid && !ti[1].valid) return;
+  const int hkv = ti[0].valid ? ti[0].hq / args.G : ti[1].hq / args.G;
+  const int nkv = max(ti[0].nkv, ti[1].nkv);
+
+  // ------------------------------------------------------------- set-up
+  if (threadIdx.x == 0) {
+    bars.abort = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.q_full[i], 1);
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.p_full[i], kBM);
+      mbar_init(&bars.o_done[i], 1);
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
+    }
+    mbar_init(&bars.teardown, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  // Coordinates of a 128-row tile in a Q / K / V tensor map.
+  auto coords = [&](int head, int nheads_b, int row0, int& c1, int& c2) {
+    if (args.varlen) {
+      c1 = head;
+      c2 = tok0 + row0;
+    } else {
+      c1 = row0;
+      c2 = seq * nheads_b + head;
+    }
+  };
+
+  if (warp == 0) {
+    // ======================================================== TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      for (int x = 0; x < 2; ++x) {
+        if (!ti[x].valid) continue;
+        int c1, c2;
+        coords(ti[x].hq, args.Hq, ti[x].mb * kBM, c1, c2);
+        mbar_expect_tx(&bars.q_full[x], C::kTileBytes);
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_3d(sQ + x * C::kTileBytes + b * C::kBoxBytes, &tm_q, &bars.q_full[x], b * 64, c1, c2);
+      }
+      int last_phase[8];
+      for (int s = 0; s < 8; ++s) last_phase[s] = -1;
+      int idx = 0;
+      bool ok = true;
+      for (int j = 0; j < nkv && ok; ++j) {
+        for (int kv = 0; kv < 2 && ok; ++kv, ++idx) {
+          const int st = idx % C::kStages;
+          const uint32_t ph = (idx / C::kStages) & 1;
+          if (!mbar_wait(&bars.kv_empty[st], ph ^ 1, guard)) { ok = false; break; }
+          int c1, c2;
+          coords(hkv, args.Hkv, j * kBN, c1, c2);
+          uint8_t* dst = sRing + st * C::kTileBytes;
+          mbar_expect_tx(&bars.kv_full[st], C::kTileBytes);
+          const CUtensorMap* tm = kv == 0 ? &tm_k : &tm_v;
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(dst + b * C::kBoxBytes, tm, &bars.kv_full[st], b * 64, c1, c2);
+          last_phase[st] = (int)ph;
+        }
+      }
+      // Never leave the CTA with copies in flight.
+      for (int x = 0; x < 2; ++x)
+        if (ti[x].valid) mbar_wait_drain(&bars.q_full[x], 0);
+      for (int s = 0; s < C::kStages; ++s)
+        if (last_phase[s] >= 0) mbar_wait_drain(&bars.kv_full[s], (uint32_t)last_phase[s]);
+    }
+  } else if (warp == 1) {
+    // ========================================================= MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      for (int x = 0; x < 2 && ok; ++x)
+        if (ti[x].valid) ok = mbar_wait(&bars.q_full[x], 0, guard);
+      const uint32_t sq_addr = smem_u32(sQ);
+      const uint32_t ring_addr = smem_u32(sRing);
+      auto issue_qk = [&](int x, int st) {
+        const uint32_t qa = sq_addr + x * C::kTileBytes;
+        const uint32_t ka = ring_addr + st * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+          mma_ss(tmem + C::col_s(x), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                 C::kIdescQK, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int x, int st, int acc) {
+        const uint32_t va = ring_addr + st * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          mma_ts(tmem + C::col_o(x), tmem + C::col_s(x) + kk * 8, sdesc_sw128(va + kk * 2048, C::kBoxBytes, 1024),
+                 C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      // K_j sits at ring index 2j, V_j at 2j + 1.
+      auto stage_of = [&](int idx) { return idx % C::kStages; };
+      auto phase_of = [&](int idx) { return (uint32_t)((idx / C::kStages) & 1); };
+      if (ok && nkv > 0) {
+        ok = mbar_wait(&bars.kv_full[stage_of(0)], phase_of(0), guard);
+        if (ok) {
+          tc_fence_after();
+          for (int x = 0; x < 2; ++x)
+            if (ti[x].nkv > 0) {
+              issue_qk(x, stage_of(0));
+              tc_commit(&bars.s_full[x]);
+            }
+          tc_commit(&bars.kv_empty[stage_of(0)]);
+        }
+      }
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int vi = 2 * j + 1, ki = 2 * j + 2;
+        ok = mbar_wait(&bars.kv_full[stage_of(vi)], phase_of(vi), guard);
+        if (ok && j + 1 < nkv) ok = mbar_wait(&bars.kv_full[stage_of(ki)], phase_of(ki), guard);
+        if (!ok) break;
+        tc_fence_after();
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (j >= ti[x].nkv) continue;
+          ok = mbar_wait(&bars.p_full[x], j & 1, guard);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(x, stage_of(vi), j > 0);
+          if (j + 1 < ti[x].nkv) {
+            issue_qk(x, stage_of(ki));
+            tc_commit(&bars.s_full[x]);
+          } else {
+            tc_commit(&bars.o_done[x]);
+          }
+        }
+        if (!ok) break;
+        tc_commit(&bars.kv_empty[stage_of(vi)]);
+        if (j + 1 < nkv) tc_commit(&bars.kv_empty[stage_of(ki)]);
+      }
+      // Let every issued MMA finish before TMEM is released.
+      tc_commit(&bars.teardown);
+      mbar_wait_drain(&bars.teardown, 0);
+    }
+  } else if (warp >= 4) {
+    // ============================================================ softmax
+    const int x = (warp - 4) >> 2;          // tile
+    const int r = threadIdx.x & 127;        // row within the tile
+    const TileInfo t = ti[x];
+    if (t.valid) {
+      const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+      const uint32_t tS = tmem + lane_base + C::col_s(x);
+      const uint32_t tO = tmem + lane_base + C::col_o(x);
+      const float c = args.scale_log2;
+      const int qi = t.mb * kBM + r;        // query index within the sequence
+      float m_run = -INFINITY;              // running max, log2 units (scale folded in)
+      float l_run = 0.f;
+      bool ok = true;
+      for (int j = 0; j < t.nkv; ++j) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[x], j & 1, guard));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t s[kBN];
+#pragma unroll
+        for (int q = 0; q < kBN / 32; ++q) tmem_ld_x32(tS + q * 32, s + q * 32);
+        tmem_ld_wait();
+        reg_fence<kBN>(s);
+        float* sf = reinterpret_cast<float*>(s);
+        const int k0 = j * kBN;
+        const bool need_mask = (args.causal && j == t.mb) || (k0 + kBN > L);
+        if (need_mask) {
+          const int lim = args.causal ? min(qi + 1, L) : L;   // visible keys: k < lim
+#pragma unroll
+          for (int i = 0; i < kBN; ++i)
+            if (k0 + i >= lim) sf[i] = -INFINITY;
+        }
+        float mx = sf[0];
+#pragma unroll
+        for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, sf[i]);
+        const float m_new = fmaxf(m_run, mx * c);
+        float alpha = 1.f;
+        bool resc = false;
+        if (j == 0) {
+          m_run = m_new;
+        } else if (m_new > m_run + kRescaleThreshold) {
+          alpha = ex2_approx(m_run - m_new);
+          m_run = m_new;
+          resc = true;
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        float rs = 0.f;
+#pragma unroll
+        for (int q = 0; q < kBN / 32; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2_approx(fmaf(sf[q * 32 + 2 * i], c, -m_use));
+            const float p1 = ex2_approx(fmaf(sf[q * 32 + 2 * i + 1], c, -m_use));
+            rs += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st_x16(tS + q * 16, pk);
+        }
+        l_run = l_run * alpha + rs;
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld_x32(tO + q * 32, o);
+            tmem_ld_wait();
+            reg_fence<32>(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st_x32(tO + q * 32, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars.p_full[x]);
+      }
+      // ------------------------------------------------------- epilogue
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_done[x], 0, guard));
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+        uint8_t* stage = sQ + x * C::kTileBytes;           // Q tile is dead now
+        const uint32_t srow = smem_u32(stage) + r * (D * 2);
+#pragma unroll 1
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + q * 32, o);
+          tmem_ld_wait();
+          reg_fence<32>(o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+#pragma unroll
+          for (int cch = 0; cch < 4; ++cch) {
+            const int chunk = q * 4 + cch;                   // 16-byte chunk in the row
+            st_shared_v4(srow + ((chunk ^ (r & 7)) << 4), pk[4 * cch], pk[4 * cch + 1], pk[4 * cch + 2],
+                         pk[4 * cch + 3]);
+          }
+        }
+        const int rows_valid = min(kBM, L - t.mb * kBM);
+        if (r < rows_valid) {
+          const float lse = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+          const long li = args.varlen ? (long)t.hq * args.total + tok0 + qi
+                                      : ((long)seq * args.Hq + t.hq) * args.T + qi;
+          args.lse[li] = lse;
+        }
+        __syncwarp();
+        // coalesced copy of this warp's 32 rows (those inside the sequence)
+        constexpr int kChunks = D * 2 / 16;
+        __nv_bfloat16* obase;
+        long ors;
+        if (args.varlen) {
+          obase = args.o + ((long)(tok0 + t.mb * kBM) * args.Hq + t.hq) * D;
+          ors = (long)args.Hq * D;
+        } else {
+          obase = args.o + (((long)seq * args.Hq + t.hq) * args.T + t.mb * kBM) * D;
+          ors = D;
+        }
+        const uint32_t sbase = smem_u32(stage);
+        const int row0 = (warp & 3) * 32;
+#pragma unroll 4
+        for (int idx = lane; idx < 32 * kChunks; idx += 32) {
+          const int row = row0 + idx / kChunks, cch = idx % kChunks;
+          if (row < rows_valid) {
+            const uint4 v = ld_shared_v4(sbase + row * (D * 2) + ((cch ^ (row & 7)) << 4));
+            *reinterpret_cast<uint4*>(obase + row * ors + cch * 8) = v;
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+template <int D>
+static cudaError_t launch_fwd_d(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                const FwdArgs& a, int grid, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  prof_begin(kProfFwd, stream);
+  attn_fwd_kernel<D><<<grid, 384, C::kSmemBytes, stream>>>(q, k, v, a);
+  prof_end(stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdArgs& a,
+                            int D, int grid, cudaStream_t stream) {
+  if (D == 128) return launch_fwd_d<128>(q, k, v, a, grid, stream);
+  return launch_fwd_d<64>(q, k, v, a, grid, stream);
+}
+
+}  // namespace gqa

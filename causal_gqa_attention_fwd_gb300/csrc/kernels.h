@@ -1,0 +1,80 @@
+// kernels.h -- internal launch interface between the C-ABI layer (api.cu) and
+// the kernel translation units.  Not part of the public header.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace gqa {
+
+// Forward.  Dense layout: Q,O [B,Hq,T,D], K,V [B,Hkv,T,D], LSE [B,Hq,T]
+// (num_seqs = B).  Packed layout (varlen = 1): Q,O [total,Hq,D],
+// K,V [total,Hkv,D], LSE [Hq,total], sequences [cu[s], cu[s+1]).
+struct FwdArgs {
+  __nv_bfloat16* o;
+  float* lse;
+  const int* cu_seqlens;  // device, varlen only
+  int* status;            // device status word
+  int num_seqs;           // B for the dense layout
+  int T;                  // dense sequence length (unused for varlen)
+  int total;              // varlen total tokens
+  int Hq, Hkv, G;
+  int causal;
+  int varlen;
+  int pair_heads;         // 1: a CTA's two tiles are heads 2p, 2p+1; 0: row blocks 2m, 2m+1
+  int pairs_per_seq;      // head pairs (pair_heads) or heads
+  int m_items;            // row-block items per sequence
+  float scale_log2;       // scale * log2(e)
+};
+
+cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdArgs& a,
+                            int D, int grid, cudaStream_t stream);
+
+// Backward.  Same layouts; dQ is accumulated in f32 (dq_accum, row-padded)
+// and converted by a final pass.
+struct BwdArgs {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dout;
+  const float* lse;
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float* delta;           // workspace: [B,Hq,T] or [Hq,total] (+ padding)
+  float* lse_log2;        // workspace: LSE * log2(e), same layout as delta
+  float* dq_accum;        // workspace: f32 dQ, [B,Hq,T_pad,D] or [Hq,total_pad,D]
+  const int* cu_seqlens;
+  int* status;
+  int num_seqs;
+  int T;                  // dense sequence length; varlen: the longest sequence
+  int T_pad;              // dense rows per head in the f32 workspaces
+  int total;
+  int total_pad;          // varlen rows per head in the f32 workspaces
+  int Hq, Hkv, G;
+  int D;
+  int causal;
+  int varlen;
+  int n_items;            // key-block items per sequence (max)
+  float scale;
+  float scale_log2;
+};
+
+// dqacc: 2-D f32 map over the dQ accumulator (D, rows), 32 x 128 boxes,
+// 128-byte swizzle (used for D = 64).
+cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& dout, const CUtensorMap& dqacc, const BwdArgs& a,
+                            cudaStream_t stream);
+
+// Query rows per step of the backward main kernel for head dimension D.
+int bwd_query_block(int D);
+
+// Kernel-level timing (opt-in instrumentation, api.cu): event pairs recorded
+// on the launch stream around each kernel.
+enum ProfKind { kProfFwd = 0, kProfBwdPre = 1, kProfBwdMain = 2, kProfBwdPost = 3, kProfKinds = 4 };
+void prof_begin(int kind, cudaStream_t s);
+void prof_end(cudaStream_t s);
+
+}  // namespace gqa

@@ -1,0 +1,127 @@
+/*
+ * gqa_attn.h -- C ABI of libgqa_attn.so: causal grouped-query scaled-dot-
+ * product attention, forward and backward, for bf16 tensors on an sm_103a GPU.
+ *
+ * The operation is the ScaledDotProductAttention / MultiHeadAttention of the
+ * "Project Overview" page of llm-from-scratch (section "Core Stack: llm/",
+ * llm/transformer.py) with the grouped-query heads and causal mask of the
+ * microLLM-rocm README (section "Why this project exists": "Decoder-only
+ * MHA/GQA ... causal attention" and the causal GQA backward), computed
+ * blockwise with running softmax statistics as in the Flash Attention kernel
+ * of "Project Overview", section "Performance Layer: kernel/ and parallel/":
+ *
+ *   S = scale * Q K^T,  key j visible to query i iff j <= i (causal != 0),
+ *   LSE_i = ln sum_j exp(S_ij) over visible j,   P = exp(S - LSE),  O = P V,
+ *   and for the loss L = sum(dO * O):
+ *   dP = dO V^T, Delta_i = sum_d dO_id O_id, dS = P * (dP - Delta),
+ *   dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO,
+ *   dK and dV summed over the G = Hq / Hkv query heads that share a K/V head
+ *   (query head h reads K/V head h / G).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers, 16-byte aligned, densely
+ *     packed (no strides).  bf16 = IEEE bfloat16 stored as uint16.
+ *   - Dense layout:  Q, O, dO, dQ  [B, Hq, T, D];  K, V, dK, dV  [B, Hkv, T, D];
+ *                    LSE  [B, Hq, T] float32 (natural log).
+ *   - Packed (varlen) layout, sequences s = 0..num_seqs-1 occupying token rows
+ *     [cu_seqlens[s], cu_seqlens[s+1]):  Q, O, dO, dQ  [total, Hq, D];
+ *     K, V, dK, dV  [total, Hkv, D];  LSE  [Hq, total] float32.  cu_seqlens
+ *     is a DEVICE int32 array of num_seqs + 1 entries, cu_seqlens[0] = 0,
+ *     non-decreasing, cu_seqlens[num_seqs] = total_tokens.  The mask is causal
+ *     within each sequence; sequences never see each other.
+ *   - D (head dim) is 64 or 128; Hq % Hkv == 0.
+ *   - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls are asynchronous on that stream; errors found on the host are
+ *     returned before anything is launched; errors found on the device (a
+ *     bounded wait that timed out, invalid cu_seqlens contents) are recorded
+ *     in a per-device status word read by attn_get_device_status().
+ *   - Ownership: the caller allocates every buffer; the library allocates no
+ *     device memory and never frees caller memory.  Outputs are fully
+ *     overwritten (no zero-initialisation needed).  Inputs are read-only.
+ *   - Sizes of zero (B, T, num_seqs or total_tokens) are no-ops returning
+ *     ATTN_OK.
+ */
+#ifndef GQA_ATTN_H_
+#define GQA_ATTN_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define GQA_ATTN_API __attribute__((visibility("default")))
+#else
+#define GQA_ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = 1,       /* a required pointer is NULL */
+    ATTN_ERR_SHAPE = 2,      /* negative size, Hq % Hkv != 0, Hq/Hkv < 1, size too large */
+    ATTN_ERR_HEADDIM = 3,    /* D not 64 or 128 */
+    ATTN_ERR_ALIGN = 4,      /* a pointer is not 16-byte aligned */
+    ATTN_ERR_SEQLENS = 5,    /* cu_seqlens invalid (device-detected: status word) */
+    ATTN_ERR_WORKSPACE = 6,  /* workspace NULL or smaller than the *_workspace_size() value */
+    ATTN_ERR_ARCH = 7,       /* current device is not compute capability 10.3 */
+    ATTN_ERR_CUDA = 8,       /* a CUDA runtime call failed (launch, tensor map, attribute) */
+    ATTN_ERR_TIMEOUT = 9     /* device-detected: a bounded in-kernel wait expired */
+} attn_status;
+
+/* Forward, dense layout.  Writes O (bf16) and LSE (float32). */
+GQA_ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int T, int D, int causal, float scale, void* stream);
+
+/* Bytes of device workspace attn_bwd needs for these sizes (0 if invalid). */
+GQA_ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int T, int D);
+
+/* Backward, dense layout.  Reads Q, K, V, the forward's O and LSE, and dO;
+ * writes dQ, dK, dV (bf16).  workspace: device memory of at least
+ * attn_bwd_workspace_size() bytes, 256-byte aligned, owned by the caller; it
+ * holds Delta, LSE*log2(e) and the float32 dQ accumulator and needs no
+ * initialisation. */
+GQA_ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                     int B, int Hq, int Hkv, int T, int D, int causal, float scale, void* stream);
+
+/* Forward, packed variable-length layout.  max_seqlen must be >= every
+ * sequence's length (it sizes the launch grid). */
+GQA_ATTN_API attn_status attn_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
+                            int Hq, int Hkv, int D, int causal, float scale, void* stream);
+
+GQA_ATTN_API size_t attn_varlen_bwd_workspace_size(int num_seqs, int total_tokens, int Hq, int Hkv, int D);
+
+/* Backward, packed variable-length layout (arguments as attn_bwd plus the
+ * sequence description of attn_varlen_fwd). */
+GQA_ATTN_API attn_status attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                            size_t workspace_bytes, const int* cu_seqlens, int num_seqs, int total_tokens,
+                            int max_seqlen, int Hq, int Hkv, int D, int causal, float scale, void* stream);
+
+/* Static description of a status code. */
+GQA_ATTN_API const char* attn_status_string(attn_status status);
+
+/* Synchronises `stream`, then reads the current device's status word into
+ * *out (ATTN_OK or the first device-detected error since it was last
+ * cleared); clears it when clear != 0.  Returns ATTN_ERR_CUDA if the copy
+ * fails (e.g. a sticky CUDA error), else ATTN_OK. */
+GQA_ATTN_API attn_status attn_get_device_status(void* stream, int* out, int clear);
+
+/* Kernel timing (instrumentation; not thread-safe).  While enabled, every
+ * kernel launch is bracketed by a CUDA event pair recorded on the caller's
+ * stream.  attn_profile_read synchronises those events and returns, for one
+ * kernel kind (0 forward, 1 backward preprocess, 2 backward main,
+ * 3 backward dQ conversion), the number of launches and their summed device
+ * time in milliseconds since the last attn_profile_reset.  At most 65536
+ * launches are recorded between resets.  Off by default. */
+GQA_ATTN_API attn_status attn_profile_enable(int enable);
+GQA_ATTN_API attn_status attn_profile_reset(void);
+GQA_ATTN_API attn_status attn_profile_read(int kind, int* launches, double* total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H_ */

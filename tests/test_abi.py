@@ -1,0 +1,131 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/gqa_attn.h declares, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from causal_gqa_attention_fwd_gb300 import build
+    build.build()
+    import causal_gqa_attention_fwd_gb300 as g
+    return g.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"GQA_ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    for n in ("attn_fwd", "attn_bwd", "attn_varlen_fwd", "attn_varlen_bwd", "attn_bwd_workspace_size",
+              "attn_varlen_bwd_workspace_size", "attn_status_string", "attn_get_device_status"):
+        assert n in names
+
+
+def test_exports_every_declared_symbol(lib):
+    import causal_gqa_attention_fwd_gb300 as g
+    names = declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+        assert n in g._binding.SIGNATURES, f"{n} has no binding"
+
+
+def test_library_does_not_need_libcuda_at_load():
+    import subprocess
+    from causal_gqa_attention_fwd_gb300 import LIB_PATH
+    out = subprocess.run(["ldd", LIB_PATH], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out
+
+
+NULL = None
+A = 256   # a 16-byte-aligned fake device address: never dereferenced, rejected earlier or not launched
+
+
+def fwd(lib, *, ptrs=(A, A, A, A, A), B=1, Hq=4, Hkv=2, T=16, D=64, causal=1, scale=0.125):
+    return lib.attn_fwd(*ptrs, B, Hq, Hkv, T, D, causal, scale, None)
+
+
+def test_fwd_validation(lib):
+    assert fwd(lib, Hq=3, Hkv=2) == 2                    # Hq % Hkv
+    assert fwd(lib, Hq=0) == 2
+    assert fwd(lib, B=-1) == 2
+    assert fwd(lib, D=96) == 3
+    assert fwd(lib, D=256) == 3
+    assert fwd(lib, ptrs=(NULL, A, A, A, A)) == 1
+    assert fwd(lib, ptrs=(A, A, A, A, NULL)) == 1
+    assert fwd(lib, ptrs=(A + 8, A, A, A, A)) == 4     # misaligned
+    assert fwd(lib, ptrs=(A, A, A, A, A + 4)) == 4
+    assert fwd(lib, ptrs=(NULL,) * 5, T=0) == 0          # empty: no-op
+    assert fwd(lib, ptrs=(NULL,) * 5, B=0) == 0
+    assert fwd(lib, scale=float("nan")) == 2
+
+
+def vfwd(lib, *, ptrs=(A, A, A, A, A, A), n=2, total=10, maxlen=6, Hq=4, Hkv=2, D=128):
+    return lib.attn_varlen_fwd(*ptrs, n, total, maxlen, Hq, Hkv, D, 1, 0.1, None)
+
+
+def test_varlen_fwd_validation(lib):
+    assert vfwd(lib, maxlen=11) == 2                     # longer than the batch
+    assert vfwd(lib, n=-1) == 2
+    assert vfwd(lib, ptrs=(A, A, A, A, A, NULL)) == 1    # cu_seqlens
+    assert vfwd(lib, D=32) == 3
+    assert vfwd(lib, ptrs=(NULL,) * 6, n=0, total=0, maxlen=0) == 0
+
+
+def bwd(lib, *, ptrs=(A,) * 10, ws_bytes=1 << 40, B=1, Hq=4, Hkv=2, T=16, D=64):
+    return lib.attn_bwd(*ptrs, ws_bytes, B, Hq, Hkv, T, D, 1, 0.125, None)
+
+
+def test_bwd_validation(lib):
+    assert bwd(lib, Hq=5) == 2
+    assert bwd(lib, D=80) == 3
+    p = list((A,) * 10)
+    p[5] = NULL                                            # dout
+    assert bwd(lib, ptrs=tuple(p)) == 1
+    p = list((A,) * 10)
+    p[8] = A + 2                                           # dv misaligned
+    assert bwd(lib, ptrs=tuple(p)) == 4
+    p = list((A,) * 10)
+    p[9] = NULL                                            # workspace
+    assert bwd(lib, ptrs=tuple(p)) == 6
+    assert bwd(lib, ws_bytes=16) == 6                      # too small
+    p = list((A,) * 10)
+    p[9] = A + 16                                          # workspace not 256-aligned
+    assert bwd(lib, ptrs=tuple(p)) == 6
+    assert bwd(lib, ptrs=(NULL,) * 10, T=0) == 0
+
+
+def test_workspace_sizes(lib):
+    # Delta + LSE*log2e (256-aligned f32 rows each) + f32 dQ rows; rows = B*Hq*roundup(T,128)
+    rows = 2 * 32 * 4096
+    assert lib.attn_bwd_workspace_size(2, 32, 8, 4096, 128) == 2 * rows * 4 + rows * 128 * 4
+    rows = 1 * 4 * 256
+    assert lib.attn_bwd_workspace_size(1, 4, 2, 129, 64) == 2 * rows * 4 + rows * 64 * 4
+    assert lib.attn_bwd_workspace_size(1, 3, 2, 16, 64) == 0
+    assert lib.attn_varlen_bwd_workspace_size(16, 17000, 16, 8, 128) > 16 * 17000 * 128 * 4
+    assert lib.attn_varlen_bwd_workspace_size(2, 10, 4, 2, 96) == 0
+
+
+def test_status_strings(lib):
+    import causal_gqa_attention_fwd_gb300 as g
+    for code in range(10):
+        s = g.status_string(code)
+        assert s and s != "unknown status"
+    assert g.status_string(99) == "unknown status"
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from causal_gqa_attention_fwd_gb300 import _binding
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        _binding.lib()
