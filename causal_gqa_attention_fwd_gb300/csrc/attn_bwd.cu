@@ -7,8 +7,9 @@
 //   Delta_i = sum_d dO_id O_id,  dS = P * (dP - Delta),
 //   dQ = scale dS K,  dK = scale dS^T Q  (dK, dV summed over the G heads of a group).
 // Three kernels:
-//   1. bwd_pre   Delta, LSE*log2(e) into workspace rows; zero the f32 dQ
-//                accumulator (HBM-bound).
+//   1. bwd_pre   -Delta, -LSE*log2(e) into workspace rows (negated so the
+//                main kernel forms P and dS with single paired ops); zero the
+//                f32 dQ accumulator (HBM-bound).
 //   2. bwd_main  key/value-stationary: one CTA per (sequence, K/V head, block
 //                of 128 keys) keeps K, V in shared memory and dK, dV in TMEM,
 //                and walks the G query heads of the group and every query
@@ -19,9 +20,10 @@
 //                                                        reduce-add into f32)
 //                dK and dV leave the CTA once, complete (no atomics).
 //   3. bwd_post  dQ = bf16(scale * accumulator).
-// Roles in bwd_main (384 threads): warp 0 TMA producer, warp 1 MMA issuer
-// (+TMEM owner), warps 4-7 compute P and dS (thread = key row), warps 8-11
-// drain dQ partials and write dK, dV.
+// Roles in bwd_main (512 threads): warp 0 TMA producer, warp 1 MMA issuer
+// (+TMEM owner), warps 4-11 two warpgroups that form P and dS (thread = key
+// row, each warpgroup half of the step's query columns), warps 12-15 drain dQ
+// partials and write dK, dV.
 #include "sm103.cuh"
 #include "kernels.h"
 
@@ -30,6 +32,8 @@ namespace gqa {
 namespace {
 
 constexpr int kBN = 128;  // keys per CTA
+constexpr int kComputeWGs = 2;                          // warpgroups forming P and dS
+constexpr int kBwdThreads = 128 * (2 + kComputeWGs);    // + control warpgroup + drain warpgroup
 
 // dst tensor (f32) += 128-byte-swizzled smem box at coordinates (x, y).
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int x, int y) {
@@ -91,7 +95,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
     const int p = blockIdx.x * 128 + rr;
     if (p >= Lr) break;
     const long w = ws_row(a, s, tok0, h, p);
-    float dl = 0.f, l2 = INFINITY;
+    float dl = 0.f, l2 = -INFINITY;       // stored negated: -Delta, -LSE*log2(e)
     if (p < L) {
       const long off = row_off(a, s, tok0, h, a.Hq, p, D);
       float acc = 0.f;
@@ -114,9 +118,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
       }
 #pragma unroll
       for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-      dl = acc;
+      dl = -acc;
       const long li = a.varlen ? (long)h * a.total + tok0 + p : ((long)s * a.Hq + h) * a.T + p;
-      l2 = a.lse[li] * 1.4426950408889634f;
+      l2 = -a.lse[li] * 1.4426950408889634f;
     }
     if (lane == 0) {
       a.delta[w] = dl;
@@ -199,7 +203,7 @@ struct __align__(8) BwdBarriers {
 }  // namespace
 
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dqacc, const BwdArgs a) {
@@ -238,8 +242,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.p_full, 128);
-    mbar_init(&bars.ds_full, 128);
+    mbar_init(&bars.p_full, 128 * kComputeWGs);
+    mbar_init(&bars.ds_full, 128 * kComputeWGs);
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.dq_empty, 128);
     mbar_init(&bars.stg_full, 128);
@@ -375,8 +379,11 @@ __global__ void __launch_bounds__(384, 1)
       tc_commit(&bars.teardown);
       mbar_wait_drain(&bars.teardown, 0);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 4 + 4 * kComputeWGs) {
     // ================================================ compute P^T and dS^T
+    // kComputeWGs warpgroups split each step's query columns; thread = key row.
+    constexpr int kCols = BM / kComputeWGs;
+    const int c0 = ((warp - 4) >> 2) * kCols;          // first query column of this warpgroup
     const int r = threadIdx.x & 127;                  // key row
     const int key = k0 + r;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -388,39 +395,41 @@ __global__ void __launch_bounds__(384, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&bars.st_full[st], (i >> 1) & 1, guard))) break;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars.s_full, par, guard))) break;
       tc_fence_after();
-      const float* lse2 = stage_lse(st);
-      const float* dl = stage_delta(st);
-      const int q0 = it_mb(i) * BM;
-      const bool need_mask = (a.causal && q0 <= k0 + kBN - 1) || (k0 + kBN > L) || (q0 + BM > L);
+      const float* nlse2 = stage_lse(st) + c0;     // -LSE*log2(e) per query column
+      const float* ndl = stage_delta(st) + c0;      // -Delta per query column
+      const int q0 = it_mb(i) * BM + c0;
+      const bool need_mask = (a.causal && q0 <= k0 + kBN - 1) || (k0 + kBN > L) || (q0 + kCols > L);
       // visible iff key < L, query < L and (not causal or key <= query)
       const int qmin = a.causal ? key : 0;     // smallest visible query index
-      uint32_t pv[BM];                          // S^T row, then P^T row (f32 bits)
+      uint32_t pv[kCols];                       // S^T row, then P^T row (f32 bits)
 #pragma unroll
-      for (int q = 0; q < BM / 32; ++q) tmem_ld_x32(tmem + lane_base + C::kColS + q * 32, pv + q * 32);
+      for (int q = 0; q < kCols / 32; ++q) tmem_ld_x32(tmem + lane_base + C::kColS + c0 + q * 32, pv + q * 32);
       tmem_ld_wait();
-      reg_fence<BM>(pv);
+      reg_fence<kCols>(pv);
       float* p = reinterpret_cast<float*>(pv);
+      const uint64_t c2 = f2(c, c);
 #pragma unroll
-      for (int j = 0; j < BM; ++j) p[j] = ex2_approx(fmaf(p[j], c, -lse2[j]));
+      for (int j = 0; j < kCols; j += 2) {
+        const uint64_t nl = *reinterpret_cast<const uint64_t*>(nlse2 + j);
+        f2_split(fma2(f2(p[j], p[j + 1]), c2, nl), p[j], p[j + 1]);
+        p[j] = ex2_approx(p[j]);
+        p[j + 1] = ex2_approx(p[j + 1]);
+      }
       if (need_mask) {
         const bool krow_ok = key < L;
 #pragma unroll
-        for (int j = 0; j < BM; ++j) {
+        for (int j = 0; j < kCols; ++j) {
           const int qi = q0 + j;
           if (!krow_ok || qi >= L || qi < qmin) p[j] = 0.f;
         }
       }
-      // P^T row -> bf16 -> sP (128-byte swizzled K-major rows).  With 128
-      // query columns the bf16 copy is also what dS is formed from (register
-      // budget); with 64 the f32 values are kept.
-      constexpr bool kPackP = BM == 128;
-      uint32_t pk[BM / 2];
+      // P^T row segment -> bf16 -> sP (128-byte swizzled K-major rows)
 #pragma unroll
-      for (int ch = 0; ch < BM / 8; ++ch) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) pk[4 * ch + e] = pack_bf16x2(p[8 * ch + 2 * e], p[8 * ch + 2 * e + 1]);
+      for (int cc = 0; cc < kCols / 8; ++cc) {
+        const int ch = c0 / 8 + cc;                      // 16-byte chunk index in the row
         const uint32_t addr = rowP + (ch >> 3) * 16384 + (((ch & 7) ^ (r & 7)) << 4);
-        st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+        st_shared_v4(addr, pack_bf16x2(p[8 * cc], p[8 * cc + 1]), pack_bf16x2(p[8 * cc + 2], p[8 * cc + 3]),
+                     pack_bf16x2(p[8 * cc + 4], p[8 * cc + 5]), pack_bf16x2(p[8 * cc + 6], p[8 * cc + 7]));
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -428,9 +437,9 @@ __global__ void __launch_bounds__(384, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&bars.dp_full, par, guard))) break;
       tc_fence_after();
 #pragma unroll
-      for (int q = 0; q < BM / 32; ++q) {
+      for (int q = 0; q < kCols / 32; ++q) {
         uint32_t dv[32];
-        tmem_ld_x32(tmem + lane_base + C::kColDP + q * 32, dv);
+        tmem_ld_x32(tmem + lane_base + C::kColDP + c0 + q * 32, dv);
         tmem_ld_wait();
         reg_fence<32>(dv);
 #pragma unroll
@@ -440,20 +449,13 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j = j0 + 2 * e;
-            float p0, p1;
-            if (kPackP) {
-              const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[j / 2]));
-              p0 = pf.x;
-              p1 = pf.y;
-            } else {
-              p0 = p[j];
-              p1 = p[j + 1];
-            }
-            const float d0 = p0 * (__uint_as_float(dv[cc * 8 + 2 * e]) - dl[j]);
-            const float d1 = p1 * (__uint_as_float(dv[cc * 8 + 2 * e + 1]) - dl[j + 1]);
+            const uint64_t nd = *reinterpret_cast<const uint64_t*>(ndl + j);
+            const uint64_t dp = f2(__uint_as_float(dv[cc * 8 + 2 * e]), __uint_as_float(dv[cc * 8 + 2 * e + 1]));
+            float d0, d1;
+            f2_split(mul2(f2(p[j], p[j + 1]), add2(dp, nd)), d0, d1);     // P (dP - Delta)
             w[e] = pack_bf16x2(d0, d1);
           }
-          const int ch = j0 / 8;
+          const int ch = (c0 + j0) / 8;
           st_shared_v4(rowDS + (ch >> 3) * 16384 + (((ch & 7) ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
         }
       }
@@ -461,7 +463,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(&bars.ds_full);
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 4 + 4 * kComputeWGs) {
     // ===================================== drain dQ partials; dK, dV epilogue
     const int r = threadIdx.x & 127;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -587,7 +589,7 @@ static cudaError_t launch_bwd_d(const CUtensorMap& q, const CUtensorMap& k, cons
   if (e != cudaSuccess) return e;
   const long grid = (long)a.n_items * a.num_seqs * a.Hkv;
   prof_begin(kProfBwdMain, stream);
-  bwd_main_kernel<D><<<(unsigned)grid, 384, C::kSmemBytes, stream>>>(q, k, v, dout, dqacc, a);
+  bwd_main_kernel<D><<<(unsigned)grid, kBwdThreads, C::kSmemBytes, stream>>>(q, k, v, dout, dqacc, a);
   prof_end(stream);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

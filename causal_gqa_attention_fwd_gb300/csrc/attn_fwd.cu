@@ -295,9 +295,15 @@ __global__ void __launch_bounds__(384, 1)
           for (int i = 0; i < kBN; ++i)
             if (k0 + i >= lim) sf[i] = -INFINITY;
         }
-        float mx = sf[0];
+        // row max: eight independent chains of three-input max
+        float m8[8];
 #pragma unroll
-        for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, sf[i]);
+        for (int e = 0; e < 8; ++e) m8[e] = fmaxf(sf[e], sf[e + 8]);
+#pragma unroll
+        for (int i = 16; i < kBN; i += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m8[e] = max3f(m8[e], sf[i + e], sf[i + 8 + e]);
+        const float mx = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         const float m_new = fmaxf(m_run, mx * c);
         float alpha = 1.f;
         bool resc = false;
@@ -309,19 +315,25 @@ __global__ void __launch_bounds__(384, 1)
           resc = true;
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        float rs = 0.f;
+        // p = 2^(s c - m): exponent arguments and the row sum in paired f32
+        const uint64_t c2 = f2(c, c), nm2 = f2(-m_use, -m_use);
+        uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int q = 0; q < kBN / 32; ++q) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2_approx(fmaf(sf[q * 32 + 2 * i], c, -m_use));
-            const float p1 = ex2_approx(fmaf(sf[q * 32 + 2 * i + 1], c, -m_use));
-            rs += p0 + p1;
+            float t0, t1;
+            f2_split(fma2(f2(sf[q * 32 + 2 * i], sf[q * 32 + 2 * i + 1]), c2, nm2), t0, t1);
+            const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+            acc[i & 3] = add2(acc[i & 3], f2(p0, p1));
             pk[i] = pack_bf16x2(p0, p1);
           }
           tmem_st_x16(tS + q * 16, pk);
         }
+        float rs0, rs1;
+        f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), rs0, rs1);
+        const float rs = rs0 + rs1;
         l_run = l_run * alpha + rs;
         if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1

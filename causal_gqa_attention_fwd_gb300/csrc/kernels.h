@@ -43,8 +43,8 @@ struct BwdArgs {
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  float* delta;           // workspace: [B,Hq,T] or [Hq,total] (+ padding)
-  float* lse_log2;        // workspace: LSE * log2(e), same layout as delta
+  float* delta;           // workspace: -Delta, [B,Hq,T_pad] or [Hq,total_pad]
+  float* lse_log2;        // workspace: -LSE * log2(e), same layout as delta
   float* dq_accum;        // workspace: f32 dQ, [B,Hq,T_pad,D] or [Hq,total_pad,D]
   const int* cu_seqlens;
   int* status;

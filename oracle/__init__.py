@@ -55,9 +55,9 @@ _L = ctypes.c_long
 
 def _bind(lib):
     lib.oracle_fwd.argtypes = [_D, _D, _D, _D, _D, _L, _L, _L, _L, _L, ctypes.c_int, ctypes.c_double]
-    lib.oracle_bwd.argtypes = [_D] * 10 + [_L, _L, _L, _L, _L, ctypes.c_int, ctypes.c_double]
+    lib.oracle_bwd.argtypes = [_D] * 13 + [_L, _L, _L, _L, _L, ctypes.c_int, ctypes.c_double]
     lib.oracle_varlen_fwd.argtypes = [_D, _D, _D, _D, _D, _I, _L, _L, _L, _L, _L, ctypes.c_int, ctypes.c_double]
-    lib.oracle_varlen_bwd.argtypes = [_D] * 10 + [_I, _L, _L, _L, _L, _L, ctypes.c_int, ctypes.c_double]
+    lib.oracle_varlen_bwd.argtypes = [_D] * 13 + [_I, _L, _L, _L, _L, _L, ctypes.c_int, ctypes.c_double]
     lib.oracle_set_threads.argtypes = [ctypes.c_int]
     for f in (lib.oracle_fwd, lib.oracle_bwd, lib.oracle_varlen_fwd, lib.oracle_varlen_bwd,
               lib.oracle_set_threads):
@@ -104,10 +104,20 @@ def fwd(q, k, v, causal: bool = True, scale: float | None = None, lib=None):
     return o, lse
 
 
-def bwd(q, k, v, dout, causal: bool = True, scale: float | None = None, lib=None):
+def _err_bufs(want, q, k):
+    if not want:
+        return None, None, None, ctypes.cast(None, _D), ctypes.cast(None, _D), ctypes.cast(None, _D)
+    eq, ek, ev = np.zeros_like(q), np.zeros_like(k), np.zeros_like(k)
+    return eq, ek, ev, _p(eq), _p(ek), _p(ev)
+
+
+def bwd(q, k, v, dout, causal: bool = True, scale: float | None = None, lib=None, err_terms: bool = False):
     """Dense backward of L = sum(dO * O).
 
-    Returns dict with dq, dk, dv and the forward's o, lse and the row term delta."""
+    Returns dict with dq, dk, dv and the forward's o, lse and the row term
+    delta; with err_terms, also edq, edk, edv: the root-sum-square rounding-
+    error scale of each output element (multiply by the unit roundoff) when
+    P, dS and the stored O are bf16 operands."""
     lib = lib or load()
     q, k, v, dout = _c(q), _c(k), _c(v), _c(dout)
     B, Hq, T, D = q.shape
@@ -117,11 +127,15 @@ def bwd(q, k, v, dout, causal: bool = True, scale: float | None = None, lib=None
     o = np.zeros_like(q)
     lse = np.zeros((B, Hq, T))
     delta = np.zeros((B, Hq, T))
+    eq, ek, ev, peq, pek, pev = _err_bufs(err_terms, q, k)
     st = lib.oracle_bwd(_p(q), _p(k), _p(v), _p(dout), _p(dq), _p(dk), _p(dv), _p(o), _p(lse), _p(delta),
-                        B, Hq, Hkv, T, D, int(causal), scale)
+                        peq, pek, pev, B, Hq, Hkv, T, D, int(causal), scale)
     if st:
         raise ValueError(f"oracle_bwd status {st}")
-    return dict(dq=dq, dk=dk, dv=dv, o=o, lse=lse, delta=delta)
+    r = dict(dq=dq, dk=dk, dv=dv, o=o, lse=lse, delta=delta)
+    if err_terms:
+        r.update(edq=np.sqrt(eq), edk=np.sqrt(ek), edv=np.sqrt(ev))
+    return r
 
 
 def _cu(cu_seqlens):
@@ -145,7 +159,8 @@ def varlen_fwd(q, k, v, cu_seqlens, causal: bool = True, scale: float | None = N
     return o, lse
 
 
-def varlen_bwd(q, k, v, dout, cu_seqlens, causal: bool = True, scale: float | None = None, lib=None):
+def varlen_bwd(q, k, v, dout, cu_seqlens, causal: bool = True, scale: float | None = None, lib=None,
+               err_terms: bool = False):
     """Packed variable-length backward; returns the same dict as ``bwd``."""
     lib = lib or load()
     q, k, v, dout = _c(q), _c(k), _c(v), _c(dout)
@@ -157,9 +172,13 @@ def varlen_bwd(q, k, v, dout, cu_seqlens, causal: bool = True, scale: float | No
     o = np.zeros_like(q)
     lse = np.zeros((Hq, total))
     delta = np.zeros((Hq, total))
+    eq, ek, ev, peq, pek, pev = _err_bufs(err_terms, q, k)
     st = lib.oracle_varlen_bwd(_p(q), _p(k), _p(v), _p(dout), _p(dq), _p(dk), _p(dv), _p(o), _p(lse),
-                               _p(delta), cu.ctypes.data_as(_I), len(cu) - 1, total, Hq, Hkv, D,
-                               int(causal), scale)
+                               _p(delta), peq, pek, pev, cu.ctypes.data_as(_I), len(cu) - 1, total, Hq, Hkv,
+                               D, int(causal), scale)
     if st:
         raise ValueError(f"oracle_varlen_bwd status {st}")
-    return dict(dq=dq, dk=dk, dv=dv, o=o, lse=lse, delta=delta)
+    r = dict(dq=dq, dk=dk, dv=dv, o=o, lse=lse, delta=delta)
+    if err_terms:
+        r.update(edq=np.sqrt(eq), edk=np.sqrt(ek), edv=np.sqrt(ev))
+    return r

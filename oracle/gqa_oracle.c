@@ -184,6 +184,63 @@ static void head_bwd(cview q, cview k, cview v, cview dout, long T, long D, int 
     cols_times(P, dout, T, D, 1.0, dv);
 }
 
+/* Rounding-error scale of the backward outputs when P, dS and the stored O
+ * are bf16 operands (unit roundoff u) and everything else is exact.  Each
+ * rounding is an independent relative error of at most u, so an output's
+ * error is a sum of independent terms whose size is u times the root of the
+ * summed squares of what each rounding multiplies (probabilistic rounding-
+ * error analysis).  With
+ *   w2_i  = sum_d dO_id^2 (O_id^2 + sum_j P_ij^2 V_jd^2)   (Delta_i from a rounded O)
+ * the squared terms are (two roundings touch each dS_ij: P and dS itself)
+ *   eq2_id  = scale^2 (2 sum_j dS_ij^2 K_jd^2 + (sum_j P_ij K_jd)^2 w2_i)
+ *   ek2_jd += scale^2 sum_i Q_id^2 (2 dS_ij^2 + P_ij^2 w2_i)
+ *   ev2_jd += sum_i P_ij^2 dO_id^2
+ * (a row's Delta error is common to all its dS entries, hence the squared
+ * sum in eq2).  The caller takes square roots.  P and dS are the head's
+ * T x T matrices. */
+static void head_err_terms(cview q, cview k, cview v, cview dout, cview o, long T, long D, double scale,
+                           const double* P, const double* dS, double* w2, mview eq2, mview ek2, mview ev2) {
+    long i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < T; ++i) {
+        double w = 0.0;
+        for (long d = 0; d < D; ++d) {
+            double pv = 0.0;
+            for (long j = 0; j < T; ++j) {
+                double x = P[i * T + j] * v.base[j * v.rs + d];
+                pv += x * x;
+            }
+            double g = dout.base[i * dout.rs + d], od = o.base[i * o.rs + d];
+            w += g * g * (od * od + pv);
+        }
+        w2[i] = w;
+        for (long d = 0; d < D; ++d) {
+            double ss = 0.0, pk = 0.0;
+            for (long j = 0; j < T; ++j) {
+                double kd = k.base[j * k.rs + d];
+                ss += dS[i * T + j] * dS[i * T + j] * kd * kd;
+                pk += P[i * T + j] * kd;
+            }
+            eq2.base[i * eq2.rs + d] = scale * scale * (2.0 * ss + pk * pk * w);
+        }
+    }
+    long j;
+#pragma omp parallel for schedule(static)
+    for (j = 0; j < T; ++j) {
+        for (long d = 0; d < D; ++d) {
+            double ak = 0.0, av = 0.0;
+            for (long i2 = 0; i2 < T; ++i2) {
+                double qd = q.base[i2 * q.rs + d], gd = dout.base[i2 * dout.rs + d];
+                double p = P[i2 * T + j], ds = dS[i2 * T + j];
+                ak += qd * qd * (2.0 * ds * ds + p * p * w2[i2]);
+                av += p * p * gd * gd;
+            }
+            ek2.base[j * ek2.rs + d] += scale * scale * ak;
+            ev2.base[j * ev2.rs + d] += av;
+        }
+    }
+}
+
 static int check_shape(long Hq, long Hkv, long D) {
     if (Hq < 1 || Hkv < 1 || D < 1) return 2;
     if (Hq % Hkv) return 2;
@@ -214,9 +271,11 @@ int oracle_fwd(const double* q, const double* k, const double* v, double* o, dou
     return 0;
 }
 
-/* o, lse, delta are outputs too (may be NULL). */
+/* o, lse, delta are outputs too (may be NULL).  edq, edk, edv (all or none):
+ * the squared rounding-error terms of head_err_terms, laid out like dq, dk, dv. */
 int oracle_bwd(const double* q, const double* k, const double* v, const double* dout,
                double* dq, double* dk, double* dv, double* o, double* lse, double* delta,
+               double* edq, double* edk, double* edv,
                long B, long Hq, long Hkv, long T, long D, int causal, double scale) {
     int st = check_shape(Hq, Hkv, D);
     if (st || B < 0 || T < 0) return st ? st : 2;
@@ -233,6 +292,13 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
     }
     memset(dk, 0, sizeof(double) * B * Hkv * T * D);
     memset(dv, 0, sizeof(double) * B * Hkv * T * D);
+    double* E = NULL;
+    if (edq) {
+        memset(edk, 0, sizeof(double) * B * Hkv * T * D);
+        memset(edv, 0, sizeof(double) * B * Hkv * T * D);
+        E = (double*)malloc(sizeof(double) * T * T);
+        if (!E) { free(P); free(dS); free(lse_tmp); free(delta_tmp); free(o_tmp); return 10; }
+    }
     for (long b = 0; b < B; ++b)
         for (long h = 0; h < Hq; ++h) {
             long g = kv_head(h, G, Hkv);
@@ -247,8 +313,15 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
             double* lr = lse ? lse + (b * Hq + h) * T : lse_tmp;
             double* dr = delta ? delta + (b * Hq + h) * T : delta_tmp;
             head_bwd(qh, kh, vh, doh, T, D, causal, scale, dqh, dkh, dvh, P, dS, lr, dr, oh);
+            if (E) {
+                cview oc = {oh.base, oh.rs};
+                mview eq = {edq + (b * Hq + h) * T * D, D};
+                mview ek = {edk + (b * Hkv + g) * T * D, D};
+                mview ev = {edv + (b * Hkv + g) * T * D, D};
+                head_err_terms(qh, kh, vh, doh, oc, T, D, scale, P, dS, E, eq, ek, ev);
+            }
         }
-    free(P); free(dS); free(lse_tmp); free(delta_tmp); free(o_tmp);
+    free(P); free(dS); free(lse_tmp); free(delta_tmp); free(o_tmp); free(E);
     return 0;
 }
 
@@ -301,7 +374,7 @@ int oracle_varlen_fwd(const double* q, const double* k, const double* v, double*
 
 int oracle_varlen_bwd(const double* q, const double* k, const double* v, const double* dout,
                       double* dq, double* dk, double* dv, double* o, double* lse, double* delta,
-                      const int* cu, long num_seqs, long total, long Hq, long Hkv, long D,
+                      double* edq, double* edk, double* edv, const int* cu, long num_seqs, long total, long Hq, long Hkv, long D,
                       int causal, double scale) {
     int st = check_shape(Hq, Hkv, D);
     if (st) return st;
@@ -309,6 +382,10 @@ int oracle_varlen_bwd(const double* q, const double* k, const double* v, const d
     long G = Hq / Hkv, L = max_len(cu, num_seqs);
     memset(dk, 0, sizeof(double) * total * Hkv * D);
     memset(dv, 0, sizeof(double) * total * Hkv * D);
+    if (edq) {
+        memset(edk, 0, sizeof(double) * total * Hkv * D);
+        memset(edv, 0, sizeof(double) * total * Hkv * D);
+    }
     if (L == 0) return 0;
     double* P = (double*)malloc(sizeof(double) * L * L);
     double* dS = (double*)malloc(sizeof(double) * L * L);
@@ -316,6 +393,11 @@ int oracle_varlen_bwd(const double* q, const double* k, const double* v, const d
     double* delta_tmp = (double*)malloc(sizeof(double) * L);
     double* o_tmp = (double*)malloc(sizeof(double) * L * D);
     if (!P || !dS || !lse_tmp || !delta_tmp || !o_tmp) {
+        free(P); free(dS); free(lse_tmp); free(delta_tmp); free(o_tmp);
+        return 10;
+    }
+    double* E = NULL;
+    if (edq && !(E = (double*)malloc(sizeof(double) * L * L))) {
         free(P); free(dS); free(lse_tmp); free(delta_tmp); free(o_tmp);
         return 10;
     }
@@ -335,9 +417,16 @@ int oracle_varlen_bwd(const double* q, const double* k, const double* v, const d
             double* lr = lse ? lse + h * total + off : lse_tmp;
             double* dr = delta ? delta + h * total + off : delta_tmp;
             head_bwd(qh, kh, vh, doh, T, D, causal, scale, dqh, dkh, dvh, P, dS, lr, dr, oh);
+            if (E) {
+                cview oc = {oh.base, oh.rs};
+                mview eq = {edq + (off * Hq + h) * D, Hq * D};
+                mview ek = {edk + (off * Hkv + g) * D, Hkv * D};
+                mview ev = {edv + (off * Hkv + g) * D, Hkv * D};
+                head_err_terms(qh, kh, vh, doh, oc, T, D, scale, P, dS, E, eq, ek, ev);
+            }
         }
     }
-    free(P); free(dS); free(lse_tmp); free(delta_tmp); free(o_tmp);
+    free(P); free(dS); free(lse_tmp); free(delta_tmp); free(o_tmp); free(E);
     return 0;
 }
 

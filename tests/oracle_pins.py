@@ -235,6 +235,47 @@ def pin_varlen_equals_slices(lib):
         np.testing.assert_allclose(res["lse"][:, a:b], d["lse"][0], atol=1e-12)
 
 
+def _bf16(x):
+    return torch.tensor(x).to(torch.bfloat16).double().numpy()
+
+
+def pin_rounding_error_terms(lib):
+    """The backward's root-sum-square rounding-error scales (edq, edk, edv):
+    lambda * u * e (lambda = 3, u = 2^-8) bounds, element by element, how far
+    a computation moves that rounds P (for PV and P^T dO), the stored O (hence
+    Delta) and dS to bf16 while accumulating exactly -- checked on a
+    large-logit GQA case (observed worst ratio about 1.6)."""
+    r = _rng(10)
+    B, Hq, Hkv, T, D, scale = 1, 4, 2, 40, 16, 0.25
+    G = Hq // Hkv
+    q = _bf16(4.0 * r.standard_normal((B, Hq, T, D)))
+    k = _bf16(r.standard_normal((B, Hkv, T, D)))
+    v = _bf16(r.standard_normal((B, Hkv, T, D)))
+    do = _bf16(r.standard_normal((B, Hq, T, D)))
+    res = oracle.bwd(q, k, v, do, causal=True, scale=scale, lib=lib, err_terms=True)
+    mask = np.tril(np.ones((T, T))) > 0
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for h in range(Hq):
+        Q, K, V, dO = q[0, h], k[0, h // G], v[0, h // G], do[0, h]
+        S = np.where(mask, scale * Q @ K.T, -np.inf)
+        P = np.exp(S - S.max(1, keepdims=True))
+        P /= P.sum(1, keepdims=True)
+        O = _bf16(_bf16(P) @ V)                       # forward with bf16 P, stored in bf16
+        delta = (dO * O).sum(1)
+        dS = _bf16(P * (dO @ V.T - delta[:, None]))
+        dq[0, h] = scale * dS @ K
+        dk[0, h // G] += scale * dS.T @ Q
+        dv[0, h // G] += _bf16(P).T @ dO
+    u = 2.0 ** -8
+    for name, x in (("dq", dq), ("dk", dk), ("dv", dv)):
+        err = np.abs(x - res[name])
+        bound = 3.0 * u * res["e" + name] + 1e-12
+        assert (err <= bound).all(), (name, float((err - bound).max()))
+    assert float(np.abs(dk - res["dk"]).max()) > 1e-4    # the case does exercise rounding
+
+
 PINS = [pin_hand_worked, pin_rows_sum_to_one, pin_single_token, pin_constant_keys, pin_shift_invariance,
         pin_gqa_equals_repeated_mha, pin_torch_sdpa, pin_finite_differences, pin_delta_identity,
-        pin_varlen_equals_slices]
+        pin_varlen_equals_slices, pin_rounding_error_terms]

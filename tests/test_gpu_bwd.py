@@ -49,10 +49,11 @@ def test_bwd_dense(gq, B, Hq, Hkv, T, D, causal):
     x = W.dense_inputs(B, Hq, Hkv, T, D, seed=1000 + T + D)
     scale = 1.0 / np.sqrt(D)
     dq, dk, dv = run_dense(gq, x, causal, scale)
-    ref = oracle.bwd(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["do"]), causal=causal, scale=scale)
-    check("dq", dq, ref["dq"], TOL_REL_GRAD)
-    check("dk", dk, ref["dk"], TOL_REL_GRAD)
-    check("dv", dv, ref["dv"], TOL_REL_GRAD)
+    ref = oracle.bwd(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["do"]), causal=causal, scale=scale,
+                     err_terms=True)
+    check("dq", dq, ref["dq"], TOL_REL_GRAD, ref["edq"])
+    check("dk", dk, ref["dk"], TOL_REL_GRAD, ref["edk"])
+    check("dv", dv, ref["dv"], TOL_REL_GRAD, ref["edv"])
 
 
 @pytest.mark.parametrize("name", ["tiny", "qwen3_0p6b_layer"])
@@ -60,10 +61,11 @@ def test_bwd_workload(gq, name):
     w = W.WORKLOADS[name]
     x = W.make_inputs(w)
     dq, dk, dv = run_dense(gq, x, True, w.softmax_scale)
-    ref = oracle.bwd(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["do"]), scale=w.softmax_scale)
-    check("dq", dq, ref["dq"], TOL_REL_GRAD)
-    check("dk", dk, ref["dk"], TOL_REL_GRAD)
-    check("dv", dv, ref["dv"], TOL_REL_GRAD)
+    ref = oracle.bwd(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["do"]), scale=w.softmax_scale,
+                     err_terms=True)
+    check("dq", dq, ref["dq"], TOL_REL_GRAD, ref["edq"])
+    check("dk", dk, ref["dk"], TOL_REL_GRAD, ref["edk"])
+    check("dv", dv, ref["dv"], TOL_REL_GRAD, ref["edv"])
 
 
 @pytest.mark.parametrize("lens,Hq,Hkv,D,q_std", [
@@ -80,7 +82,8 @@ def test_bwd_varlen(gq, lens, Hq, Hkv, D, q_std):
     o, lse = gq.attn_varlen_fwd(q, k, v, cud, x["max_seqlen"], scale=scale)
     dq, dk, dv = gq.attn_varlen_bwd(q, k, v, o, lse, do, cud, x["max_seqlen"], scale=scale)
     assert gq.get_device_status() == 0
-    ref = oracle.varlen_bwd(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["do"]), cu.numpy(), scale=scale)
-    check("dq", dq, ref["dq"], TOL_REL_GRAD)
-    check("dk", dk, ref["dk"], TOL_REL_GRAD)
-    check("dv", dv, ref["dv"], TOL_REL_GRAD)
+    ref = oracle.varlen_bwd(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["do"]), cu.numpy(), scale=scale,
+                            err_terms=True)
+    check("dq", dq, ref["dq"], TOL_REL_GRAD, ref["edq"])
+    check("dk", dk, ref["dk"], TOL_REL_GRAD, ref["edk"])
+    check("dv", dv, ref["dv"], TOL_REL_GRAD, ref["edv"])

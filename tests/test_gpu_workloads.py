@@ -36,11 +36,12 @@ def test_gpt2_small_mha_full(gq):
     w = W.WORKLOADS["gpt2_small_mha"]
     x = W.make_inputs(w)
     g = gpu_dense(gq, w, x)
-    ref = oracle.bwd(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["do"]), scale=w.softmax_scale)
+    ref = oracle.bwd(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["do"]), scale=w.softmax_scale,
+                     err_terms=True)
     check("o", g["o"], ref["o"], TOL_REL_O)
     check_lse(g["lse"], ref["lse"])
     for n in ("dq", "dk", "dv"):
-        check(n, g[n], ref[n], TOL_REL_GRAD)
+        check(n, g[n], ref[n], TOL_REL_GRAD, ref["e" + n])
 
 
 def test_varlen16_full(gq):
@@ -53,11 +54,11 @@ def test_varlen16_full(gq):
     dq, dk, dv = gq.attn_varlen_bwd(q, k, v, o, lse, do, cud, x["max_seqlen"], scale=w.softmax_scale)
     assert gq.get_device_status() == 0
     ref = oracle.varlen_bwd(to64(x["q"]), to64(x["k"]), to64(x["v"]), to64(x["do"]), cu.numpy(),
-                            scale=w.softmax_scale)
+                            scale=w.softmax_scale, err_terms=True)
     check("o", o, ref["o"], TOL_REL_O)
     check_lse(lse, ref["lse"])
     for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-        check(n, t, ref[n], TOL_REL_GRAD)
+        check(n, t, ref[n], TOL_REL_GRAD, ref["e" + n])
 
 
 @pytest.mark.parametrize("b,g", [(1, 5)])
@@ -68,9 +69,9 @@ def test_long_gqa_t4096_sampled_group(gq, b, g):
     G = w.Hq // w.Hkv
     hs = slice(g * G, (g + 1) * G)
     ref = oracle.bwd(to64(x["q"][b:b + 1, hs]), to64(x["k"][b:b + 1, g:g + 1]), to64(x["v"][b:b + 1, g:g + 1]),
-                     to64(x["do"][b:b + 1, hs]), scale=w.softmax_scale)
+                     to64(x["do"][b:b + 1, hs]), scale=w.softmax_scale, err_terms=True)
     check("o", out["o"][b:b + 1, hs], ref["o"], TOL_REL_O)
     check_lse(out["lse"][b:b + 1, hs], ref["lse"])
-    check("dq", out["dq"][b:b + 1, hs], ref["dq"], TOL_REL_GRAD)
-    check("dk", out["dk"][b:b + 1, g:g + 1], ref["dk"], TOL_REL_GRAD)
-    check("dv", out["dv"][b:b + 1, g:g + 1], ref["dv"], TOL_REL_GRAD)
+    check("dq", out["dq"][b:b + 1, hs], ref["dq"], TOL_REL_GRAD, ref["edq"])
+    check("dk", out["dk"][b:b + 1, g:g + 1], ref["dk"], TOL_REL_GRAD, ref["edk"])
+    check("dv", out["dv"][b:b + 1, g:g + 1], ref["dv"], TOL_REL_GRAD, ref["edv"])
