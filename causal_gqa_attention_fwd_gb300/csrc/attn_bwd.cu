@@ -21,7 +21,7 @@
 //                dK and dV leave the CTA once, complete (no atomics).
 //   3. bwd_post  dQ = bf16(scale * accumulator).
 // Roles in bwd_main (512 threads): warp 0 TMA producer, warp 1 MMA issuer
-// (+TMEM owner), warps 4-11 two warpgroups that form P and dS (thread = key
+// (warp-uniform, one elected lane issues; TMEM owner), warps 4-11 two warpgroups that form P and dS (thread = key
 // row, each warpgroup half of the step's query columns), warps 12-15 drain dQ
 // partials and write dK, dV.
 #include "sm103.cuh"
@@ -311,22 +311,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (last_phase[st] >= 0) mbar_wait_drain(&bars.st_full[st], (uint32_t)last_phase[st]);
     }
   } else if (warp == 1) {
-    // ========================================================= MMA issuer
-    if (lane == 0) {
+    // ============================================ MMA issuer (whole warp, one lane issues)
+    {
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP), aDS = smem_u32(sDS);
       // X^T = A B^T with A a [128 x D] K-major tile (K or V) and B a [BM x D]
       // K-major stage tile (Q or dO).
       auto mma_t = [&](uint32_t d, uint32_t a_base, uint32_t b_base) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(d, sdesc_sw128(a_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+          mma_ss_warp(d, sdesc_sw128(a_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(b_base + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024), C::kIdescS, kk > 0);
       };
       // Acc += A^T-tile [128 x BM] (K-major, smem) * B [BM x D] (MN-major stage tile)
       auto mma_acc = [&](uint32_t d, uint32_t a_base, uint32_t b_base, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ss(d, sdesc_sw128(a_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+          mma_ss_warp(d, sdesc_sw128(a_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                  sdesc_sw128(b_base + kk * 2048, C::kQBoxBytes, 1024), C::kIdescKV, (acc || kk > 0) ? 1u : 0u);
       };
       // dQ^T = K^T dS^T (D = 128) or dQ = dS K (D = 64): both operands MN-major,
@@ -335,48 +335,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t qa = D == 128 ? aK : aDS, qb = D == 128 ? aDS : aK;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ss(tmem + C::kColDQ, sdesc_sw128(qa + kk * 2048, 16384, 1024), sdesc_sw128(qb + kk * 2048, 16384, 1024),
+          mma_ss_warp(tmem + C::kColDQ, sdesc_sw128(qa + kk * 2048, 16384, 1024), sdesc_sw128(qb + kk * 2048, 16384, 1024),
                  C::kIdescQ, kk > 0);
       };
-      bool ok = mbar_wait(&bars.kv_full, 0, guard);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full, 0, guard));
       if (ok && n_it > 0) {
-        ok = mbar_wait(&bars.st_full[0], 0, guard);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[0], 0, guard));
         if (ok) {
           tc_fence_after();
           mma_t(tmem + C::kColS, aK, smem_u32(stage_q(0)));
-          tc_commit(&bars.s_full);
+          tc_commit_warp(&bars.s_full);
           mma_t(tmem + C::kColDP, aV, smem_u32(stage_do(0)));
-          tc_commit(&bars.dp_full);
+          tc_commit_warp(&bars.dp_full);
         }
       }
       for (int i = 0; i < n_it && ok; ++i) {
         const int st = i & 1;
         const uint32_t par = i & 1;
-        if (!(ok = mbar_wait(&bars.p_full, par, guard))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_full, par, guard)))) break;
         tc_fence_after();
         mma_acc(tmem + C::kColDV, aP, smem_u32(stage_do(st)), i > 0);
         if (i + 1 < n_it) {
           const int st1 = (i + 1) & 1;
-          if (!(ok = mbar_wait(&bars.st_full[st1], ((i + 1) >> 1) & 1, guard))) break;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[st1], ((i + 1) >> 1) & 1, guard)))) break;
           tc_fence_after();
           mma_t(tmem + C::kColS, aK, smem_u32(stage_q(st1)));
-          tc_commit(&bars.s_full);
+          tc_commit_warp(&bars.s_full);
         }
-        if (!(ok = mbar_wait(&bars.ds_full, par, guard))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.ds_full, par, guard)))) break;
         tc_fence_after();
         mma_acc(tmem + C::kColDK, aDS, smem_u32(stage_q(st)), i > 0);
-        if (!(ok = mbar_wait(&bars.dq_empty, par ^ 1, guard))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_empty, par ^ 1, guard)))) break;
         tc_fence_after();
         mma_dq();
-        tc_commit(&bars.dq_full);
-        tc_commit(&bars.st_empty[st]);
+        tc_commit_warp(&bars.dq_full);
+        tc_commit_warp(&bars.st_empty[st]);
         if (i + 1 < n_it) {
           mma_t(tmem + C::kColDP, aV, smem_u32(stage_do((i + 1) & 1)));
-          tc_commit(&bars.dp_full);
+          tc_commit_warp(&bars.dp_full);
         }
       }
-      if (ok) tc_commit(&bars.dkdv_done);
-      tc_commit(&bars.teardown);
+      if (ok) tc_commit_warp(&bars.dkdv_done);
+      tc_commit_warp(&bars.teardown);
       mbar_wait_drain(&bars.teardown, 0);
     }
   } else if (warp >= 4 && warp < 4 + 4 * kComputeWGs) {

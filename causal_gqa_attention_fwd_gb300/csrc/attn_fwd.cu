@@ -13,8 +13,9 @@
 // two query heads of one GQA group at the same rows (G even), or two
 // consecutive row blocks of one head (G odd).  Roles (384 threads):
 //   warp 0      TMA producer: Q tiles once, then K_j, V_j through a ring.
-//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM (SS form), then
-//               O += P V with P read from TMEM (TS form); allocates TMEM.
+//   warp 1      MMA issuer (warp-uniform, one elected lane issues): S = Q K^T
+//               into TMEM (SS form), then O += P V with P read from TMEM (TS
+//               form); allocates TMEM.
 //   warps 4-7   softmax for tile A, warps 8-11 for tile B; thread = row.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A, O_B (D columns each).
 // P (bf16) overwrites the first 64 columns of its S block.
@@ -196,11 +197,11 @@ __global__ void __launch_bounds__(384, 1)
         if (last_phase[s] >= 0) mbar_wait_drain(&bars.kv_full[s], (uint32_t)last_phase[s]);
     }
   } else if (warp == 1) {
-    // ========================================================= MMA issuer
-    if (lane == 0) {
+    // ============================================ MMA issuer (whole warp, one lane issues)
+    {
       bool ok = true;
       for (int x = 0; x < 2 && ok; ++x)
-        if (ti[x].valid) ok = mbar_wait(&bars.q_full[x], 0, guard);
+        if (ti[x].valid) ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_full[x], 0, guard));
       const uint32_t sq_addr = smem_u32(sQ);
       const uint32_t ring_addr = smem_u32(sRing);
       auto issue_qk = [&](int x, int st) {
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::col_s(x), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+          mma_ss_warp(tmem + C::col_s(x), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
                  C::kIdescQK, kk > 0);
         }
       };
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t va = ring_addr + st * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          mma_ts(tmem + C::col_o(x), tmem + C::col_s(x) + kk * 8, sdesc_sw128(va + kk * 2048, C::kBoxBytes, 1024),
+          mma_ts_warp(tmem + C::col_o(x), tmem + C::col_s(x) + kk * 8, sdesc_sw128(va + kk * 2048, C::kBoxBytes, 1024),
                  C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
         }
       };
@@ -225,42 +226,42 @@ __global__ void __launch_bounds__(384, 1)
       auto stage_of = [&](int idx) { return idx % C::kStages; };
       auto phase_of = [&](int idx) { return (uint32_t)((idx / C::kStages) & 1); };
       if (ok && nkv > 0) {
-        ok = mbar_wait(&bars.kv_full[stage_of(0)], phase_of(0), guard);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full[stage_of(0)], phase_of(0), guard));
         if (ok) {
           tc_fence_after();
           for (int x = 0; x < 2; ++x)
             if (ti[x].nkv > 0) {
               issue_qk(x, stage_of(0));
-              tc_commit(&bars.s_full[x]);
+              tc_commit_warp(&bars.s_full[x]);
             }
-          tc_commit(&bars.kv_empty[stage_of(0)]);
+          tc_commit_warp(&bars.kv_empty[stage_of(0)]);
         }
       }
       for (int j = 0; j < nkv && ok; ++j) {
         const int vi = 2 * j + 1, ki = 2 * j + 2;
-        ok = mbar_wait(&bars.kv_full[stage_of(vi)], phase_of(vi), guard);
-        if (ok && j + 1 < nkv) ok = mbar_wait(&bars.kv_full[stage_of(ki)], phase_of(ki), guard);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full[stage_of(vi)], phase_of(vi), guard));
+        if (ok && j + 1 < nkv) ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full[stage_of(ki)], phase_of(ki), guard));
         if (!ok) break;
         tc_fence_after();
         for (int x = 0; x < 2 && ok; ++x) {
           if (j >= ti[x].nkv) continue;
-          ok = mbar_wait(&bars.p_full[x], j & 1, guard);
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_full[x], j & 1, guard));
           if (!ok) break;
           tc_fence_after();
           issue_pv(x, stage_of(vi), j > 0);
           if (j + 1 < ti[x].nkv) {
             issue_qk(x, stage_of(ki));
-            tc_commit(&bars.s_full[x]);
+            tc_commit_warp(&bars.s_full[x]);
           } else {
-            tc_commit(&bars.o_done[x]);
+            tc_commit_warp(&bars.o_done[x]);
           }
         }
         if (!ok) break;
-        tc_commit(&bars.kv_empty[stage_of(vi)]);
-        if (j + 1 < nkv) tc_commit(&bars.kv_empty[stage_of(ki)]);
+        tc_commit_warp(&bars.kv_empty[stage_of(vi)]);
+        if (j + 1 < nkv) tc_commit_warp(&bars.kv_empty[stage_of(ki)]);
       }
       // Let every issued MMA finish before TMEM is released.
-      tc_commit(&bars.teardown);
+      tc_commit_warp(&bars.teardown);
       mbar_wait_drain(&bars.teardown, 0);
     }
   } else if (warp >= 4) {

@@ -185,6 +185,33 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// One lane of a converged warp (the lowest); every lane gets the same answer
+// pattern on every call, so the same lane issues all of a warp's tcgen05 work.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(p));
+  return p != 0;
+}
+
+// Warp-collective issue: all 32 lanes call with identical (warp-uniform)
+// operands, one elected lane issues.  Keeping the operands warp-uniform lets
+// them live in uniform registers; issuing from a single divergent lane costs
+// roughly 100 cycles per MMA instead.
+__device__ __forceinline__ void mma_ss_warp(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if (elect_one()) mma_ss(d, a, b, idesc, acc);
+  __syncwarp();
+}
+__device__ __forceinline__ void mma_ts_warp(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if (elect_one()) mma_ts(d, a, b, idesc, acc);
+  __syncwarp();
+}
+__device__ __forceinline__ void tc_commit_warp(uint64_t* bar) {
+  if (elect_one()) tc_commit(bar);
+  __syncwarp();
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, f32 accumulator, M x N.
 // a_mn / b_mn select the MN-major (transposed) shared-memory layout.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
