@@ -167,35 +167,44 @@ struct BwdCfg {
   static constexpr int kQBytes = kBM * D * 2;          // Q or dO tile
   static constexpr int kQBoxBytes = kBM * 128;         // one 64-column box of a Q tile
   static constexpr int kStatBytes = kBM * 4;
-  static constexpr int kStageBytes = 2 * kQBytes + 1024;   // Q, dO, LSE2 + Delta (padded)
-  static constexpr int kPBytes = kBN * kBM * 2;        // P^T or dS^T tile
+  static constexpr int kStageBytes = 2 * kQBytes + 1024;   // Q, dO, -LSE2 and -Delta (padded)
+  static constexpr int kPBytes = kBN * kBM * 2;        // dS^T tile (for the dQ MMA)
   static constexpr int kStgBytes = kBM * D * 4;        // f32 dQ staging
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKVBytes;
   static constexpr int kOffStage = kOffV + kKVBytes;
-  static constexpr int kOffP = kOffStage + kStages * kStageBytes;
-  static constexpr int kOffDS = kOffP + kPBytes;
+  static constexpr int kOffDS = kOffStage + kStages * kStageBytes;
   static constexpr int kOffStg = kOffDS + kPBytes;
   static constexpr int kSmemBytes = kOffStg + kStgBytes + 1024;
-  // TMEM columns
+  // TMEM columns.  P^T (bf16) is written over S^T and dS^T over dP^T: each
+  // compute warpgroup packs its own kCols query columns into the first half
+  // of the same kCols columns it read them from.
+  static constexpr int kCols = kBM / kComputeWGs;
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColDP = kBM;
   static constexpr uint32_t kColDQ = 2 * kBM;
-  static constexpr uint32_t kColDK = D == 128 ? 256 : 320;
+  static constexpr uint32_t kColK = 2 * kBM + 64;      // K tile as a TMEM A operand (D/2 columns)
+  static constexpr uint32_t kColDK = D == 128 ? 256 : 352;
   static constexpr uint32_t kColDV = kColDK + D;
+  static_assert(kColK + D / 2 <= kColDK && kColDV + D <= 512, "TMEM budget");
   static constexpr uint32_t kIdescS = idesc_bf16(kBN, kBM, false, false);    // S^T, dP^T
   static constexpr uint32_t kIdescKV = idesc_bf16(kBN, D, false, true);      // dV, dK
   static constexpr uint32_t kIdescQ = idesc_bf16(128, 64, true, true);       // dQ^T (D=128) / dQ (D=64)
+  // TMEM column of the packed bf16 operand for the 16 queries of K-step kk
+  __device__ static constexpr uint32_t packed_col(uint32_t base, int kk) {
+    return base + (uint32_t)((16 * kk) / kCols * kCols + ((16 * kk) % kCols) / 2);
+  }
 };
 
 struct __align__(8) BwdBarriers {
-  uint64_t kv_full;
+  uint64_t kv_full, k_tmem;
   uint64_t st_full[2];
   uint64_t st_empty[2];
   uint64_t s_full, dp_full, p_full, ds_full;
   uint64_t dq_full, dq_empty;
   uint64_t stg_full, stg_free;
-  uint64_t dkdv_done, teardown;
+  uint64_t dkdv_done;
+  uint64_t teardown[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -236,9 +245,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     bars.abort = 0;
     mbar_init(&bars.kv_full, 1);
+    mbar_init(&bars.k_tmem, 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.st_full[i], 1);
-      mbar_init(&bars.st_empty[i], 1);
+      mbar_init(&bars.st_empty[i], 2);      // one commit from each MMA issuer
+      mbar_init(&bars.teardown[i], 1);
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_full, 1);
@@ -248,8 +259,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars.dq_empty, 128);
     mbar_init(&bars.stg_full, 128);
     mbar_init(&bars.stg_free, 1);
-    mbar_init(&bars.dkdv_done, 1);
-    mbar_init(&bars.teardown, 1);
+    mbar_init(&bars.dkdv_done, 2);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -262,7 +272,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
-  uint8_t* sP = smem + C::kOffP;
   uint8_t* sDS = smem + C::kOffDS;
   uint8_t* sStg = smem + C::kOffStg;
   auto stage_q = [&](int st) { return smem + C::kOffStage + st * C::kStageBytes; };
@@ -311,85 +320,132 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (last_phase[st] >= 0) mbar_wait_drain(&bars.st_full[st], (uint32_t)last_phase[st]);
     }
   } else if (warp == 1) {
-    // ============================================ MMA issuer (whole warp, one lane issues)
-    {
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP), aDS = smem_u32(sDS);
-      // X^T = A B^T with A a [128 x D] K-major tile (K or V) and B a [BM x D]
-      // K-major stage tile (Q or dO).
-      auto mma_t = [&](uint32_t d, uint32_t a_base, uint32_t b_base) {
+    // ===================================== MMA issuer A: S^T = K Q^T, dV += P^T dO
+    // (whole warp, warp-uniform operands, one elected lane issues)
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full, 0, guard));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.k_tmem, 0, guard));
+    auto mma_s = [&](int st) {             // A = K (TMEM), B = Q stage tile (K-major)
+      const uint32_t qb = smem_u32(stage_q(st));
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss_warp(d, sdesc_sw128(a_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(b_base + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024), C::kIdescS, kk > 0);
-      };
-      // Acc += A^T-tile [128 x BM] (K-major, smem) * B [BM x D] (MN-major stage tile)
-      auto mma_acc = [&](uint32_t d, uint32_t a_base, uint32_t b_base, bool acc) {
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ts_warp(tmem + C::kColS, tmem + C::kColK + kk * 8,
+                    sdesc_sw128(qb + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024), C::kIdescS, kk > 0);
+    };
+    if (ok && n_it > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[0], 0, guard));
+      if (ok) {
+        tc_fence_after();
+        mma_s(0);
+        tc_commit_warp(&bars.s_full);
+      }
+    }
+    for (int i = 0; i < n_it && ok; ++i) {
+      const int st = i & 1;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_full, i & 1, guard)))) break;
+      tc_fence_after();
+      const uint32_t dob = smem_u32(stage_do(st));      // dO as [N = D x K = queries], MN-major
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ss_warp(d, sdesc_sw128(a_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(b_base + kk * 2048, C::kQBoxBytes, 1024), C::kIdescKV, (acc || kk > 0) ? 1u : 0u);
-      };
-      // dQ^T = K^T dS^T (D = 128) or dQ = dS K (D = 64): both operands MN-major,
-      // contraction over the 128 keys.
-      auto mma_dq = [&]() {
-        const uint32_t qa = D == 128 ? aK : aDS, qb = D == 128 ? aDS : aK;
+      for (int kk = 0; kk < BM / 16; ++kk)
+        mma_ts_warp(tmem + C::kColDV, tmem + C::packed_col(C::kColS, kk),
+                    sdesc_sw128(dob + kk * 2048, C::kQBoxBytes, 1024), C::kIdescKV, (i > 0 || kk > 0) ? 1u : 0u);
+      tc_commit_warp(&bars.st_empty[st]);
+      if (i + 1 < n_it) {
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[(i + 1) & 1], ((i + 1) >> 1) & 1, guard))))
+          break;
+        tc_fence_after();
+        mma_s((i + 1) & 1);
+        tc_commit_warp(&bars.s_full);
+      }
+    }
+    if (ok) tc_commit_warp(&bars.dkdv_done);
+    tc_commit_warp(&bars.teardown[0]);
+    mbar_wait_drain(&bars.teardown[0], 0);
+  } else if (warp == 2) {
+    // =========== MMA issuer B: dP^T = V dO^T, dK += dS^T Q, dQ partial (dS K)
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full, 0, guard));
+    const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aDS = smem_u32(sDS);
+    auto mma_dp = [&](int st) {            // A = V (smem, K-major), B = dO stage tile (K-major)
+      const uint32_t db = smem_u32(stage_do(st));
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss_warp(tmem + C::kColDP, sdesc_sw128(aV + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                    sdesc_sw128(db + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024), C::kIdescS, kk > 0);
+    };
+    if (ok && n_it > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[0], 0, guard));
+      if (ok) {
+        tc_fence_after();
+        mma_dp(0);
+        tc_commit_warp(&bars.dp_full);
+      }
+    }
+    for (int i = 0; i < n_it && ok; ++i) {
+      const int st = i & 1;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.ds_full, i & 1, guard)))) break;
+      tc_fence_after();
+      const uint32_t qb = smem_u32(stage_q(st));        // Q as [N = D x K = queries], MN-major
+#pragma unroll
+      for (int kk = 0; kk < BM / 16; ++kk)
+        mma_ts_warp(tmem + C::kColDK, tmem + C::packed_col(C::kColDP, kk),
+                    sdesc_sw128(qb + kk * 2048, C::kQBoxBytes, 1024), C::kIdescKV, (i > 0 || kk > 0) ? 1u : 0u);
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_empty, (i & 1) ^ 1, guard)))) break;
+      tc_fence_after();
+      {
+        // dQ^T = K^T dS^T (D = 128) or dQ = dS K (D = 64): both operands
+        // MN-major in smem, contraction over the 128 keys.
+        const uint32_t qa = D == 128 ? aK : aDS, qbb = D == 128 ? aDS : aK;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ss_warp(tmem + C::kColDQ, sdesc_sw128(qa + kk * 2048, 16384, 1024), sdesc_sw128(qb + kk * 2048, 16384, 1024),
-                 C::kIdescQ, kk > 0);
-      };
-      bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full, 0, guard));
-      if (ok && n_it > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[0], 0, guard));
-        if (ok) {
-          tc_fence_after();
-          mma_t(tmem + C::kColS, aK, smem_u32(stage_q(0)));
-          tc_commit_warp(&bars.s_full);
-          mma_t(tmem + C::kColDP, aV, smem_u32(stage_do(0)));
-          tc_commit_warp(&bars.dp_full);
-        }
+          mma_ss_warp(tmem + C::kColDQ, sdesc_sw128(qa + kk * 2048, 16384, 1024),
+                      sdesc_sw128(qbb + kk * 2048, 16384, 1024), C::kIdescQ, kk > 0);
       }
-      for (int i = 0; i < n_it && ok; ++i) {
-        const int st = i & 1;
-        const uint32_t par = i & 1;
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_full, par, guard)))) break;
+      tc_commit_warp(&bars.dq_full);
+      tc_commit_warp(&bars.st_empty[st]);
+      if (i + 1 < n_it) {
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[(i + 1) & 1], ((i + 1) >> 1) & 1, guard))))
+          break;
         tc_fence_after();
-        mma_acc(tmem + C::kColDV, aP, smem_u32(stage_do(st)), i > 0);
-        if (i + 1 < n_it) {
-          const int st1 = (i + 1) & 1;
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[st1], ((i + 1) >> 1) & 1, guard)))) break;
-          tc_fence_after();
-          mma_t(tmem + C::kColS, aK, smem_u32(stage_q(st1)));
-          tc_commit_warp(&bars.s_full);
-        }
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.ds_full, par, guard)))) break;
-        tc_fence_after();
-        mma_acc(tmem + C::kColDK, aDS, smem_u32(stage_q(st)), i > 0);
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_empty, par ^ 1, guard)))) break;
-        tc_fence_after();
-        mma_dq();
-        tc_commit_warp(&bars.dq_full);
-        tc_commit_warp(&bars.st_empty[st]);
-        if (i + 1 < n_it) {
-          mma_t(tmem + C::kColDP, aV, smem_u32(stage_do((i + 1) & 1)));
-          tc_commit_warp(&bars.dp_full);
-        }
+        mma_dp((i + 1) & 1);
+        tc_commit_warp(&bars.dp_full);
       }
-      if (ok) tc_commit_warp(&bars.dkdv_done);
-      tc_commit_warp(&bars.teardown);
-      mbar_wait_drain(&bars.teardown, 0);
     }
+    if (ok) tc_commit_warp(&bars.dkdv_done);
+    tc_commit_warp(&bars.teardown[1]);
+    mbar_wait_drain(&bars.teardown[1], 0);
   } else if (warp >= 4 && warp < 4 + 4 * kComputeWGs) {
     // ================================================ compute P^T and dS^T
     // kComputeWGs warpgroups split each step's query columns; thread = key row.
-    constexpr int kCols = BM / kComputeWGs;
+    constexpr int kCols = C::kCols;
     const int c0 = ((warp - 4) >> 2) * kCols;          // first query column of this warpgroup
     const int r = threadIdx.x & 127;                  // key row
     const int key = k0 + r;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float c = a.scale_log2;
-    const uint32_t rowP = smem_u32(sP) + r * 128, rowDS = smem_u32(sDS) + r * 128;
-    for (int i = 0; i < n_it; ++i) {
+    const uint32_t rowDS = smem_u32(sDS) + r * 128;
+    bool ok = true;
+    if (c0 == 0) {
+      // K tile -> TMEM (A operand of S^T = K Q^T): row r = key r, D/2 packed columns
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full, 0, guard));
+      if (ok) {
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          uint32_t kr[32];
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 x = ld_shared_v4(smem_u32(sK) + h * 16384 + r * 128 + ((ch ^ (r & 7)) << 4));
+            kr[4 * ch] = x.x;
+            kr[4 * ch + 1] = x.y;
+            kr[4 * ch + 2] = x.z;
+            kr[4 * ch + 3] = x.w;
+          }
+          tmem_st_x32(tmem + lane_base + C::kColK + h * 32, kr);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars.k_tmem);
+      }
+    }
+    for (int i = 0; i < n_it && ok; ++i) {
       const int st = i & 1;
       const uint32_t par = i & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars.st_full[st], (i >> 1) & 1, guard))) break;
@@ -423,15 +479,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!krow_ok || qi >= L || qi < qmin) p[j] = 0.f;
         }
       }
-      // P^T row segment -> bf16 -> sP (128-byte swizzled K-major rows)
+      // P^T row segment -> bf16 pairs -> TMEM over this warpgroup's S^T columns
 #pragma unroll
-      for (int cc = 0; cc < kCols / 8; ++cc) {
-        const int ch = c0 / 8 + cc;                      // 16-byte chunk index in the row
-        const uint32_t addr = rowP + (ch >> 3) * 16384 + (((ch & 7) ^ (r & 7)) << 4);
-        st_shared_v4(addr, pack_bf16x2(p[8 * cc], p[8 * cc + 1]), pack_bf16x2(p[8 * cc + 2], p[8 * cc + 3]),
-                     pack_bf16x2(p[8 * cc + 4], p[8 * cc + 5]), pack_bf16x2(p[8 * cc + 6], p[8 * cc + 7]));
+      for (int q = 0; q < kCols / 32; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(p[32 * q + 2 * e], p[32 * q + 2 * e + 1]);
+        tmem_st_x16(tmem + lane_base + C::kColS + c0 + q * 16, pk);
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.p_full);
       if (!__all_sync(0xffffffffu, mbar_wait(&bars.dp_full, par, guard))) break;
@@ -442,23 +498,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld_x32(tmem + lane_base + C::kColDP + c0 + q * 32, dv);
         tmem_ld_wait();
         reg_fence<32>(dv);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int j = q * 32 + 2 * e;
+          const uint64_t nd = *reinterpret_cast<const uint64_t*>(ndl + j);
+          float d0, d1;
+          f2_split(mul2(f2(p[j], p[j + 1]), add2(f2(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])), nd)),
+                   d0, d1);                                  // P (dP - Delta)
+          w[e] = pack_bf16x2(d0, d1);
+        }
+        // dS^T: into TMEM over this warpgroup's dP^T columns (A of dK += dS^T Q)
+        // and into smem (operand of the dQ MMA), 128-byte swizzled K-major rows
+        tmem_st_x16(tmem + lane_base + C::kColDP + c0 + q * 16, w);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          const int j0 = q * 32 + cc * 8;
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = j0 + 2 * e;
-            const uint64_t nd = *reinterpret_cast<const uint64_t*>(ndl + j);
-            const uint64_t dp = f2(__uint_as_float(dv[cc * 8 + 2 * e]), __uint_as_float(dv[cc * 8 + 2 * e + 1]));
-            float d0, d1;
-            f2_split(mul2(f2(p[j], p[j + 1]), add2(dp, nd)), d0, d1);     // P (dP - Delta)
-            w[e] = pack_bf16x2(d0, d1);
-          }
-          const int ch = (c0 + j0) / 8;
-          st_shared_v4(rowDS + (ch >> 3) * 16384 + (((ch & 7) ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+          const int ch = (c0 + q * 32) / 8 + cc;
+          st_shared_v4(rowDS + (ch >> 3) * 16384 + (((ch & 7) ^ (r & 7)) << 4), w[4 * cc], w[4 * cc + 1],
+                       w[4 * cc + 2], w[4 * cc + 3]);
         }
       }
+      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars.ds_full);
@@ -519,7 +579,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.dkdv_done, 0, guard));
     if (ok) {
       tc_fence_after();
-      // dK (scaled) into sK, dV into sV (both dead now): row r, swizzled 16-byte chunks
+      // dK (scaled) into sK, dV into sV (both dead now: every MMA is done): row r,
+      // swizzled 16-byte chunks
       for (int t = 0; t < 2; ++t) {
         const uint32_t col = t == 0 ? C::kColDK : C::kColDV;
         const float mul = t == 0 ? a.scale : 1.f;
