@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     LIB_PATH,
     AttnError,
     attn_bwd,
+    attn_bwd_noalloc,
     attn_bwd_workspace_size,
     attn_fwd,
     attn_varlen_bwd,

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgqa_attn
 STATUS = {
     0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_SHAPE", 3: "ATTN_ERR_HEADDIM", 4: "ATTN_ERR_ALIGN",
     5: "ATTN_ERR_SEQLENS", 6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_ARCH", 8: "ATTN_ERR_CUDA",
-    9: "ATTN_ERR_TIMEOUT",
+    9: "ATTN_ERR_TIMEOUT", 10: "ATTN_ERR_SCRATCH_LIMIT",
 }
 
 # name -> (restype, argtypes)
@@ -32,6 +32,8 @@ SIGNATURES = {
     "attn_varlen_bwd": (_I, [_P] * 10 + [_Z, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_get_device_status": (_I, [_P, ctypes.POINTER(_I), _I]),
+    "attn_bwd_noalloc": (_I, [_P] * 9 + [_I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_bwd_noalloc_scratch_bytes": (_Z, []),
     "attn_profile_enable": (_I, [_I]),
     "attn_profile_reset": (_I, []),
     "attn_profile_read": (_I, [_I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)]),
@@ -162,6 +164,24 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = True, scale=None, dq=None, dk
                         _need(dv, "dv"), _need(workspace, "workspace", torch.uint8), workspace.numel(),
                         B, Hq, Hkv, T, D, int(causal), _scale(scale, D), _stream(stream))
     _check(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, dout, causal: bool = True, scale=None, dq=None, dk=None, dv=None,
+                     stream=None):
+    """Dense backward through attn_bwd_noalloc: no workspace and no allocation
+    inside the library (it uses its built-in scratch array).  Outputs are
+    allocated here unless passed in."""
+    B, Hq, T, D = q.shape
+    Hkv = k.shape[1]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = lib().attn_bwd_noalloc(_need(q, "q"), _need(k, "k"), _need(v, "v"), _need(o, "o"),
+                                _need(lse, "lse", torch.float32), _need(dout, "dout"), _need(dq, "dq"),
+                                _need(dk, "dk"), _need(dv, "dv"), B, Hq, Hkv, T, D, int(causal), _scale(scale, D),
+                                _stream(stream))
+    _check(st, "attn_bwd_noalloc")
     return dq, dk, dv
 
 

@@ -336,6 +336,45 @@ attn_status attn_varlen_bwd(const void* q, const void* k, const void* v, const v
                     max_seqlen, Hq, Hkv, D, causal, scale, stream, true);
 }
 
+// ------------------------------------------------- allocation-free backward
+// Scratch for attn_bwd_noalloc: a file-scope device array, so the library
+// never has to allocate device memory for it.  Every device that loads the
+// library holds these bytes until the process exits.
+#define GQA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+static __device__ __align__(256) unsigned char g_bwd_scratch[GQA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_bwd_scratch on the current device.  The name is only a
+// host-side stand-in in host code, so the address is looked up once per
+// device (with that device current) and cached.
+static void* noalloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  static void* cache[kMaxDevices] = {};
+  if (dev < kMaxDevices && cache[dev]) return cache[dev];
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_bwd_scratch) != cudaSuccess) return nullptr;
+  if (dev < kMaxDevices) cache[dev] = ptr;
+  return ptr;
+}
+
+size_t attn_bwd_noalloc_scratch_bytes(void) { return GQA_NOALLOC_SCRATCH_BYTES; }
+
+attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                             const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int T, int D,
+                             int causal, float scale, void* stream) {
+  if (B < 0 || T < 0) return ATTN_ERR_SHAPE;
+  attn_status st = check_heads(Hq, Hkv, D);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || T == 0) return ATTN_OK;
+  if (attn_bwd_workspace_size(B, Hq, Hkv, T, D) > GQA_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_SCRATCH_LIMIT;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return ATTN_ERR_NULL;
+  if ((st = check_arch()) != ATTN_OK) return st;
+  void* scratch = noalloc_scratch();
+  if (!scratch) return ATTN_ERR_CUDA;
+  return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, scratch, GQA_NOALLOC_SCRATCH_BYTES, B, Hq, Hkv, T, D, causal,
+                  scale, stream);
+}
+
 const char* attn_status_string(attn_status s) {
   switch (s) {
     case ATTN_OK: return "ok";
@@ -348,6 +387,8 @@ const char* attn_status_string(attn_status s) {
     case ATTN_ERR_ARCH: return "the current device is not compute capability 10.3 (sm_103a)";
     case ATTN_ERR_CUDA: return "a CUDA runtime call failed";
     case ATTN_ERR_TIMEOUT: return "a bounded in-kernel wait expired";
+    case ATTN_ERR_SCRATCH_LIMIT:
+      return "the problem needs more backward scratch than attn_bwd_noalloc's built-in array holds";
   }
   return "unknown status";
 }

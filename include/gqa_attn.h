@@ -66,7 +66,8 @@ typedef enum {
     ATTN_ERR_WORKSPACE = 6,  /* workspace NULL or smaller than the *_workspace_size() value */
     ATTN_ERR_ARCH = 7,       /* current device is not compute capability 10.3 */
     ATTN_ERR_CUDA = 8,       /* a CUDA runtime call failed (launch, tensor map, attribute) */
-    ATTN_ERR_TIMEOUT = 9     /* device-detected: a bounded in-kernel wait expired */
+    ATTN_ERR_TIMEOUT = 9,    /* device-detected: a bounded in-kernel wait expired */
+    ATTN_ERR_SCRATCH_LIMIT = 10 /* attn_bwd_noalloc: sizes need more than its built-in scratch */
 } attn_status;
 
 /* Forward, dense layout.  Writes O (bf16) and LSE (float32). */
@@ -84,6 +85,33 @@ GQA_ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int T, int D
 GQA_ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                      const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                      int B, int Hq, int Hkv, int T, int D, int causal, float scale, void* stream);
+
+/* Backward, dense layout, without a caller-provided workspace and without
+ * allocating anything.  (No counterpart in the pages: an operational
+ * variant of attn_bwd.)  It is for callers that cannot hand the library
+ * device memory or let it allocate: code running where allocation is not
+ * allowed or not available -- e.g. a host framework that has reserved every
+ * byte of the device for its own pool, a plugin that only ever receives the
+ * tensors it must read and write, or a stream that is being captured into a
+ * CUDA graph, during which cudaMalloc is not permitted.
+ * The scratch is a static device array of attn_bwd_noalloc_scratch_bytes()
+ * bytes (64 MiB) inside the library; every GPU that loads the library holds
+ * it until the process exits.  Sizes whose attn_bwd_workspace_size() exceeds
+ * it return ATTN_ERR_SCRATCH_LIMIT before anything is launched.  The first
+ * call on a device looks up the array's device address (once per device,
+ * with that device current), so make that first call before any stream
+ * capture.  All calls share the one array and the kernels re-initialise
+ * everything they read from it, but calls whose work overlaps on the GPU
+ * (other streams, other host threads) race on it: serialise them.
+ * Otherwise identical to attn_bwd (same arguments minus the workspace, same
+ * results). */
+GQA_ATTN_API attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                                          const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                          int B, int Hq, int Hkv, int T, int D, int causal, float scale,
+                                          void* stream);
+
+/* Size in bytes of attn_bwd_noalloc's built-in scratch array. */
+GQA_ATTN_API size_t attn_bwd_noalloc_scratch_bytes(void);
 
 /* Forward, packed variable-length layout.  max_seqlen must be >= every
  * sequence's length (it sizes the launch grid). */

@@ -104,6 +104,16 @@ def test_bwd_validation(lib):
     assert bwd(lib, ptrs=(NULL,) * 10, T=0) == 0
 
 
+def test_noalloc_validation(lib):
+    # returns before any CUDA call: shape, scratch limit, NULL pointers
+    args = (A,) * 9
+    assert lib.attn_bwd_noalloc(*args, 1, 3, 2, 16, 64, 1, 0.1, None) == 2
+    assert lib.attn_bwd_noalloc(*args, 1, 64, 8, 8192, 128, 1, 0.1, None) == 10
+    assert lib.attn_bwd_noalloc(*((NULL,) * 9), 1, 4, 2, 0, 64, 1, 0.1, None) == 0
+    assert lib.attn_bwd_noalloc(*((NULL,) * 9), 1, 4, 2, 16, 64, 1, 0.1, None) == 1
+    assert lib.attn_bwd_noalloc_scratch_bytes() == 64 << 20
+
+
 def test_workspace_sizes(lib):
     # Delta + LSE*log2e (256-aligned f32 rows each) + f32 dQ rows; rows = B*Hq*roundup(T,128)
     rows = 2 * 32 * 4096
@@ -117,7 +127,7 @@ def test_workspace_sizes(lib):
 
 def test_status_strings(lib):
     import causal_gqa_attention_fwd_gb300 as g
-    for code in range(10):
+    for code in range(11):
         s = g.status_string(code)
         assert s and s != "unknown status"
     assert g.status_string(99) == "unknown status"
