@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     bars.abort = 0;
     mbar_init(&bars.kv_full, 1);
-    mbar_init(&bars.k_tmem, 128);
+    mbar_init(&bars.k_tmem, 4);                 // barriers fed by whole warps count warps
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.st_full[i], 1);
       mbar_init(&bars.st_empty[i], 2);      // one commit from each MMA issuer
@@ -253,11 +253,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.p_full, 128 * kComputeWGs);
-    mbar_init(&bars.ds_full, 128 * kComputeWGs);
+    mbar_init(&bars.p_full, 4 * kComputeWGs);
+    mbar_init(&bars.ds_full, 4 * kComputeWGs);
     mbar_init(&bars.dq_full, 1);
-    mbar_init(&bars.dq_empty, 128);
-    mbar_init(&bars.stg_full, 128);
+    mbar_init(&bars.dq_empty, 4);
+    mbar_init(&bars.stg_full, 4);
     mbar_init(&bars.stg_free, 1);
     mbar_init(&bars.dkdv_done, 2);
     fence_barrier_init();
@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars.k_tmem);
+        mbar_arrive_warp(&bars.k_tmem);
       }
     }
     for (int i = 0; i < n_it && ok; ++i) {
@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars.p_full);
+      mbar_arrive_warp(&bars.p_full);
       if (!__all_sync(0xffffffffu, mbar_wait(&bars.dp_full, par, guard))) break;
       tc_fence_after();
 #pragma unroll
@@ -521,7 +521,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars.ds_full);
+      mbar_arrive_warp(&bars.ds_full);
     }
   } else if (warp >= 4 + 4 * kComputeWGs) {
     // ===================================== drain dQ partials; dK, dV epilogue
@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld_wait();
       reg_fence<64>(v);
       tc_fence_before();
-      mbar_arrive(&bars.dq_empty);
+      mbar_arrive_warp(&bars.dq_empty);
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.stg_free, par ^ 1, guard)))) break;
       if (D == 128) {
         // lane = feature d, columns = 64 queries: staging [q][d]
@@ -558,7 +558,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                          v[32 * b + 4 * ch + 1], v[32 * b + 4 * ch + 2], v[32 * b + 4 * ch + 3]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bars.stg_full);
+      mbar_arrive_warp(&bars.stg_full);
       if (leader) {
         if (!mbar_wait(&bars.stg_full, par, guard)) { ok = false; }
         if (ok) {

@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.q_full[i], 1);
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.p_full[i], kBM);
+      mbar_init(&bars.p_full[i], kBM / 32);      // one arrive per softmax warp
       mbar_init(&bars.o_done[i], 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars.p_full[x]);
+        mbar_arrive_warp(&bars.p_full[x]);
       }
       // ------------------------------------------------------- epilogue
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_done[x], 0, guard));
