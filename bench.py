@@ -56,6 +56,23 @@ def peaks():
     return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+    from the committed ncu capture, or None if there is none for this
+    workload or the kernel's sources changed since it was taken."""
+    import hashlib
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tp):
+        return None
+    entry = json.load(open(tp)).get(workload, {}).get(kernel)
+    if not entry:
+        return None
+    h = hashlib.sha256()
+    for f in entry["sources"]:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return entry["dram_bytes_per_launch"] if h.hexdigest()[:16] == entry["source_sha256_16"] else None
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
@@ -179,6 +196,12 @@ def max_over_ranks(world, value: float) -> float:
     return float(t.item())
 
 
+def whole_job_tflops(world: int, flops_per_step: float, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank runs the same per-step work (weak
+    scaling), the job takes as long as its slowest rank."""
+    return world * flops_per_step * steps / (max_ms / 1e3) / 1e12
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -290,7 +313,7 @@ def main():
     local_ms = sum(step_ms)
     total_ms = max_over_ranks(world, local_ms)
     ms_per_step = total_ms / args.steps
-    value = world * (f_fwd + f_bwd) * args.steps / (total_ms / 1e3) / 1e12
+    value = whole_job_tflops(world, f_fwd + f_bwd, args.steps, total_ms)
     n_fwd, t_fwd = prof["attn_fwd"]
     n_main, t_main = prof["bwd_main"]
     bwd_ms = sum(prof[k][1] for k in ("bwd_pre", "bwd_main", "bwd_post")) / args.steps
@@ -301,13 +324,9 @@ def main():
     # roofline of the dominant kernel (the backward main kernel)
     main_ms = t_main / max(n_main, 1)
     achieved = f_bwd / (main_ms / 1e3) / 1e12
-    traffic = None
-    tp = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tp):
-        tj = json.load(open(tp)).get(w.name, {}).get("bwd_main")
-        traffic = tj
+    roofline_traffic = measured_traffic(w.name, "bwd_main")
     roofline = {"kernel": "bwd_main", "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": roofline_traffic,
                 "peak_source": pk["source"] + " (burst bf16)"}
 
     # end to end through the public API with host buffers

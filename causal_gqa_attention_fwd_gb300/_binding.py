@@ -34,6 +34,7 @@ SIGNATURES = {
     "attn_get_device_status": (_I, [_P, ctypes.POINTER(_I), _I]),
     "attn_bwd_noalloc": (_I, [_P] * 9 + [_I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_noalloc_scratch_bytes": (_Z, []),
+    "attn_selftest_wait_timeout": (_I, [_I, _P]),
     "attn_profile_enable": (_I, [_I]),
     "attn_profile_reset": (_I, []),
     "attn_profile_read": (_I, [_I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)]),

@@ -9,6 +9,7 @@
 
 #include "gqa_attn.h"
 #include "kernels.h"
+#include "sm103.cuh"
 #include "tmap.h"
 
 namespace {
@@ -184,6 +185,22 @@ attn_status fwd_common(const void* q, const void* k, const void* v, void* o, flo
          map_dense(&tv, v, D, T, (long)num_seqs * Hkv);
   if (!ok) return ATTN_ERR_CUDA;
   return launch_status(gqa::launch_attn_fwd(tq, tk, tv, a, D, (int)grid, static_cast<cudaStream_t>(stream)));
+}
+
+// Waits, through the same bounded mbarrier wait every pipeline uses, on a
+// barrier phase that nothing completes; the wait expires after limit_ns,
+// records the timeout in the status word and the kernel returns.
+__global__ void selftest_wait_timeout_kernel(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    gqa::mbar_init(&bar, 1);
+    gqa::fence_barrier_init();
+  }
+  __syncthreads();
+  gqa::Guard g{&abort_flag, status};
+  (void)gqa::mbar_wait(&bar, 0, g, limit_ns);
 }
 
 }  // namespace
@@ -373,6 +390,17 @@ attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const 
   if (!scratch) return ATTN_ERR_CUDA;
   return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, scratch, GQA_NOALLOC_SCRATCH_BYTES, B, Hq, Hkv, T, D, causal,
                   scale, stream);
+}
+
+attn_status attn_selftest_wait_timeout(int limit_ms, void* stream) {
+  if (limit_ms < 1 || limit_ms > 5000) return ATTN_ERR_SHAPE;
+  attn_status st = check_arch();
+  if (st != ATTN_OK) return st;
+  int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
+  selftest_wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status,
+                                                                                 (uint64_t)limit_ms * 1000000ull);
+  return launch_status(cudaGetLastError());
 }
 
 const char* attn_status_string(attn_status s) {

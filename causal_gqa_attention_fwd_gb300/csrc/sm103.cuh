@@ -80,14 +80,15 @@ struct Guard {
 // Wait for phase `parity` of `bar` to complete.  Returns false (after
 // flagging a timeout) if it does not within kWaitLimitNs, or if another role
 // of the CTA already gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Guard& g) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Guard& g,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (g.aborted()) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         g.fail(kDevTimeout);
         return false;
       }

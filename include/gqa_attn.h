@@ -137,6 +137,14 @@ GQA_ATTN_API const char* attn_status_string(attn_status status);
  * fails (e.g. a sticky CUDA error), else ATTN_OK. */
 GQA_ATTN_API attn_status attn_get_device_status(void* stream, int* out, int clear);
 
+/* Failure-path self-test (no counterpart in the pages).  Launches one small
+ * kernel that waits, through the library's bounded in-kernel wait, on a
+ * barrier that nothing ever completes, with a limit of limit_ms milliseconds
+ * (1..5000).  The wait expires, ATTN_ERR_TIMEOUT is recorded in the device
+ * status word and the kernel returns normally: the GPU is neither hung nor
+ * faulted, and attn_get_device_status() then reports the timeout. */
+GQA_ATTN_API attn_status attn_selftest_wait_timeout(int limit_ms, void* stream);
+
 /* Kernel timing (instrumentation; not thread-safe).  While enabled, every
  * kernel launch is bracketed by a CUDA event pair recorded on the caller's
  * stream.  attn_profile_read synchronises those events and returns, for one
