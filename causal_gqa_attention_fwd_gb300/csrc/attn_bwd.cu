@@ -80,9 +80,14 @@ __device__ __forceinline__ long row_off(const BwdArgs& a, int s, int tok0, int h
 }  // namespace
 
 // =========================================================== 1. preprocess
-// grid: (row blocks of 128, num_seqs * Hq); 256 threads, one warp per row.
+// grid: (row blocks of 128, num_seqs * Hq); 256 threads.  A row is handled by
+// D/8 lanes (16 bytes of O and of dO each); a warp covers 32/(D/8) rows per
+// pass and keeps four passes of loads in flight.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerPass = 32 / kLanesPerRow;            // per warp
+  constexpr int kPasses = 4;
   const int s = blockIdx.y / a.Hq, h = blockIdx.y % a.Hq;
   int tok0, L;
   if (!seq_bounds(a, s, tok0, L)) {
@@ -91,46 +96,51 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
   }
   const int Lr = (L + 127) & ~127;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int rr = warp; rr < 128; rr += 8) {
-    const int p = blockIdx.x * 128 + rr;
-    if (p >= Lr) break;
-    const long w = ws_row(a, s, tok0, h, p);
-    float dl = 0.f, l2 = -INFINITY;       // stored negated: -Delta, -LSE*log2(e)
-    if (p < L) {
-      const long off = row_off(a, s, tok0, h, a.Hq, p, D);
-      float acc = 0.f;
-      if (D == 128) {
-        const uint2 ov = *reinterpret_cast<const uint2*>(a.o + off + lane * 4);
-        const uint2 gv = *reinterpret_cast<const uint2*>(a.dout + off + lane * 4);
+  const int sub = lane / kLanesPerRow, part = lane % kLanesPerRow;
+  for (int base = warp * kRowsPerPass * kPasses; base < 128; base += 8 * kRowsPerPass * kPasses) {
+    float acc[kPasses];
+    int prow[kPasses];
+#pragma unroll
+    for (int u = 0; u < kPasses; ++u) {
+      const int p = blockIdx.x * 128 + base + u * kRowsPerPass + sub;
+      prow[u] = p;
+      acc[u] = 0.f;
+      if (p < L) {
+        const long off = row_off(a, s, tok0, h, a.Hq, p, D) + part * 8;
+        const uint4 ov = *reinterpret_cast<const uint4*>(a.o + off);
+        const uint4 gv = *reinterpret_cast<const uint4*>(a.dout + off);
         const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
         const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const float2 of = __bfloat1622float2(o2[i]), gf = __bfloat1622float2(g2[i]);
-          acc = fmaf(of.x, gf.x, acc);
-          acc = fmaf(of.y, gf.y, acc);
+        for (int e = 0; e < 4; ++e) {
+          const float2 of = __bfloat1622float2(o2[e]), gf = __bfloat1622float2(g2[e]);
+          acc[u] = fmaf(of.x, gf.x, acc[u]);
+          acc[u] = fmaf(of.y, gf.y, acc[u]);
         }
-      } else {
-        const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(a.o + off + lane * 2);
-        const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(a.dout + off + lane * 2);
-        const float2 of = __bfloat1622float2(o2), gf = __bfloat1622float2(g2);
-        acc = fmaf(of.x, gf.x, of.y * gf.y);
       }
+    }
 #pragma unroll
-      for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-      dl = -acc;
-      const long li = a.varlen ? (long)h * a.total + tok0 + p : ((long)s * a.Hq + h) * a.T + p;
-      l2 = -a.lse[li] * 1.4426950408889634f;
+    for (int u = 0; u < kPasses; ++u) {
+#pragma unroll
+      for (int m = kLanesPerRow / 2; m > 0; m >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], m);
+      const int p = prow[u];
+      if (p >= Lr) continue;
+      const long w = ws_row(a, s, tok0, h, p);
+      if (part == 0) {
+        float dl = 0.f, l2 = -INFINITY;       // stored negated: -Delta, -LSE*log2(e)
+        if (p < L) {
+          const long li = a.varlen ? (long)h * a.total + tok0 + p : ((long)s * a.Hq + h) * a.T + p;
+          dl = -acc[u];
+          l2 = -a.lse[li] * 1.4426950408889634f;
+        }
+        a.delta[w] = dl;
+        a.lse_log2[w] = l2;
+      }
+      // zero this row of the f32 dQ accumulator (D floats: 2 x 16 bytes per lane)
+      float4* z = reinterpret_cast<float4*>(a.dq_accum + w * D) + part * 2;
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (lane == 0) {
-      a.delta[w] = dl;
-      a.lse_log2[w] = l2;
-    }
-    float* acc_row = a.dq_accum + w * D;
-    if (D == 128)
-      *reinterpret_cast<float4*>(acc_row + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-    else
-      *reinterpret_cast<float2*>(acc_row + lane * 2) = make_float2(0.f, 0.f);
   }
 }
 
