@@ -58,9 +58,10 @@ def _bind(lib):
     lib.oracle_bwd.argtypes = [_D] * 13 + [_L, _L, _L, _L, _L, ctypes.c_int, ctypes.c_double]
     lib.oracle_varlen_fwd.argtypes = [_D, _D, _D, _D, _D, _I, _L, _L, _L, _L, _L, ctypes.c_int, ctypes.c_double]
     lib.oracle_varlen_bwd.argtypes = [_D] * 13 + [_I, _L, _L, _L, _L, _L, ctypes.c_int, ctypes.c_double]
+    lib.oracle_decode_fwd.argtypes = [_D, _D, _D, _I, _D, _D, _L, _L, _L, _L, _L, _L, ctypes.c_double]
     lib.oracle_set_threads.argtypes = [ctypes.c_int]
     for f in (lib.oracle_fwd, lib.oracle_bwd, lib.oracle_varlen_fwd, lib.oracle_varlen_bwd,
-              lib.oracle_set_threads):
+              lib.oracle_decode_fwd, lib.oracle_set_threads):
         f.restype = ctypes.c_int
     return lib
 
@@ -182,3 +183,24 @@ def varlen_bwd(q, k, v, dout, cu_seqlens, causal: bool = True, scale: float | No
     if err_terms:
         r.update(edq=np.sqrt(eq), edk=np.sqrt(ek), edv=np.sqrt(ev))
     return r
+
+
+def decode_fwd(q, k_cache, v_cache, cache_lens, scale: float | None = None, lib=None):
+    """Attention of the newest Tq positions over a KV cache.
+
+    q [B,Hq,Tq,D]; k_cache, v_cache [B,Hkv,S,D]; cache_lens [B] (keys held per
+    row, including the Tq new ones).  Query t of row b attends to keys
+    j <= cache_lens[b] - Tq + t.  Returns (O [B,Hq,Tq,D], LSE [B,Hq,Tq])."""
+    lib = lib or load()
+    q, k, v = _c(q), _c(k_cache), _c(v_cache)
+    lens = _cu(cache_lens)
+    B, Hq, Tq, D = q.shape
+    Hkv, S = k.shape[1], k.shape[2]
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    o = np.zeros_like(q)
+    lse = np.zeros((B, Hq, Tq))
+    st = lib.oracle_decode_fwd(_p(q), _p(k), _p(v), lens.ctypes.data_as(_I), _p(o), _p(lse), B, Hq, Hkv, Tq, S, D,
+                               scale)
+    if st:
+        raise ValueError(f"oracle_decode_fwd status {st}")
+    return o, lse

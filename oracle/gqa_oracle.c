@@ -430,6 +430,54 @@ int oracle_varlen_bwd(const double* q, const double* k, const double* v, const d
     return 0;
 }
 
+/* ------------------------------------------------- decode over a KV cache */
+/* Cached attention (the "cached GQA" / per-row-prefix cached attention of the
+ * microLLM-rocm README, section "Why this project exists"): row b holds
+ * cache_lens[b] keys; its Tq queries are the newest Tq positions, so query t
+ * sits at absolute position len_b - Tq + t and sees keys j <= that position
+ * (the causal mask aligned to the end of the cache).
+ * q, o [B,Hq,Tq,D]; k_cache, v_cache [B,Hkv,S,D] (S = cache capacity);
+ * lse [B,Hq,Tq]; lens: host int32 [B], Tq <= lens[b] <= S. */
+int oracle_decode_fwd(const double* q, const double* k, const double* v, const int* lens, double* o, double* lse,
+                      long B, long Hq, long Hkv, long Tq, long S, long D, double scale) {
+    int st = check_shape(Hq, Hkv, D);
+    if (st || B < 0 || Tq < 1 || S < 1) return st ? st : 2;
+    for (long b = 0; b < B; ++b)
+        if (lens[b] < Tq || lens[b] > S) return 5;
+    long G = Hq / Hkv;
+    double* row = (double*)malloc(sizeof(double) * S);
+    if (!row) return 10;
+    for (long b = 0; b < B; ++b)
+        for (long h = 0; h < Hq; ++h) {
+            long g = kv_head(h, G, Hkv), len = lens[b];
+            const double* kh = k + (b * Hkv + g) * S * D;
+            const double* vh = v + (b * Hkv + g) * S * D;
+            for (long t = 0; t < Tq; ++t) {
+                const double* qr = q + ((b * Hq + h) * Tq + t) * D;
+                long last = len - Tq + t;               /* newest visible key */
+                double m = -INFINITY;
+                for (long j = 0; j <= last; ++j) {
+                    double acc = 0.0;
+                    for (long d = 0; d < D; ++d) acc += qr[d] * kh[j * D + d];
+                    row[j] = scale * acc;
+                    if (row[j] > m) m = row[j];
+                }
+                double sum = 0.0;
+                for (long j = 0; j <= last; ++j) sum += exp(row[j] - m);
+                double l = m + log(sum);
+                lse[(b * Hq + h) * Tq + t] = l;
+                double* orow = o + ((b * Hq + h) * Tq + t) * D;
+                for (long d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (long j = 0; j <= last; ++j) acc += exp(row[j] - l) * vh[j * D + d];
+                    orow[d] = acc;
+                }
+            }
+        }
+    free(row);
+    return 0;
+}
+
 int oracle_set_threads(int n) {
 #ifdef _OPENMP
     if (n > 0) omp_set_num_threads(n);

@@ -276,6 +276,29 @@ def pin_rounding_error_terms(lib):
     assert float(np.abs(dk - res["dk"]).max()) > 1e-4    # the case does exercise rounding
 
 
+def pin_decode_is_dense_suffix(lib):
+    """Cached attention of the newest Tq positions equals the last Tq rows of
+    dense causal attention over the row's first cache_lens[b] positions
+    (reduction to the dense oracle), for every row and query head; a cache of
+    one key gives O = V."""
+    r = _rng(11)
+    B, Hq, Hkv, Tq, S, D, scale = 3, 6, 2, 3, 21, 8, 0.3
+    lens = [3, 21, 10]
+    q_full = r.standard_normal((B, Hq, S, D))
+    k = r.standard_normal((B, Hkv, S, D))
+    v = r.standard_normal((B, Hkv, S, D))
+    q = np.stack([q_full[b, :, lens[b] - Tq:lens[b]] for b in range(B)])
+    o, lse = oracle.decode_fwd(q, k, v, lens, scale=scale, lib=lib)
+    for b in range(B):
+        L = lens[b]
+        od, ld = oracle.fwd(q_full[b:b + 1, :, :L], k[b:b + 1, :, :L], v[b:b + 1, :, :L], causal=True, scale=scale,
+                            lib=lib)
+        np.testing.assert_allclose(o[b], od[0, :, L - Tq:L], atol=1e-12)
+        np.testing.assert_allclose(lse[b], ld[0, :, L - Tq:L], atol=1e-12)
+    o1, _ = oracle.decode_fwd(q[:, :, :1], k, v, [1, 1, 1], scale=scale, lib=lib)
+    np.testing.assert_allclose(o1[:, :, 0], np.repeat(v[:, :, 0], Hq // Hkv, axis=1), atol=1e-14)
+
+
 PINS = [pin_hand_worked, pin_rows_sum_to_one, pin_single_token, pin_constant_keys, pin_shift_invariance,
         pin_gqa_equals_repeated_mha, pin_torch_sdpa, pin_finite_differences, pin_delta_identity,
-        pin_varlen_equals_slices, pin_rounding_error_terms]
+        pin_varlen_equals_slices, pin_rounding_error_terms, pin_decode_is_dense_suffix]
