@@ -10,6 +10,13 @@ i.e. 2*B*Hq*T^2*D and 5*B*Hq*T^2*D.
 
 Prints one JSON line.  --impl reference times the fp64 CPU oracle (the only
 reference this method has) on a bounded sample of the same workload.
+
+--workload decode_* measures cached (decode) attention instead: one step is
+one attn_decode_fwd call over a KV cache resident in HBM (larger than L2 for
+the long-context workload, and L2 is flushed before every step anyway); the
+figure is algorithmic HBM bytes per second -- the K and V rows each batch
+row actually holds (cache_lens[b] keys, Hkv heads, D features, bf16) plus Q,
+O, LSE and the lengths -- against the measured copy bandwidth.
 Multi-GPU: each rank runs an independent replica (the path has no exchange
 step); value = all ranks' FLOPs / max over ranks of the timed region.
 """
@@ -170,6 +177,181 @@ def oracle_sample(w: W.Workload, x, budget_s: float, t_prefix: int | None = None
     return done_flops / elapsed, desc, cores, elapsed
 
 
+# ---------------------------------------------------------------- decode
+DECODE_METRIC = "cached GQA decode attention: algorithmic HBM GB/s and % of GB300 copy bandwidth"
+DECODE_UNIT = "GB/s"
+
+
+def decode_bytes(w: W.DecodeWorkload, lens) -> int:
+    """Algorithmic bytes of one decode call: K and V rows inside each row's
+    cache, Q read, O written (bf16), LSE written (f32), the lengths."""
+    kv = 2 * w.Hkv * w.D * 2 * int(torch.as_tensor(lens, dtype=torch.int64).sum())
+    qo = 2 * w.B * w.Hq * w.Tq * w.D * 2
+    return kv + qo + w.B * w.Hq * w.Tq * 4 + w.B * 4
+
+
+def oracle_decode_sample(w: W.DecodeWorkload, x, budget_s: float):
+    """Time the fp64 oracle on whole batch rows of a decode workload until
+    about budget_s seconds (at least one row).  Returns (bytes/s, sample
+    description, cores, seconds)."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    f = lambda t: t.float().numpy().astype(np.float64)
+    done, elapsed, rows = 0, 0.0, 0
+    while rows == 0 or (elapsed < budget_s and rows < w.B):
+        b = rows
+        xb = {"q": x["q"][b:b + 1], "k_cache": x["k_cache"][b:b + 1], "v_cache": x["v_cache"][b:b + 1],
+              "cache_lens": x["cache_lens"][b:b + 1]}
+        args = (f(xb["q"]), f(xb["k_cache"]), f(xb["v_cache"]), xb["cache_lens"].numpy())
+        t0 = time.perf_counter()
+        oracle.decode_fwd(*args, scale=w.softmax_scale)
+        elapsed += time.perf_counter() - t0
+        rows += 1
+        one = W.DecodeWorkload("s", B=1, Hq=w.Hq, Hkv=w.Hkv, Tq=w.Tq, S=w.S, D=w.D, min_len=0, max_len=0)
+        done += decode_bytes(one, xb["cache_lens"])
+    desc = f"{rows} of {w.B} batch rows of {w.name} (whole caches), fp64, {elapsed:.1f} s"
+    return done / elapsed, desc, cores, elapsed
+
+
+def decode_config(w: W.DecodeWorkload, world: int, l2: str):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Tq": w.Tq, "S": w.S, "D": w.D,
+            "cache_lens": f"uniform in [{w.min_len}, {w.max_len}]",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "l2": l2}
+
+
+def run_decode(args, world, rank, local):
+    import causal_gqa_attention_fwd_gb300 as gq
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.DECODE_WORKLOADS[args.workload]
+    x = W.make_decode_inputs(w, seed=rank)
+    stream = torch.cuda.current_stream()
+    q, kc, vc, lens = (x[n].to(dev) for n in ("q", "k_cache", "v_cache", "cache_lens"))
+    scale = w.softmax_scale
+    o, lse = gq.attn_decode_fwd(q, kc, vc, lens, scale=scale)
+    ws_bytes = gq.attn_decode_workspace_size(w.B, w.Hq, w.Hkv, w.Tq, w.S, w.D)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+
+    def step():
+        gq.attn_decode_fwd(q, kc, vc, lens, scale=scale, o=o, lse=lse, workspace=ws)
+
+    nbytes = decode_bytes(w, x["cache_lens"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    assert gq.get_device_status() == 0, "device status after warm-up"
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    gq.profile_reset()
+    gq.profile_enable(True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark(0)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks.mark(1)
+    gq.profile_enable(False)
+    prof = gq.profile_read()
+    clk = clocks.stop()
+    status = gq.get_device_status()
+    total_ms = max_over_ranks(world, sum(a.elapsed_time(b) for a, b in ev))
+    ms_per_step = total_ms / args.steps
+    value = world * nbytes * args.steps / (total_ms / 1e3) / 1e9
+    pk = peaks()
+    n_part, t_part = prof["decode"]
+    part_ms = t_part / max(n_part, 1)
+    achieved = nbytes / (part_ms / 1e3) / 1e9
+    roofline = {"kernel": "decode_partial", "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": measured_traffic(w.name, "decode"),
+                "peak_source": pk["source"] + " (copy bandwidth)", "algorithmic_bytes_per_launch": nbytes}
+
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hl = (x[n].pin_memory() for n in ("q", "k_cache", "v_cache", "cache_lens"))
+        ho, hlse = torch.empty_like(hq).pin_memory(), torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hl))
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hlse))
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            kc.copy_(hk, non_blocking=True)
+            vc.copy_(hv, non_blocking=True)
+            lens.copy_(hl, non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 10))
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_s = max_over_ranks(world, time.perf_counter() - t0)
+        e2e = {"value": world * nbytes * n_e2e / e2e_s / 1e9, "unit": DECODE_UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "note": "the whole KV cache crosses host->device every step"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, desc, cores, el = oracle_decode_sample(w, x, args.cpu_budget)
+        cpu = {"value": rate / 1e9, "unit": DECODE_UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": DECODE_METRIC, "value": value, "unit": DECODE_UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 in, f32 arithmetic", "data": "synthetic",
+            "config": decode_config(w, world, "inputs larger than L2 for decode_long_gqa_s32k; "
+                                              "flushed before every timed step (256 MiB write)"),
+            "frac_of_peak": value / pk["hbm_gbs"],
+            "tokens_per_s": world * w.B * w.Tq * args.steps / (total_ms / 1e3),
+            "kernel_ms": {k: (t / n if n else None) for k, (n, t) in prof.items() if n},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": sum(prof[k][0] for k in prof), "clocks": clk, "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_decode_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = W.DECODE_WORKLOADS[args.workload]
+    x = W.make_decode_inputs(w, seed=0)
+    rates, desc, cores = [], "", 0
+    for _ in range(args.warmup + args.steps):
+        r, desc, cores, el = oracle_decode_sample(w, x, budget_s=0.0)   # one batch row per step
+        rates.append(r)
+    value = statistics.mean(rates[args.warmup:]) / 1e9
+    line = {
+        "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": DECODE_UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": decode_config(w, 1, "n/a (CPU)"),
+        "cpu_baseline": {"value": value, "unit": DECODE_UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": value, "unit": DECODE_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------- main
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -237,13 +419,22 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
+    if args.workload in W.DECODE_WORKLOADS:
+        if args.impl == "reference":
+            run_decode_reference(args, world, rank)
+        else:
+            run_decode(args, world, rank, local)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     if args.impl == "reference":
         run_reference(args, world, rank)
         return

@@ -38,9 +38,11 @@ SIGNATURES = {
     "attn_profile_enable": (_I, [_I]),
     "attn_profile_reset": (_I, []),
     "attn_profile_read": (_I, [_I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)]),
+    "attn_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "attn_decode_fwd": (_I, [_P] * 7 + [_Z, _I, _I, _I, _I, _I, _I, _F, _P]),
 }
 
-PROFILE_KINDS = {"attn_fwd": 0, "bwd_pre": 1, "bwd_main": 2, "bwd_post": 3}
+PROFILE_KINDS = {"attn_fwd": 0, "bwd_pre": 1, "bwd_main": 2, "bwd_post": 3, "decode": 4, "decode_merge": 5}
 
 _lib = None
 
@@ -226,3 +228,32 @@ def attn_varlen_bwd(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: 
                                int(max_seqlen), Hq, Hkv, D, int(causal), _scale(scale, D), _stream(stream))
     _check(st, "attn_varlen_bwd")
     return dq, dk, dv
+
+
+def attn_decode_workspace_size(B, Hq, Hkv, Tq, S, D) -> int:
+    return int(lib().attn_decode_workspace_size(B, Hq, Hkv, Tq, S, D))
+
+
+def attn_decode_fwd(q, k_cache, v_cache, cache_lens, scale=None, o=None, lse=None, workspace=None, stream=None):
+    """Cached (decode) attention.  q [B,Hq,Tq,D]; k_cache, v_cache [B,Hkv,S,D] bf16; cache_lens int32
+    (device) [B], keys held per row including the Tq new ones; query t of row b sees keys
+    j <= cache_lens[b] - Tq + t -> (o [B,Hq,Tq,D] bf16, lse [B,Hq,Tq] f32)."""
+    B, Hq, Tq, D = q.shape
+    Hkv, S = k_cache.shape[1], k_cache.shape[2]
+    if k_cache.shape != (B, Hkv, S, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache, v_cache must be [B, Hkv, S, D] matching q")
+    if cache_lens.shape != (B,):
+        raise ValueError("cache_lens must be [B]")
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws_bytes = attn_decode_workspace_size(B, Hq, Hkv, Tq, S, D)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ws_ptr = _need(workspace, "workspace", torch.uint8) if workspace is not None else None
+    ws_len = workspace.numel() if workspace is not None else 0
+    st = lib().attn_decode_fwd(_need(q, "q"), _need(k_cache, "k_cache"), _need(v_cache, "v_cache"),
+                               _need(cache_lens, "cache_lens", torch.int32), _need(o, "o"),
+                               _need(lse, "lse", torch.float32), ws_ptr, ws_len, B, Hq, Hkv, Tq, S, D,
+                               _scale(scale, D), _stream(stream))
+    _check(st, "attn_decode_fwd")
+    return o, lse

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgqa_attn.so")
 
-SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu"]
+SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_decode.cu"]
 HEADERS = ["sm103.cuh", "kernels.h", "tmap.h"]
 
 NVCC_FLAGS = [

@@ -353,6 +353,125 @@ attn_status attn_varlen_bwd(const void* q, const void* k, const void* v, const v
                     max_seqlen, Hq, Hkv, D, causal, scale, stream, true);
 }
 
+}  // extern "C"
+
+// ------------------------------------------------------ cached (decode) attention
+namespace {
+
+// Work split of the decode kernels; a pure function of the sizes, so the
+// workspace size never depends on the device.  Query rows go in blocks of
+// 4, 8 or 16.  The key range of a (row, K/V head, row block) unit is cut into
+// splits of cps 128-key chunks: at least 2 (one per consumer group of a CTA),
+// enough that the whole problem makes about 8 items per CTA of a 152-SM
+// GPU, and at most kDecodeMaxSplits splits (the merge kernel's limit).
+struct DecodePlan {
+  int R, rb_rows, nrb, n_splits, cps;
+  long n_items;
+};
+
+constexpr long kDecodePlanItems = 152 * 8;
+constexpr long kDecodeMaxSplits = 1024;
+constexpr int kDecodeChunk = 128;
+
+DecodePlan decode_plan(int B, int Hq, int Hkv, int Tq, int S) {
+  DecodePlan p{};
+  p.R = (Hq / Hkv) * Tq;
+  p.rb_rows = p.R <= 4 ? 4 : p.R <= 8 ? 8 : 16;
+  p.nrb = (p.R + p.rb_rows - 1) / p.rb_rows;
+  const long chunks = ((long)S + kDecodeChunk - 1) / kDecodeChunk;
+  const long units = (long)B * Hkv * p.nrb;
+  long cps = (units * chunks + kDecodePlanItems - 1) / kDecodePlanItems;
+  if (cps < 2) cps = 2;
+  const long cps_min = (chunks + kDecodeMaxSplits - 1) / kDecodeMaxSplits;
+  if (cps < cps_min) cps = cps_min;
+  if (cps > chunks) cps = chunks;
+  if (cps < 1) cps = 1;
+  p.cps = (int)cps;
+  p.n_splits = (int)((chunks + cps - 1) / cps);
+  p.n_items = units * p.n_splits;
+  return p;
+}
+
+size_t decode_ws_bytes(int B, int Hkv, const DecodePlan& p, int D) {
+  if (p.n_splits <= 1) return 0;
+  const size_t rows = (size_t)B * Hkv * p.n_splits * p.R;
+  return round_up(rows * D * 4, 256) + rows * 8;
+}
+
+attn_status decode_check(int B, int Hq, int Hkv, int Tq, int S, int D) {
+  if (B < 0 || Tq < 0 || S < 0) return ATTN_ERR_SHAPE;
+  attn_status st = check_heads(Hq, Hkv, D);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || Tq == 0) return ATTN_OK;
+  if (Tq > S) return ATTN_ERR_SHAPE;
+  if ((long)B * Hq * Tq > 0x7fffffffL || (long)B * Hkv > 0x7fffffffL) return ATTN_ERR_SHAPE;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Tq, int S, int D) {
+  if (decode_check(B, Hq, Hkv, Tq, S, D) != ATTN_OK || B == 0 || Tq == 0) return 0;
+  return decode_ws_bytes(B, Hkv, decode_plan(B, Hq, Hkv, Tq, S), D);
+}
+
+attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, const int* cache_lens,
+                            void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                            int Tq, int S, int D, float scale, void* stream) {
+  attn_status st = decode_check(B, Hq, Hkv, Tq, S, D);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || Tq == 0) return ATTN_OK;
+  if (!isfinite(scale)) return ATTN_ERR_SHAPE;
+  if (!q || !k_cache || !v_cache || !cache_lens || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse) ||
+      (reinterpret_cast<uintptr_t>(cache_lens) & 3u))
+    return ATTN_ERR_ALIGN;
+  const DecodePlan p = decode_plan(B, Hq, Hkv, Tq, S);
+  const size_t need = decode_ws_bytes(B, Hkv, p, D);
+  if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return ATTN_ERR_WORKSPACE;
+  if (p.n_items > 0x7fffffffL) return ATTN_ERR_SHAPE;
+  if ((st = check_arch()) != ATTN_OK) return st;
+  int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return ATTN_ERR_CUDA;
+  gqa::DecodeArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.cache_lens = cache_lens;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  if (need > 0) {
+    const size_t rows = (size_t)B * Hkv * p.n_splits * p.R;
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + round_up(rows * D * 4, 256));
+  }
+  a.status = status;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = Hq / Hkv;
+  a.Tq = Tq;
+  a.S = S;
+  a.D = D;
+  a.R = p.R;
+  a.rb_rows = p.rb_rows;
+  a.nrb = p.nrb;
+  a.n_splits = p.n_splits;
+  a.cps = p.cps;
+  a.n_items = (int)p.n_items;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  CUtensorMap tk, tv;
+  if (!map_dense(&tk, k_cache, D, S, (long)B * Hkv) || !map_dense(&tv, v_cache, D, S, (long)B * Hkv))
+    return ATTN_ERR_CUDA;
+  const int grid = (int)(p.n_items < sms ? p.n_items : sms);
+  return launch_status(gqa::launch_attn_decode(tk, tv, a, grid, static_cast<cudaStream_t>(stream)));
+}
+
 // ------------------------------------------------- allocation-free backward
 // Scratch for attn_bwd_noalloc: a file-scope device array, so the library
 // never has to allocate device memory for it.  Every device that loads the
@@ -410,7 +529,7 @@ const char* attn_status_string(attn_status s) {
     case ATTN_ERR_SHAPE: return "invalid sizes (negative, Hq % Hkv != 0, or too large)";
     case ATTN_ERR_HEADDIM: return "head dimension must be 64 or 128";
     case ATTN_ERR_ALIGN: return "a pointer is not 16-byte aligned";
-    case ATTN_ERR_SEQLENS: return "cu_seqlens is invalid";
+    case ATTN_ERR_SEQLENS: return "cu_seqlens or cache_lens is invalid";
     case ATTN_ERR_WORKSPACE: return "workspace is NULL or too small";
     case ATTN_ERR_ARCH: return "the current device is not compute capability 10.3 (sm_103a)";
     case ATTN_ERR_CUDA: return "a CUDA runtime call failed";

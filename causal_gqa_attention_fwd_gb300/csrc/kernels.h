@@ -71,9 +71,40 @@ cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CU
 // Query rows per step of the backward main kernel for head dimension D.
 int bwd_query_block(int D);
 
+// Cached (decode) attention.  Q, O [B,Hq,Tq,D]; K/V cache [B,Hkv,S,D];
+// LSE [B,Hq,Tq]; cache_lens [B].  The R = G*Tq query rows of a (row, K/V
+// head) pair are processed in blocks of rb_rows (4, 8 or 16; nrb blocks);
+// the key range is cut into n_splits splits of cps 128-key chunks.  With
+// n_splits > 1 the partial kernel writes unnormalised partials to ws_o /
+// ws_ml ([B*Hkv][n_splits][R]) and a merge kernel produces O and LSE.
+struct DecodeArgs {
+  const __nv_bfloat16* q;
+  const int* cache_lens;  // device
+  __nv_bfloat16* o;
+  float* lse;
+  float* ws_o;            // [B*Hkv*n_splits*R, D] f32
+  float2* ws_ml;          // [B*Hkv*n_splits*R] (max in log2 units, sum)
+  int* status;
+  int B, Hq, Hkv, G, Tq, S, D, R;
+  int rb_rows, nrb, n_splits, cps, n_items;
+  float scale_log2;
+};
+
+// k, v: dense maps over the caches ([B*Hkv, S, D], 64 x 128 boxes).
+cudaError_t launch_attn_decode(const CUtensorMap& k, const CUtensorMap& v, const DecodeArgs& a, int grid,
+                               cudaStream_t stream);
+
 // Kernel-level timing (opt-in instrumentation, api.cu): event pairs recorded
 // on the launch stream around each kernel.
-enum ProfKind { kProfFwd = 0, kProfBwdPre = 1, kProfBwdMain = 2, kProfBwdPost = 3, kProfKinds = 4 };
+enum ProfKind {
+  kProfFwd = 0,
+  kProfBwdPre = 1,
+  kProfBwdMain = 2,
+  kProfBwdPost = 3,
+  kProfDecode = 4,
+  kProfDecodeMerge = 5,
+  kProfKinds = 6
+};
 void prof_begin(int kind, cudaStream_t s);
 void prof_end(cudaStream_t s);
 

@@ -10,6 +10,13 @@ V, dO.
 The five workloads are shaped after the models the pages train: a tiny GQA
 check, a Qwen3-0.6B-shaped layer, a GPT-2-small-shaped MHA layer, a long
 context GQA layer (T = 4096, D = 128) and a packed variable-length batch.
+
+The cached (decode) workloads put Tq new query positions per batch row
+against a KV cache of capacity S holding cache_lens[b] keys: two are shaped
+after the steady-decode rows the microLLM-rocm README reports (context 2048,
+batch 8, Qwen2.5-0.5B and DeepSeek-R1-Distill-Qwen-1.5B attention shapes),
+one is a long-context GQA cache larger than the L2 cache (per-row lengths
+drawn between S/2 and S).  Draw order: cache lengths, Q, K cache, V cache.
 """
 from __future__ import annotations
 
@@ -52,6 +59,36 @@ WORKLOADS = {
 }
 
 HEADLINE = "long_gqa_t4096"
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Tq: int
+    S: int                  # cache capacity (keys per row)
+    D: int
+    min_len: int            # cache_lens drawn uniformly in [min_len, max_len]
+    max_len: int
+    scale: float = field(default=0.0)
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale else 1.0 / math.sqrt(self.D)
+
+
+DECODE_WORKLOADS = {
+    "decode_qwen25_0p5b_t2048_b8": DecodeWorkload("decode_qwen25_0p5b_t2048_b8", B=8, Hq=14, Hkv=2, Tq=1,
+                                                  S=2048, D=64, min_len=2048, max_len=2048),
+    "decode_r1distill_1p5b_t2048_b8": DecodeWorkload("decode_r1distill_1p5b_t2048_b8", B=8, Hq=12, Hkv=2, Tq=1,
+                                                     S=2048, D=128, min_len=2048, max_len=2048),
+    "decode_long_gqa_s32k": DecodeWorkload("decode_long_gqa_s32k", B=8, Hq=32, Hkv=8, Tq=1, S=32768, D=128,
+                                           min_len=16384, max_len=32768),
+}
+
+DECODE_HEADLINE = "decode_long_gqa_s32k"
 
 
 def _randn(g, shape, std=1.0):
@@ -99,3 +136,23 @@ def make_inputs(w: Workload, seed=0):
         return varlen_inputs(lengths, w.Hq, w.Hkv, w.D, q_std=w.q_std, g=g)
     return dense_inputs(w.B, w.Hq, w.Hkv, w.T, w.D, seed=seed, q_std=w.q_std)
 
+
+
+def decode_inputs(B, Hq, Hkv, Tq, S, D, cache_lens=None, min_len=None, max_len=None, seed=0):
+    """q [B,Hq,Tq,D], k_cache/v_cache [B,Hkv,S,D] bf16 and cache_lens int32 [B], CPU.  The whole
+    cache (rows past each length too) is drawn, so a kernel that reads past a row's length sees
+    finite, wrong keys rather than zeros."""
+    g = torch.Generator().manual_seed(seed)
+    if cache_lens is None:
+        lo = Tq if min_len is None else min_len
+        hi = S if max_len is None else max_len
+        cache_lens = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64)
+    lens = torch.as_tensor(cache_lens, dtype=torch.int32)
+    q = _randn(g, (B, Hq, Tq, D))
+    k = _randn(g, (B, Hkv, S, D))
+    v = _randn(g, (B, Hkv, S, D))
+    return dict(q=q, k_cache=k, v_cache=v, cache_lens=lens)
+
+
+def make_decode_inputs(w: DecodeWorkload, seed=0):
+    return decode_inputs(w.B, w.Hq, w.Hkv, w.Tq, w.S, w.D, min_len=w.min_len, max_len=w.max_len, seed=seed)

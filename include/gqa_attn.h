@@ -62,7 +62,7 @@ typedef enum {
     ATTN_ERR_SHAPE = 2,      /* negative size, Hq % Hkv != 0, Hq/Hkv < 1, size too large */
     ATTN_ERR_HEADDIM = 3,    /* D not 64 or 128 */
     ATTN_ERR_ALIGN = 4,      /* a pointer is not 16-byte aligned */
-    ATTN_ERR_SEQLENS = 5,    /* cu_seqlens invalid (device-detected: status word) */
+    ATTN_ERR_SEQLENS = 5,    /* cu_seqlens / cache_lens invalid (device-detected: status word) */
     ATTN_ERR_WORKSPACE = 6,  /* workspace NULL or smaller than the *_workspace_size() value */
     ATTN_ERR_ARCH = 7,       /* current device is not compute capability 10.3 */
     ATTN_ERR_CUDA = 8,       /* a CUDA runtime call failed (launch, tensor map, attribute) */
@@ -128,6 +128,36 @@ GQA_ATTN_API attn_status attn_varlen_bwd(const void* q, const void* k, const voi
                             size_t workspace_bytes, const int* cu_seqlens, int num_seqs, int total_tokens,
                             int max_seqlen, int Hq, int Hkv, int D, int causal, float scale, void* stream);
 
+/* Cached (decode) attention: the newest Tq positions of each batch row
+ * attend to that row's KV cache -- the cached GQA / per-row-prefix cached
+ * attention and KV-cache decode of the microLLM-rocm README (section "Why
+ * this project exists"), with the forward's mathematics above restricted to
+ * Tq query rows per sequence:
+ *
+ *   row b holds n_b = cache_lens[b] keys (the Tq new ones included); query
+ *   t (0 <= t < Tq) of row b is position n_b - Tq + t and sees the keys
+ *   j <= n_b - Tq + t of its own row (the causal mask aligned to the end of
+ *   the cache); query head h reads K/V head h / (Hq / Hkv).
+ *
+ * Layouts (device pointers, 16-byte aligned, densely packed):
+ *   q, o      bf16 [B, Hq, Tq, D]     (the new queries, the output)
+ *   k_cache,
+ *   v_cache   bf16 [B, Hkv, S, D]     (S = cache capacity; rows past n_b are
+ *                                      never used and may hold anything)
+ *   lse       float32 [B, Hq, Tq]     (natural log)
+ *   cache_lens DEVICE int32 [B], Tq <= cache_lens[b] <= S.  A row outside
+ *             that range is reported through the device status word
+ *             (ATTN_ERR_SEQLENS) and its outputs are left unwritten.
+ * workspace: attn_decode_workspace_size() bytes, 256-byte aligned, no
+ * initialisation needed; the size is 0 (workspace may be NULL) when the
+ * key range is not split.  Limits: Tq <= S; B*Hq*Tq < 2^31. */
+GQA_ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Tq, int S, int D);
+
+GQA_ATTN_API attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
+                                         const int* cache_lens, void* o, float* lse, void* workspace,
+                                         size_t workspace_bytes, int B, int Hq, int Hkv, int Tq, int S, int D,
+                                         float scale, void* stream);
+
 /* Static description of a status code. */
 GQA_ATTN_API const char* attn_status_string(attn_status status);
 
@@ -149,7 +179,8 @@ GQA_ATTN_API attn_status attn_selftest_wait_timeout(int limit_ms, void* stream);
  * kernel launch is bracketed by a CUDA event pair recorded on the caller's
  * stream.  attn_profile_read synchronises those events and returns, for one
  * kernel kind (0 forward, 1 backward preprocess, 2 backward main,
- * 3 backward dQ conversion), the number of launches and their summed device
+ * 3 backward dQ conversion, 4 decode partial, 5 decode split merge), the
+ * number of launches and their summed device
  * time in milliseconds since the last attn_profile_reset.  At most 65536
  * launches are recorded between resets.  Off by default. */
 GQA_ATTN_API attn_status attn_profile_enable(int enable);

@@ -139,3 +139,46 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         _binding.lib()
+
+
+def dec(lib, *, ptrs=(A,) * 7, ws_bytes=1 << 40, B=1, Hq=4, Hkv=2, Tq=1, S=4096, D=64, scale=0.125):
+    return lib.attn_decode_fwd(*ptrs, ws_bytes, B, Hq, Hkv, Tq, S, D, scale, None)
+
+
+def test_decode_validation(lib):
+    assert dec(lib, Tq=5, S=4) == 2                        # more new queries than the cache holds
+    assert dec(lib, Hq=6, Hkv=4) == 2
+    assert dec(lib, D=96) == 3
+    assert dec(lib, B=-1) == 2
+    assert dec(lib, scale=float("inf")) == 2
+    p = list((A,) * 7)
+    p[3] = NULL                                            # cache_lens
+    assert dec(lib, ptrs=tuple(p)) == 1
+    p = list((A,) * 7)
+    p[1] = A + 8                                           # k_cache misaligned
+    assert dec(lib, ptrs=tuple(p)) == 4
+    p = list((A,) * 7)
+    p[3] = A + 2                                           # cache_lens not 4-byte aligned
+    assert dec(lib, ptrs=tuple(p)) == 4
+    p = list((A,) * 7)
+    p[6] = NULL                                            # workspace needed (split key range)
+    assert dec(lib, ptrs=tuple(p)) == 6
+    assert dec(lib, ws_bytes=64) == 6
+    assert dec(lib, ptrs=(NULL,) * 7, B=0) == 0
+    assert dec(lib, ptrs=(NULL,) * 7, Tq=0) == 0
+
+
+def test_decode_workspace_size(lib):
+    # 32 chunks of 128 keys, two (row, K/V head) units: 2 chunks per split (the
+    # minimum) -> 16 splits; R = G * Tq = 2 rows: f32 partial O + (max, sum) pairs
+    rows = 1 * 2 * 16 * 2
+    assert lib.attn_decode_workspace_size(1, 4, 2, 1, 4096, 64) == rows * 64 * 4 + rows * 8
+    assert lib.attn_decode_workspace_size(4, 8, 2, 1, 256, 128) == 0      # two chunks: no split
+    assert lib.attn_decode_workspace_size(64, 32, 32, 1, 8192, 64) == 0   # 2048 units: one split each
+    # long context: 64 units x 256 chunks -> 14 chunks per split, 19 splits; R = 4
+    rows = 8 * 8 * 19 * 4
+    assert lib.attn_decode_workspace_size(8, 32, 8, 1, 32768, 128) == rows * 128 * 4 + rows * 8
+    # 2^20 keys in one unit: splits capped at 1024
+    rows = 1 * 1 * 1024 * 1
+    assert lib.attn_decode_workspace_size(1, 1, 1, 1, 1 << 20, 64) == rows * 64 * 4 + rows * 8
+    assert lib.attn_decode_workspace_size(1, 4, 2, 1, 4096, 80) == 0       # invalid D
