@@ -358,43 +358,36 @@ attn_status attn_varlen_bwd(const void* q, const void* k, const void* v, const v
 // ------------------------------------------------------ cached (decode) attention
 namespace {
 
-// Work split of the decode kernels; a pure function of the sizes, so the
+// Work layout of the decode kernels; a pure function of the sizes, so the
 // workspace size never depends on the device.  Query rows go in blocks of
-// 4, 8 or 16.  The key range of a (row, K/V head, row block) unit is cut into
-// splits of cps 128-key chunks: at least 2 (one per consumer group of a CTA),
-// enough that the whole problem makes about 8 items per CTA of a 152-SM
-// GPU, and at most kDecodeMaxSplits splits (the merge kernel's limit).
+// 16 (the N of the kernel's MMAs); a (batch row, K/V head, row block) is a
+// unit.  The kernel's CTAs (at most gqa::kDecodeMaxSlots) share the units'
+// 128-key chunks evenly, so a unit of n chunks is cut into at most
+// min(n, CTAs) pieces: the workspace holds that many partials per unit.
 struct DecodePlan {
-  int R, rb_rows, nrb, n_splits, cps;
-  long n_items;
+  int R, nrb, slots, rows_ws;
+  long units;
 };
 
-constexpr long kDecodePlanItems = 152 * 8;
-constexpr long kDecodeMaxSplits = 1024;
 constexpr int kDecodeChunk = 128;
+constexpr int kDecodeRows = 16;
 
 DecodePlan decode_plan(int B, int Hq, int Hkv, int Tq, int S) {
   DecodePlan p{};
   p.R = (Hq / Hkv) * Tq;
-  p.rb_rows = p.R <= 4 ? 4 : p.R <= 8 ? 8 : 16;
-  p.nrb = (p.R + p.rb_rows - 1) / p.rb_rows;
+  p.nrb = (p.R + kDecodeRows - 1) / kDecodeRows;
+  p.rows_ws = p.R < kDecodeRows ? p.R : kDecodeRows;
+  p.units = (long)B * Hkv * p.nrb;
   const long chunks = ((long)S + kDecodeChunk - 1) / kDecodeChunk;
-  const long units = (long)B * Hkv * p.nrb;
-  long cps = (units * chunks + kDecodePlanItems - 1) / kDecodePlanItems;
-  if (cps < 2) cps = 2;
-  const long cps_min = (chunks + kDecodeMaxSplits - 1) / kDecodeMaxSplits;
-  if (cps < cps_min) cps = cps_min;
-  if (cps > chunks) cps = chunks;
-  if (cps < 1) cps = 1;
-  p.cps = (int)cps;
-  p.n_splits = (int)((chunks + cps - 1) / cps);
-  p.n_items = units * p.n_splits;
+  p.slots = (int)(chunks < gqa::kDecodeMaxSlots ? chunks : gqa::kDecodeMaxSlots);
   return p;
 }
 
-size_t decode_ws_bytes(int B, int Hkv, const DecodePlan& p, int D) {
-  if (p.n_splits <= 1) return 0;
-  const size_t rows = (size_t)B * Hkv * p.n_splits * p.R;
+// Workspace: f32 partial O [units][slots][rows_ws][D] and (max, sum) pairs
+// [units][slots][rows_ws], 256-byte aligned; none when no unit can be cut.
+size_t decode_ws_bytes(const DecodePlan& p, int D) {
+  if (p.slots <= 1) return 0;
+  const size_t rows = (size_t)p.units * p.slots * p.rows_ws;
   return round_up(rows * D * 4, 256) + rows * 8;
 }
 
@@ -405,6 +398,8 @@ attn_status decode_check(int B, int Hq, int Hkv, int Tq, int S, int D) {
   if (B == 0 || Tq == 0) return ATTN_OK;
   if (Tq > S) return ATTN_ERR_SHAPE;
   if ((long)B * Hq * Tq > 0x7fffffffL || (long)B * Hkv > 0x7fffffffL) return ATTN_ERR_SHAPE;
+  const DecodePlan p = decode_plan(B, Hq, Hkv, Tq, S);
+  if (p.units * ((S + 127L) / 128) > 0x7fffffffL) return ATTN_ERR_SHAPE;  // chunk stream indices
   return ATTN_OK;
 }
 
@@ -414,7 +409,7 @@ extern "C" {
 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Tq, int S, int D) {
   if (decode_check(B, Hq, Hkv, Tq, S, D) != ATTN_OK || B == 0 || Tq == 0) return 0;
-  return decode_ws_bytes(B, Hkv, decode_plan(B, Hq, Hkv, Tq, S), D);
+  return decode_ws_bytes(decode_plan(B, Hq, Hkv, Tq, S), D);
 }
 
 attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, const int* cache_lens,
@@ -429,10 +424,9 @@ attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_ca
       (reinterpret_cast<uintptr_t>(cache_lens) & 3u))
     return ATTN_ERR_ALIGN;
   const DecodePlan p = decode_plan(B, Hq, Hkv, Tq, S);
-  const size_t need = decode_ws_bytes(B, Hkv, p, D);
+  const size_t need = decode_ws_bytes(p, D);
   if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return ATTN_ERR_WORKSPACE;
-  if (p.n_items > 0x7fffffffL) return ATTN_ERR_SHAPE;
   if ((st = check_arch()) != ATTN_OK) return st;
   int* status = status_word();
   if (!status) return ATTN_ERR_CUDA;
@@ -446,7 +440,7 @@ attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_ca
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
   if (need > 0) {
-    const size_t rows = (size_t)B * Hkv * p.n_splits * p.R;
+    const size_t rows = (size_t)p.units * p.slots * p.rows_ws;
     a.ws_o = static_cast<float*>(workspace);
     a.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + round_up(rows * D * 4, 256));
   }
@@ -459,17 +453,21 @@ attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_ca
   a.S = S;
   a.D = D;
   a.R = p.R;
-  a.rb_rows = p.rb_rows;
   a.nrb = p.nrb;
-  a.n_splits = p.n_splits;
-  a.cps = p.cps;
-  a.n_items = (int)p.n_items;
+  a.slots = p.slots;
+  a.rows_ws = p.rows_ws;
+  // one CTA per SM (the kernel holds most of an SM's shared memory), never
+  // more than the workspace has slots for
+  a.ctas = sms < gqa::kDecodeMaxSlots ? sms : gqa::kDecodeMaxSlots;
   a.scale_log2 = scale * 1.4426950408889634f;
-  CUtensorMap tk, tv;
-  if (!map_dense(&tk, k_cache, D, S, (long)B * Hkv) || !map_dense(&tv, v_cache, D, S, (long)B * Hkv))
+  CUtensorMap tk, tv, tq;
+  const uint64_t qdims[2] = {(uint64_t)D, (uint64_t)B * Hq * Tq};
+  const uint64_t qstrides[1] = {(uint64_t)D * 2};
+  const uint32_t qbox[2] = {64, (uint32_t)kDecodeRows};
+  if (!map_dense(&tk, k_cache, D, S, (long)B * Hkv) || !map_dense(&tv, v_cache, D, S, (long)B * Hkv) ||
+      !gqa::make_tmap(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qdims, qstrides, qbox, CU_TENSOR_MAP_SWIZZLE_128B))
     return ATTN_ERR_CUDA;
-  const int grid = (int)(p.n_items < sms ? p.n_items : sms);
-  return launch_status(gqa::launch_attn_decode(tk, tv, a, grid, static_cast<cudaStream_t>(stream)));
+  return launch_status(gqa::launch_attn_decode(tk, tv, tq, a, a.ctas, static_cast<cudaStream_t>(stream)));
 }
 
 // ------------------------------------------------- allocation-free backward

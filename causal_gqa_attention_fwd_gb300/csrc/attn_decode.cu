@@ -6,25 +6,43 @@
 // of the cache).  This is the cached GQA / per-row-prefix cached attention of
 // the microLLM-rocm README, section "Why this project exists" (KV-cache
 // decode for batch rows B1/2/4/8).  A few query rows meet a long stream of
-// keys, so the work is bound by reading the cache from HBM; it runs on the
-// CUDA cores, and the design is about keeping that stream full:
+// keys: the kernel has to keep the HBM stream full, and with G query heads
+// per K/V head it does G flops per cache byte, more than the CUDA cores
+// sustain next to that stream -- so both contractions run on tcgen05 with
+// the long side (128 keys, or the D features) as M and the query rows as N:
 //
-//   decode_partial  persistent, one CTA per SM.  Work items are (batch row,
-//     K/V head, block of <= 16 query rows, split of the key range); a CTA
-//     takes items blockIdx.x, blockIdx.x + gridDim.x, ...  Warp 8 is the
-//     producer: it TMA-loads 128-key K/V chunks (128-byte swizzled boxes)
-//     into a ring of stages, running ahead across item boundaries, and
-//     stages each item's query rows in shared memory as f32.  Warps 0-7 are
-//     consumers in two groups that take alternate chunks; inside a group,
-//     warp w owns keys [32w, 32w+32) of the chunk.  Per chunk a warp scores
-//     its keys (lane = key) against every query row of the block, updates
-//     its own running max / sum (log2 units), writes the probabilities to a
-//     warp-private buffer and accumulates P V with each lane owning 2 (or 4)
-//     output features.  At the end of an item the eight warps' states are
-//     combined in the stage that held the item's last chunk and written
-//     out: the final O / LSE when the key range is not split, else an
-//     unnormalised partial with its max and sum.
-//   decode_merge  combines a row's splits with the usual rescaling.
+//   S^T[key][row]  = sum_d K[key][d] Q[row][d]          (M = 128 keys, N = 16)
+//   O^T[d][row]   += sum_key V[key][d] P[row][key]       (M = 128 features, N = 16)
+//
+// decode_partial  persistent, one CTA per SM.  The work is a stream of
+//   128-key chunks: unit by unit (batch row, K/V head, block of 16 query
+//   rows), each unit's chunks in key order.  CTA c takes the contiguous
+//   share [c*C/G, (c+1)*C/G) of the C chunks, so every CTA streams the same
+//   number of chunks whatever the rows' lengths.  A share cuts units into
+//   pieces; a unit processed as one piece writes O / LSE, the pieces of a
+//   cut unit write partials that decode_merge combines.
+//   Roles (256 threads):
+//   warp 0     producer: TMA-loads the share's 128-key K chunks (128-byte
+//              swizzled boxes) into the K ring, running ahead across pieces,
+//              and each piece's 16 query rows (a K-major swizzled tile).
+//   warp 6     producer of the V ring.  K and V have rings of their own: a
+//              K chunk is released as soon as its score MMA is done, a V
+//              chunk only after P V, so K refills run further ahead.
+//   warp 1     score MMA issuer (S^T into a double buffer, so the softmax of
+//              one chunk overlaps the score MMA of the next); TMEM owner.
+//   warp 7     P V MMA issuer: O^T += V^T P^T as soon as a chunk's P and V
+//              are ready, independently of the score issuer.
+//   warps 2-5  softmax: thread = key for S^T (and = feature for O^T); row
+//              maxima cross the four warps through shared memory; P (bf16)
+//              goes to a K-major swizzled tile; O^T is rescaled lazily, only
+//              when a row's maximum grows by more than 2^8; at the end of an
+//              item they write O / LSE (unsplit key range) or an unnormalised
+//              partial with its max and sum.
+// TMEM: S^T buffers at columns 0 and 16, O^T buffers at 32 and 48.
+//
+// decode_merge  combines the pieces of a cut unit with the usual rescaling;
+//   it is launched as a programmatic dependent of decode_partial, so its
+//   launch overlaps the partial kernel's tail.
 #include "sm103.cuh"
 #include "kernels.h"
 
@@ -32,57 +50,193 @@ namespace gqa {
 
 namespace {
 
-constexpr int kCK = 128;          // keys per chunk (rows of one TMA box)
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kBoxBytes = kCK * 128;  // one 64-feature x 128-key bf16 box
+constexpr int kCK = 128;                  // keys per chunk (rows of one TMA box; M of the score MMA)
+constexpr int kRows = 16;                 // query rows per piece (N of both MMAs)
+constexpr int kBoxBytes = kCK * 128;      // 64 features x 128 keys, bf16
+constexpr int kRowBoxBytes = kRows * 128; // 64 features (or keys) x 16 rows, bf16
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 64;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D, int RB>
+template <int D>
 struct DecCfg {
-  static constexpr int kChunkBytes = 2 * (D / 64) * kBoxBytes;  // K then V
-  static constexpr int kStages = D == 128 ? 3 : 6;
-  static constexpr int kOffQ = kStages * kChunkBytes;          // f32 [2][RB][D]
-  static constexpr int kOffP = kOffQ + 2 * RB * D * 4;          // f32 [8 warps][32][RB]
-  static constexpr int kOffML = kOffP + kConsumerWarps * 32 * RB * 4;  // float2 [8][RB]
-  static constexpr int kSmemBytes = kOffML + kConsumerWarps * RB * 8 + 1024;  // + alignment slack
-  static_assert(kConsumerWarps * RB * D * 4 <= kChunkBytes, "item combine must fit in one stage");
-  static_assert(kSmemBytes + 256 <= 232448, "shared memory");
+  static constexpr int NB = D / 64;                       // 64-feature boxes per K or V chunk
+  static constexpr int kTileBytes = NB * kBoxBytes;       // one K or V chunk
+  static constexpr int kSlots = D == 128 ? 3 : 6;          // per ring (K ring, then V ring)
+  static constexpr int kOffV = kSlots * kTileBytes;
+  static constexpr int kQBytes = NB * kRowBoxBytes;       // 16 query rows, K-major
+  static constexpr int kPBytes = 2 * kRowBoxBytes;        // 16 rows x 128 keys, K-major
+  static constexpr int kOffQ = 2 * kSlots * kTileBytes;
+  static constexpr int kOffP = kOffQ + 2 * kQBytes;
+  static constexpr int kOffMax = kOffP + 2 * kPBytes;           // f32 [2][16 rows][4 warps]
+  static constexpr int kOffSum = kOffMax + 2 * kRows * 4 * 4;   // f32 [16 rows][4 warps]
+  static constexpr int kOffFin = kOffSum + kRows * 4 * 4;       // float2 [2 pieces][16 rows]: (max, sum)
+  static constexpr int kSmemBytes = kOffFin + 2 * kRows * 8 + 1024;  // + alignment slack
+  static constexpr uint32_t kIdescS = idesc_bf16(kCK, kRows, false, false);
+  static constexpr uint32_t kIdescO = idesc_bf16(128, kRows, true, false);
+  // V^T as an MN-major A operand of 128 rows: the second 64-feature atom is
+  // the second box (D = 128) or the first one again (D = 64; rows 64-127 of
+  // O^T are then a copy and are never read).
+  static constexpr uint32_t kLboV = D == 128 ? kBoxBytes : 0;
+  static_assert(kSmemBytes + 512 <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ uint32_t col_s(int b) { return (uint32_t)b * kRows; }
+__device__ __forceinline__ uint32_t col_o(int b) { return 32u + (uint32_t)b * kRows; }
+
+// One piece: a run of a unit's chunks inside one CTA's share.
+struct Piece {
+  int u, b, hkv, bh;
+  int r0, rows;       // query rows [r0, r0 + rows) of the group's R rows
+  int len;            // keys in the row's cache
+  int kbeg, nch;      // first key of the piece, chunks in it
+  int slot, npieces;  // piece index within its unit, pieces of the unit
 };
 
 struct __align__(8) DecBarriers {
-  uint64_t full[6];
-  uint64_t empty[6];
-  uint64_t qfull[2];
-  uint64_t qempty[2];
+  uint64_t k_full[6], k_empty[6];
+  uint64_t v_full[6], v_empty[6];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full[2], p_empty[2];
+  uint64_t o_full[2], o_empty[2];
+  uint64_t teardown[2];
+  uint32_t tmem_base;
   int abort;
 };
 
-// One work item, decoded identically by the producer and every consumer.
-struct Item {
-  int bh, b, hkv, rb, split;
-  int r0, rows;       // query rows [r0, r0 + rows) of the group's R rows
-  int len;            // keys in the row's cache
-  int kbeg, nch;      // first key of the split, chunks in it (0: nothing to do)
+constexpr int kLenCache = 1024;  // batch rows whose lengths are kept in shared memory
+
+// Chunks of batch row b's cache: ceil(len / 128), 0 for an invalid length.
+// `lens` is the shared-memory copy of cache_lens (B <= kLenCache) or cache_lens itself.
+__device__ __forceinline__ int row_chunks(const DecodeArgs& a, const int* lens, int b, int& len) {
+  len = lens[b];
+  return (len >= a.Tq && len <= a.S) ? (len + kCK - 1) / kCK : 0;
+}
+
+// The CTA's share of the chunk stream.  The stream holds the chunks of every
+// unit in order (units u = 0, 1, ..., each unit's chunks in key order); of
+// its C chunks, CTA c < G takes [c*C/G, (c+1)*C/G), G = min(CTAs, C) so
+// that no share is empty.
+struct Share {
+  long C;
+  int G;
+  long g0, g1;    // this CTA's share
+  int b0;         // batch row holding chunk g0
+  long P0;        // stream index of row b0's first chunk
 };
 
-__device__ __forceinline__ Item decode_item(const DecodeArgs& a, int item, int RBmax) {
-  Item it;
-  it.bh = item % (a.B * a.Hkv);
-  const int rest = item / (a.B * a.Hkv);
-  it.rb = rest % a.nrb;
-  it.split = rest / a.nrb;
-  it.b = it.bh / a.Hkv;
-  it.hkv = it.bh % a.Hkv;
-  it.r0 = it.rb * RBmax;
-  it.rows = min(RBmax, a.R - it.r0);
-  it.len = a.cache_lens[it.b];
-  it.kbeg = it.split * a.cps * kCK;
-  it.nch = 0;
-  if (it.len >= a.Tq && it.len <= a.S && it.kbeg < it.len) {
-    const int kend = min(it.len, it.kbeg + a.cps * kCK);
-    it.nch = (kend - it.kbeg + kCK - 1) / kCK;
+// The CTA whose share holds stream chunk g.
+__device__ __forceinline__ int owner_of(long g, long C, int G) { return (int)(((g + 1) * G - 1) / C); }
+
+// Position in the CTA's stream of (piece, chunk) pairs; every role walks it.
+struct Cursor {
+  Piece it;
+  int c;      // chunk within the piece
+  int cs;     // chunk index in the CTA's stream
+  int uses;   // pieces before this one
+  bool valid;
+  long g, g1; // stream index of the piece's first chunk; end of the share
+  int b, nb;  // batch row of the piece, chunks per unit of that row
+  long Pb;    // stream index of row b's first chunk
+};
+
+__device__ __forceinline__ void cursor_piece(const DecodeArgs& a, const Share& sh, Cursor& cur) {
+  const int upb = a.Hkv * a.nrb;  // units per batch row
+  const long off = cur.g - cur.Pb;
+  const int k = (int)(off / cur.nb), cu = (int)(off % cur.nb);
+  Piece& p = cur.it;
+  p.b = cur.b;
+  p.u = cur.b * upb + k;
+  p.hkv = k / a.nrb;
+  p.bh = cur.b * a.Hkv + p.hkv;
+  p.r0 = (k % a.nrb) * kRows;
+  p.rows = min(kRows, a.R - p.r0);
+  p.kbeg = cu * kCK;
+  p.nch = (int)min((long)(cur.nb - cu), cur.g1 - cur.g);
+  const long Pu = cur.Pb + (long)k * cur.nb;
+  const int first = owner_of(Pu, sh.C, sh.G);
+  p.slot = (int)blockIdx.x - first;
+  p.npieces = owner_of(Pu + cur.nb - 1, sh.C, sh.G) - first + 1;
+  cur.valid = true;
+}
+
+__device__ __forceinline__ Cursor cursor_begin(const DecodeArgs& a, const Share& sh, const int* lens) {
+  Cursor cur;
+  cur.c = 0;
+  cur.cs = 0;
+  cur.uses = 0;
+  cur.valid = false;
+  cur.g = sh.g0;
+  cur.g1 = sh.g1;
+  if (sh.g0 >= sh.g1) return cur;
+  cur.b = sh.b0;
+  cur.Pb = sh.P0;
+  cur.nb = row_chunks(a, lens, cur.b, cur.it.len);
+  cursor_piece(a, sh, cur);
+  return cur;
+}
+
+__device__ __forceinline__ void cursor_next(const DecodeArgs& a, const Share& sh, const int* lens, Cursor& cur) {
+  ++cur.cs;
+  if (++cur.c < cur.it.nch) return;
+  cur.c = 0;
+  ++cur.uses;
+  cur.g += cur.it.nch;
+  if (cur.g >= cur.g1) {
+    cur.valid = false;
+    return;
   }
-  return it;
+  const long upb = (long)a.Hkv * a.nrb;
+  while (cur.g >= cur.Pb + upb * cur.nb) {  // past row b: next row with chunks
+    cur.Pb += upb * cur.nb;
+    ++cur.b;
+    cur.nb = row_chunks(a, lens, cur.b, cur.it.len);
+  }
+  cursor_piece(a, sh, cur);
+}
+
+// The share of CTA `cta` among G = min(ctas, C): one warp, lengths read
+// through `lens`.  Used by the partial kernel (its own share) and by the
+// merge kernel (to find how many pieces a unit was cut into).
+__device__ Share find_share(const DecodeArgs& a, const int* lens, int cta, int ctas) {
+  const int lane = threadIdx.x & 31;
+  const long upb = (long)a.Hkv * a.nrb;
+  long C = 0;
+  for (int b0 = 0; b0 < a.B; b0 += 32) {
+    int len = 0, n = 0;
+    if (b0 + lane < a.B) n = row_chunks(a, lens, b0 + lane, len);
+    C += upb * (long)__reduce_add_sync(0xffffffffu, (unsigned)n);
+  }
+  Share sh;
+  sh.C = C;
+  sh.G = (int)min((long)ctas, C);
+  sh.g0 = cta < sh.G ? (long)cta * C / sh.G : 0;
+  sh.g1 = cta < sh.G ? (long)(cta + 1) * C / sh.G : 0;
+  sh.b0 = 0;
+  sh.P0 = 0;
+  if (sh.g0 < sh.g1) {
+    long P = 0;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+      int len = 0, n = 0;
+      if (b0 + lane < a.B) n = row_chunks(a, lens, b0 + lane, len);
+      long incl = upb * n;  // inclusive prefix over the 32 rows
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, P + incl > sh.g0);
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        sh.b0 = b0 + l;
+        sh.P0 = P + __shfl_sync(0xffffffffu, incl - upb * n, l);
+        break;
+      }
+      P += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  return sh;
 }
 
 __device__ __forceinline__ float warp_max(float x) {
@@ -91,374 +245,541 @@ __device__ __forceinline__ float warp_max(float x) {
   return r;
 }
 
+// Named barrier over `n` threads that also ORs a predicate across them.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %3, 0;\n\tbar.red.or.pred p, %1, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(n), "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
 }
 
-// bf16 pair (low half = first element) -> two f32 in one 64-bit register pair
-__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t x) {
-  return f2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
-}
-
 }  // namespace
 
-template <int D, int RB>
+// A piece's output (softmax warps, once per piece, out of line): wait for
+// its O^T, read this thread's feature row of it, release the buffer and
+// write O / LSE (one-split unit) or the unnormalised partial and its
+// (max, sum) -- the row statistics wait in shared memory (s_fin).
+template <int D>
+__device__ __noinline__ void decode_write_out(const DecodeArgs& a, const Piece& it, int uses, uint32_t tmem_lane,
+                                              uint64_t* o_full, uint64_t* o_empty, const float2* s_fin, int j,
+                                              const Guard& guard) {
+  const int ob = uses & 1;
+  mbar_wait(&o_full[ob], (uses >> 1) & 1, guard);
+  tc_fence_after();
+  uint32_t ov[kRows];
+  tmem_ld_x16(tmem_lane + col_o(ob), ov);
+  tmem_ld_wait();
+  reg_fence<kRows>(ov);
+  tc_fence_before();
+  mbar_arrive_warp(&o_empty[ob]);
+  if (guard.aborted() || j >= D) return;
+  const bool whole = it.npieces == 1;
+  const long pbase = ((long)it.u * a.slots + it.slot) * a.rows_ws;
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    if (r >= it.rows) break;
+    const int rg = it.r0 + r;  // row within the group: query head rg / Tq, position rg % Tq
+    const float O = __uint_as_float(ov[r]);
+    const float2 ml = s_fin[ob * kRows + r];
+    if (whole) {
+      const long orow = ((long)it.b * a.Hq + (long)it.hkv * a.G) * a.Tq + rg;
+      a.o[orow * D + j] = __float2bfloat16_rn(O / ml.y);
+      if (j == 0) a.lse[orow] = (ml.x + __log2f(ml.y)) * 0.69314718055994531f;
+    } else {
+      a.ws_o[(pbase + r) * D + j] = O;
+      if (j == 0) a.ws_ml[pbase + r] = ml;
+    }
+  }
+}
+
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                          const DecodeArgs a) {
-  using C = DecCfg<D, RB>;
-  constexpr int S = C::kStages;
-  constexpr int NB = D / 64;  // boxes (64 features each) per K or V chunk
-  constexpr int kSU = RB <= 8 ? D / 8 : 2;  // score loop unroll (16-byte K pieces)
-  constexpr int kPU = RB <= 8 ? 4 : 2;      // keys per P V step
+                          const __grid_constant__ CUtensorMap tm_q, const DecodeArgs a) {
+  using C = DecCfg<D>;
+  constexpr int SL = C::kSlots;
+  constexpr int NB = C::NB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* sQ = reinterpret_cast<float*>(smem + C::kOffQ);
-  float* sPall = reinterpret_cast<float*>(smem + C::kOffP);
-  float2* sML = reinterpret_cast<float2*>(smem + C::kOffML);
   __shared__ DecBarriers bars;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Guard guard{&bars.abort, a.status};
+  __shared__ int s_len[kLenCache];
+  const int* lens = a.B <= kLenCache ? s_len : a.cache_lens;
+  __shared__ Share share;
+  if (warp == 0) {
+    // the rows' lengths, kept in shared memory (invalid ones reported once),
+    // then this CTA's share of the chunk stream
+    bool bad = false;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+      if (b0 + lane < a.B) {
+        const int len = a.cache_lens[b0 + lane];
+        if (a.B <= kLenCache) s_len[b0 + lane] = len;
+        bad |= len < a.Tq || len > a.S;
+      }
+    }
+    if (__any_sync(0xffffffffu, bad) && blockIdx.x == 0 && lane == 0) atomicCAS(a.status, 0, kDevBadSeqlens);
+    __syncwarp();
+    const Share sh0 = find_share(a, lens, blockIdx.x, gridDim.x);
+    if (lane == 0) share = sh0;
+  }
   if (threadIdx.x == 0) {
     bars.abort = 0;
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&bars.full[i], 1);
-      mbar_init(&bars.empty[i], 4);              // the four warps of the consuming group
+    for (int i = 0; i < SL; ++i) {
+      mbar_init(&bars.k_full[i], 1);
+      mbar_init(&bars.k_empty[i], 1);
+      mbar_init(&bars.v_full[i], 1);
+      mbar_init(&bars.v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars.qfull[i], 1);
-      mbar_init(&bars.qempty[i], kConsumerWarps);
+      mbar_init(&bars.q_full[i], 1);
+      mbar_init(&bars.q_empty[i], 1);
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.s_empty[i], 4);   // one arrive per softmax warp
+      mbar_init(&bars.p_full[i], 4);
+      mbar_init(&bars.p_empty[i], 1);
+      mbar_init(&bars.o_full[i], 1);
+      mbar_init(&bars.o_empty[i], 4);
     }
+    mbar_init(&bars.teardown[0], 1);
+    mbar_init(&bars.teardown[1], 1);
     fence_barrier_init();
   }
+  if (warp == 1) {
+    tmem_alloc(&bars.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  const uint32_t sbase = smem_u32(smem);
+  // let the merge kernel's CTAs be scheduled; they wait for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------ producer
+  const Share sh = share;
+  auto begin = [&]() { return cursor_begin(a, sh, lens); };
+  auto next = [&](Cursor& cur) { cursor_next(a, sh, lens, cur); };
+
+  if (warp == 0 || warp == 6) {
+    // ============================== producers: warp 0 K chunks and query rows, warp 6 V chunks
+    const bool is_k = warp == 0;
+    const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+    uint64_t* full = is_k ? bars.k_full : bars.v_full;
+    uint64_t* empty = is_k ? bars.k_empty : bars.v_empty;
+    uint8_t* ring = smem + (is_k ? 0 : C::kOffV);
     if (lane == 0) {
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(tm);
+      if (is_k) tma_prefetch_desc(&tm_q);
     }
-    int cs = 0, uses = 0;
-    for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
-      const Item it = decode_item(a, item, RB);
-      if (it.len < a.Tq || it.len > a.S) {
-        if (lane == 0 && it.rb == 0 && it.split == 0 && it.hkv == 0) atomicCAS(a.status, 0, kDevBadSeqlens);
-      }
-      if (it.nch == 0) continue;
-      // query rows of the block -> f32 shared memory (rows past `rows` are zero)
-      const int slot = uses & 1;
-      if (uses >= 2) mbar_wait(&bars.qempty[slot], ((uses >> 1) - 1) & 1, guard);
-      const __nv_bfloat16* qg = a.q + (((long)it.b * a.Hq + (long)it.hkv * a.G) * a.Tq + it.r0) * D;
-      float* sq = sQ + slot * RB * D;
-      for (int idx = lane; idx < RB * D / 8; idx += 32) {
-        const int r = idx / (D / 8);
-        uint4 x = make_uint4(0, 0, 0, 0);
-        if (r < it.rows) x = *reinterpret_cast<const uint4*>(qg + (long)idx * 8);
-        float4 lo, hi;
-        lo.x = __uint_as_float(x.x << 16); lo.y = __uint_as_float(x.x & 0xffff0000u);
-        lo.z = __uint_as_float(x.y << 16); lo.w = __uint_as_float(x.y & 0xffff0000u);
-        hi.x = __uint_as_float(x.z << 16); hi.y = __uint_as_float(x.z & 0xffff0000u);
-        hi.z = __uint_as_float(x.w << 16); hi.w = __uint_as_float(x.w & 0xffff0000u);
-        reinterpret_cast<float4*>(sq)[2 * idx] = lo;
-        reinterpret_cast<float4*>(sq)[2 * idx + 1] = hi;
-      }
-      mbar_arrive_warp(&bars.qfull[slot]);
-      ++uses;
-      // K/V chunks of the item
-      for (int c = 0; c < it.nch; ++c, ++cs) {
-        const int stage = cs % S, fill = cs / S;
-        if (fill >= 1) mbar_wait(&bars.empty[stage], (fill - 1) & 1, guard);
-        if (lane == 0) {
-          uint8_t* dst = smem + stage * C::kChunkBytes;
-          uint64_t* bar = &bars.full[stage];
-          if (guard.aborted()) {
-            mbar_arrive(bar);  // nothing loaded; consumers run on without data and write nothing
-          } else {
-            mbar_expect_tx(bar, C::kChunkBytes);
-            const int y = it.kbeg + c * kCK;
+    int last_fill[SL], last_q[2] = {-1, -1};
 #pragma unroll
-            for (int x = 0; x < NB; ++x) {
-              tma_load_3d(dst + x * kBoxBytes, &tm_k, bar, x * 64, y, it.bh);
-              tma_load_3d(dst + (NB + x) * kBoxBytes, &tm_v, bar, x * 64, y, it.bh);
-            }
+    for (int i = 0; i < SL; ++i) last_fill[i] = -1;
+    int cs = 0;
+    // one piece's loads (and, for K, its query rows)
+    auto load_item = [&](const Piece& it, int uses) {
+      if (is_k) {
+        // the piece's 16 query rows (K-major, 128-byte swizzled, as the score
+        // MMA reads them); rows past it.rows belong to other heads or lie
+        // past the tensor (zero) and only fill unused columns of S^T
+        const int qslot = uses & 1;
+        if (uses >= 2) mbar_wait(&bars.q_empty[qslot], ((uses >> 1) - 1) & 1, guard);
+        if (lane == 0) {
+          if (guard.aborted()) {
+            mbar_arrive(&bars.q_full[qslot]);
+          } else {
+            const int row0 = (it.b * a.Hq + it.hkv * a.G) * a.Tq + it.r0;
+            mbar_expect_tx(&bars.q_full[qslot], C::kQBytes);
+#pragma unroll
+            for (int x = 0; x < NB; ++x)
+              tma_load_2d(smem + C::kOffQ + qslot * C::kQBytes + x * kRowBoxBytes, &tm_q, &bars.q_full[qslot], x * 64,
+                          row0);
+            last_q[qslot] = (uses >> 1) & 1;
           }
         }
         __syncwarp();
       }
+      for (int c = 0; c < it.nch; ++c, ++cs) {
+        const int slot = cs % SL, fill = cs / SL;
+        if (fill >= 1) mbar_wait(&empty[slot], (fill - 1) & 1, guard);
+        if (lane == 0) {
+          uint64_t* bar = &full[slot];
+          if (guard.aborted()) {
+            mbar_arrive(bar);  // nothing loaded; the other roles are on their way out
+          } else {
+            uint8_t* dst = ring + slot * C::kTileBytes;
+            mbar_expect_tx(bar, C::kTileBytes);
+            const int y = it.kbeg + c * kCK;
+#pragma unroll
+            for (int x = 0; x < NB; ++x) tma_load_3d(dst + x * kBoxBytes, tm, bar, x * 64, y, it.bh);
+            last_fill[slot] = fill;
+          }
+        }
+        __syncwarp();
+      }
+    };
+    for (Cursor cur = begin(); cur.valid;) {
+      load_item(cur.it, cur.uses);
+      const int n = cur.it.nch;
+      for (int c = 0; c < n; ++c) next(cur);  // on to the next piece
     }
-    return;
-  }
-
-  // ---------------------------------------------------------------- consumers
-  const int group = warp >> 2, wg = warp & 3;
-  float* sP = sPall + warp * 32 * RB;
-  const int j = 32 * wg + lane;  // this lane's key within a chunk (score phase)
-  int cs = 0, uses = 0;
-  for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
-    const Item it = decode_item(a, item, RB);
-    if (it.nch == 0) continue;
-    const int slot = uses & 1;
-    mbar_wait(&bars.qfull[slot], (uses >> 1) & 1, guard);
-    const float* sq = sQ + slot * RB * D;
-    float m[RB], l[RB];
-    uint64_t o[RB][NB];
-#pragma unroll
-    for (int r = 0; r < RB; ++r) {
-      m[r] = -INFINITY;
-      l[r] = 0.f;
-#pragma unroll
-      for (int x = 0; x < NB; ++x) o[r][x] = 0;
+    // never leave the CTA with copies in flight
+    if (lane == 0) {
+      for (int i = 0; i < SL; ++i)
+        if (last_fill[i] >= 0) mbar_wait_drain(&full[i], (uint32_t)last_fill[i] & 1);
+      for (int i = 0; i < 2; ++i)
+        if (last_q[i] >= 0) mbar_wait_drain(&bars.q_full[i], (uint32_t)last_q[i]);
     }
-    const int last_vis0 = it.len - a.Tq;  // last visible key of a row with t = 0
-
-    for (int c = 0; c < it.nch; ++c) {
-      const int csc = cs + c;
-      if ((csc & 1) != group) continue;
-      const int stage = csc % S;
-      mbar_wait(&bars.full[stage], (csc / S) & 1, guard);
-      const uint8_t* sK = smem + stage * C::kChunkBytes;
-      const uint8_t* sV = sK + NB * kBoxBytes;
-      const int k0 = it.kbeg + c * kCK;
-      const int nvis = min(kCK, it.len - k0);  // keys of the chunk inside the cache
-
-      // scores: lane = key j, all RB rows, f32x2 accumulation
-      uint64_t acc[RB];
+    __syncwarp();
+  } else if (warp == 1) {
+    // ===================== score MMA issuer (warp-uniform, one elected lane issues)
+    for (Cursor cur = begin(); cur.valid; next(cur)) {
+      const int qslot = cur.uses & 1, slot = cur.cs % SL, sb = cur.cs & 1;
+      if (cur.c == 0) mbar_wait(&bars.q_full[qslot], (cur.uses >> 1) & 1, guard);
+      mbar_wait(&bars.k_full[slot], (cur.cs / SL) & 1, guard);
+      if (cur.cs >= 2) mbar_wait(&bars.s_empty[sb], ((cur.cs >> 1) - 1) & 1, guard);
+      tc_fence_after();
+      if (!guard.aborted()) {
+        const uint32_t ka = sbase + slot * C::kTileBytes;
+        const uint32_t qa = sbase + C::kOffQ + qslot * C::kQBytes;
 #pragma unroll
-      for (int r = 0; r < RB; ++r) acc[r] = 0;
-#pragma unroll kSU
-      for (int cc = 0; cc < D / 8; ++cc) {
-        const int box = cc >> 3, ch = cc & 7;
-        const uint4 kx = *reinterpret_cast<const uint4*>(sK + box * kBoxBytes + j * 128 + ((ch ^ (j & 7)) << 4));
-        const uint64_t k01 = bf2_to_f2(kx.x), k23 = bf2_to_f2(kx.y), k45 = bf2_to_f2(kx.z),
-                       k67 = bf2_to_f2(kx.w);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss_warp(tmem + col_s(sb), sdesc_sw128(ka + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                      sdesc_sw128(qa + (kk >> 2) * kRowBoxBytes + (kk & 3) * 32, 16, 1024), C::kIdescS, kk > 0);
+      }
+      tc_commit_warp(&bars.s_full[sb]);
+      tc_commit_warp(&bars.k_empty[slot]);
+      if (cur.c == cur.it.nch - 1) tc_commit_warp(&bars.q_empty[qslot]);
+    }
+    // every issued MMA finishes before TMEM is released
+    tc_commit_warp(&bars.teardown[0]);
+    mbar_wait_drain(&bars.teardown[0], 0);
+  } else if (warp == 7) {
+    // ===================== P V MMA issuer: independent of the score issuer, so
+    // that a V chunk is released as soon as its own P is ready
+    for (Cursor cur = begin(); cur.valid; next(cur)) {
+      const int ob = cur.uses & 1, pb = cur.cs & 1, slot = cur.cs % SL;
+      if (cur.c == 0 && cur.uses >= 2) mbar_wait(&bars.o_empty[ob], ((cur.uses >> 1) - 1) & 1, guard);
+      mbar_wait(&bars.v_full[slot], (cur.cs / SL) & 1, guard);
+      mbar_wait(&bars.p_full[pb], (cur.cs >> 1) & 1, guard);
+      tc_fence_after();
+      if (!guard.aborted()) {
+        const uint32_t va = sbase + C::kOffV + slot * C::kTileBytes;
+        const uint32_t pa = sbase + C::kOffP + pb * C::kPBytes;
 #pragma unroll
-        for (int r = 0; r < RB; ++r) {
-          const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(sq + r * D + cc * 8);
-          const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(sq + r * D + cc * 8 + 4);
-          uint64_t t = acc[r];
-          t = fma2(qa.x, k01, t);
-          t = fma2(qa.y, k23, t);
-          t = fma2(qb.x, k45, t);
-          t = fma2(qb.y, k67, t);
-          acc[r] = t;
+        for (int kk = 0; kk < kCK / 16; ++kk)
+          mma_ss_warp(tmem + col_o(ob), sdesc_sw128(va + kk * 2048, C::kLboV, 1024),
+                      sdesc_sw128(pa + (kk >> 2) * kRowBoxBytes + (kk & 3) * 32, 16, 1024), C::kIdescO,
+                      (cur.c > 0 || kk > 0) ? 1u : 0u);
+      }
+      tc_commit_warp(&bars.p_empty[pb]);
+      tc_commit_warp(&bars.v_empty[slot]);
+      if (cur.c == cur.it.nch - 1) tc_commit_warp(&bars.o_full[ob]);
+    }
+    tc_commit_warp(&bars.teardown[1]);
+    mbar_wait_drain(&bars.teardown[1], 0);
+  } else if (warp >= 2 && warp <= 5) {
+    // ============================================================ softmax
+    const int wq = warp & 3;                  // TMEM lane quarter of this warp
+    const int j = 32 * wq + lane;             // key of the chunk (S^T row) / feature (O^T row)
+    const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
+    float* s_max = reinterpret_cast<float*>(smem + C::kOffMax);
+    float* s_sum = reinterpret_cast<float*>(smem + C::kOffSum);
+    const float sc_log2 = a.scale_log2;
+    float m_used[kRows], lpart[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      m_used[r] = -INFINITY;
+      lpart[r] = 0.f;
+    }
+    float2* s_fin = reinterpret_cast<float2*>(smem + C::kOffFin);
+    bool pend = false;  // a piece whose O / partial is still to be written
+    Piece pend_it;
+    int pend_uses = 0;
+    auto write_out = [&]() {
+      pend = false;
+      decode_write_out<D>(a, pend_it, pend_uses, tmem + lane_off, bars.o_full, bars.o_empty, s_fin, j, guard);
+    };
+    for (Cursor cur = begin(); cur.valid; next(cur)) {
+      const Piece& it = cur.it;
+      const int i = cur.cs, sb = i & 1;
+      if (cur.c == 0) {
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+          m_used[r] = -INFINITY;
+          lpart[r] = 0.f;
         }
       }
-      // online softmax per row over this warp's 32 keys
-      const int kpos = k0 + j;
+      mbar_wait(&bars.s_full[sb], (i >> 1) & 1, guard);
+      tc_fence_after();
+      uint32_t sr[kRows];
+      tmem_ld_x16(tmem + lane_off + col_s(sb), sr);
+      tmem_ld_wait();
+      reg_fence<kRows>(sr);
+      tc_fence_before();
+      mbar_arrive_warp(&bars.s_empty[sb]);
+
+      // mask: key j (position k0 + j) is visible to the row of position t iff
+      // k0 + j <= len - Tq + t; keys at or past len never are.
+      const int k0 = it.kbeg + cur.c * kCK;
+      const int lim0 = it.len - a.Tq - k0;
+      float s[kRows];
 #pragma unroll
-      for (int r = 0; r < RB; ++r) {
-        float lo, hi;
-        f2_split(acc[r], lo, hi);
+      for (int r = 0; r < kRows; ++r) {
         const int t = (it.r0 + r) % a.Tq;
-        const float s = (j < nvis && kpos <= last_vis0 + t) ? (lo + hi) * a.scale_log2 : -INFINITY;
-        const float m_new = fmaxf(m[r], warp_max(s));
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = ex2_approx(m[r] - m_use);
-        const float p = ex2_approx(s - m_use);
-        l[r] = fmaf(l[r], alpha, p);
-        m[r] = m_new;
-        const uint64_t al = f2(alpha, alpha);
-#pragma unroll
-        for (int x = 0; x < NB; ++x) o[r][x] = mul2(o[r][x], al);
-        sP[lane * RB + r] = p;
+        s[r] = j <= lim0 + t ? __uint_as_float(sr[r]) * sc_log2 : -INFINITY;
       }
-      __syncwarp();
-      // O += P V over this warp's keys; lane owns features (2*lane, 2*lane+1) of each box.
-      // kPU keys per step: their shared-memory loads are issued before the FMAs.
-      const int nk = min(32, nvis - 32 * wg);
-      int jj = 0;
-      for (; jj + kPU <= nk; jj += kPU) {
-        uint64_t v2[kPU][NB];
-        float4 p4[kPU][RB / 4];
+      // The maximum in use moves only when a score exceeds it by more than
+      // 2^8 (or at a piece's first chunk): one barrier-reduction tells
+      // whether any of the 128 threads needs that; only then are the chunk's
+      // row maxima exchanged across the four warps.
+      bool over = false;
 #pragma unroll
-        for (int u = 0; u < kPU; ++u) {
-          const int row = 32 * wg + jj + u;
-          const int voff = row * 128 + (((lane >> 2) ^ (row & 7)) << 4) + 4 * (lane & 3);
+      for (int r = 0; r < kRows; ++r) over |= s[r] > m_used[r] + kRescaleThreshold;
+      float alpha[kRows];
+      bool resc = false;
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) alpha[r] = 1.f;
+      if (bar_red_or(1, 128, over)) {
+        float mine = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+          const float mr = warp_max(s[r]);
+          if (lane == r) mine = mr;
+        }
+        float* mxb = s_max + sb * kRows * 4;
+        if (lane < kRows) mxb[lane * 4 + wq] = mine;
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+          const float4 v = *reinterpret_cast<const float4*>(mxb + r * 4);
+          const float mc = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+          if (mc > m_used[r] + kRescaleThreshold) {  // also when m_used is -inf and mc is finite
+            alpha[r] = ex2_approx(m_used[r] - mc);
+            m_used[r] = mc;
+            resc = true;
+          }
+        }
+      }
+      // cache rows at or past len are outside the cache and may hold
+      // anything: zero their V (once it has landed) so that 0 * V stays 0
+      // in the MMA
+      const int nvis = it.len - k0;
+      if (nvis < kCK) {
+        mbar_wait(&bars.v_full[i % SL], (i / SL) & 1, guard);
+        uint8_t* vs = smem + C::kOffV + (i % SL) * C::kTileBytes;
+        if (j >= nvis) {
 #pragma unroll
           for (int x = 0; x < NB; ++x)
-            v2[u][x] = bf2_to_f2(*reinterpret_cast<const uint32_t*>(sV + x * kBoxBytes + voff));
 #pragma unroll
-          for (int r4 = 0; r4 < RB / 4; ++r4) p4[u][r4] = *reinterpret_cast<const float4*>(sP + (jj + u) * RB + 4 * r4);
-        }
-#pragma unroll
-        for (int u = 0; u < kPU; ++u)
-#pragma unroll
-          for (int r4 = 0; r4 < RB / 4; ++r4) {
-            const float pv[4] = {p4[u][r4].x, p4[u][r4].y, p4[u][r4].z, p4[u][r4].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint64_t pp = f2(pv[e], pv[e]);
-#pragma unroll
-              for (int x = 0; x < NB; ++x) o[4 * r4 + e][x] = fma2(pp, v2[u][x], o[4 * r4 + e][x]);
-            }
-          }
-      }
-      for (; jj < nk; ++jj) {
-        const int row = 32 * wg + jj;
-        const int voff = row * 128 + (((lane >> 2) ^ (row & 7)) << 4) + 4 * (lane & 3);
-        uint64_t v2[NB];
-#pragma unroll
-        for (int x = 0; x < NB; ++x)
-          v2[x] = bf2_to_f2(*reinterpret_cast<const uint32_t*>(sV + x * kBoxBytes + voff));
-#pragma unroll
-        for (int r4 = 0; r4 < RB; r4 += 4) {
-          const float4 p4 = *reinterpret_cast<const float4*>(sP + jj * RB + r4);
-          const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint64_t pp = f2(pv[e], pv[e]);
-#pragma unroll
-            for (int x = 0; x < NB; ++x) o[r4 + e][x] = fma2(pp, v2[x], o[r4 + e][x]);
-          }
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<uint4*>(vs + x * kBoxBytes + j * 128 + q * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      __syncwarp();
-      if (c != it.nch - 1) mbar_arrive_warp(&bars.empty[stage]);
-    }
+      // P = 2^(s - m) as bf16 into the K-major swizzled P tile; partial row sums
+      const int pb = i & 1;
+      if (i >= 2) mbar_wait(&bars.p_empty[pb], ((i >> 1) - 1) & 1, guard);
+      uint8_t* pt = smem + C::kOffP + pb * C::kPBytes + (j >> 6) * kRowBoxBytes + (j & 7) * 2;
+      const int pch = (j & 63) >> 3;
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) {
+        const float mu = m_used[r] == -INFINITY ? 0.f : m_used[r];
+        const float pr = ex2_approx(s[r] - mu);
+        lpart[r] = fmaf(lpart[r], alpha[r], pr);
+        *reinterpret_cast<__nv_bfloat16*>(pt + r * 128 + ((pch ^ (r & 7)) << 4)) = __float2bfloat16_rn(pr);
+      }
+      fence_proxy_async_smem();
+      if (resc && cur.c > 0) {
+        // rows whose maximum moved: scale their O^T columns once the previous P V is done
+        const int pp = (i - 1) & 1;
+        mbar_wait(&bars.p_empty[pp], ((i - 1) >> 1) & 1, guard);
+        tc_fence_after();
+        const uint32_t to = tmem + lane_off + col_o(cur.uses & 1);
+        uint32_t ov[kRows];
+        tmem_ld_x16(to, ov);
+        tmem_ld_wait();
+        reg_fence<kRows>(ov);
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) ov[r] = __float_as_uint(__uint_as_float(ov[r]) * alpha[r]);
+        tmem_st_x16(to, ov);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive_warp(&bars.p_full[pb]);
 
-    // ------------------------------------------------ combine the 8 warps
-    const int cs_last = cs + it.nch - 1;
-    float* scratch = reinterpret_cast<float*>(smem + (cs_last % S) * C::kChunkBytes);  // [8][RB][D]
-    named_bar_sync(1, kConsumerWarps * 32);  // every warp is done with the item's chunks
+      if (cur.c == it.nch - 1) {
+        // ---------------------------------------------------- piece end
+        // row sums over the 128 threads' keys; with the maxima in use they go
+        // to shared memory until the piece's O^T is read (write_out)
+        // (recursive halving: 16 shuffles leave lane l with the warp's sum of
+        // row (l >> 1) & 15)
+        float w8[8], w4[4], w2[2];
+        const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2;
 #pragma unroll
-    for (int r = 0; r < RB; ++r) {
-      const float lw = warp_sum(l[r]);
-      if (lane == 0) sML[warp * RB + r] = make_float2(m[r], lw);
+        for (int k = 0; k < 8; ++k)
+          w8[k] = (h16 ? lpart[k + 8] : lpart[k]) + __shfl_xor_sync(0xffffffffu, h16 ? lpart[k] : lpart[k + 8], 16);
 #pragma unroll
-      for (int x = 0; x < NB; ++x)
-        *reinterpret_cast<uint64_t*>(scratch + (warp * RB + r) * D + x * 64 + 2 * lane) = o[r][x];
-    }
-    named_bar_sync(1, kConsumerWarps * 32);
-    const bool single = a.n_splits == 1;
-    for (int e = threadIdx.x; e < it.rows * D; e += kConsumerWarps * 32) {
-      const int r = e / D, d = e % D;
-      float M = -INFINITY;
+        for (int k = 0; k < 4; ++k)
+          w4[k] = (h8 ? w8[k + 4] : w8[k]) + __shfl_xor_sync(0xffffffffu, h8 ? w8[k] : w8[k + 4], 8);
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sML[w * RB + r].x);
-      const float Mu = M == -INFINITY ? 0.f : M;
-      float L = 0.f, O = 0.f;
+        for (int k = 0; k < 2; ++k)
+          w2[k] = (h4 ? w4[k + 2] : w4[k]) + __shfl_xor_sync(0xffffffffu, h4 ? w4[k] : w4[k + 2], 4);
+        float wsum = (h2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, h2 ? w2[0] : w2[1], 2);
+        wsum += __shfl_xor_sync(0xffffffffu, wsum, 1);
+        if ((lane & 1) == 0) s_sum[((lane >> 1) & 15) * 4 + wq] = wsum;
+        named_bar_sync(1, 128);
+        if (j < kRows) {
+          const float4 v = *reinterpret_cast<const float4*>(s_sum + j * 4);
+          float mj = m_used[0];
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float2 ml = sML[w * RB + r];
-        const float wgt = ex2_approx(ml.x - Mu);
-        L = fmaf(ml.y, wgt, L);
-        O = fmaf(scratch[(w * RB + r) * D + d], wgt, O);
-      }
-      if (guard.aborted()) continue;
-      const int rg = it.r0 + r;  // row within the group: query head (rg / Tq), position t (rg % Tq)
-      if (single) {
-        const long orow = ((long)it.b * a.Hq + (long)it.hkv * a.G) * a.Tq + rg;
-        a.o[orow * D + d] = __float2bfloat16_rn(O / L);
-        if (d == 0) a.lse[orow] = (M + __log2f(L)) * 0.69314718055994531f;
-      } else {
-        const long prow = ((long)it.bh * a.n_splits + it.split) * a.R + rg;
-        a.ws_o[prow * D + d] = O;
-        if (d == 0) a.ws_ml[prow] = make_float2(M, L);
+          for (int r = 1; r < kRows; ++r) mj = j == r ? m_used[r] : mj;
+          s_fin[(cur.uses & 1) * kRows + j] = make_float2(mj, (v.x + v.y) + (v.z + v.w));
+        }
+        named_bar_sync(1, 128);  // s_sum is read (and s_fin written) before anyone goes on
+        // the previous piece's output, deferred to here (a whole piece after
+        // its last P V was issued, so its O^T is ready); its O^T buffer is
+        // needed again only by the next piece
+        if (pend) write_out();
+        pend = true;
+        pend_it = it;
+        pend_uses = cur.uses;
       }
     }
-    fence_proxy_async_smem();  // generic accesses to the stage before the next TMA write into it
-    named_bar_sync(1, kConsumerWarps * 32);
-    if ((cs_last & 1) == group) mbar_arrive_warp(&bars.empty[cs_last % S]);
-    mbar_arrive_warp(&bars.qempty[slot]);
-    cs += it.nch;
-    ++uses;
+    if (pend) write_out();
   }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// One CTA per output row (b, h, t).  Warp 0 turns the splits' (max, sum)
-// pairs into weights 2^(m_s - M) / L in shared memory; then every thread
-// (= feature) sums its weighted partials with independent loads.  Splits
-// that hold no key visible to the row (max = -inf) get weight 0.
-constexpr int kMergeMaxSplits = 1024;
-
+// One CTA per output row (b, h, t) of a cut unit (rows of units processed
+// whole were written by decode_partial).  Warp 0 finds how many pieces the
+// unit was cut into (the partial kernel's share arithmetic, from the
+// lengths) and turns their (max, sum) pairs into weights 2^(m_s - M) / L in
+// shared memory; then every thread (= feature) sums its weighted partials
+// with independent loads.  Pieces that hold no key visible to the row
+// (max = -inf) get weight 0.
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
-  __shared__ float s_w[kMergeMaxSplits];
+  __shared__ float s_w[kDecodeMaxSlots];
   __shared__ float s_lse;
+  __shared__ int s_np;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // decode_partial has finished and its writes are visible
   const int row = blockIdx.x;  // (b * Hq + h) * Tq + t
   const int t = row % a.Tq, bq = row / a.Tq;
   const int h = bq % a.Hq, b = bq / a.Hq;
   const int len = a.cache_lens[b];
   if (len < a.Tq || len > a.S) return;
-  const int bh = b * a.Hkv + h / a.G;
   const int rg = (h % a.G) * a.Tq + t;
-  const int n_act = min(((len + kCK - 1) / kCK + a.cps - 1) / a.cps, kMergeMaxSplits);
-  const float2* ml = a.ws_ml + (long)bh * a.n_splits * a.R + rg;
-  const float* wo = a.ws_o + ((long)bh * a.n_splits * a.R + rg) * a.D;
+  const int k = (h / a.G) * a.nrb + rg / kRows;  // unit within the batch row
+  const int u = b * a.Hkv * a.nrb + k;
+  const long base = (long)u * a.slots * a.rows_ws + rg % kRows;  // (max, sum) of piece s: base + s * rows_ws
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
-    float M = -INFINITY;
-    for (int s = lane; s < n_act; s += 32) M = fmaxf(M, ml[(long)s * a.R].x);
-    M = warp_max(M);
-    float L = 0.f;
-    for (int s = lane; s < n_act; s += 32) {
-      const float2 v = ml[(long)s * a.R];
-      const float w = v.x == -INFINITY ? 0.f : ex2_approx(v.x - M);
-      s_w[s] = w;
-      L = fmaf(v.y, w, L);
+    const long upb = (long)a.Hkv * a.nrb;
+    long C = 0, Pb = 0;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+      int n = 0, lb = 0;
+      if (b0 + lane < a.B) n = row_chunks(a, a.cache_lens, b0 + lane, lb);
+      C += upb * (long)__reduce_add_sync(0xffffffffu, (unsigned)n);
+      Pb += upb * (long)__reduce_add_sync(0xffffffffu, (unsigned)(b0 + lane < b ? n : 0));
     }
-    L = warp_sum(L);
-    const float inv = 1.f / L;
-    for (int s = lane; s < n_act; s += 32) s_w[s] *= inv;
-    if (lane == 0) s_lse = (M + __log2f(L)) * 0.69314718055994531f;
+    const int nb = (len + kCK - 1) / kCK;
+    const long Pu = Pb + (long)k * nb;
+    const int G = (int)min((long)a.ctas, C);
+    const int np = owner_of(Pu + nb - 1, C, G) - owner_of(Pu, C, G) + 1;
+    if (np > 1 && np <= a.slots) {
+      float M = -INFINITY;
+      for (int s = lane; s < np; s += 32) M = fmaxf(M, a.ws_ml[base + (long)s * a.rows_ws].x);
+      M = warp_max(M);
+      float L = 0.f;
+      for (int s = lane; s < np; s += 32) {
+        const float2 v = a.ws_ml[base + (long)s * a.rows_ws];
+        const float w = v.x == -INFINITY ? 0.f : ex2_approx(v.x - M);
+        s_w[s] = w;
+        L = fmaf(v.y, w, L);
+      }
+      L = warp_sum(L);
+      const float inv = 1.f / L;
+      for (int s = lane; s < np; s += 32) s_w[s] *= inv;
+      if (lane == 0) s_lse = (M + __log2f(L)) * 0.69314718055994531f;
+    }
+    if (lane == 0) s_np = np;
   }
   __syncthreads();
+  const int np = s_np;
+  if (np <= 1 || np > a.slots) return;  // one piece: decode_partial wrote the row
+  const long step = (long)a.rows_ws * a.D;
   for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
+    const float* wo = a.ws_o + base * a.D + d;
     float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
     int s = 0;
-    for (; s + 4 <= n_act; s += 4) {
-      const float x0 = wo[(long)s * a.R * a.D + d], x1 = wo[(long)(s + 1) * a.R * a.D + d];
-      const float x2 = wo[(long)(s + 2) * a.R * a.D + d], x3 = wo[(long)(s + 3) * a.R * a.D + d];
+    for (; s + 4 <= np; s += 4) {
+      const float x0 = wo[s * step], x1 = wo[(s + 1) * step], x2 = wo[(s + 2) * step], x3 = wo[(s + 3) * step];
       acc0 = fmaf(x0, s_w[s], acc0);
       acc1 = fmaf(x1, s_w[s + 1], acc1);
       acc2 = fmaf(x2, s_w[s + 2], acc2);
       acc3 = fmaf(x3, s_w[s + 3], acc3);
     }
-    for (; s < n_act; ++s) acc0 = fmaf(wo[(long)s * a.R * a.D + d], s_w[s], acc0);
+    for (; s < np; ++s) acc0 = fmaf(wo[s * step], s_w[s], acc0);
     a.o[(long)row * a.D + d] = __float2bfloat16_rn((acc0 + acc1) + (acc2 + acc3));
   }
   if (threadIdx.x == 0) a.lse[row] = s_lse;
 }
 
-template <int D, int RB>
-static cudaError_t launch_decode_rb(const CUtensorMap& k, const CUtensorMap& v, const DecodeArgs& a, int grid,
-                                    cudaStream_t stream) {
-  using C = DecCfg<D, RB>;
+template <int D>
+static cudaError_t launch_decode_d(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
+                                   const DecodeArgs& a, int grid, cudaStream_t stream) {
+  using C = DecCfg<D>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<D, RB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   prof_begin(kProfDecode, stream);
-  decode_partial_kernel<D, RB><<<grid, kThreads, C::kSmemBytes, stream>>>(k, v, a);
+  decode_partial_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(k, v, q, a);
   prof_end(stream);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || a.n_splits == 1) return e;
+  if (e != cudaSuccess || a.slots <= 1) return e;  // no unit can be cut
+  // programmatic dependent launch: the merge grid may start while the
+  // partial grid drains; it waits (griddepcontrol.wait) before reading
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.B * a.Hq * a.Tq));
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   prof_begin(kProfDecodeMerge, stream);
-  decode_merge_kernel<<<a.B * a.Hq * a.Tq, D, 0, stream>>>(a);
+  e = cudaLaunchKernelEx(&cfg, decode_merge_kernel, a);
   prof_end(stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int D>
-static cudaError_t launch_decode_d(const CUtensorMap& k, const CUtensorMap& v, const DecodeArgs& a, int grid,
-                                   cudaStream_t stream) {
-  if (a.rb_rows == 4) return launch_decode_rb<D, 4>(k, v, a, grid, stream);
-  if (a.rb_rows == 8) return launch_decode_rb<D, 8>(k, v, a, grid, stream);
-  return launch_decode_rb<D, 16>(k, v, a, grid, stream);
-}
-
-cudaError_t launch_attn_decode(const CUtensorMap& k, const CUtensorMap& v, const DecodeArgs& a, int grid,
-                               cudaStream_t stream) {
-  if (a.D == 128) return launch_decode_d<128>(k, v, a, grid, stream);
-  return launch_decode_d<64>(k, v, a, grid, stream);
+cudaError_t launch_attn_decode(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const DecodeArgs& a,
+                               int grid, cudaStream_t stream) {
+  if (a.D == 128) return launch_decode_d<128>(k, v, q, a, grid, stream);
+  return launch_decode_d<64>(k, v, q, a, grid, stream);
 }
 
 }  // namespace gqa

@@ -73,26 +73,33 @@ int bwd_query_block(int D);
 
 // Cached (decode) attention.  Q, O [B,Hq,Tq,D]; K/V cache [B,Hkv,S,D];
 // LSE [B,Hq,Tq]; cache_lens [B].  The R = G*Tq query rows of a (row, K/V
-// head) pair are processed in blocks of rb_rows (4, 8 or 16; nrb blocks);
-// the key range is cut into n_splits splits of cps 128-key chunks.  With
-// n_splits > 1 the partial kernel writes unnormalised partials to ws_o /
-// ws_ml ([B*Hkv][n_splits][R]) and a merge kernel produces O and LSE.
+// head) pair are processed in nrb blocks of 16; a (row, K/V head, block) is
+// a unit, u = (b*Hkv + hkv)*nrb + block.  The ctas CTAs share the stream of
+// the units' 128-key chunks evenly; a unit cut between CTAs leaves one
+// partial per piece in ws_o / ws_ml ([unit][slot][rows_ws]) and a merge
+// kernel produces its O and LSE.
+constexpr int kDecodeMaxSlots = 160;  // pieces per unit the workspace holds (>= CTAs launched)
+
 struct DecodeArgs {
   const __nv_bfloat16* q;
   const int* cache_lens;  // device
   __nv_bfloat16* o;
   float* lse;
-  float* ws_o;            // [B*Hkv*n_splits*R, D] f32
-  float2* ws_ml;          // [B*Hkv*n_splits*R] (max in log2 units, sum)
+  float* ws_o;            // [units * slots * rows_ws, D] f32 (slots > 1)
+  float2* ws_ml;          // [units * slots * rows_ws] (max in log2 units, sum)
   int* status;
   int B, Hq, Hkv, G, Tq, S, D, R;
-  int rb_rows, nrb, n_splits, cps, n_items;
+  int nrb;                // row blocks per (row, K/V head)
+  int slots;              // workspace slots per unit: min(chunks at capacity S, kDecodeMaxSlots)
+  int rows_ws;            // rows per slot: min(R, 16)
+  int ctas;               // CTAs of the partial kernel
   float scale_log2;
 };
 
-// k, v: dense maps over the caches ([B*Hkv, S, D], 64 x 128 boxes).
-cudaError_t launch_attn_decode(const CUtensorMap& k, const CUtensorMap& v, const DecodeArgs& a, int grid,
-                               cudaStream_t stream);
+// k, v: dense maps over the caches ([B*Hkv, S, D], 64 x 128 boxes); q: 2-D
+// map over the query rows ([B*Hq*Tq, D], 64 x 16 boxes).
+cudaError_t launch_attn_decode(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const DecodeArgs& a,
+                               int grid, cudaStream_t stream);
 
 // Kernel-level timing (opt-in instrumentation, api.cu): event pairs recorded
 // on the launch stream around each kernel.

@@ -168,17 +168,22 @@ def test_decode_validation(lib):
     assert dec(lib, ptrs=(NULL,) * 7, Tq=0) == 0
 
 
+def ws_decode(units, slots, rows_ws, D):
+    """partial O (f32, 256-byte aligned) + (max, sum) pairs per (unit, slot, row); none when
+    a unit cannot be cut (one slot)"""
+    if slots <= 1:
+        return 0
+    rows = units * slots * rows_ws
+    return (rows * D * 4 + 255) // 256 * 256 + rows * 8
+
+
 def test_decode_workspace_size(lib):
-    # 32 chunks of 128 keys, two (row, K/V head) units: 2 chunks per split (the
-    # minimum) -> 16 splits; R = G * Tq = 2 rows: f32 partial O + (max, sum) pairs
-    rows = 1 * 2 * 16 * 2
-    assert lib.attn_decode_workspace_size(1, 4, 2, 1, 4096, 64) == rows * 64 * 4 + rows * 8
-    assert lib.attn_decode_workspace_size(4, 8, 2, 1, 256, 128) == 0      # two chunks: no split
-    assert lib.attn_decode_workspace_size(64, 32, 32, 1, 8192, 64) == 0   # 2048 units: one split each
-    # long context: 64 units x 256 chunks -> 14 chunks per split, 19 splits; R = 4
-    rows = 8 * 8 * 19 * 4
-    assert lib.attn_decode_workspace_size(8, 32, 8, 1, 32768, 128) == rows * 128 * 4 + rows * 8
-    # 2^20 keys in one unit: splits capped at 1024
-    rows = 1 * 1 * 1024 * 1
-    assert lib.attn_decode_workspace_size(1, 1, 1, 1, 1 << 20, 64) == rows * 64 * 4 + rows * 8
-    assert lib.attn_decode_workspace_size(1, 4, 2, 1, 4096, 80) == 0       # invalid D
+    # units = B * Hkv * ceil(G*Tq / 16); slots per unit = min(ceil(S / 128), 160); rows = min(G*Tq, 16)
+    assert lib.attn_decode_workspace_size(1, 4, 2, 1, 4096, 64) == ws_decode(2, 32, 2, 64)
+    assert lib.attn_decode_workspace_size(4, 8, 2, 1, 128, 128) == 0                            # one chunk
+    assert lib.attn_decode_workspace_size(4, 8, 2, 1, 256, 128) == ws_decode(8, 2, 4, 128)
+    assert lib.attn_decode_workspace_size(8, 32, 8, 1, 32768, 128) == ws_decode(64, 160, 4, 128)
+    assert lib.attn_decode_workspace_size(2, 16, 2, 4, 640, 128) == ws_decode(8, 5, 16, 128)   # R = 32
+    assert lib.attn_decode_workspace_size(8, 12, 2, 1, 2048, 128) == ws_decode(16, 16, 6, 128)
+    assert lib.attn_decode_workspace_size(1, 1, 1, 1, 1 << 20, 64) == ws_decode(1, 160, 1, 64)
+    assert lib.attn_decode_workspace_size(1, 4, 2, 1, 4096, 80) == 0                            # invalid D

@@ -113,3 +113,19 @@ def test_decode_workloads_full(gq, name):
     ro, rlse = run_oracle(x, w.softmax_scale)
     check("o", o, ro, TOL_REL_O)
     check_lse(lse, rlse)
+
+
+def test_decode_workspace_reuse(gq):
+    """One workspace across calls: a unit cut into pieces in the first call is
+    processed whole in the second, whose result must not pick up the first
+    call's partials."""
+    B, Hq, Hkv, Tq, S, D = 2, 8, 2, 1, 4096, 128
+    ws = torch.empty(gq.attn_decode_workspace_size(B, Hq, Hkv, Tq, S, D), dtype=torch.uint8, device="cuda")
+    for lens in ([4096, 4096], [100, 4096], [4096, 1]):
+        x = W.decode_inputs(B, Hq, Hkv, Tq, S, D, cache_lens=lens, seed=len(lens) + lens[0])
+        q, k, v, ln = (x[n].cuda() for n in ("q", "k_cache", "v_cache", "cache_lens"))
+        o, lse = gq.attn_decode_fwd(q, k, v, ln, scale=0.1, workspace=ws)
+        assert gq.get_device_status() == 0
+        ro, rlse = run_oracle(x, 0.1)
+        check("o", o, ro, TOL_REL_O)
+        check_lse(lse, rlse)
