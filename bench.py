@@ -3,7 +3,9 @@
 One step = one forward (attn_fwd) and one backward (attn_bwd) of the long
 context GQA layer (B=2, Hq=32, Hkv=8, T=4096, D=128, causal, bf16) over one
 batch of synthetic inputs already resident in HBM.  The L2 cache (129 MB) is
-flushed by a 256 MiB write before every timed step; the step itself is timed
+evicted before every timed step by reading a 256 MiB buffer (clean lines:
+nothing is written back during the step; --flush write writes it instead);
+the step itself is timed
 with CUDA events on the launching stream.  FLOPs follow the causal convention
 (half of dense): forward 4*D and backward 10*D per visible (query, key) pair,
 i.e. 2*B*Hq*T^2*D and 5*B*Hq*T^2*D.
@@ -13,7 +15,7 @@ reference this method has) on a bounded sample of the same workload.
 
 --workload decode_* measures cached (decode) attention instead: one step is
 one attn_decode_fwd call over a KV cache resident in HBM (larger than L2 for
-the long-context workload, and L2 is flushed before every step anyway); the
+the long-context workload, and L2 is evicted before every step anyway); the
 figure is algorithmic HBM bytes per second -- the K and V rows each batch
 row actually holds (cache_lens[b] keys, Hkv heads, D features, bf16) plus Q,
 O, LSE and the lengths -- against the measured copy bandwidth.
@@ -39,6 +41,30 @@ import torch  # noqa: E402
 from causal_gqa_attention_fwd_gb300 import workloads as W  # noqa: E402
 
 METRIC = "causal GQA attention fwd+bwd TFLOP/s (bf16) and % of GB300 tensor peak"
+
+
+class L2Flush:
+    """Evicts the L2 cache (129 MB) between timed steps with a 256 MiB buffer:
+    'read' reads it (the evicted lines are clean, so nothing is written back
+    while the next step runs), 'write' writes it (its dirty lines are then
+    written back to HBM during the next step), 'none' does nothing."""
+
+    def __init__(self, mode: str, dev):
+        self.mode = mode
+        self.buf = None if mode == "none" else torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.sink = None
+
+    def __call__(self, i: int = 0):
+        if self.mode == "read":
+            self.sink = torch.amax(self.buf)
+        elif self.mode == "write":
+            self.buf.fill_(i & 0xFF)
+
+    def describe(self) -> str:
+        return {"read": "evicted before every timed step by reading a 256 MiB buffer",
+                "write": "flushed before every timed step by writing a 256 MiB buffer",
+                "none": "not flushed"}[self.mode]
+
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 
@@ -239,11 +265,28 @@ def run_decode(args, world, rank, local):
     def step():
         gq.attn_decode_fwd(q, kc, vc, lens, scale=scale, o=o, lse=lse, workspace=ws)
 
+    # A decode step is a few microseconds of launches around a short kernel:
+    # the timed steps replay the call captured in a CUDA graph (the call
+    # allocates nothing and never synchronises), as a serving loop would.
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+    run = graph.replay if graph is not None else step
+
     nbytes = decode_bytes(w, x["cache_lens"])
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(args.flush, dev)
     for _ in range(args.warmup):
-        flush.fill_(1)
-        step()
+        flush(1)
+        run()
     torch.cuda.synchronize()
     assert gq.get_device_status() == 0, "device status after warm-up"
 
@@ -255,9 +298,9 @@ def run_decode(args, world, rank, local):
     torch.cuda.synchronize()
     clocks.mark(0)
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush(i)
         ev[i][0].record(stream)
-        step()
+        run()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -268,7 +311,7 @@ def run_decode(args, world, rank, local):
     gq.profile_reset()
     gq.profile_enable(True)
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush(i)
         step()
     torch.cuda.synchronize()
     gq.profile_enable(False)
@@ -327,13 +370,13 @@ def run_decode(args, world, rank, local):
             "metric": DECODE_METRIC, "value": value, "unit": DECODE_UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 in, f32 arithmetic", "data": "synthetic",
-            "config": decode_config(w, world, "inputs larger than L2 for decode_long_gqa_s32k; "
-                                              "flushed before every timed step (256 MiB write)"),
+            "config": decode_config(w, world, flush.describe()),
             "frac_of_peak": value / pk["hbm_gbs"],
             "tokens_per_s": world * w.B * w.Tq * args.steps / (total_ms / 1e3),
             "kernel_ms": {k: (t / n if n else None) for k, (n, t) in prof.items() if n},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": sum(prof[k][0] for k in prof), "kernel_ms_pass": "second pass, same steps, events per kernel",
+            "launch": "CUDA graph replay of the call" if graph is not None else "eager calls",
             "clocks": clk, "device_status": status,
         }
         print(json.dumps(line), flush=True)
@@ -431,6 +474,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="decode workloads: time eager calls, not graph replays")
+    ap.add_argument("--flush", default="read", choices=["read", "write", "none"],
+                    help="L2 eviction between timed steps (see L2Flush)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
@@ -477,10 +523,10 @@ def main():
             gq.attn_fwd(q, k, v, scale=scale, o=o, lse=lse)
             gq.attn_bwd(q, k, v, o, lse, do, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
 
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(args.flush, dev)
     f_fwd, f_bwd = flops(w, cu)
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush(1)
         step()
     torch.cuda.synchronize()
     assert gq.get_device_status() == 0, "device status after warm-up"
@@ -496,7 +542,7 @@ def main():
     clocks.mark(0)
     t_wall = time.perf_counter()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush(i)
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -577,7 +623,7 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T, "D": w.D,
                        "causal": w.causal, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "flushed before every timed step (256 MiB write)"},
+                       "l2": flush.describe()},
             "frac_of_peak": value / pk["bf16_tflops"],
             "fwd_tflops": f_fwd / (fwd_ms / 1e3) / 1e12,
             "bwd_tflops": f_bwd / (bwd_ms / 1e3) / 1e12,

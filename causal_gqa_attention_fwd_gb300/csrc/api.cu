@@ -49,6 +49,18 @@ attn_status check_arch() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// SM count of the current device (looked up once per device; 0 on error).
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static int cache[kMaxDevices] = {};
+  if (dev < kMaxDevices && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < kMaxDevices) cache[dev] = n;
+  return n;
+}
+
 attn_status check_heads(int Hq, int Hkv, int D) {
   if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_SHAPE;
   if (Hq > 65535 || Hkv > 65535) return ATTN_ERR_SHAPE;
@@ -430,10 +442,8 @@ attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_ca
   if ((st = check_arch()) != ATTN_OK) return st;
   int* status = status_word();
   if (!status) return ATTN_ERR_CUDA;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
-    return ATTN_ERR_CUDA;
+  const int sms = sm_count();
+  if (sms < 1) return ATTN_ERR_CUDA;
   gqa::DecodeArgs a{};
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.cache_lens = cache_lens;
