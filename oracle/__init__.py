@@ -13,7 +13,10 @@ K/V [total,Hkv,D], LSE/Delta [Hq,total].
 What is computed is stated in the header of ``gqa_oracle.c`` with its sources
 ("Project Overview" of llm-from-scratch, section "Performance Layer: kernel/
 and parallel/" and the llm/transformer.py component list; the microLLM-rocm
-README, section "Why this project exists").
+README, section "Why this project exists").  ``paged_decode_fwd`` reads a
+paged KV cache (the RoseLLM README, section "Inference and serving": global
+paged KV-cache management) by gathering each row's pages into a contiguous
+cache, then runs ``decode_fwd``.
 """
 from __future__ import annotations
 
@@ -204,3 +207,28 @@ def decode_fwd(q, k_cache, v_cache, cache_lens, scale: float | None = None, lib=
     if st:
         raise ValueError(f"oracle_decode_fwd status {st}")
     return o, lse
+
+
+def paged_decode_fwd(q, k_pages, v_pages, block_table, cache_lens, scale: float | None = None, lib=None):
+    """Cached attention over a paged KV cache.
+
+    k_pages, v_pages [num_pages, Hkv, page_size, D] (each page holds page_size
+    consecutive positions of one batch row, all K/V heads); block_table
+    [B, max_pages] int: key position j of row b is row j % page_size of page
+    block_table[b, j // page_size].  Only the pages that hold one of the row's
+    cache_lens[b] keys are read.  Same queries, mask and results as
+    ``decode_fwd`` over the gathered cache [B, Hkv, max_pages * page_size, D]."""
+    kp, vp = _c(k_pages), _c(v_pages)
+    bt = np.asarray(block_table)
+    lens = np.asarray(cache_lens)
+    B = q.shape[0]
+    _, Hkv, psz, D = kp.shape
+    S = bt.shape[1] * psz
+    k = np.zeros((B, Hkv, S, D))
+    v = np.zeros((B, Hkv, S, D))
+    for b in range(B):
+        for i in range((int(lens[b]) + psz - 1) // psz):
+            page = int(bt[b, i])
+            k[b, :, i * psz:(i + 1) * psz] = kp[page]
+            v[b, :, i * psz:(i + 1) * psz] = vp[page]
+    return decode_fwd(q, k, v, lens, scale=scale, lib=lib)

@@ -299,6 +299,40 @@ def pin_decode_is_dense_suffix(lib):
     np.testing.assert_allclose(o1[:, :, 0], np.repeat(v[:, :, 0], Hq // Hkv, axis=1), atol=1e-14)
 
 
+def pin_paged_decode_is_contiguous_decode(lib):
+    """A cache scattered into shuffled pages (page sizes 1, 4 and the whole
+    capacity; unused block-table entries pointing anywhere) gives the same
+    result as the contiguous cache it came from."""
+    r = _rng(12)
+    B, Hq, Hkv, Tq, D, scale = 3, 4, 2, 2, 8, 0.4
+    for psz in (1, 4, 24):
+        maxp = 24 // psz
+        S = maxp * psz
+        lens = [S, 5, 2]
+        q = r.standard_normal((B, Hq, Tq, D))
+        k = r.standard_normal((B, Hkv, S, D))
+        v = r.standard_normal((B, Hkv, S, D))
+        order = r.permutation(B * maxp)               # page of (row b, slot i): order[b * maxp + i]
+        kp = np.zeros((B * maxp, Hkv, psz, D))
+        vp = np.zeros((B * maxp, Hkv, psz, D))
+        bt = np.zeros((B, maxp), dtype=np.int64)
+        for b in range(B):
+            for i in range(maxp):
+                pg = order[b * maxp + i]
+                bt[b, i] = pg
+                for h in range(Hkv):
+                    for t in range(psz):
+                        kp[pg, h, t] = k[b, h, i * psz + t]
+                        vp[pg, h, t] = v[b, h, i * psz + t]
+        for b in range(B):                           # entries past a row's pages may hold anything
+            bt[b, (lens[b] + psz - 1) // psz:] = -7
+        o, lse = oracle.paged_decode_fwd(q, kp, vp, bt, lens, scale=scale, lib=lib)
+        oc, lc = oracle.decode_fwd(q, k, v, lens, scale=scale, lib=lib)
+        np.testing.assert_array_equal(o, oc)
+        np.testing.assert_array_equal(lse, lc)
+
+
 PINS = [pin_hand_worked, pin_rows_sum_to_one, pin_single_token, pin_constant_keys, pin_shift_invariance,
         pin_gqa_equals_repeated_mha, pin_torch_sdpa, pin_finite_differences, pin_delta_identity,
-        pin_varlen_equals_slices, pin_rounding_error_terms, pin_decode_is_dense_suffix]
+        pin_varlen_equals_slices, pin_rounding_error_terms, pin_decode_is_dense_suffix,
+        pin_paged_decode_is_contiguous_decode]
