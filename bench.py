@@ -210,10 +210,13 @@ DECODE_UNIT = "GB/s"
 
 def decode_bytes(w: W.DecodeWorkload, lens) -> int:
     """Algorithmic bytes of one decode call: K and V rows inside each row's
-    cache, Q read, O written (bf16), LSE written (f32), the lengths."""
-    kv = 2 * w.Hkv * w.D * 2 * int(torch.as_tensor(lens, dtype=torch.int64).sum())
+    cache, Q read, O written (bf16), LSE written (f32), the lengths (paged:
+    and the block-table entries of the pages that hold keys)."""
+    lens = torch.as_tensor(lens, dtype=torch.int64)
+    kv = 2 * w.Hkv * w.D * 2 * int(lens.sum())
     qo = 2 * w.B * w.Hq * w.Tq * w.D * 2
-    return kv + qo + w.B * w.Hq * w.Tq * 4 + w.B * 4
+    table = 4 * int(((lens + w.page_size - 1) // w.page_size).sum()) if w.page_size else 0
+    return kv + qo + w.B * w.Hq * w.Tq * 4 + w.B * 4 + table
 
 
 def oracle_decode_sample(w: W.DecodeWorkload, x, budget_s: float):
@@ -228,25 +231,36 @@ def oracle_decode_sample(w: W.DecodeWorkload, x, budget_s: float):
     oracle.set_threads(cores)
     f = lambda t: t.float().numpy().astype(np.float64)
     done, elapsed, rows = 0, 0.0, 0
+    kp = vp = None
+    if w.page_size:
+        kp, vp = f(x["k_pages"]), f(x["v_pages"])
     while rows == 0 or (elapsed < budget_s and rows < w.B):
         b = rows
-        xb = {"q": x["q"][b:b + 1], "k_cache": x["k_cache"][b:b + 1], "v_cache": x["v_cache"][b:b + 1],
-              "cache_lens": x["cache_lens"][b:b + 1]}
-        args = (f(xb["q"]), f(xb["k_cache"]), f(xb["v_cache"]), xb["cache_lens"].numpy())
+        lens = x["cache_lens"][b:b + 1]
+        if w.page_size:
+            args = (f(x["q"][b:b + 1]), kp, vp, x["block_table"][b:b + 1].numpy(), lens.numpy())
+            fn = oracle.paged_decode_fwd
+        else:
+            args = (f(x["q"][b:b + 1]), f(x["k_cache"][b:b + 1]), f(x["v_cache"][b:b + 1]), lens.numpy())
+            fn = oracle.decode_fwd
         t0 = time.perf_counter()
-        oracle.decode_fwd(*args, scale=w.softmax_scale)
+        fn(*args, scale=w.softmax_scale)
         elapsed += time.perf_counter() - t0
         rows += 1
-        one = W.DecodeWorkload("s", B=1, Hq=w.Hq, Hkv=w.Hkv, Tq=w.Tq, S=w.S, D=w.D, min_len=0, max_len=0)
-        done += decode_bytes(one, xb["cache_lens"])
+        one = W.DecodeWorkload("s", B=1, Hq=w.Hq, Hkv=w.Hkv, Tq=w.Tq, S=w.S, D=w.D, min_len=0, max_len=0,
+                               page_size=w.page_size)
+        done += decode_bytes(one, lens)
     desc = f"{rows} of {w.B} batch rows of {w.name} (whole caches), fp64, {elapsed:.1f} s"
     return done / elapsed, desc, cores, elapsed
 
 
 def decode_config(w: W.DecodeWorkload, world: int, l2: str):
-    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Tq": w.Tq, "S": w.S, "D": w.D,
-            "cache_lens": f"uniform in [{w.min_len}, {w.max_len}]",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "l2": l2}
+    c = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Tq": w.Tq, "S": w.S, "D": w.D,
+         "cache_lens": f"uniform in [{w.min_len}, {w.max_len}]",
+         "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "l2": l2}
+    if w.page_size:
+        c["paged"] = f"pages of {w.page_size} positions, [num_pages, Hkv, page, D], shuffled over the pool"
+    return c
 
 
 def run_decode(args, world, rank, local):
@@ -256,14 +270,24 @@ def run_decode(args, world, rank, local):
     w = W.DECODE_WORKLOADS[args.workload]
     x = W.make_decode_inputs(w, seed=rank)
     stream = torch.cuda.current_stream()
-    q, kc, vc, lens = (x[n].to(dev) for n in ("q", "k_cache", "v_cache", "cache_lens"))
+    names = ("q", "k_pages", "v_pages", "block_table", "cache_lens") if w.page_size else \
+        ("q", "k_cache", "v_cache", "cache_lens")
+    dx = {n: x[n].to(dev) for n in names}
+    q, lens = dx["q"], dx["cache_lens"]
     scale = w.softmax_scale
-    o, lse = gq.attn_decode_fwd(q, kc, vc, lens, scale=scale)
     ws_bytes = gq.attn_decode_workspace_size(w.B, w.Hq, w.Hkv, w.Tq, w.S, w.D)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Tq), dtype=torch.float32, device=dev)
 
     def step():
-        gq.attn_decode_fwd(q, kc, vc, lens, scale=scale, o=o, lse=lse, workspace=ws)
+        if w.page_size:
+            gq.attn_decode_paged_fwd(q, dx["k_pages"], dx["v_pages"], dx["block_table"], lens, scale=scale, o=o,
+                                     lse=lse, workspace=ws)
+        else:
+            gq.attn_decode_fwd(q, dx["k_cache"], dx["v_cache"], lens, scale=scale, o=o, lse=lse, workspace=ws)
+
+    step()
 
     # A decode step is a few microseconds of launches around a short kernel:
     # the timed steps replay the call captured in a CUDA graph (the call
@@ -331,16 +355,14 @@ def run_decode(args, world, rank, local):
 
     e2e = None
     if not args.no_e2e:
-        hq, hk, hv, hl = (x[n].pin_memory() for n in ("q", "k_cache", "v_cache", "cache_lens"))
-        ho, hlse = torch.empty_like(hq).pin_memory(), torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hl))
+        hx = {n: x[n].pin_memory() for n in names}
+        ho, hlse = torch.empty_like(hx["q"]).pin_memory(), torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in hx.values())
         d2h = sum(t.numel() * t.element_size() for t in (ho, hlse))
 
         def e2e_step():
-            q.copy_(hq, non_blocking=True)
-            kc.copy_(hk, non_blocking=True)
-            vc.copy_(hv, non_blocking=True)
-            lens.copy_(hl, non_blocking=True)
+            for n in names:
+                dx[n].copy_(hx[n], non_blocking=True)
             step()
             ho.copy_(o, non_blocking=True)
             hlse.copy_(lse, non_blocking=True)

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgqa_attn
 STATUS = {
     0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_SHAPE", 3: "ATTN_ERR_HEADDIM", 4: "ATTN_ERR_ALIGN",
     5: "ATTN_ERR_SEQLENS", 6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_ARCH", 8: "ATTN_ERR_CUDA",
-    9: "ATTN_ERR_TIMEOUT", 10: "ATTN_ERR_SCRATCH_LIMIT",
+    9: "ATTN_ERR_TIMEOUT", 10: "ATTN_ERR_SCRATCH_LIMIT", 11: "ATTN_ERR_PAGES",
 }
 
 # name -> (restype, argtypes)
@@ -40,6 +40,7 @@ SIGNATURES = {
     "attn_profile_read": (_I, [_I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)]),
     "attn_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
     "attn_decode_fwd": (_I, [_P] * 7 + [_Z, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_decode_paged_fwd": (_I, [_P] * 8 + [_Z] + [_I] * 8 + [_F, _P]),
 }
 
 PROFILE_KINDS = {"attn_fwd": 0, "bwd_pre": 1, "bwd_main": 2, "bwd_post": 3, "decode": 4, "decode_merge": 5}
@@ -256,4 +257,32 @@ def attn_decode_fwd(q, k_cache, v_cache, cache_lens, scale=None, o=None, lse=Non
                                _need(lse, "lse", torch.float32), ws_ptr, ws_len, B, Hq, Hkv, Tq, S, D,
                                _scale(scale, D), _stream(stream))
     _check(st, "attn_decode_fwd")
+    return o, lse
+
+
+def attn_decode_paged_fwd(q, k_pages, v_pages, block_table, cache_lens, scale=None, o=None, lse=None, workspace=None,
+                          stream=None):
+    """Cached attention over a paged KV cache.  q [B,Hq,Tq,D]; k_pages, v_pages [num_pages,Hkv,page_size,D]
+    bf16; block_table int32 (device) [B, max_pages]; cache_lens int32 (device) [B]
+    -> (o [B,Hq,Tq,D] bf16, lse [B,Hq,Tq] f32)."""
+    B, Hq, Tq, D = q.shape
+    num_pages, Hkv, page_size = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    if k_pages.shape != (num_pages, Hkv, page_size, D) or v_pages.shape != k_pages.shape:
+        raise ValueError("k_pages, v_pages must be [num_pages, Hkv, page_size, D] matching q")
+    if block_table.dim() != 2 or block_table.shape[0] != B or cache_lens.shape != (B,):
+        raise ValueError("block_table must be [B, max_pages], cache_lens [B]")
+    max_pages = block_table.shape[1]
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws_bytes = attn_decode_workspace_size(B, Hq, Hkv, Tq, max_pages * page_size, D)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ws_ptr = _need(workspace, "workspace", torch.uint8) if workspace is not None else None
+    ws_len = workspace.numel() if workspace is not None else 0
+    st = lib().attn_decode_paged_fwd(_need(q, "q"), _need(k_pages, "k_pages"), _need(v_pages, "v_pages"),
+                                     _need(block_table, "block_table", torch.int32),
+                                     _need(cache_lens, "cache_lens", torch.int32), _need(o, "o"),
+                                     _need(lse, "lse", torch.float32), ws_ptr, ws_len, B, Hq, Hkv, Tq, page_size,
+                                     num_pages, max_pages, D, _scale(scale, D), _stream(stream))
+    _check(st, "attn_decode_paged_fwd")
     return o, lse

@@ -417,29 +417,19 @@ attn_status decode_check(int B, int Hq, int Hkv, int Tq, int S, int D) {
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Tq, int S, int D) {
-  if (decode_check(B, Hq, Hkv, Tq, S, D) != ATTN_OK || B == 0 || Tq == 0) return 0;
-  return decode_ws_bytes(decode_plan(B, Hq, Hkv, Tq, S), D);
-}
-
-attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, const int* cache_lens,
-                            void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
-                            int Tq, int S, int D, float scale, void* stream) {
-  attn_status st = decode_check(B, Hq, Hkv, Tq, S, D);
-  if (st != ATTN_OK) return st;
-  if (B == 0 || Tq == 0) return ATTN_OK;
-  if (!isfinite(scale)) return ATTN_ERR_SHAPE;
-  if (!q || !k_cache || !v_cache || !cache_lens || !o || !lse) return ATTN_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse) ||
-      (reinterpret_cast<uintptr_t>(cache_lens) & 3u))
-    return ATTN_ERR_ALIGN;
+// Shared part of the contiguous and paged decode entry points: everything
+// after the layout-specific checks (capacity S = keys per row at most).
+attn_status decode_common(const void* q, const CUtensorMap& tk, const CUtensorMap& tv, const int* cache_lens,
+                          void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                          int Tq, int S, int D, float scale, const int* block_table, int page_size, int max_pages,
+                          int num_pages, void* stream) {
   const DecodePlan p = decode_plan(B, Hq, Hkv, Tq, S);
-  const size_t need = decode_ws_bytes(p, D);
-  if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
-    return ATTN_ERR_WORKSPACE;
-  if ((st = check_arch()) != ATTN_OK) return st;
+  const size_t need = decode_ws_bytes(p, D);  // checked by the caller
+  (void)workspace_bytes;
+  attn_status st = check_arch();
+  if (st != ATTN_OK) return st;
   int* status = status_word();
   if (!status) return ATTN_ERR_CUDA;
   const int sms = sm_count();
@@ -470,14 +460,84 @@ attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_ca
   // more than the workspace has slots for
   a.ctas = sms < gqa::kDecodeMaxSlots ? sms : gqa::kDecodeMaxSlots;
   a.scale_log2 = scale * 1.4426950408889634f;
-  CUtensorMap tk, tv, tq;
+  a.block_table = block_table;
+  a.page_size = page_size;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  CUtensorMap tq;
   const uint64_t qdims[2] = {(uint64_t)D, (uint64_t)B * Hq * Tq};
   const uint64_t qstrides[1] = {(uint64_t)D * 2};
   const uint32_t qbox[2] = {64, (uint32_t)kDecodeRows};
-  if (!map_dense(&tk, k_cache, D, S, (long)B * Hkv) || !map_dense(&tv, v_cache, D, S, (long)B * Hkv) ||
-      !gqa::make_tmap(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qdims, qstrides, qbox, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!gqa::make_tmap(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qdims, qstrides, qbox, CU_TENSOR_MAP_SWIZZLE_128B))
     return ATTN_ERR_CUDA;
   return launch_status(gqa::launch_attn_decode(tk, tv, tq, a, a.ctas, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status decode_check_workspace(int B, int Hq, int Hkv, int Tq, int S, int D, const void* workspace,
+                                   size_t workspace_bytes) {
+  const size_t need = decode_ws_bytes(decode_plan(B, Hq, Hkv, Tq, S), D);
+  if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return ATTN_ERR_WORKSPACE;
+  return ATTN_OK;
+}
+
+bool decode_page_size_ok(int page_size) {
+  return page_size == 16 || page_size == 32 || page_size == 64 || (page_size > 0 && page_size % 128 == 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Tq, int S, int D) {
+  if (decode_check(B, Hq, Hkv, Tq, S, D) != ATTN_OK || B == 0 || Tq == 0) return 0;
+  return decode_ws_bytes(decode_plan(B, Hq, Hkv, Tq, S), D);
+}
+
+attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, const int* cache_lens,
+                            void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                            int Tq, int S, int D, float scale, void* stream) {
+  attn_status st = decode_check(B, Hq, Hkv, Tq, S, D);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || Tq == 0) return ATTN_OK;
+  if (!isfinite(scale)) return ATTN_ERR_SHAPE;
+  if (!q || !k_cache || !v_cache || !cache_lens || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse) ||
+      (reinterpret_cast<uintptr_t>(cache_lens) & 3u))
+    return ATTN_ERR_ALIGN;
+  if ((st = decode_check_workspace(B, Hq, Hkv, Tq, S, D, workspace, workspace_bytes)) != ATTN_OK) return st;
+  CUtensorMap tk, tv;
+  if (!map_dense(&tk, k_cache, D, S, (long)B * Hkv) || !map_dense(&tv, v_cache, D, S, (long)B * Hkv))
+    return ATTN_ERR_CUDA;
+  return decode_common(q, tk, tv, cache_lens, o, lse, workspace, workspace_bytes, B, Hq, Hkv, Tq, S, D, scale,
+                       nullptr, 0, 0, 0, stream);
+}
+
+attn_status attn_decode_paged_fwd(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                                  const int* cache_lens, void* o, float* lse, void* workspace,
+                                  size_t workspace_bytes, int B, int Hq, int Hkv, int Tq, int page_size,
+                                  int num_pages, int max_pages, int D, float scale, void* stream) {
+  if (page_size < 0 || num_pages < 0 || max_pages < 0) return ATTN_ERR_SHAPE;
+  const long S = (long)page_size * max_pages;
+  if (S > 0x7fffffffL) return ATTN_ERR_SHAPE;
+  attn_status st = decode_check(B, Hq, Hkv, Tq, (int)S, D);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || Tq == 0) return ATTN_OK;
+  if (!decode_page_size_ok(page_size) || num_pages < 1 || (long)num_pages * Hkv > 0x7fffffffL ||
+      (long)B * max_pages > 0x7fffffffL || !isfinite(scale))
+    return ATTN_ERR_SHAPE;
+  if (!q || !k_pages || !v_pages || !block_table || !cache_lens || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) || !aligned16(lse) ||
+      (reinterpret_cast<uintptr_t>(cache_lens) & 3u) || (reinterpret_cast<uintptr_t>(block_table) & 3u))
+    return ATTN_ERR_ALIGN;
+  if ((st = decode_check_workspace(B, Hq, Hkv, Tq, (int)S, D, workspace, workspace_bytes)) != ATTN_OK) return st;
+  const int box = page_size < 128 ? page_size : 128;
+  CUtensorMap tk, tv;
+  if (!map_dense(&tk, k_pages, D, page_size, (long)num_pages * Hkv, box) ||
+      !map_dense(&tv, v_pages, D, page_size, (long)num_pages * Hkv, box))
+    return ATTN_ERR_CUDA;
+  return decode_common(q, tk, tv, cache_lens, o, lse, workspace, workspace_bytes, B, Hq, Hkv, Tq, (int)S, D, scale,
+                       block_table, page_size, max_pages, num_pages, stream);
 }
 
 // ------------------------------------------------- allocation-free backward
@@ -544,6 +604,7 @@ const char* attn_status_string(attn_status s) {
     case ATTN_ERR_TIMEOUT: return "a bounded in-kernel wait expired";
     case ATTN_ERR_SCRATCH_LIMIT:
       return "the problem needs more backward scratch than attn_bwd_noalloc's built-in array holds";
+    case ATTN_ERR_PAGES: return "a block-table entry names no page of the pool";
   }
   return "unknown status";
 }

@@ -301,7 +301,7 @@ __device__ __noinline__ void decode_write_out(const DecodeArgs& a, const Piece& 
   }
 }
 
-template <int D>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_q, const DecodeArgs a) {
@@ -411,6 +411,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int c = 0; c < it.nch; ++c, ++cs) {
         const int slot = cs % SL, fill = cs / SL;
+        const int k0 = it.kbeg + c * kCK;
+        // paged: lane i looks up the chunk's i-th page (before the slot wait,
+        // so the lookup's latency overlaps it); pages that hold none of the
+        // row's keys, and invalid entries (reported), get a coordinate past
+        // the tensor, which the TMA fills with zeros
+        int pages[kCK / 16];
+        int npc = 1;
+        if constexpr (PAGED) {
+          const int psz = a.page_size;
+          npc = psz >= kCK ? 1 : kCK / psz;
+          const int idx = k0 / psz + lane;
+          const int used = (it.len + psz - 1) / psz;
+          int pg = -1;
+          bool bad = false;
+          if (lane < npc && idx < used) {
+            const int e = a.block_table[(long)it.b * a.max_pages + idx];
+            if (e >= 0 && e < a.num_pages) pg = e;
+            else bad = true;
+          }
+          if (__any_sync(0xffffffffu, bad) && lane == 0) atomicCAS(a.status, 0, kDevBadPages);
+#pragma unroll
+          for (int i = 0; i < kCK / 16; ++i) pages[i] = __shfl_sync(0xffffffffu, pg, i);
+        }
         if (fill >= 1) mbar_wait(&empty[slot], (fill - 1) & 1, guard);
         if (lane == 0) {
           uint64_t* bar = &full[slot];
@@ -419,9 +442,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             uint8_t* dst = ring + slot * C::kTileBytes;
             mbar_expect_tx(bar, C::kTileBytes);
-            const int y = it.kbeg + c * kCK;
+            if constexpr (PAGED) {
+              const int psz = a.page_size;
+              const int row = psz >= kCK ? k0 % psz : 0;  // first row of the chunk inside its page
+              for (int i = 0; i < npc; ++i) {
+                const int z = pages[i] >= 0 ? pages[i] * a.Hkv + it.hkv : a.num_pages * a.Hkv;
 #pragma unroll
-            for (int x = 0; x < NB; ++x) tma_load_3d(dst + x * kBoxBytes, tm, bar, x * 64, y, it.bh);
+                for (int x = 0; x < NB; ++x)
+                  tma_load_3d(dst + x * kBoxBytes + i * psz * 128, tm, bar, x * 64, row, z);
+              }
+            } else {
+#pragma unroll
+              for (int x = 0; x < NB; ++x) tma_load_3d(dst + x * kBoxBytes, tm, bar, x * 64, k0, it.bh);
+            }
             last_fill[slot] = fill;
           }
         }
@@ -739,21 +772,21 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
   if (threadIdx.x == 0) a.lse[row] = s_lse;
 }
 
-template <int D>
-static cudaError_t launch_decode_d(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
-                                   const DecodeArgs& a, int grid, cudaStream_t stream) {
+template <int D, bool PAGED>
+static cudaError_t launch_decode_dp(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
+                                    const DecodeArgs& a, int grid, cudaStream_t stream) {
   using C = DecCfg<D>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<D, PAGED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   prof_begin(kProfDecode, stream);
-  decode_partial_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(k, v, q, a);
+  decode_partial_kernel<D, PAGED><<<grid, kThreads, C::kSmemBytes, stream>>>(k, v, q, a);
   prof_end(stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.slots <= 1) return e;  // no unit can be cut
@@ -774,6 +807,13 @@ static cudaError_t launch_decode_d(const CUtensorMap& k, const CUtensorMap& v, c
   prof_end(stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_decode_d(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
+                                   const DecodeArgs& a, int grid, cudaStream_t stream) {
+  if (a.block_table != nullptr) return launch_decode_dp<D, true>(k, v, q, a, grid, stream);
+  return launch_decode_dp<D, false>(k, v, q, a, grid, stream);
 }
 
 cudaError_t launch_attn_decode(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const DecodeArgs& a,

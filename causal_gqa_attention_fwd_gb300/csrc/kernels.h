@@ -94,10 +94,15 @@ struct DecodeArgs {
   int rows_ws;            // rows per slot: min(R, 16)
   int ctas;               // CTAs of the partial kernel
   float scale_log2;
+  // paged caches (k, v maps over [num_pages * Hkv, page_size, D]): key
+  // position j of row b is row j % page_size of page block_table[b * max_pages + j / page_size]
+  const int* block_table; // device, nullptr for contiguous caches
+  int page_size, max_pages, num_pages;
 };
 
-// k, v: dense maps over the caches ([B*Hkv, S, D], 64 x 128 boxes); q: 2-D
-// map over the query rows ([B*Hq*Tq, D], 64 x 16 boxes).
+// k, v: dense maps over the caches ([B*Hkv, S, D], 64 x 128 boxes) or, paged,
+// over the pages ([num_pages*Hkv, page_size, D], 64 x min(page_size, 128)
+// boxes); q: 2-D map over the query rows ([B*Hq*Tq, D], 64 x 16 boxes).
 cudaError_t launch_attn_decode(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const DecodeArgs& a,
                                int grid, cudaStream_t stream);
 

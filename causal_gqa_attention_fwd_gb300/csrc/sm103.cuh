@@ -17,7 +17,7 @@
 namespace gqa {
 
 // Device status word values (mirrors attn_status in include/gqa_attn.h).
-enum : int { kDevOk = 0, kDevTimeout = 9, kDevBadSeqlens = 5 };
+enum : int { kDevOk = 0, kDevTimeout = 9, kDevBadSeqlens = 5, kDevBadPages = 11 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 

@@ -16,7 +16,10 @@ against a KV cache of capacity S holding cache_lens[b] keys: two are shaped
 after the steady-decode rows the microLLM-rocm README reports (context 2048,
 batch 8, Qwen2.5-0.5B and DeepSeek-R1-Distill-Qwen-1.5B attention shapes),
 one is a long-context GQA cache larger than the L2 cache (per-row lengths
-drawn between S/2 and S).  Draw order: cache lengths, Q, K cache, V cache.
+drawn between S/2 and S), and the same long-context cache is also paged
+(pages of 64 and of 16 positions, shuffled over the pool).  Draw order:
+cache lengths, Q, K cache, V cache (paged: K pages, V pages, then the page
+permutation).
 """
 from __future__ import annotations
 
@@ -73,6 +76,7 @@ class DecodeWorkload:
     min_len: int            # cache_lens drawn uniformly in [min_len, max_len]
     max_len: int
     scale: float = field(default=0.0)
+    page_size: int = 0      # > 0: paged cache of S / page_size pages per row
 
     @property
     def softmax_scale(self) -> float:
@@ -87,6 +91,13 @@ DECODE_WORKLOADS = {
     "decode_long_gqa_s32k": DecodeWorkload("decode_long_gqa_s32k", B=8, Hq=32, Hkv=8, Tq=1, S=32768, D=128,
                                            min_len=16384, max_len=32768),
 }
+
+DECODE_WORKLOADS["decode_paged_long_gqa_s32k_p64"] = DecodeWorkload(
+    "decode_paged_long_gqa_s32k_p64", B=8, Hq=32, Hkv=8, Tq=1, S=32768, D=128, min_len=16384, max_len=32768,
+    page_size=64)
+DECODE_WORKLOADS["decode_paged_long_gqa_s32k_p16"] = DecodeWorkload(
+    "decode_paged_long_gqa_s32k_p16", B=8, Hq=32, Hkv=8, Tq=1, S=32768, D=128, min_len=16384, max_len=32768,
+    page_size=16)
 
 DECODE_HEADLINE = "decode_long_gqa_s32k"
 
@@ -154,5 +165,31 @@ def decode_inputs(B, Hq, Hkv, Tq, S, D, cache_lens=None, min_len=None, max_len=N
     return dict(q=q, k_cache=k, v_cache=v, cache_lens=lens)
 
 
+def paged_decode_inputs(B, Hq, Hkv, Tq, page_size, max_pages, D, cache_lens=None, min_len=None, max_len=None,
+                        spare_pages=0, seed=0):
+    """q [B,Hq,Tq,D], a page pool k_pages/v_pages [num_pages,Hkv,page_size,D] bf16 (num_pages =
+    B * max_pages + spare_pages), block_table int32 [B, max_pages] and cache_lens int32 [B], CPU.
+    The table is a random permutation of the pool's pages; entries past each row's last page are -1.
+    Draw order: cache lengths, Q, K pages, V pages, the permutation."""
+    g = torch.Generator().manual_seed(seed)
+    S = page_size * max_pages
+    if cache_lens is None:
+        lo = Tq if min_len is None else min_len
+        hi = S if max_len is None else max_len
+        cache_lens = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64)
+    lens = torch.as_tensor(cache_lens, dtype=torch.int32)
+    num_pages = B * max_pages + spare_pages
+    q = _randn(g, (B, Hq, Tq, D))
+    kp = _randn(g, (num_pages, Hkv, page_size, D))
+    vp = _randn(g, (num_pages, Hkv, page_size, D))
+    table = torch.randperm(num_pages, generator=g)[:B * max_pages].reshape(B, max_pages).to(torch.int32)
+    for b in range(B):
+        table[b, (int(lens[b]) + page_size - 1) // page_size:] = -1
+    return dict(q=q, k_pages=kp, v_pages=vp, block_table=table, cache_lens=lens)
+
+
 def make_decode_inputs(w: DecodeWorkload, seed=0):
+    if w.page_size:
+        return paged_decode_inputs(w.B, w.Hq, w.Hkv, w.Tq, w.page_size, w.S // w.page_size, w.D, min_len=w.min_len,
+                                   max_len=w.max_len, seed=seed)
     return decode_inputs(w.B, w.Hq, w.Hkv, w.Tq, w.S, w.D, min_len=w.min_len, max_len=w.max_len, seed=seed)

@@ -67,7 +67,8 @@ typedef enum {
     ATTN_ERR_ARCH = 7,       /* current device is not compute capability 10.3 */
     ATTN_ERR_CUDA = 8,       /* a CUDA runtime call failed (launch, tensor map, attribute) */
     ATTN_ERR_TIMEOUT = 9,    /* device-detected: a bounded in-kernel wait expired */
-    ATTN_ERR_SCRATCH_LIMIT = 10 /* attn_bwd_noalloc: sizes need more than its built-in scratch */
+    ATTN_ERR_SCRATCH_LIMIT = 10, /* attn_bwd_noalloc: sizes need more than its built-in scratch */
+    ATTN_ERR_PAGES = 11      /* device-detected: a block-table entry names no page of the pool */
 } attn_status;
 
 /* Forward, dense layout.  Writes O (bf16) and LSE (float32). */
@@ -157,6 +158,28 @@ GQA_ATTN_API attn_status attn_decode_fwd(const void* q, const void* k_cache, con
                                          const int* cache_lens, void* o, float* lse, void* workspace,
                                          size_t workspace_bytes, int B, int Hq, int Hkv, int Tq, int S, int D,
                                          float scale, void* stream);
+
+/* Cached attention over a PAGED KV cache (the paged KV-cache management of
+ * the RoseLLM README, section "Inference and serving").  Same queries, mask
+ * and outputs as attn_decode_fwd; the cache is a pool of pages:
+ *   k_pages, v_pages  bf16 [num_pages, Hkv, page_size, D]: a page holds
+ *                     page_size consecutive positions of one batch row,
+ *                     every K/V head (each (page, head) block contiguous)
+ *   block_table       DEVICE int32 [B, max_pages]: key position j of row b
+ *                     is row j % page_size of page block_table[b*max_pages + j/page_size];
+ *                     only the entries of pages that hold one of the row's
+ *                     cache_lens[b] keys are read
+ *   cache_lens        DEVICE int32 [B], Tq <= cache_lens[b] <= max_pages * page_size
+ * page_size: 16, 32, 64 or a multiple of 128.  workspace: as attn_decode_fwd
+ * with S = max_pages * page_size (attn_decode_workspace_size).  An entry
+ * outside [0, num_pages) is reported through the device status word
+ * (ATTN_ERR_PAGES) and the page is read as zeros (the row's result is then
+ * meaningless, no memory outside the pool is touched). */
+GQA_ATTN_API attn_status attn_decode_paged_fwd(const void* q, const void* k_pages, const void* v_pages,
+                                               const int* block_table, const int* cache_lens, void* o, float* lse,
+                                               void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                                               int Tq, int page_size, int num_pages, int max_pages, int D,
+                                               float scale, void* stream);
 
 /* Static description of a status code. */
 GQA_ATTN_API const char* attn_status_string(attn_status status);

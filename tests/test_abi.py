@@ -127,7 +127,7 @@ def test_workspace_sizes(lib):
 
 def test_status_strings(lib):
     import causal_gqa_attention_fwd_gb300 as g
-    for code in range(11):
+    for code in range(12):
         s = g.status_string(code)
         assert s and s != "unknown status"
     assert g.status_string(99) == "unknown status"
@@ -187,3 +187,29 @@ def test_decode_workspace_size(lib):
     assert lib.attn_decode_workspace_size(8, 12, 2, 1, 2048, 128) == ws_decode(16, 16, 6, 128)
     assert lib.attn_decode_workspace_size(1, 1, 1, 1, 1 << 20, 64) == ws_decode(1, 160, 1, 64)
     assert lib.attn_decode_workspace_size(1, 4, 2, 1, 4096, 80) == 0                            # invalid D
+
+
+def paged(lib, *, ptrs=(A,) * 8, ws_bytes=1 << 40, B=1, Hq=4, Hkv=2, Tq=1, psz=64, num_pages=8, max_pages=8, D=64):
+    return lib.attn_decode_paged_fwd(*ptrs, ws_bytes, B, Hq, Hkv, Tq, psz, num_pages, max_pages, D, 0.125, None)
+
+
+def test_decode_paged_validation(lib):
+    assert paged(lib, psz=48) == 2                          # page size: 16, 32, 64 or a multiple of 128
+    assert paged(lib, psz=8) == 2
+    assert paged(lib, psz=0) == 2                           # no capacity
+    assert paged(lib, num_pages=0) == 2
+    assert paged(lib, Tq=3, psz=16, max_pages=0) == 2
+    assert paged(lib, D=80) == 3
+    p = list((A,) * 8)
+    p[3] = NULL                                             # block_table
+    assert paged(lib, ptrs=tuple(p)) == 1
+    p = list((A,) * 8)
+    p[3] = A + 2                                            # block_table not 4-byte aligned
+    assert paged(lib, ptrs=tuple(p)) == 4
+    p = list((A,) * 8)
+    p[1] = A + 8                                            # k_pages misaligned
+    assert paged(lib, ptrs=tuple(p)) == 4
+    p = list((A,) * 8)
+    p[7] = NULL                                             # workspace (8 pages of 64 = 4 chunks: units can be cut)
+    assert paged(lib, ptrs=tuple(p)) == 6
+    assert paged(lib, ptrs=(NULL,) * 8, B=0) == 0
