@@ -193,3 +193,14 @@ def make_decode_inputs(w: DecodeWorkload, seed=0):
         return paged_decode_inputs(w.B, w.Hq, w.Hkv, w.Tq, w.page_size, w.S // w.page_size, w.D, min_len=w.min_len,
                                    max_len=w.max_len, seed=seed)
     return decode_inputs(w.B, w.Hq, w.Hkv, w.Tq, w.S, w.D, min_len=w.min_len, max_len=w.max_len, seed=seed)
+
+
+def rope_cos_sin_table(positions: int, D: int, base: float = 10000.0):
+    """Rotary table [positions, D] float32: row p holds cos(p * theta_i) for
+    i < D/2, then sin(p * theta_i), theta_i = base^(-2i/D) -- an input of both
+    the kernels and the oracle (as the cos/sin caches serving stacks keep),
+    computed in float64 and rounded once."""
+    i = torch.arange(D // 2, dtype=torch.float64)
+    theta = base ** (-2.0 * i / D)
+    ang = torch.arange(positions, dtype=torch.float64)[:, None] * theta[None, :]
+    return torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32)

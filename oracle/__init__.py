@@ -188,13 +188,36 @@ def varlen_bwd(q, k, v, dout, cu_seqlens, causal: bool = True, scale: float | No
     return r
 
 
-def decode_fwd(q, k_cache, v_cache, cache_lens, scale: float | None = None, lib=None):
+def rope_rotate(x, positions, cos_sin):
+    """Rotary position embedding of vectors x [..., D] at integer positions
+    [...] (the RoPE of MultiHeadAttentionWithRoPE, llm-from-scratch "Project
+    Overview", and the positions-aware RoPE of the microLLM-rocm README):
+    with c = cos_sin[p, :D/2], s = cos_sin[p, D/2:], feature i pairs with
+    feature i + D/2:  x'_i = x_i c_i - x_{i+D/2} s_i,  x'_{i+D/2} = x_{i+D/2} c_i + x_i s_i."""
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    h = D // 2
+    cs = np.asarray(cos_sin, dtype=np.float64)[np.asarray(positions)]
+    c, s = cs[..., :h], cs[..., h:]
+    lo, hi = x[..., :h], x[..., h:]
+    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
+
+
+def decode_fwd(q, k_cache, v_cache, cache_lens, scale: float | None = None, lib=None, rope_cos_sin=None):
     """Attention of the newest Tq positions over a KV cache.
 
     q [B,Hq,Tq,D]; k_cache, v_cache [B,Hkv,S,D]; cache_lens [B] (keys held per
     row, including the Tq new ones).  Query t of row b attends to keys
-    j <= cache_lens[b] - Tq + t.  Returns (O [B,Hq,Tq,D], LSE [B,Hq,Tq])."""
+    j <= cache_lens[b] - Tq + t.  With rope_cos_sin [positions, D] the
+    queries are first rotated (rope_rotate) at their positions
+    cache_lens[b] - Tq + t (the cache holds keys already rotated at theirs).
+    Returns (O [B,Hq,Tq,D], LSE [B,Hq,Tq])."""
     lib = lib or load()
+    if rope_cos_sin is not None:
+        lens_ = np.asarray(cache_lens)
+        Tq_ = np.asarray(q).shape[2]
+        pos = lens_[:, None, None] - Tq_ + np.arange(Tq_)[None, None, :]
+        q = rope_rotate(q, np.broadcast_to(pos, np.asarray(q).shape[:3]), rope_cos_sin)
     q, k, v = _c(q), _c(k_cache), _c(v_cache)
     lens = _cu(cache_lens)
     B, Hq, Tq, D = q.shape
@@ -209,7 +232,8 @@ def decode_fwd(q, k_cache, v_cache, cache_lens, scale: float | None = None, lib=
     return o, lse
 
 
-def paged_decode_fwd(q, k_pages, v_pages, block_table, cache_lens, scale: float | None = None, lib=None):
+def paged_decode_fwd(q, k_pages, v_pages, block_table, cache_lens, scale: float | None = None, lib=None,
+                     rope_cos_sin=None):
     """Cached attention over a paged KV cache.
 
     k_pages, v_pages [num_pages, Hkv, page_size, D] (each page holds page_size
@@ -231,4 +255,4 @@ def paged_decode_fwd(q, k_pages, v_pages, block_table, cache_lens, scale: float 
             page = int(bt[b, i])
             k[b, :, i * psz:(i + 1) * psz] = kp[page]
             v[b, :, i * psz:(i + 1) * psz] = vp[page]
-    return decode_fwd(q, k, v, lens, scale=scale, lib=lib)
+    return decode_fwd(q, k, v, lens, scale=scale, lib=lib, rope_cos_sin=rope_cos_sin)

@@ -332,7 +332,58 @@ def pin_paged_decode_is_contiguous_decode(lib):
         np.testing.assert_array_equal(lse, lc)
 
 
+def _rope_table(P, D, base=10000.0):
+    i = np.arange(D // 2)
+    ang = np.arange(P)[:, None] * base ** (-2.0 * i / D)[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1)
+
+
+def pin_rope_decode(lib):
+    """Rotary decode: position 0 leaves a query as it is and rotation keeps
+    its norm; the scores depend only on relative position, so with keys
+    rotated (here, in test code, by explicit 2x2 rotations) at their
+    positions, shifting every position of a row by the same amount leaves
+    O and LSE unchanged; a non-rotary query differs."""
+    r = _rng(13)
+    D = 8
+    tab = _rope_table(400, D)
+    x = r.standard_normal((5, D))
+    np.testing.assert_allclose(oracle.rope_rotate(x, np.zeros(5, dtype=int), tab), x, atol=0)
+    y = oracle.rope_rotate(x, np.array([1, 7, 50, 300, 399]), tab)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+
+    def rotate_keys(k, start):          # [Hkv, L, D]: pair (i, i + D/2) turned by (start + j) * theta_i
+        out = k.copy()
+        for j in range(k.shape[1]):
+            for i in range(D // 2):
+                a = (start + j) * 10000.0 ** (-2.0 * i / D)
+                c, s = np.cos(a), np.sin(a)
+                lo, hi = k[:, j, i].copy(), k[:, j, i + D // 2].copy()
+                out[:, j, i] = lo * c - hi * s
+                out[:, j, i + D // 2] = hi * c + lo * s
+        return out
+
+    B, Hq, Hkv, Tq, L = 1, 4, 2, 2, 11
+    q = r.standard_normal((B, Hq, Tq, D))
+    k0 = r.standard_normal((B, Hkv, L, D))
+    v = r.standard_normal((B, Hkv, L, D))
+    outs = []
+    for shift in (0, 37, 200):
+        # the same keys, positions shifted: cache rows are positions shift .. shift + L - 1;
+        # the table is indexed from position `shift` on by passing a table that starts there
+        kr = rotate_keys(k0[0], shift)[None]
+        tab_s = _rope_table(400, D)[shift:]
+        outs.append(oracle.decode_fwd(q, kr, v, [L], scale=0.5, lib=lib, rope_cos_sin=tab_s))
+        # positions in the table are relative to the cache start; rotate_keys used absolute shift + j,
+        # tab_s[p] = table[shift + p]: both sides rotate by shift + position
+    for o, l in outs[1:]:
+        np.testing.assert_allclose(o, outs[0][0], atol=1e-12)
+        np.testing.assert_allclose(l, outs[0][1], atol=1e-12)
+    o_plain, _ = oracle.decode_fwd(q, rotate_keys(k0[0], 0)[None], v, [L], scale=0.5, lib=lib)
+    assert np.abs(o_plain - outs[0][0]).max() > 1e-3
+
+
 PINS = [pin_hand_worked, pin_rows_sum_to_one, pin_single_token, pin_constant_keys, pin_shift_invariance,
         pin_gqa_equals_repeated_mha, pin_torch_sdpa, pin_finite_differences, pin_delta_identity,
         pin_varlen_equals_slices, pin_rounding_error_terms, pin_decode_is_dense_suffix,
-        pin_paged_decode_is_contiguous_decode]
+        pin_paged_decode_is_contiguous_decode, pin_rope_decode]
