@@ -39,8 +39,8 @@ SIGNATURES = {
     "attn_profile_reset": (_I, []),
     "attn_profile_read": (_I, [_I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)]),
     "attn_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
-    "attn_decode_fwd": (_I, [_P] * 7 + [_Z, _I, _I, _I, _I, _I, _I, _F, _P]),
-    "attn_decode_paged_fwd": (_I, [_P] * 8 + [_Z] + [_I] * 8 + [_F, _P]),
+    "attn_decode_fwd": (_I, [_P] * 7 + [_Z, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P]),
+    "attn_decode_paged_fwd": (_I, [_P] * 8 + [_Z] + [_I] * 8 + [_F, _P, _I, _P]),
 }
 
 PROFILE_KINDS = {"attn_fwd": 0, "bwd_pre": 1, "bwd_main": 2, "bwd_post": 3, "decode": 4, "decode_merge": 5}
@@ -235,10 +235,18 @@ def attn_decode_workspace_size(B, Hq, Hkv, Tq, S, D) -> int:
     return int(lib().attn_decode_workspace_size(B, Hq, Hkv, Tq, S, D))
 
 
-def attn_decode_fwd(q, k_cache, v_cache, cache_lens, scale=None, o=None, lse=None, workspace=None, stream=None):
+def _rope(rope_cos_sin):
+    if rope_cos_sin is None:
+        return None, 0
+    return _need(rope_cos_sin, "rope_cos_sin", torch.float32), int(rope_cos_sin.shape[0])
+
+
+def attn_decode_fwd(q, k_cache, v_cache, cache_lens, scale=None, o=None, lse=None, workspace=None, stream=None,
+                    rope_cos_sin=None):
     """Cached (decode) attention.  q [B,Hq,Tq,D]; k_cache, v_cache [B,Hkv,S,D] bf16; cache_lens int32
     (device) [B], keys held per row including the Tq new ones; query t of row b sees keys
-    j <= cache_lens[b] - Tq + t -> (o [B,Hq,Tq,D] bf16, lse [B,Hq,Tq] f32)."""
+    j <= cache_lens[b] - Tq + t -> (o [B,Hq,Tq,D] bf16, lse [B,Hq,Tq] f32).  rope_cos_sin: optional
+    float32 (device) [positions, D] rotary table; the queries are rotated at their positions."""
     B, Hq, Tq, D = q.shape
     Hkv, S = k_cache.shape[1], k_cache.shape[2]
     if k_cache.shape != (B, Hkv, S, D) or v_cache.shape != k_cache.shape:
@@ -252,19 +260,20 @@ def attn_decode_fwd(q, k_cache, v_cache, cache_lens, scale=None, o=None, lse=Non
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     ws_ptr = _need(workspace, "workspace", torch.uint8) if workspace is not None else None
     ws_len = workspace.numel() if workspace is not None else 0
+    rope_ptr, rope_n = _rope(rope_cos_sin)
     st = lib().attn_decode_fwd(_need(q, "q"), _need(k_cache, "k_cache"), _need(v_cache, "v_cache"),
                                _need(cache_lens, "cache_lens", torch.int32), _need(o, "o"),
                                _need(lse, "lse", torch.float32), ws_ptr, ws_len, B, Hq, Hkv, Tq, S, D,
-                               _scale(scale, D), _stream(stream))
+                               _scale(scale, D), rope_ptr, rope_n, _stream(stream))
     _check(st, "attn_decode_fwd")
     return o, lse
 
 
 def attn_decode_paged_fwd(q, k_pages, v_pages, block_table, cache_lens, scale=None, o=None, lse=None, workspace=None,
-                          stream=None):
+                          stream=None, rope_cos_sin=None):
     """Cached attention over a paged KV cache.  q [B,Hq,Tq,D]; k_pages, v_pages [num_pages,Hkv,page_size,D]
     bf16; block_table int32 (device) [B, max_pages]; cache_lens int32 (device) [B]
-    -> (o [B,Hq,Tq,D] bf16, lse [B,Hq,Tq] f32)."""
+    -> (o [B,Hq,Tq,D] bf16, lse [B,Hq,Tq] f32).  rope_cos_sin as attn_decode_fwd."""
     B, Hq, Tq, D = q.shape
     num_pages, Hkv, page_size = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
     if k_pages.shape != (num_pages, Hkv, page_size, D) or v_pages.shape != k_pages.shape:
@@ -283,6 +292,6 @@ def attn_decode_paged_fwd(q, k_pages, v_pages, block_table, cache_lens, scale=No
                                      _need(block_table, "block_table", torch.int32),
                                      _need(cache_lens, "cache_lens", torch.int32), _need(o, "o"),
                                      _need(lse, "lse", torch.float32), ws_ptr, ws_len, B, Hq, Hkv, Tq, page_size,
-                                     num_pages, max_pages, D, _scale(scale, D), _stream(stream))
+                                     num_pages, max_pages, D, _scale(scale, D), *_rope(rope_cos_sin), _stream(stream))
     _check(st, "attn_decode_paged_fwd")
     return o, lse

@@ -424,7 +424,7 @@ namespace {
 attn_status decode_common(const void* q, const CUtensorMap& tk, const CUtensorMap& tv, const int* cache_lens,
                           void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
                           int Tq, int S, int D, float scale, const int* block_table, int page_size, int max_pages,
-                          int num_pages, void* stream) {
+                          int num_pages, const float* rope_cos_sin, void* stream) {
   const DecodePlan p = decode_plan(B, Hq, Hkv, Tq, S);
   const size_t need = decode_ws_bytes(p, D);  // checked by the caller
   (void)workspace_bytes;
@@ -464,6 +464,7 @@ attn_status decode_common(const void* q, const CUtensorMap& tk, const CUtensorMa
   a.page_size = page_size;
   a.max_pages = max_pages;
   a.num_pages = num_pages;
+  a.rope_cs = rope_cos_sin;
   CUtensorMap tq;
   const uint64_t qdims[2] = {(uint64_t)D, (uint64_t)B * Hq * Tq};
   const uint64_t qstrides[1] = {(uint64_t)D * 2};
@@ -478,6 +479,15 @@ attn_status decode_check_workspace(int B, int Hq, int Hkv, int Tq, int S, int D,
   const size_t need = decode_ws_bytes(decode_plan(B, Hq, Hkv, Tq, S), D);
   if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return ATTN_ERR_WORKSPACE;
+  return ATTN_OK;
+}
+
+// Rotary table: none, or [rope_positions, D] f32, 16-byte aligned, covering
+// every position a query can take (< S).
+attn_status decode_check_rope(const float* rope_cos_sin, int rope_positions, int S) {
+  if (!rope_cos_sin) return ATTN_OK;
+  if ((reinterpret_cast<uintptr_t>(rope_cos_sin) & 15u)) return ATTN_ERR_ALIGN;
+  if (rope_positions < S) return ATTN_ERR_SHAPE;
   return ATTN_OK;
 }
 
@@ -496,7 +506,8 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Tq, int S, int D) 
 
 attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, const int* cache_lens,
                             void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
-                            int Tq, int S, int D, float scale, void* stream) {
+                            int Tq, int S, int D, float scale, const float* rope_cos_sin, int rope_positions,
+                            void* stream) {
   attn_status st = decode_check(B, Hq, Hkv, Tq, S, D);
   if (st != ATTN_OK) return st;
   if (B == 0 || Tq == 0) return ATTN_OK;
@@ -505,18 +516,20 @@ attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_ca
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse) ||
       (reinterpret_cast<uintptr_t>(cache_lens) & 3u))
     return ATTN_ERR_ALIGN;
+  if ((st = decode_check_rope(rope_cos_sin, rope_positions, S)) != ATTN_OK) return st;
   if ((st = decode_check_workspace(B, Hq, Hkv, Tq, S, D, workspace, workspace_bytes)) != ATTN_OK) return st;
   CUtensorMap tk, tv;
   if (!map_dense(&tk, k_cache, D, S, (long)B * Hkv) || !map_dense(&tv, v_cache, D, S, (long)B * Hkv))
     return ATTN_ERR_CUDA;
   return decode_common(q, tk, tv, cache_lens, o, lse, workspace, workspace_bytes, B, Hq, Hkv, Tq, S, D, scale,
-                       nullptr, 0, 0, 0, stream);
+                       nullptr, 0, 0, 0, rope_cos_sin, stream);
 }
 
 attn_status attn_decode_paged_fwd(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
                                   const int* cache_lens, void* o, float* lse, void* workspace,
                                   size_t workspace_bytes, int B, int Hq, int Hkv, int Tq, int page_size,
-                                  int num_pages, int max_pages, int D, float scale, void* stream) {
+                                  int num_pages, int max_pages, int D, float scale, const float* rope_cos_sin,
+                                  int rope_positions, void* stream) {
   if (page_size < 0 || num_pages < 0 || max_pages < 0) return ATTN_ERR_SHAPE;
   const long S = (long)page_size * max_pages;
   if (S > 0x7fffffffL) return ATTN_ERR_SHAPE;
@@ -530,6 +543,7 @@ attn_status attn_decode_paged_fwd(const void* q, const void* k_pages, const void
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) || !aligned16(lse) ||
       (reinterpret_cast<uintptr_t>(cache_lens) & 3u) || (reinterpret_cast<uintptr_t>(block_table) & 3u))
     return ATTN_ERR_ALIGN;
+  if ((st = decode_check_rope(rope_cos_sin, rope_positions, (int)S)) != ATTN_OK) return st;
   if ((st = decode_check_workspace(B, Hq, Hkv, Tq, (int)S, D, workspace, workspace_bytes)) != ATTN_OK) return st;
   const int box = page_size < 128 ? page_size : 128;
   CUtensorMap tk, tv;
@@ -537,7 +551,7 @@ attn_status attn_decode_paged_fwd(const void* q, const void* k_pages, const void
       !map_dense(&tv, v_pages, D, page_size, (long)num_pages * Hkv, box))
     return ATTN_ERR_CUDA;
   return decode_common(q, tk, tv, cache_lens, o, lse, workspace, workspace_bytes, B, Hq, Hkv, Tq, (int)S, D, scale,
-                       block_table, page_size, max_pages, num_pages, stream);
+                       block_table, page_size, max_pages, num_pages, rope_cos_sin, stream);
 }
 
 // ------------------------------------------------- allocation-free backward

@@ -29,7 +29,11 @@
 //              K chunk is released as soon as its score MMA is done, a V
 //              chunk only after P V, so K refills run further ahead.
 //   warp 1     score MMA issuer (S^T into a double buffer, so the softmax of
-//              one chunk overlaps the score MMA of the next); TMEM owner.
+//              one chunk overlaps the score MMA of the next); TMEM owner;
+//              with a rotary table it first rotates each piece's query
+//              rows in place at their positions (positions-aware RoPE),
+//              keeping the rounding remainder in a second bf16 tile that a
+//              second set of score MMAs adds in.
 //   warp 7     P V MMA issuer: O^T += V^T P^T as soon as a chunk's P and V
 //              are ready, independently of the score issuer.
 //   warps 2-5  softmax: thread = key for S^T (and = feature for O^T); row
@@ -66,8 +70,8 @@ struct DecCfg {
   static constexpr int kOffV = kSlots * kTileBytes;
   static constexpr int kQBytes = NB * kRowBoxBytes;       // 16 query rows, K-major
   static constexpr int kPBytes = 2 * kRowBoxBytes;        // 16 rows x 128 keys, K-major
-  static constexpr int kOffQ = 2 * kSlots * kTileBytes;
-  static constexpr int kOffP = kOffQ + 2 * kQBytes;
+  static constexpr int kOffQ = 2 * kSlots * kTileBytes;         // [2 slots][value tile, remainder tile]
+  static constexpr int kOffP = kOffQ + 4 * kQBytes;
   static constexpr int kOffMax = kOffP + 2 * kPBytes;           // f32 [2][16 rows][4 warps]
   static constexpr int kOffSum = kOffMax + 2 * kRows * 4 * 4;   // f32 [16 rows][4 warps]
   static constexpr int kOffFin = kOffSum + kRows * 4 * 4;       // float2 [2 pieces][16 rows]: (max, sum)
@@ -264,6 +268,63 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 }  // namespace
 
+// Rotary embedding of a piece's query rows (one warp, out of line), written
+// back as bf16 value (over the loaded rows) plus bf16 remainder (qrem):
+// row r is query position t = (r0 + r) % Tq of its head, at position
+// len - Tq + t of the row; feature i pairs with i + D/2 (rotate-half),
+// x'_i = x_i c - x_{i+D/2} s, x'_{i+D/2} = x_{i+D/2} c + x_i s with c, s from
+// the table row of that position.  The tile is K-major, 128-byte swizzled:
+// feature d of row r sits in box d / 64, 16-byte chunk ((d % 64) / 8) ^ (r % 8).
+template <int D>
+__device__ __noinline__ void rope_rotate_tile(uint8_t* qs, uint8_t* qrem, const Piece& it, const DecodeArgs& a,
+                                              int lane) {
+  constexpr int H = D / 2;
+  constexpr int kChunks = H / 8;  // 8-feature chunks of the low half
+  auto off = [&](int r, int d) { return (d >> 6) * kRowBoxBytes + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4); };
+  auto at = [&](int r, int d) -> uint4* { return reinterpret_cast<uint4*>(qs + off(r, d)); };
+  auto rem = [&](int r, int d) -> uint4* { return reinterpret_cast<uint4*>(qrem + off(r, d)); };
+  for (int idx = lane; idx < kRows * kChunks; idx += 32) {
+    const int r = idx / kChunks, d0 = (idx % kChunks) * 8;
+    if (r >= it.rows) {  // unused rows: no remainder
+      *rem(r, d0) = make_uint4(0, 0, 0, 0);
+      *rem(r, d0 + H) = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const int pos = it.len - a.Tq + (it.r0 + r) % a.Tq;
+    const float* cs = a.rope_cs + (long)pos * D;
+    const float4 c0 = *reinterpret_cast<const float4*>(cs + d0), c1 = *reinterpret_cast<const float4*>(cs + d0 + 4);
+    const float4 s0 = *reinterpret_cast<const float4*>(cs + H + d0);
+    const float4 s1 = *reinterpret_cast<const float4*>(cs + H + d0 + 4);
+    const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    uint4 lo = *at(r, d0), hi = *at(r, d0 + H), rlo, rhi;
+    uint32_t* l32 = reinterpret_cast<uint32_t*>(&lo);
+    uint32_t* h32 = reinterpret_cast<uint32_t*>(&hi);
+    uint32_t* rl32 = reinterpret_cast<uint32_t*>(&rlo);
+    uint32_t* rh32 = reinterpret_cast<uint32_t*>(&rhi);
+    // value = bf16(y), remainder = bf16(y - value): the pair carries y to ~2^-16
+    auto split = [](float y0, float y1, uint32_t& v, uint32_t& rm) {
+      v = pack_bf16x2(y0, y1);
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+      rm = pack_bf16x2(y0 - b.x, y1 - b.y);
+    };
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 xl = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&l32[e]));
+      const float2 xh = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&h32[e]));
+      const float yl0 = fmaf(xl.x, c[2 * e], -xh.x * sn[2 * e]), yh0 = fmaf(xh.x, c[2 * e], xl.x * sn[2 * e]);
+      const float yl1 = fmaf(xl.y, c[2 * e + 1], -xh.y * sn[2 * e + 1]);
+      const float yh1 = fmaf(xh.y, c[2 * e + 1], xl.y * sn[2 * e + 1]);
+      split(yl0, yl1, l32[e], rl32[e]);
+      split(yh0, yh1, h32[e], rh32[e]);
+    }
+    *at(r, d0) = lo;
+    *at(r, d0 + H) = hi;
+    *rem(r, d0) = rlo;
+    *rem(r, d0 + H) = rhi;
+  }
+}
+
 // A piece's output (softmax warps, once per piece, out of line): wait for
 // its O^T, read this thread's feature row of it, release the buffer and
 // write O / LSE (one-split unit) or the unnormalised partial and its
@@ -402,8 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_expect_tx(&bars.q_full[qslot], C::kQBytes);
 #pragma unroll
             for (int x = 0; x < NB; ++x)
-              tma_load_2d(smem + C::kOffQ + qslot * C::kQBytes + x * kRowBoxBytes, &tm_q, &bars.q_full[qslot], x * 64,
-                          row0);
+              tma_load_2d(smem + C::kOffQ + qslot * 2 * C::kQBytes + x * kRowBoxBytes, &tm_q, &bars.q_full[qslot],
+                          x * 64, row0);
             last_q[qslot] = (uses >> 1) & 1;
           }
         }
@@ -478,17 +539,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ===================== score MMA issuer (warp-uniform, one elected lane issues)
     for (Cursor cur = begin(); cur.valid; next(cur)) {
       const int qslot = cur.uses & 1, slot = cur.cs % SL, sb = cur.cs & 1;
-      if (cur.c == 0) mbar_wait(&bars.q_full[qslot], (cur.uses >> 1) & 1, guard);
+      if (cur.c == 0) {
+        mbar_wait(&bars.q_full[qslot], (cur.uses >> 1) & 1, guard);
+        if (a.rope_cs != nullptr) {
+          uint8_t* qt = smem + C::kOffQ + qslot * 2 * C::kQBytes;
+          rope_rotate_tile<D>(qt, qt + C::kQBytes, cur.it, a, lane);
+          fence_proxy_async_smem();  // the rotated tiles are read by the MMAs below
+          __syncwarp();
+        }
+      }
       mbar_wait(&bars.k_full[slot], (cur.cs / SL) & 1, guard);
       if (cur.cs >= 2) mbar_wait(&bars.s_empty[sb], ((cur.cs >> 1) - 1) & 1, guard);
       tc_fence_after();
       if (!guard.aborted()) {
         const uint32_t ka = sbase + slot * C::kTileBytes;
-        const uint32_t qa = sbase + C::kOffQ + qslot * C::kQBytes;
+        const uint32_t qa = sbase + C::kOffQ + qslot * 2 * C::kQBytes;
+        // rotary queries are a bf16 value tile plus a bf16 remainder tile: both accumulate
+        const int tiles = a.rope_cs != nullptr ? 2 : 1;
+        for (int tq = 0; tq < tiles; ++tq)
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss_warp(tmem + col_s(sb), sdesc_sw128(ka + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
-                      sdesc_sw128(qa + (kk >> 2) * kRowBoxBytes + (kk & 3) * 32, 16, 1024), C::kIdescS, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss_warp(tmem + col_s(sb), sdesc_sw128(ka + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                        sdesc_sw128(qa + tq * C::kQBytes + (kk >> 2) * kRowBoxBytes + (kk & 3) * 32, 16, 1024),
+                        C::kIdescS, (tq > 0 || kk > 0) ? 1u : 0u);
       }
       tc_commit_warp(&bars.s_full[sb]);
       tc_commit_warp(&bars.k_empty[slot]);

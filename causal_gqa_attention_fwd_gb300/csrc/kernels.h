@@ -98,6 +98,8 @@ struct DecodeArgs {
   // position j of row b is row j % page_size of page block_table[b * max_pages + j / page_size]
   const int* block_table; // device, nullptr for contiguous caches
   int page_size, max_pages, num_pages;
+  // rotary queries: rope_cs [positions, D] f32 (cos half, then sin half), nullptr = none
+  const float* rope_cs;
 };
 
 // k, v: dense maps over the caches ([B*Hkv, S, D], 64 x 128 boxes) or, paged,

@@ -154,10 +154,21 @@ GQA_ATTN_API attn_status attn_varlen_bwd(const void* q, const void* k, const voi
  * key range is not split.  Limits: Tq <= S; B*Hq*Tq < 2^31. */
 GQA_ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Tq, int S, int D);
 
+/* Rotary queries (positions-aware RoPE of the microLLM-rocm README, section
+ * "Why this project exists"; RoPE / MultiHeadAttentionWithRoPE of the
+ * llm-from-scratch "Project Overview"), for both decode entry points:
+ * rope_cos_sin NULL = none; otherwise a DEVICE float32 table
+ * [rope_positions, D], 16-byte aligned, rope_positions >= the cache capacity
+ * (S, or max_pages * page_size): row p holds cos(p*theta_i) for i < D/2, then
+ * sin(p*theta_i).  Each query t of row b is rotated at its position
+ * p = cache_lens[b] - Tq + t before the scores: feature i pairs with feature
+ * i + D/2, x'_i = x_i cos - x_{i+D/2} sin, x'_{i+D/2} = x_{i+D/2} cos + x_i sin,
+ * rounded to bf16.  The cache must hold keys already rotated at their
+ * positions (as appending them rotated leaves them). */
 GQA_ATTN_API attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
                                          const int* cache_lens, void* o, float* lse, void* workspace,
                                          size_t workspace_bytes, int B, int Hq, int Hkv, int Tq, int S, int D,
-                                         float scale, void* stream);
+                                         float scale, const float* rope_cos_sin, int rope_positions, void* stream);
 
 /* Cached attention over a PAGED KV cache (the paged KV-cache management of
  * the RoseLLM README, section "Inference and serving").  Same queries, mask
@@ -179,7 +190,8 @@ GQA_ATTN_API attn_status attn_decode_paged_fwd(const void* q, const void* k_page
                                                const int* block_table, const int* cache_lens, void* o, float* lse,
                                                void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
                                                int Tq, int page_size, int num_pages, int max_pages, int D,
-                                               float scale, void* stream);
+                                               float scale, const float* rope_cos_sin, int rope_positions,
+                                               void* stream);
 
 /* Static description of a status code. */
 GQA_ATTN_API const char* attn_status_string(attn_status status);

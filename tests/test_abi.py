@@ -141,8 +141,8 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
         _binding.lib()
 
 
-def dec(lib, *, ptrs=(A,) * 7, ws_bytes=1 << 40, B=1, Hq=4, Hkv=2, Tq=1, S=4096, D=64, scale=0.125):
-    return lib.attn_decode_fwd(*ptrs, ws_bytes, B, Hq, Hkv, Tq, S, D, scale, None)
+def dec(lib, *, ptrs=(A,) * 7, ws_bytes=1 << 40, B=1, Hq=4, Hkv=2, Tq=1, S=4096, D=64, scale=0.125, rope=(None, 0)):
+    return lib.attn_decode_fwd(*ptrs, ws_bytes, B, Hq, Hkv, Tq, S, D, scale, *rope, None)
 
 
 def test_decode_validation(lib):
@@ -166,6 +166,8 @@ def test_decode_validation(lib):
     assert dec(lib, ws_bytes=64) == 6
     assert dec(lib, ptrs=(NULL,) * 7, B=0) == 0
     assert dec(lib, ptrs=(NULL,) * 7, Tq=0) == 0
+    assert dec(lib, rope=(A + 4, 4096)) == 4                 # rotary table not 16-byte aligned
+    assert dec(lib, rope=(A, 4095)) == 2                     # table shorter than the cache capacity
 
 
 def ws_decode(units, slots, rows_ws, D):
@@ -189,8 +191,9 @@ def test_decode_workspace_size(lib):
     assert lib.attn_decode_workspace_size(1, 4, 2, 1, 4096, 80) == 0                            # invalid D
 
 
-def paged(lib, *, ptrs=(A,) * 8, ws_bytes=1 << 40, B=1, Hq=4, Hkv=2, Tq=1, psz=64, num_pages=8, max_pages=8, D=64):
-    return lib.attn_decode_paged_fwd(*ptrs, ws_bytes, B, Hq, Hkv, Tq, psz, num_pages, max_pages, D, 0.125, None)
+def paged(lib, *, ptrs=(A,) * 8, ws_bytes=1 << 40, B=1, Hq=4, Hkv=2, Tq=1, psz=64, num_pages=8, max_pages=8, D=64,
+          rope=(None, 0)):
+    return lib.attn_decode_paged_fwd(*ptrs, ws_bytes, B, Hq, Hkv, Tq, psz, num_pages, max_pages, D, 0.125, *rope, None)
 
 
 def test_decode_paged_validation(lib):
@@ -213,3 +216,4 @@ def test_decode_paged_validation(lib):
     p[7] = NULL                                             # workspace (8 pages of 64 = 4 chunks: units can be cut)
     assert paged(lib, ptrs=tuple(p)) == 6
     assert paged(lib, ptrs=(NULL,) * 8, B=0) == 0
+    assert paged(lib, rope=(A, 511)) == 2                     # capacity 8 pages x 64

@@ -129,3 +129,30 @@ def test_decode_workspace_reuse(gq):
         ro, rlse = run_oracle(x, 0.1)
         check("o", o, ro, TOL_REL_O)
         check_lse(lse, rlse)
+
+
+ROPE_CASES = [
+    # B, Hq, Hkv, Tq, S, D, cache_lens
+    (3, 8, 2, 2, 700, 128, [700, 2, 389]),
+    (2, 14, 2, 1, 600, 64, [600, 130]),
+    (2, 4, 1, 3, 20000, 128, [20000, 16385]),
+    (2, 16, 2, 4, 640, 128, [640, 385]),
+]
+
+
+@pytest.mark.parametrize("case", ROPE_CASES, ids=lambda c: "B%d_Hq%d_Hkv%d_Tq%d_S%d_D%d" % c[:6])
+def test_rope_decode_matches_oracle(gq, case):
+    """Queries rotated in the kernel at cache_lens[b] - Tq + t (positions up to 20K)."""
+    B, Hq, Hkv, Tq, S, D, lens = case
+    x = W.decode_inputs(B, Hq, Hkv, Tq, S, D, cache_lens=lens, seed=17)
+    tab = W.rope_cos_sin_table(S, D)
+    scale = 1.0 / np.sqrt(D)
+    q, k, v, ln = (x[n].cuda() for n in ("q", "k_cache", "v_cache", "cache_lens"))
+    o, lse = gq.attn_decode_fwd(q, k, v, ln, scale=scale, rope_cos_sin=tab.cuda())
+    assert gq.get_device_status() == 0
+    ro, rlse = oracle.decode_fwd(to64(x["q"]), to64(x["k_cache"]), to64(x["v_cache"]), x["cache_lens"].numpy(),
+                                 scale=scale, rope_cos_sin=tab.double().numpy())
+    check("o", o, ro, TOL_REL_O)
+    check_lse(lse, rlse)
+    plain, _ = run_gpu(gq, x, scale)
+    assert not torch.equal(plain, o)

@@ -96,3 +96,16 @@ def test_paged_decode_workloads_full(gq, name):
     ro, rlse = run_oracle(x, w.softmax_scale)
     check("o", o, ro, TOL_REL_O)
     check_lse(lse, rlse)
+
+
+def test_paged_rope_decode(gq):
+    B, Hq, Hkv, Tq, psz, maxp, D = 3, 8, 2, 2, 32, 40, 128
+    x = W.paged_decode_inputs(B, Hq, Hkv, Tq, psz, maxp, D, cache_lens=[1280, 2, 777], seed=8)
+    tab = W.rope_cos_sin_table(psz * maxp, D)
+    o, lse = run_gpu(gq, x, 0.09, rope_cos_sin=tab.cuda())
+    assert gq.get_device_status() == 0
+    ro, rlse = oracle.paged_decode_fwd(to64(x["q"]), to64(x["k_pages"]), to64(x["v_pages"]),
+                                       x["block_table"].numpy(), x["cache_lens"].numpy(), scale=0.09,
+                                       rope_cos_sin=tab.double().numpy())
+    check("o", o, ro, TOL_REL_O)
+    check_lse(lse, rlse)
