@@ -256,3 +256,26 @@ def paged_decode_fwd(q, k_pages, v_pages, block_table, cache_lens, scale: float 
             k[b, :, i * psz:(i + 1) * psz] = kp[page]
             v[b, :, i * psz:(i + 1) * psz] = vp[page]
     return decode_fwd(q, k, v, lens, scale=scale, lib=lib, rope_cos_sin=rope_cos_sin)
+
+
+def e4m3_decode(codes):
+    """Values of FP8 E4M3 codes (uint8): sign bit, 4 exponent bits (bias 7), 3
+    mantissa bits; exponent 0 is subnormal (m/8 * 2^-6); no infinities; the
+    two codes with all exponent and mantissa bits set are NaN."""
+    c = np.asarray(codes).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    val = np.where((e == 15) & (m == 7), np.nan, val)
+    return sign * val
+
+
+def fp8_decode_fwd(q, k8, v8, k_scale, v_scale, cache_lens, scale: float | None = None, lib=None, rope_cos_sin=None):
+    """Cached attention over FP8 E4M3 caches with per-tensor scales (the FP8
+    quantize / dequantize and KV-cache work of the microLLM-rocm README,
+    section "Why this project exists"): K = e4m3(k8) * k_scale,
+    V = e4m3(v8) * v_scale, then ``decode_fwd``."""
+    k = e4m3_decode(k8) * float(k_scale)
+    v = e4m3_decode(v8) * float(v_scale)
+    return decode_fwd(q, k, v, cache_lens, scale=scale, lib=lib, rope_cos_sin=rope_cos_sin)

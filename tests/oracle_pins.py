@@ -383,7 +383,31 @@ def pin_rope_decode(lib):
     assert np.abs(o_plain - outs[0][0]).max() > 1e-3
 
 
+def pin_fp8_decode(lib):
+    """E4M3 decoding matches PyTorch's float8_e4m3fn for all 256 codes (NaN
+    codes included) and the worked values of the format (1.0, 448, 2^-9);
+    FP8-cache decode equals decode over the decoded, scaled caches."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(mine[ok], ref[ok])
+    assert mine[0x38] == 1.0 and mine[0x7E] == 448.0 and mine[0x01] == 2.0 ** -9 and mine[0xB8] == -1.0
+    r = _rng(14)
+    B, Hq, Hkv, Tq, S, D = 2, 4, 2, 1, 9, 8
+    q = r.standard_normal((B, Hq, Tq, D))
+    k8 = r.integers(0, 0x7E, (B, Hkv, S, D)).astype(np.uint8) | (r.integers(0, 2, (B, Hkv, S, D)) << 7).astype(np.uint8)
+    v8 = r.integers(0, 0x7E, (B, Hkv, S, D)).astype(np.uint8)
+    lens = [9, 4]
+    o, l = oracle.fp8_decode_fwd(q, k8, v8, 0.01, 0.02, lens, scale=0.3, lib=lib)
+    o2, l2 = oracle.decode_fwd(q, mine[k8] * 0.01, mine[v8] * 0.02, lens, scale=0.3, lib=lib)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(l, l2)
+
+
 PINS = [pin_hand_worked, pin_rows_sum_to_one, pin_single_token, pin_constant_keys, pin_shift_invariance,
         pin_gqa_equals_repeated_mha, pin_torch_sdpa, pin_finite_differences, pin_delta_identity,
         pin_varlen_equals_slices, pin_rounding_error_terms, pin_decode_is_dense_suffix,
-        pin_paged_decode_is_contiguous_decode, pin_rope_decode]
+        pin_paged_decode_is_contiguous_decode, pin_rope_decode, pin_fp8_decode]
