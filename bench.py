@@ -210,10 +210,11 @@ DECODE_UNIT = "GB/s"
 
 def decode_bytes(w: W.DecodeWorkload, lens) -> int:
     """Algorithmic bytes of one decode call: K and V rows inside each row's
-    cache, Q read, O written (bf16), LSE written (f32), the lengths (paged:
-    and the block-table entries of the pages that hold keys)."""
+    cache (2 bytes each, 1 for E4M3 caches), Q read, O written (bf16), LSE
+    written (f32), the lengths (paged: and the block-table entries of the
+    pages that hold keys)."""
     lens = torch.as_tensor(lens, dtype=torch.int64)
-    kv = 2 * w.Hkv * w.D * 2 * int(lens.sum())
+    kv = 2 * w.Hkv * w.D * (1 if w.fp8 else 2) * int(lens.sum())
     qo = 2 * w.B * w.Hq * w.Tq * w.D * 2
     table = 4 * int(((lens + w.page_size - 1) // w.page_size).sum()) if w.page_size else 0
     return kv + qo + w.B * w.Hq * w.Tq * 4 + w.B * 4 + table
@@ -237,7 +238,11 @@ def oracle_decode_sample(w: W.DecodeWorkload, x, budget_s: float):
     while rows == 0 or (elapsed < budget_s and rows < w.B):
         b = rows
         lens = x["cache_lens"][b:b + 1]
-        if w.page_size:
+        if w.fp8:
+            args = (f(x["q"][b:b + 1]), x["k8"][b:b + 1].numpy(), x["v8"][b:b + 1].numpy(), x["k_scale"],
+                    x["v_scale"], lens.numpy())
+            fn = oracle.fp8_decode_fwd
+        elif w.page_size:
             args = (f(x["q"][b:b + 1]), kp, vp, x["block_table"][b:b + 1].numpy(), lens.numpy())
             fn = oracle.paged_decode_fwd
         else:
@@ -248,7 +253,7 @@ def oracle_decode_sample(w: W.DecodeWorkload, x, budget_s: float):
         elapsed += time.perf_counter() - t0
         rows += 1
         one = W.DecodeWorkload("s", B=1, Hq=w.Hq, Hkv=w.Hkv, Tq=w.Tq, S=w.S, D=w.D, min_len=0, max_len=0,
-                               page_size=w.page_size)
+                               page_size=w.page_size, fp8=w.fp8)
         done += decode_bytes(one, lens)
     desc = f"{rows} of {w.B} batch rows of {w.name} (whole caches), fp64, {elapsed:.1f} s"
     return done / elapsed, desc, cores, elapsed
@@ -260,6 +265,8 @@ def decode_config(w: W.DecodeWorkload, world: int, l2: str):
          "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "l2": l2}
     if w.page_size:
         c["paged"] = f"pages of {w.page_size} positions, [num_pages, Hkv, page, D], shuffled over the pool"
+    if w.fp8:
+        c["kv_cache"] = "E4M3 codes with one scale per cache (amax -> 448), N(0,1) source values"
     return c
 
 
@@ -270,8 +277,12 @@ def run_decode(args, world, rank, local):
     w = W.DECODE_WORKLOADS[args.workload]
     x = W.make_decode_inputs(w, seed=rank)
     stream = torch.cuda.current_stream()
-    names = ("q", "k_pages", "v_pages", "block_table", "cache_lens") if w.page_size else \
-        ("q", "k_cache", "v_cache", "cache_lens")
+    if w.fp8:
+        names = ("q", "k8", "v8", "cache_lens")
+    elif w.page_size:
+        names = ("q", "k_pages", "v_pages", "block_table", "cache_lens")
+    else:
+        names = ("q", "k_cache", "v_cache", "cache_lens")
     dx = {n: x[n].to(dev) for n in names}
     q, lens = dx["q"], dx["cache_lens"]
     scale = w.softmax_scale
@@ -281,7 +292,10 @@ def run_decode(args, world, rank, local):
     lse = torch.empty((w.B, w.Hq, w.Tq), dtype=torch.float32, device=dev)
 
     def step():
-        if w.page_size:
+        if w.fp8:
+            gq.attn_decode_fp8_fwd(q, dx["k8"], dx["v8"], x["k_scale"], x["v_scale"], lens, scale=scale, o=o,
+                                   lse=lse, workspace=ws)
+        elif w.page_size:
             gq.attn_decode_paged_fwd(q, dx["k_pages"], dx["v_pages"], dx["block_table"], lens, scale=scale, o=o,
                                      lse=lse, workspace=ws)
         else:
@@ -391,7 +405,8 @@ def run_decode(args, world, rank, local):
         line = {
             "metric": DECODE_METRIC, "value": value, "unit": DECODE_UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16 in, f32 arithmetic", "data": "synthetic",
+            "vs_baseline": None, "data": "synthetic",
+            "dtype": "E4M3 K/V + bf16 q, f16 MMA operands, f32 arithmetic" if w.fp8 else "bf16 in, f32 arithmetic",
             "config": decode_config(w, world, flush.describe()),
             "frac_of_peak": value / pk["hbm_gbs"],
             "tokens_per_s": world * w.B * w.Tq * args.steps / (total_ms / 1e3),

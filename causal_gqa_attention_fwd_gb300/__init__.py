@@ -9,6 +9,7 @@ PyTorch CUDA tensors (PyTorch supplies device memory and the stream):
     attn_varlen_bwd(q, k, v, o, lse, dout, cu_seqlens, max_seqlen, ...) -> (dq, dk, dv)
     attn_decode_fwd(q, k_cache, v_cache, cache_lens, scale=None) -> (o, lse)
     attn_decode_paged_fwd(q, k_pages, v_pages, block_table, cache_lens, scale=None) -> (o, lse)
+    attn_decode_fp8_fwd / attn_decode_paged_fp8_fwd: the same over E4M3 caches with per-tensor scales
 
 All arithmetic runs in the library's hand-written sm_103a kernels; a call
 raises if the library is not built.
@@ -19,7 +20,9 @@ from ._binding import (  # noqa: F401
     attn_bwd,
     attn_bwd_noalloc,
     attn_bwd_workspace_size,
+    attn_decode_fp8_fwd,
     attn_decode_fwd,
+    attn_decode_paged_fp8_fwd,
     attn_decode_paged_fwd,
     attn_decode_workspace_size,
     attn_fwd,

@@ -41,6 +41,8 @@ SIGNATURES = {
     "attn_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
     "attn_decode_fwd": (_I, [_P] * 7 + [_Z, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P]),
     "attn_decode_paged_fwd": (_I, [_P] * 8 + [_Z] + [_I] * 8 + [_F, _P, _I, _P]),
+    "attn_decode_fp8_fwd": (_I, [_P, _P, _P, _F, _F] + [_P] * 4 + [_Z] + [_I] * 6 + [_F, _P, _I, _P]),
+    "attn_decode_paged_fp8_fwd": (_I, [_P, _P, _P, _F, _F] + [_P] * 5 + [_Z] + [_I] * 8 + [_F, _P, _I, _P]),
 }
 
 PROFILE_KINDS = {"attn_fwd": 0, "bwd_pre": 1, "bwd_main": 2, "bwd_post": 3, "decode": 4, "decode_merge": 5}
@@ -294,4 +296,54 @@ def attn_decode_paged_fwd(q, k_pages, v_pages, block_table, cache_lens, scale=No
                                      _need(lse, "lse", torch.float32), ws_ptr, ws_len, B, Hq, Hkv, Tq, page_size,
                                      num_pages, max_pages, D, _scale(scale, D), *_rope(rope_cos_sin), _stream(stream))
     _check(st, "attn_decode_paged_fwd")
+    return o, lse
+
+
+def attn_decode_fp8_fwd(q, k8, v8, k_scale: float, v_scale: float, cache_lens, scale=None, o=None, lse=None,
+                        workspace=None, stream=None, rope_cos_sin=None):
+    """Cached attention over FP8 (E4M3) caches.  k8, v8 uint8 [B,Hkv,S,D] (E4M3 codes), K = e4m3(k8) * k_scale,
+    V = e4m3(v8) * v_scale; everything else as attn_decode_fwd."""
+    B, Hq, Tq, D = q.shape
+    Hkv, S = k8.shape[1], k8.shape[2]
+    if k8.shape != (B, Hkv, S, D) or v8.shape != k8.shape:
+        raise ValueError("k8, v8 must be [B, Hkv, S, D] matching q")
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws_bytes = attn_decode_workspace_size(B, Hq, Hkv, Tq, S, D)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ws_ptr = _need(workspace, "workspace", torch.uint8) if workspace is not None else None
+    ws_len = workspace.numel() if workspace is not None else 0
+    st = lib().attn_decode_fp8_fwd(_need(q, "q"), _need(k8, "k8", torch.uint8), _need(v8, "v8", torch.uint8),
+                                   float(k_scale), float(v_scale), _need(cache_lens, "cache_lens", torch.int32),
+                                   _need(o, "o"), _need(lse, "lse", torch.float32), ws_ptr, ws_len, B, Hq, Hkv, Tq, S,
+                                   D, _scale(scale, D), *_rope(rope_cos_sin), _stream(stream))
+    _check(st, "attn_decode_fp8_fwd")
+    return o, lse
+
+
+def attn_decode_paged_fp8_fwd(q, k8_pages, v8_pages, k_scale: float, v_scale: float, block_table, cache_lens,
+                              scale=None, o=None, lse=None, workspace=None, stream=None, rope_cos_sin=None):
+    """Cached attention over paged FP8 (E4M3) caches: k8_pages, v8_pages uint8 [num_pages,Hkv,page_size,D];
+    otherwise as attn_decode_paged_fwd and attn_decode_fp8_fwd."""
+    B, Hq, Tq, D = q.shape
+    num_pages, Hkv, page_size = k8_pages.shape[0], k8_pages.shape[1], k8_pages.shape[2]
+    if k8_pages.shape != (num_pages, Hkv, page_size, D) or v8_pages.shape != k8_pages.shape:
+        raise ValueError("k8_pages, v8_pages must be [num_pages, Hkv, page_size, D] matching q")
+    max_pages = block_table.shape[1]
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws_bytes = attn_decode_workspace_size(B, Hq, Hkv, Tq, max_pages * page_size, D)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ws_ptr = _need(workspace, "workspace", torch.uint8) if workspace is not None else None
+    ws_len = workspace.numel() if workspace is not None else 0
+    st = lib().attn_decode_paged_fp8_fwd(_need(q, "q"), _need(k8_pages, "k8_pages", torch.uint8),
+                                         _need(v8_pages, "v8_pages", torch.uint8), float(k_scale), float(v_scale),
+                                         _need(block_table, "block_table", torch.int32),
+                                         _need(cache_lens, "cache_lens", torch.int32), _need(o, "o"),
+                                         _need(lse, "lse", torch.float32), ws_ptr, ws_len, B, Hq, Hkv, Tq, page_size,
+                                         num_pages, max_pages, D, _scale(scale, D), *_rope(rope_cos_sin),
+                                         _stream(stream))
+    _check(st, "attn_decode_paged_fp8_fwd")
     return o, lse

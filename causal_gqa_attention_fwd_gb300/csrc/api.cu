@@ -424,7 +424,8 @@ namespace {
 attn_status decode_common(const void* q, const CUtensorMap& tk, const CUtensorMap& tv, const int* cache_lens,
                           void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
                           int Tq, int S, int D, float scale, const int* block_table, int page_size, int max_pages,
-                          int num_pages, const float* rope_cos_sin, void* stream) {
+                          int num_pages, const float* rope_cos_sin, bool fp8, float k_scale, float v_scale,
+                          void* stream) {
   const DecodePlan p = decode_plan(B, Hq, Hkv, Tq, S);
   const size_t need = decode_ws_bytes(p, D);  // checked by the caller
   (void)workspace_bytes;
@@ -459,7 +460,9 @@ attn_status decode_common(const void* q, const CUtensorMap& tk, const CUtensorMa
   // one CTA per SM (the kernel holds most of an SM's shared memory), never
   // more than the workspace has slots for
   a.ctas = sms < gqa::kDecodeMaxSlots ? sms : gqa::kDecodeMaxSlots;
-  a.scale_log2 = scale * 1.4426950408889634f;
+  a.scale_log2 = scale * (fp8 ? k_scale : 1.f) * 1.4426950408889634f;
+  a.fp8 = fp8 ? 1 : 0;
+  a.v_scale = fp8 ? v_scale : 1.f;
   a.block_table = block_table;
   a.page_size = page_size;
   a.max_pages = max_pages;
@@ -489,6 +492,15 @@ attn_status decode_check_rope(const float* rope_cos_sin, int rope_positions, int
   if ((reinterpret_cast<uintptr_t>(rope_cos_sin) & 15u)) return ATTN_ERR_ALIGN;
   if (rope_positions < S) return ATTN_ERR_SHAPE;
   return ATTN_OK;
+}
+
+// 8-bit cache [N, T, D] seen as 3-D (D, T, N): unswizzled boxes of whole
+// D-byte rows, box_rows rows.
+bool map_bytes(CUtensorMap* m, const void* base, int D, int T, long n, int box_rows) {
+  const uint64_t dims[3] = {(uint64_t)D, (uint64_t)T, (uint64_t)n};
+  const uint64_t strides[2] = {(uint64_t)D, (uint64_t)T * D};
+  const uint32_t box[3] = {(uint32_t)D, (uint32_t)box_rows, 1};
+  return gqa::make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 bool decode_page_size_ok(int page_size) {
@@ -522,7 +534,7 @@ attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_ca
   if (!map_dense(&tk, k_cache, D, S, (long)B * Hkv) || !map_dense(&tv, v_cache, D, S, (long)B * Hkv))
     return ATTN_ERR_CUDA;
   return decode_common(q, tk, tv, cache_lens, o, lse, workspace, workspace_bytes, B, Hq, Hkv, Tq, S, D, scale,
-                       nullptr, 0, 0, 0, rope_cos_sin, stream);
+                       nullptr, 0, 0, 0, rope_cos_sin, false, 1.f, 1.f, stream);
 }
 
 attn_status attn_decode_paged_fwd(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
@@ -551,7 +563,57 @@ attn_status attn_decode_paged_fwd(const void* q, const void* k_pages, const void
       !map_dense(&tv, v_pages, D, page_size, (long)num_pages * Hkv, box))
     return ATTN_ERR_CUDA;
   return decode_common(q, tk, tv, cache_lens, o, lse, workspace, workspace_bytes, B, Hq, Hkv, Tq, (int)S, D, scale,
-                       block_table, page_size, max_pages, num_pages, rope_cos_sin, stream);
+                       block_table, page_size, max_pages, num_pages, rope_cos_sin, false, 1.f, 1.f, stream);
+}
+
+attn_status attn_decode_fp8_fwd(const void* q, const void* k8, const void* v8, float k_scale, float v_scale,
+                                const int* cache_lens, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                                int B, int Hq, int Hkv, int Tq, int S, int D, float scale, const float* rope_cos_sin,
+                                int rope_positions, void* stream) {
+  attn_status st = decode_check(B, Hq, Hkv, Tq, S, D);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || Tq == 0) return ATTN_OK;
+  if (!isfinite(scale) || !isfinite(k_scale) || !isfinite(v_scale)) return ATTN_ERR_SHAPE;
+  if (!q || !k8 || !v8 || !cache_lens || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) || !aligned16(lse) ||
+      (reinterpret_cast<uintptr_t>(cache_lens) & 3u))
+    return ATTN_ERR_ALIGN;
+  if ((st = decode_check_rope(rope_cos_sin, rope_positions, S)) != ATTN_OK) return st;
+  if ((st = decode_check_workspace(B, Hq, Hkv, Tq, S, D, workspace, workspace_bytes)) != ATTN_OK) return st;
+  CUtensorMap tk, tv;
+  if (!map_bytes(&tk, k8, D, S, (long)B * Hkv, 128) || !map_bytes(&tv, v8, D, S, (long)B * Hkv, 128))
+    return ATTN_ERR_CUDA;
+  return decode_common(q, tk, tv, cache_lens, o, lse, workspace, workspace_bytes, B, Hq, Hkv, Tq, S, D, scale,
+                       nullptr, 0, 0, 0, rope_cos_sin, true, k_scale, v_scale, stream);
+}
+
+attn_status attn_decode_paged_fp8_fwd(const void* q, const void* k8_pages, const void* v8_pages, float k_scale,
+                                      float v_scale, const int* block_table, const int* cache_lens, void* o,
+                                      float* lse, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                                      int Tq, int page_size, int num_pages, int max_pages, int D, float scale,
+                                      const float* rope_cos_sin, int rope_positions, void* stream) {
+  if (page_size < 0 || num_pages < 0 || max_pages < 0) return ATTN_ERR_SHAPE;
+  const long S = (long)page_size * max_pages;
+  if (S > 0x7fffffffL) return ATTN_ERR_SHAPE;
+  attn_status st = decode_check(B, Hq, Hkv, Tq, (int)S, D);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || Tq == 0) return ATTN_OK;
+  if (!decode_page_size_ok(page_size) || num_pages < 1 || (long)num_pages * Hkv > 0x7fffffffL ||
+      (long)B * max_pages > 0x7fffffffL || !isfinite(scale) || !isfinite(k_scale) || !isfinite(v_scale))
+    return ATTN_ERR_SHAPE;
+  if (!q || !k8_pages || !v8_pages || !block_table || !cache_lens || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k8_pages) || !aligned16(v8_pages) || !aligned16(o) || !aligned16(lse) ||
+      (reinterpret_cast<uintptr_t>(cache_lens) & 3u) || (reinterpret_cast<uintptr_t>(block_table) & 3u))
+    return ATTN_ERR_ALIGN;
+  if ((st = decode_check_rope(rope_cos_sin, rope_positions, (int)S)) != ATTN_OK) return st;
+  if ((st = decode_check_workspace(B, Hq, Hkv, Tq, (int)S, D, workspace, workspace_bytes)) != ATTN_OK) return st;
+  const int box = page_size < 128 ? page_size : 128;
+  CUtensorMap tk, tv;
+  if (!map_bytes(&tk, k8_pages, D, page_size, (long)num_pages * Hkv, box) ||
+      !map_bytes(&tv, v8_pages, D, page_size, (long)num_pages * Hkv, box))
+    return ATTN_ERR_CUDA;
+  return decode_common(q, tk, tv, cache_lens, o, lse, workspace, workspace_bytes, B, Hq, Hkv, Tq, (int)S, D, scale,
+                       block_table, page_size, max_pages, num_pages, rope_cos_sin, true, k_scale, v_scale, stream);
 }
 
 // ------------------------------------------------- allocation-free backward

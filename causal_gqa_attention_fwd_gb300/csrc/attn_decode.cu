@@ -47,6 +47,9 @@
 // decode_merge  combines the pieces of a cut unit with the usual rescaling;
 //   it is launched as a programmatic dependent of decode_partial, so its
 //   launch overlaps the partial kernel's tail.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "sm103.cuh"
 #include "kernels.h"
 
@@ -62,27 +65,39 @@ constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 64;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D>
+// kind::f16 instruction descriptor with f32 accumulation and bf16 (f16 = false)
+// or f16 (f16 = true) A and B.
+__host__ __device__ constexpr uint32_t idesc_16(int M, int N, bool a_mn, bool b_mn, bool f16) {
+  return f16 ? (idesc_bf16(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10))) : idesc_bf16(M, N, a_mn, b_mn);
+}
+
+template <int D, bool FP8>
 struct DecCfg {
   static constexpr int NB = D / 64;                       // 64-feature boxes per K or V chunk
-  static constexpr int kTileBytes = NB * kBoxBytes;       // one K or V chunk
-  static constexpr int kSlots = D == 128 ? 3 : 6;          // per ring (K ring, then V ring)
+  static constexpr int kTileBytes = NB * kBoxBytes;       // one K or V chunk as an MMA operand (16-bit)
+  // operand slots per ring (K ring, then V ring); FP8 caches land in staging
+  // rings of 8-bit chunks first and are converted into one operand slot each
+  static constexpr int kSlots = FP8 ? 1 : (D == 128 ? 3 : 6);
+  static constexpr int kStage8 = FP8 ? (D == 128 ? 4 : 8) : 0;
+  static constexpr int kTile8 = kCK * D;                  // one 8-bit chunk, rows of D bytes
   static constexpr int kOffV = kSlots * kTileBytes;
+  static constexpr int kOffStage = 2 * kSlots * kTileBytes;     // [K stages][V stages] of kTile8
+  static constexpr int kOffQ = kOffStage + 2 * kStage8 * kTile8;  // [2 slots][value tile, remainder tile]
   static constexpr int kQBytes = NB * kRowBoxBytes;       // 16 query rows, K-major
   static constexpr int kPBytes = 2 * kRowBoxBytes;        // 16 rows x 128 keys, K-major
-  static constexpr int kOffQ = 2 * kSlots * kTileBytes;         // [2 slots][value tile, remainder tile]
   static constexpr int kOffP = kOffQ + 4 * kQBytes;
   static constexpr int kOffMax = kOffP + 2 * kPBytes;           // f32 [2][16 rows][4 warps]
   static constexpr int kOffSum = kOffMax + 2 * kRows * 4 * 4;   // f32 [16 rows][4 warps]
   static constexpr int kOffFin = kOffSum + kRows * 4 * 4;       // float2 [2 pieces][16 rows]: (max, sum)
   static constexpr int kSmemBytes = kOffFin + 2 * kRows * 8 + 1024;  // + alignment slack
-  static constexpr uint32_t kIdescS = idesc_bf16(kCK, kRows, false, false);
-  static constexpr uint32_t kIdescO = idesc_bf16(128, kRows, true, false);
+  // 16-bit operands: bf16, or f16 for FP8 caches (every E4M3 value is an f16)
+  static constexpr uint32_t kIdescS = idesc_16(kCK, kRows, false, false, FP8);
+  static constexpr uint32_t kIdescO = idesc_16(128, kRows, true, false, FP8);
   // V^T as an MN-major A operand of 128 rows: the second 64-feature atom is
   // the second box (D = 128) or the first one again (D = 64; rows 64-127 of
   // O^T are then a copy and are never read).
   static constexpr uint32_t kLboV = D == 128 ? kBoxBytes : 0;
-  static_assert(kSmemBytes + 512 <= 232448, "shared memory");
+  static_assert(kSmemBytes + 5120 <= 232448, "shared memory (dynamic + static)");
 };
 
 __device__ __forceinline__ uint32_t col_s(int b) { return (uint32_t)b * kRows; }
@@ -100,6 +115,7 @@ struct Piece {
 struct __align__(8) DecBarriers {
   uint64_t k_full[6], k_empty[6];
   uint64_t v_full[6], v_empty[6];
+  uint64_t st_full[2][8];  // FP8 staging rings (K, V): an 8-bit chunk has landed
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], p_empty[2];
@@ -268,6 +284,72 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 }  // namespace
 
+// Two 16-bit floats (low half = first element) from two f32: bf16 or f16.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
+  if constexpr (F16) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    return pack_bf16x2(lo, hi);
+  }
+}
+
+template <bool F16>
+__device__ __forceinline__ float2 unpack16x2(uint32_t v) {
+  if constexpr (F16) return __half22float2(*reinterpret_cast<const __half2*>(&v));
+  else return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+}
+
+// One landed 8-bit chunk (128 key rows of D E4M3 codes, row-major) into the
+// 16-bit operand tile (K-major, 128-byte swizzled boxes of 64 features): one
+// warp, out of line.  Every E4M3 value is an f16, so the conversion is exact.
+// Rows r >= nrows (keys at or past the row's length, whose codes may be
+// anything, NaN included) are written as zeros.
+template <int D>
+__device__ __noinline__ void convert_e4m3_tile(const uint8_t* src, uint8_t* dst, int lane, int nrows) {
+  constexpr int kChunks = D / 16;  // 16-code pieces per row
+  for (int idx = lane; idx < kCK * kChunks; idx += 32) {
+    const int r = idx / kChunks, c = idx % kChunks;
+    uint4 x = make_uint4(0, 0, 0, 0);
+    if (r < nrows) x = *reinterpret_cast<const uint4*>(src + r * D + c * 16);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[e] & 0xffffu), __NV_E4M3);
+      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[e] >> 16), __NV_E4M3);
+      h[2 * e] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+      h[2 * e + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int f = 16 * c + 8 * half;  // first feature of this 16-byte operand piece
+      *reinterpret_cast<uint4*>(dst + (f >> 6) * kBoxBytes + r * 128 + ((((f & 63) >> 3) ^ (r & 7)) << 4)) =
+          make_uint4(h[4 * half], h[4 * half + 1], h[4 * half + 2], h[4 * half + 3]);
+    }
+  }
+}
+
+// A query tile loaded as bf16 rewritten as f16 in place (FP8 caches: the
+// score MMA takes f16 for both operands).  Queries are expected inside the
+// f16 range.
+template <int D>
+__device__ __noinline__ void q_tile_to_f16(uint8_t* qs, int lane) {
+  constexpr int kPieces = kRows * D / 8;  // 16-byte pieces of the tile
+  for (int idx = lane; idx < kPieces; idx += 32) {
+    uint4* p = reinterpret_cast<uint4*>(qs) + idx;
+    uint4 x = *p;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack16x2<false>(w[e]);
+      w[e] = pack16x2<true>(f.x, f.y);
+    }
+    *p = x;
+  }
+}
+
 // Rotary embedding of a piece's query rows (one warp, out of line), written
 // back as bf16 value (over the loaded rows) plus bf16 remainder (qrem):
 // row r is query position t = (r0 + r) % Tq of its head, at position
@@ -275,7 +357,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 // x'_i = x_i c - x_{i+D/2} s, x'_{i+D/2} = x_{i+D/2} c + x_i s with c, s from
 // the table row of that position.  The tile is K-major, 128-byte swizzled:
 // feature d of row r sits in box d / 64, 16-byte chunk ((d % 64) / 8) ^ (r % 8).
-template <int D>
+template <int D, bool F16>
 __device__ __noinline__ void rope_rotate_tile(uint8_t* qs, uint8_t* qrem, const Piece& it, const DecodeArgs& a,
                                               int lane) {
   constexpr int H = D / 2;
@@ -302,11 +384,12 @@ __device__ __noinline__ void rope_rotate_tile(uint8_t* qs, uint8_t* qrem, const 
     uint32_t* h32 = reinterpret_cast<uint32_t*>(&hi);
     uint32_t* rl32 = reinterpret_cast<uint32_t*>(&rlo);
     uint32_t* rh32 = reinterpret_cast<uint32_t*>(&rhi);
-    // value = bf16(y), remainder = bf16(y - value): the pair carries y to ~2^-16
+    // value = r16(y), remainder = r16(y - value): the pair carries y to well
+    // below the 16-bit format's precision
     auto split = [](float y0, float y1, uint32_t& v, uint32_t& rm) {
-      v = pack_bf16x2(y0, y1);
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
-      rm = pack_bf16x2(y0 - b.x, y1 - b.y);
+      v = pack16x2<F16>(y0, y1);
+      const float2 b = unpack16x2<F16>(v);
+      rm = pack16x2<F16>(y0 - b.x, y1 - b.y);
     };
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -349,7 +432,7 @@ __device__ __noinline__ void decode_write_out(const DecodeArgs& a, const Piece& 
   for (int r = 0; r < kRows; ++r) {
     if (r >= it.rows) break;
     const int rg = it.r0 + r;  // row within the group: query head rg / Tq, position rg % Tq
-    const float O = __uint_as_float(ov[r]);
+    const float O = __uint_as_float(ov[r]) * a.v_scale;
     const float2 ml = s_fin[ob * kRows + r];
     if (whole) {
       const long orow = ((long)it.b * a.Hq + (long)it.hkv * a.G) * a.Tq + rg;
@@ -362,13 +445,14 @@ __device__ __noinline__ void decode_write_out(const DecodeArgs& a, const Piece& 
   }
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_q, const DecodeArgs a) {
-  using C = DecCfg<D>;
+  using C = DecCfg<D, FP8>;
   constexpr int SL = C::kSlots;
   constexpr int NB = C::NB;
+  constexpr int S8 = C::kStage8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ DecBarriers bars;
@@ -402,6 +486,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.v_full[i], 1);
       mbar_init(&bars.v_empty[i], 1);
     }
+    for (int i = 0; i < S8; ++i) {
+      mbar_init(&bars.st_full[0][i], 1);
+      mbar_init(&bars.st_full[1][i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.q_full[i], 1);
       mbar_init(&bars.q_empty[i], 1);
@@ -433,118 +521,151 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto next = [&](Cursor& cur) { cursor_next(a, sh, lens, cur); };
 
   if (warp == 0 || warp == 6) {
-    // ============================== producers: warp 0 K chunks and query rows, warp 6 V chunks
+    // ============================== producers: warp 0 K chunks, warp 6 V chunks
     const bool is_k = warp == 0;
     const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
     uint64_t* full = is_k ? bars.k_full : bars.v_full;
     uint64_t* empty = is_k ? bars.k_empty : bars.v_empty;
     uint8_t* ring = smem + (is_k ? 0 : C::kOffV);
-    if (lane == 0) {
-      tma_prefetch_desc(tm);
-      if (is_k) tma_prefetch_desc(&tm_q);
-    }
-    int last_fill[SL], last_q[2] = {-1, -1};
+    uint8_t* stage = smem + C::kOffStage + (is_k ? 0 : S8 * C::kTile8);
+    uint64_t* st_full = bars.st_full[is_k ? 0 : 1];
+    if (lane == 0) tma_prefetch_desc(tm);
+    constexpr int NF = FP8 ? S8 : SL;  // TMA destinations: staging slots (FP8) or operand slots
+    int last_fill[NF];
 #pragma unroll
-    for (int i = 0; i < SL; ++i) last_fill[i] = -1;
-    int cs = 0;
-    // one piece's loads (and, for K, its query rows)
-    auto load_item = [&](const Piece& it, int uses) {
-      if (is_k) {
-        // the piece's 16 query rows (K-major, 128-byte swizzled, as the score
-        // MMA reads them); rows past it.rows belong to other heads or lie
-        // past the tensor (zero) and only fill unused columns of S^T
-        const int qslot = uses & 1;
-        if (uses >= 2) mbar_wait(&bars.q_empty[qslot], ((uses >> 1) - 1) & 1, guard);
-        if (lane == 0) {
-          if (guard.aborted()) {
-            mbar_arrive(&bars.q_full[qslot]);
-          } else {
-            const int row0 = (it.b * a.Hq + it.hkv * a.G) * a.Tq + it.r0;
-            mbar_expect_tx(&bars.q_full[qslot], C::kQBytes);
-#pragma unroll
-            for (int x = 0; x < NB; ++x)
-              tma_load_2d(smem + C::kOffQ + qslot * 2 * C::kQBytes + x * kRowBoxBytes, &tm_q, &bars.q_full[qslot],
-                          x * 64, row0);
-            last_q[qslot] = (uses >> 1) & 1;
-          }
+    for (int i = 0; i < NF; ++i) last_fill[i] = -1;
+    // TMA of stream chunk cs (piece it, chunk c of it) into `dst` (a tile of
+    // 16-bit operand boxes, or an 8-bit staging tile), completing on `bar`.
+    // Paged: lane i looks up the chunk's i-th page (before the slot wait, so
+    // the lookup's latency overlaps it); pages that hold none of the row's
+    // keys, and invalid entries (reported), get a coordinate past the tensor,
+    // which the TMA fills with zeros.
+    auto load_chunk = [&](const Piece& it, int c, uint8_t* dst, uint64_t* bar, uint64_t* wait_bar, int wait_parity,
+                          int* fill_rec, int fill) {
+      const int k0 = it.kbeg + c * kCK;
+      int pages[kCK / 16];
+      int npc = 1;
+      if constexpr (PAGED) {
+        const int psz = a.page_size;
+        npc = psz >= kCK ? 1 : kCK / psz;
+        const int idx = k0 / psz + lane;
+        const int used = (it.len + psz - 1) / psz;
+        int pg = -1;
+        bool bad = false;
+        if (lane < npc && idx < used) {
+          const int e = a.block_table[(long)it.b * a.max_pages + idx];
+          if (e >= 0 && e < a.num_pages) pg = e;
+          else bad = true;
         }
-        __syncwarp();
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicCAS(a.status, 0, kDevBadPages);
+#pragma unroll
+        for (int i = 0; i < kCK / 16; ++i) pages[i] = __shfl_sync(0xffffffffu, pg, i);
       }
-      for (int c = 0; c < it.nch; ++c, ++cs) {
-        const int slot = cs % SL, fill = cs / SL;
-        const int k0 = it.kbeg + c * kCK;
-        // paged: lane i looks up the chunk's i-th page (before the slot wait,
-        // so the lookup's latency overlaps it); pages that hold none of the
-        // row's keys, and invalid entries (reported), get a coordinate past
-        // the tensor, which the TMA fills with zeros
-        int pages[kCK / 16];
-        int npc = 1;
-        if constexpr (PAGED) {
-          const int psz = a.page_size;
-          npc = psz >= kCK ? 1 : kCK / psz;
-          const int idx = k0 / psz + lane;
-          const int used = (it.len + psz - 1) / psz;
-          int pg = -1;
-          bool bad = false;
-          if (lane < npc && idx < used) {
-            const int e = a.block_table[(long)it.b * a.max_pages + idx];
-            if (e >= 0 && e < a.num_pages) pg = e;
-            else bad = true;
-          }
-          if (__any_sync(0xffffffffu, bad) && lane == 0) atomicCAS(a.status, 0, kDevBadPages);
+      if (wait_bar != nullptr) mbar_wait(wait_bar, wait_parity, guard);
+      if (lane == 0) {
+        if (guard.aborted()) {
+          mbar_arrive(bar);  // nothing loaded; the other roles are on their way out
+        } else {
+          constexpr int kRowBytes = FP8 ? D : 128;      // bytes per key row of one TMA box
+          constexpr int kBoxes = FP8 ? 1 : NB;          // boxes per key row
+          mbar_expect_tx(bar, FP8 ? C::kTile8 : C::kTileBytes);
+          if constexpr (PAGED) {
+            const int psz = a.page_size;
+            const int row = psz >= kCK ? k0 % psz : 0;  // first row of the chunk inside its page
+            for (int i = 0; i < npc; ++i) {
+              const int z = pages[i] >= 0 ? pages[i] * a.Hkv + it.hkv : a.num_pages * a.Hkv;
 #pragma unroll
-          for (int i = 0; i < kCK / 16; ++i) pages[i] = __shfl_sync(0xffffffffu, pg, i);
-        }
-        if (fill >= 1) mbar_wait(&empty[slot], (fill - 1) & 1, guard);
-        if (lane == 0) {
-          uint64_t* bar = &full[slot];
-          if (guard.aborted()) {
-            mbar_arrive(bar);  // nothing loaded; the other roles are on their way out
-          } else {
-            uint8_t* dst = ring + slot * C::kTileBytes;
-            mbar_expect_tx(bar, C::kTileBytes);
-            if constexpr (PAGED) {
-              const int psz = a.page_size;
-              const int row = psz >= kCK ? k0 % psz : 0;  // first row of the chunk inside its page
-              for (int i = 0; i < npc; ++i) {
-                const int z = pages[i] >= 0 ? pages[i] * a.Hkv + it.hkv : a.num_pages * a.Hkv;
-#pragma unroll
-                for (int x = 0; x < NB; ++x)
-                  tma_load_3d(dst + x * kBoxBytes + i * psz * 128, tm, bar, x * 64, row, z);
-              }
-            } else {
-#pragma unroll
-              for (int x = 0; x < NB; ++x) tma_load_3d(dst + x * kBoxBytes, tm, bar, x * 64, k0, it.bh);
+              for (int x = 0; x < kBoxes; ++x)
+                tma_load_3d(dst + x * kBoxBytes + i * psz * kRowBytes, tm, bar, x * 64, row, z);
             }
-            last_fill[slot] = fill;
+          } else {
+#pragma unroll
+            for (int x = 0; x < kBoxes; ++x) tma_load_3d(dst + x * kBoxBytes, tm, bar, x * 64, k0, it.bh);
           }
+          *fill_rec = fill;
         }
-        __syncwarp();
       }
+      __syncwarp();
     };
-    for (Cursor cur = begin(); cur.valid;) {
-      load_item(cur.it, cur.uses);
-      const int n = cur.it.nch;
-      for (int c = 0; c < n; ++c) next(cur);  // on to the next piece
+    if constexpr (!FP8) {
+      int cs = 0;
+      for (Cursor cur = begin(); cur.valid; next(cur), ++cs) {
+        const int slot = cs % SL, fill = cs / SL;
+        load_chunk(cur.it, cur.c, ring + slot * C::kTileBytes, &full[slot], fill >= 1 ? &empty[slot] : nullptr,
+                   (fill - 1) & 1, &last_fill[slot], fill);
+      }
+    } else {
+      // FP8: a load cursor runs S8 chunks ahead through the staging ring; the
+      // convert cursor turns each landed 8-bit chunk into the f16 operand
+      // slot (exact: every E4M3 value is an f16) once the MMA that read the
+      // previous one is done, then refills the staging slot it just read
+      Cursor ld = begin();
+      int lcs = 0;
+      for (; lcs < S8 && ld.valid; ++lcs, next(ld))
+        load_chunk(ld.it, ld.c, stage + lcs * C::kTile8, &st_full[lcs], nullptr, 0, &last_fill[lcs], 0);
+      for (Cursor cv = begin(); cv.valid; next(cv)) {
+        const int ci = cv.cs, sg = ci % S8;
+        mbar_wait(&st_full[sg], (ci / S8) & 1, guard);
+        if (ci >= 1) mbar_wait(&empty[0], (ci - 1) & 1, guard);
+        // V rows past the length become zeros here (so that 0 * V stays 0 in
+        // the P V MMA); K rows there only meet masked scores
+        const int nrows = is_k ? kCK : cv.it.len - (cv.it.kbeg + cv.c * kCK);
+        convert_e4m3_tile<D>(stage + sg * C::kTile8, ring, lane, nrows);
+        fence_proxy_async_smem();  // generic writes (operand) and reads (staging) before async-proxy use
+        mbar_arrive_warp(&full[0]);
+        if (ld.valid) {
+          load_chunk(ld.it, ld.c, stage + sg * C::kTile8, &st_full[sg], nullptr, 0, &last_fill[sg], lcs / S8);
+          ++lcs;
+          next(ld);
+        }
+      }
     }
     // never leave the CTA with copies in flight
-    if (lane == 0) {
-      for (int i = 0; i < SL; ++i)
-        if (last_fill[i] >= 0) mbar_wait_drain(&full[i], (uint32_t)last_fill[i] & 1);
-      for (int i = 0; i < 2; ++i)
-        if (last_q[i] >= 0) mbar_wait_drain(&bars.q_full[i], (uint32_t)last_q[i]);
-    }
+    if (lane == 0)
+      for (int i = 0; i < NF; ++i)
+        if (last_fill[i] >= 0) mbar_wait_drain(FP8 ? &st_full[i] : &full[i], (uint32_t)last_fill[i] & 1);
     __syncwarp();
   } else if (warp == 1) {
     // ===================== score MMA issuer (warp-uniform, one elected lane issues)
+    // The query rows of each piece: TMA one piece ahead (the piece's 16 rows,
+    // K-major, 128-byte swizzled, as the score MMA reads them; rows past
+    // it.rows belong to other heads or lie past the tensor and only fill
+    // unused columns of S^T).
+    if (lane == 0) tma_prefetch_desc(&tm_q);
+    Cursor qc = begin();
+    int last_q[2] = {-1, -1};
+    auto load_q = [&]() {
+      if (!qc.valid) return;
+      const int u = qc.uses, qslot = u & 1;
+      if (u >= 2) mbar_wait(&bars.q_empty[qslot], ((u >> 1) - 1) & 1, guard);
+      if (lane == 0) {
+        if (guard.aborted()) {
+          mbar_arrive(&bars.q_full[qslot]);
+        } else {
+          const int row0 = (qc.it.b * a.Hq + qc.it.hkv * a.G) * a.Tq + qc.it.r0;
+          mbar_expect_tx(&bars.q_full[qslot], C::kQBytes);
+#pragma unroll
+          for (int x = 0; x < NB; ++x)
+            tma_load_2d(smem + C::kOffQ + qslot * 2 * C::kQBytes + x * kRowBoxBytes, &tm_q, &bars.q_full[qslot],
+                        x * 64, row0);
+          last_q[qslot] = (u >> 1) & 1;
+        }
+      }
+      __syncwarp();
+      const int n = qc.it.nch;
+      for (int c = 0; c < n; ++c) next(qc);
+    };
+    load_q();
     for (Cursor cur = begin(); cur.valid; next(cur)) {
       const int qslot = cur.uses & 1, slot = cur.cs % SL, sb = cur.cs & 1;
       if (cur.c == 0) {
+        load_q();  // the next piece's rows
         mbar_wait(&bars.q_full[qslot], (cur.uses >> 1) & 1, guard);
-        if (a.rope_cs != nullptr) {
-          uint8_t* qt = smem + C::kOffQ + qslot * 2 * C::kQBytes;
-          rope_rotate_tile<D>(qt, qt + C::kQBytes, cur.it, a, lane);
-          fence_proxy_async_smem();  // the rotated tiles are read by the MMAs below
+        uint8_t* qt = smem + C::kOffQ + qslot * 2 * C::kQBytes;
+        if (a.rope_cs != nullptr) rope_rotate_tile<D, FP8>(qt, qt + C::kQBytes, cur.it, a, lane);
+        else if (FP8) q_tile_to_f16<D>(qt, lane);
+        if (FP8 || a.rope_cs != nullptr) {
+          fence_proxy_async_smem();  // the rewritten tiles are read by the MMAs below
           __syncwarp();
         }
       }
@@ -567,9 +688,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit_warp(&bars.k_empty[slot]);
       if (cur.c == cur.it.nch - 1) tc_commit_warp(&bars.q_empty[qslot]);
     }
-    // every issued MMA finishes before TMEM is released
+    // every issued MMA finishes, and no copy is in flight, before TMEM and
+    // shared memory are released
     tc_commit_warp(&bars.teardown[0]);
     mbar_wait_drain(&bars.teardown[0], 0);
+    if (lane == 0)
+      for (int i = 0; i < 2; ++i)
+        if (last_q[i] >= 0) mbar_wait_drain(&bars.q_full[i], (uint32_t)last_q[i]);
+    __syncwarp();
   } else if (warp == 7) {
     // ===================== P V MMA issuer: independent of the score issuer, so
     // that a V chunk is released as soon as its own P is ready
@@ -679,9 +805,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // cache rows at or past len are outside the cache and may hold
       // anything: zero their V (once it has landed) so that 0 * V stays 0
-      // in the MMA
+      // in the MMA.  (FP8: the converter writes those rows as zeros; its
+      // single operand slot can be two fills behind this warp, where a
+      // parity wait on it would not tell the fills apart.)
       const int nvis = it.len - k0;
-      if (nvis < kCK) {
+      if (!FP8 && nvis < kCK) {
         mbar_wait(&bars.v_full[i % SL], (i / SL) & 1, guard);
         uint8_t* vs = smem + C::kOffV + (i % SL) * C::kTileBytes;
         if (j >= nvis) {
@@ -702,7 +830,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mu = m_used[r] == -INFINITY ? 0.f : m_used[r];
         const float pr = ex2_approx(s[r] - mu);
         lpart[r] = fmaf(lpart[r], alpha[r], pr);
-        *reinterpret_cast<__nv_bfloat16*>(pt + r * 128 + ((pch ^ (r & 7)) << 4)) = __float2bfloat16_rn(pr);
+        if constexpr (FP8)
+          *reinterpret_cast<__half*>(pt + r * 128 + ((pch ^ (r & 7)) << 4)) = __float2half_rn(pr);
+        else
+          *reinterpret_cast<__nv_bfloat16*>(pt + r * 128 + ((pch ^ (r & 7)) << 4)) = __float2bfloat16_rn(pr);
       }
       fence_proxy_async_smem();
       if (resc && cur.c > 0) {
@@ -845,21 +976,21 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
   if (threadIdx.x == 0) a.lse[row] = s_lse;
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool FP8>
 static cudaError_t launch_decode_dp(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
                                     const DecodeArgs& a, int grid, cudaStream_t stream) {
-  using C = DecCfg<D>;
+  using C = DecCfg<D, FP8>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<D, PAGED>,
+    cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<D, PAGED, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   prof_begin(kProfDecode, stream);
-  decode_partial_kernel<D, PAGED><<<grid, kThreads, C::kSmemBytes, stream>>>(k, v, q, a);
+  decode_partial_kernel<D, PAGED, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(k, v, q, a);
   prof_end(stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.slots <= 1) return e;  // no unit can be cut
@@ -885,8 +1016,12 @@ static cudaError_t launch_decode_dp(const CUtensorMap& k, const CUtensorMap& v, 
 template <int D>
 static cudaError_t launch_decode_d(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
                                    const DecodeArgs& a, int grid, cudaStream_t stream) {
-  if (a.block_table != nullptr) return launch_decode_dp<D, true>(k, v, q, a, grid, stream);
-  return launch_decode_dp<D, false>(k, v, q, a, grid, stream);
+  if (a.fp8) {
+    if (a.block_table != nullptr) return launch_decode_dp<D, true, true>(k, v, q, a, grid, stream);
+    return launch_decode_dp<D, false, true>(k, v, q, a, grid, stream);
+  }
+  if (a.block_table != nullptr) return launch_decode_dp<D, true, false>(k, v, q, a, grid, stream);
+  return launch_decode_dp<D, false, false>(k, v, q, a, grid, stream);
 }
 
 cudaError_t launch_attn_decode(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const DecodeArgs& a,

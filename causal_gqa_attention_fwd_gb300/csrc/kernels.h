@@ -100,6 +100,10 @@ struct DecodeArgs {
   int page_size, max_pages, num_pages;
   // rotary queries: rope_cs [positions, D] f32 (cos half, then sin half), nullptr = none
   const float* rope_cs;
+  // FP8 (E4M3) caches: the k, v maps are 8-bit ([.., D] rows, 128-key
+  // boxes, no swizzle); K's scale is folded into scale_log2, V's applied to O
+  int fp8;
+  float v_scale;          // 1 for 16-bit caches
 };
 
 // k, v: dense maps over the caches ([B*Hkv, S, D], 64 x 128 boxes) or, paged,

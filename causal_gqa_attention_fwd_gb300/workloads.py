@@ -77,6 +77,7 @@ class DecodeWorkload:
     max_len: int
     scale: float = field(default=0.0)
     page_size: int = 0      # > 0: paged cache of S / page_size pages per row
+    fp8: bool = False       # E4M3 caches with per-tensor scales
 
     @property
     def softmax_scale(self) -> float:
@@ -98,6 +99,9 @@ DECODE_WORKLOADS["decode_paged_long_gqa_s32k_p64"] = DecodeWorkload(
 DECODE_WORKLOADS["decode_paged_long_gqa_s32k_p16"] = DecodeWorkload(
     "decode_paged_long_gqa_s32k_p16", B=8, Hq=32, Hkv=8, Tq=1, S=32768, D=128, min_len=16384, max_len=32768,
     page_size=16)
+
+DECODE_WORKLOADS["decode_fp8_long_gqa_s32k"] = DecodeWorkload(
+    "decode_fp8_long_gqa_s32k", B=8, Hq=32, Hkv=8, Tq=1, S=32768, D=128, min_len=16384, max_len=32768, fp8=True)
 
 DECODE_HEADLINE = "decode_long_gqa_s32k"
 
@@ -189,6 +193,8 @@ def paged_decode_inputs(B, Hq, Hkv, Tq, page_size, max_pages, D, cache_lens=None
 
 
 def make_decode_inputs(w: DecodeWorkload, seed=0):
+    if w.fp8:
+        return fp8_decode_inputs(w.B, w.Hq, w.Hkv, w.Tq, w.S, w.D, min_len=w.min_len, max_len=w.max_len, seed=seed)
     if w.page_size:
         return paged_decode_inputs(w.B, w.Hq, w.Hkv, w.Tq, w.page_size, w.S // w.page_size, w.D, min_len=w.min_len,
                                    max_len=w.max_len, seed=seed)
@@ -204,3 +210,30 @@ def rope_cos_sin_table(positions: int, D: int, base: float = 10000.0):
     theta = base ** (-2.0 * i / D)
     ang = torch.arange(positions, dtype=torch.float64)[:, None] * theta[None, :]
     return torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32)
+
+
+def to_e4m3(x, scale: float):
+    """E4M3 codes (uint8) of x / scale, rounded to nearest (PyTorch's float8_e4m3fn cast) -- input
+    preparation: the kernels and the oracle both take the codes and the scale."""
+    return (x.to(torch.float32) / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def fp8_cache(x):
+    """(codes, scale) of an f32 cache with one scale: amax maps to the format's largest finite value, 448."""
+    scale = float(x.abs().max()) / 448.0
+    return to_e4m3(x, scale), scale
+
+
+def fp8_decode_inputs(B, Hq, Hkv, Tq, S, D, cache_lens=None, min_len=None, max_len=None, seed=0):
+    """q bf16 [B,Hq,Tq,D]; k8, v8 uint8 [B,Hkv,S,D] E4M3 codes with scales k_scale, v_scale (caches drawn
+    N(0,1) in f32, each mapped onto the E4M3 range by its own amax); cache_lens int32 [B]."""
+    g = torch.Generator().manual_seed(seed)
+    if cache_lens is None:
+        lo = Tq if min_len is None else min_len
+        hi = S if max_len is None else max_len
+        cache_lens = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64)
+    lens = torch.as_tensor(cache_lens, dtype=torch.int32)
+    q = _randn(g, (B, Hq, Tq, D))
+    k8, ks = fp8_cache(torch.randn(B, Hkv, S, D, generator=g, dtype=torch.float32))
+    v8, vs = fp8_cache(torch.randn(B, Hkv, S, D, generator=g, dtype=torch.float32))
+    return dict(q=q, k8=k8, v8=v8, k_scale=ks, v_scale=vs, cache_lens=lens)

@@ -193,6 +193,32 @@ GQA_ATTN_API attn_status attn_decode_paged_fwd(const void* q, const void* k_page
                                                float scale, const float* rope_cos_sin, int rope_positions,
                                                void* stream);
 
+/* Cached attention over FP8 K/V caches (the FP8 E4M3 quantize/dequantize
+ * and KV-cache decode of the microLLM-rocm README, section "Why this project
+ * exists"): same queries, mask and outputs as attn_decode_fwd /
+ * attn_decode_paged_fwd, with the caches stored as E4M3 codes (1 byte each:
+ * sign, 4 exponent bits with bias 7, 3 mantissa bits, no infinities) and one
+ * scale per cache: K = e4m3(k8) * k_scale, V = e4m3(v8) * v_scale.
+ *   k8, v8           uint8 [B, Hkv, S, D]  (contiguous), or
+ *   k8_pages, v8_pages uint8 [num_pages, Hkv, page_size, D]  (paged, as
+ *                    attn_decode_paged_fwd)
+ * The codes are widened exactly to f16 on the chip; the scores and P V use
+ * f16 operands (queries and probabilities included) with f32 accumulation,
+ * so the queries must lie inside the f16 range (|q| < 65504).  Workspace,
+ * rotary table and errors as attn_decode_fwd. */
+GQA_ATTN_API attn_status attn_decode_fp8_fwd(const void* q, const void* k8, const void* v8, float k_scale,
+                                             float v_scale, const int* cache_lens, void* o, float* lse,
+                                             void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Tq,
+                                             int S, int D, float scale, const float* rope_cos_sin,
+                                             int rope_positions, void* stream);
+
+GQA_ATTN_API attn_status attn_decode_paged_fp8_fwd(const void* q, const void* k8_pages, const void* v8_pages,
+                                                   float k_scale, float v_scale, const int* block_table,
+                                                   const int* cache_lens, void* o, float* lse, void* workspace,
+                                                   size_t workspace_bytes, int B, int Hq, int Hkv, int Tq,
+                                                   int page_size, int num_pages, int max_pages, int D, float scale,
+                                                   const float* rope_cos_sin, int rope_positions, void* stream);
+
 /* Static description of a status code. */
 GQA_ATTN_API const char* attn_status_string(attn_status status);
 

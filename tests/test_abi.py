@@ -217,3 +217,13 @@ def test_decode_paged_validation(lib):
     assert paged(lib, ptrs=tuple(p)) == 6
     assert paged(lib, ptrs=(NULL,) * 8, B=0) == 0
     assert paged(lib, rope=(A, 511)) == 2                     # capacity 8 pages x 64
+
+
+def test_decode_fp8_validation(lib):
+    f = lambda **kw: lib.attn_decode_fp8_fwd(A, A, A, kw.get("ks", 0.01), 0.01, A, A, A, A, 1 << 40, 1, 4, 2, 1,
+                                             4096, kw.get("D", 64), 0.125, None, 0, None)
+    assert f(D=96) == 3
+    assert f(ks=float("nan")) == 2
+    g = lambda **kw: lib.attn_decode_paged_fp8_fwd(A, A, A, 0.01, 0.01, A, A, A, A, A, 1 << 40, 1, 4, 2, 1,
+                                                   kw.get("psz", 64), 8, 8, 64, 0.125, None, 0, None)
+    assert g(psz=40) == 2
