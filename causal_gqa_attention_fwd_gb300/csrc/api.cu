@@ -494,13 +494,15 @@ attn_status decode_check_rope(const float* rope_cos_sin, int rope_positions, int
   return ATTN_OK;
 }
 
-// 8-bit cache [N, T, D] seen as 3-D (D, T, N): unswizzled boxes of whole
-// D-byte rows, box_rows rows.
+// 8-bit cache [N, T, D] seen as 3-D (D, T, N): boxes of whole D-byte rows,
+// box_rows rows, swizzled as the 8-bit K-major MMA operand reads them
+// (128-byte swizzle for D = 128, 64-byte for D = 64).
 bool map_bytes(CUtensorMap* m, const void* base, int D, int T, long n, int box_rows) {
   const uint64_t dims[3] = {(uint64_t)D, (uint64_t)T, (uint64_t)n};
   const uint64_t strides[2] = {(uint64_t)D, (uint64_t)T * D};
   const uint32_t box[3] = {(uint32_t)D, (uint32_t)box_rows, 1};
-  return gqa::make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  return gqa::make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box,
+                        D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 bool decode_page_size_ok(int page_size) {

@@ -44,11 +44,21 @@
 //              partial with its max and sum.
 // TMEM: S^T buffers at columns 0 and 16, O^T buffers at 32 and 48.
 //
+// E4M3 (FP8) caches, one scale per cache: K and V arrive as 8-bit codes,
+//   half the bytes of bf16.  The score MMA reads the K codes as they land
+//   (kind::f8f6f4, E4M3 x E4M3): the score issuer splits each piece's query
+//   rows into three E4M3 parts with a scale per row, q = s_r (h0 + h1 + h2)
+//   to about 2^-12, and all three accumulate into the same S^T, which the
+//   softmax multiplies by s_r.  V lands in a staging ring; four converter
+//   warps (8-11, 384 threads in all, one per SM sub-partition beside its
+//   softmax warp) convert each landed chunk to f16 (exact) into an operand
+//   tile, one key row per thread, so the P V MMA stays kind::f16 with an
+//   f16 P.  k_scale is folded into the score scale, v_scale into the output.
+//
 // decode_merge  combines the pieces of a cut unit with the usual rescaling;
 //   it is launched as a programmatic dependent of decode_partial, so its
 //   launch overlaps the partial kernel's tail.
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include "sm103.cuh"
 #include "kernels.h"
@@ -61,7 +71,8 @@ constexpr int kCK = 128;                  // keys per chunk (rows of one TMA box
 constexpr int kRows = 16;                 // query rows per piece (N of both MMAs)
 constexpr int kBoxBytes = kCK * 128;      // 64 features x 128 keys, bf16
 constexpr int kRowBoxBytes = kRows * 128; // 64 features (or keys) x 16 rows, bf16
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;             // 16-bit caches: 8 warps
+constexpr int kThreads8 = 384;            // E4M3 caches: 8 warps + 4 V converter warps
 constexpr uint32_t kTmemCols = 64;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -74,29 +85,44 @@ __host__ __device__ constexpr uint32_t idesc_16(int M, int N, bool a_mn, bool b_
 template <int D, bool FP8>
 struct DecCfg {
   static constexpr int NB = D / 64;                       // 64-feature boxes per K or V chunk
-  static constexpr int kTileBytes = NB * kBoxBytes;       // one K or V chunk as an MMA operand (16-bit)
-  // operand slots per ring (K ring, then V ring); FP8 caches land in staging
-  // rings of 8-bit chunks first and are converted into one operand slot each
-  static constexpr int kSlots = FP8 ? 1 : (D == 128 ? 3 : 6);
-  static constexpr int kStage8 = FP8 ? (D == 128 ? 4 : 8) : 0;
-  static constexpr int kTile8 = kCK * D;                  // one 8-bit chunk, rows of D bytes
-  static constexpr int kOffV = kSlots * kTileBytes;
-  static constexpr int kOffStage = 2 * kSlots * kTileBytes;     // [K stages][V stages] of kTile8
-  static constexpr int kOffQ = kOffStage + 2 * kStage8 * kTile8;  // [2 slots][value tile, remainder tile]
-  static constexpr int kQBytes = NB * kRowBoxBytes;       // 16 query rows, K-major
+  static constexpr int kTileBytes = NB * kBoxBytes;       // one K or V chunk as a 16-bit MMA operand
+  static constexpr int kTile8 = kCK * D;                  // one chunk of 8-bit codes, rows of D bytes
+  // bf16 caches: a K ring and a V ring of kSlotsK operand tiles each.
+  // FP8 caches: a K ring of kSlotsK 8-bit tiles (the score MMA reads the
+  // codes as they land), a V staging ring of kSlotsV 8-bit tiles, and kVop
+  // f16 V operand tiles (chunk i is converted into tile i % kVop).  Loads
+  // take microseconds to land under full load, so the shared memory goes to
+  // 8-bit slots in flight rather than to a second operand tile.
+  static constexpr int kSlotsK = FP8 ? (D == 128 ? 6 : 8) : (D == 128 ? 3 : 6);
+  static constexpr int kSlotsV = FP8 ? (D == 128 ? 3 : 8) : kSlotsK;
+  static constexpr int kVop = FP8 ? (D == 128 ? 1 : 2) : 0;
+  static constexpr int kTileK = FP8 ? kTile8 : kTileBytes;          // bytes per K ring slot
+  static constexpr int kOffV = kSlotsK * kTileK;                    // V ring / FP8 V operand tiles
+  static constexpr int kOffStage = kOffV + (FP8 ? kVop : kSlotsV) * kTileBytes;  // FP8 V staging ring
+  static constexpr int kOffQ = kOffStage + (FP8 ? kSlotsV * kTile8 : 0);
+  static constexpr int kQBytes = NB * kRowBoxBytes;       // 16 query rows, bf16, K-major
+  // query slots (one per piece, two pieces): bf16 [value tile, remainder
+  // tile]; FP8 [bf16 tile] followed by [three E4M3 part tiles] per slot
+  static constexpr int kQSlot = (FP8 ? 1 : 2) * kQBytes;
+  static constexpr int kQ8Bytes = kRows * D;              // one E4M3 part: 16 rows of D bytes, K-major
+  static constexpr int kOffQ8 = kOffQ + 2 * kQSlot;
   static constexpr int kPBytes = 2 * kRowBoxBytes;        // 16 rows x 128 keys, K-major
-  static constexpr int kOffP = kOffQ + 4 * kQBytes;
+  static constexpr int kOffP = kOffQ8 + (FP8 ? 2 * 3 * kQ8Bytes : 0);
   static constexpr int kOffMax = kOffP + 2 * kPBytes;           // f32 [2][16 rows][4 warps]
   static constexpr int kOffSum = kOffMax + 2 * kRows * 4 * 4;   // f32 [16 rows][4 warps]
   static constexpr int kOffFin = kOffSum + kRows * 4 * 4;       // float2 [2 pieces][16 rows]: (max, sum)
-  static constexpr int kSmemBytes = kOffFin + 2 * kRows * 8 + 1024;  // + alignment slack
-  // 16-bit operands: bf16, or f16 for FP8 caches (every E4M3 value is an f16)
+  static constexpr int kOffQs = kOffFin + 2 * kRows * 8;        // f32 [2 slots][16 rows]: FP8 query row scales
+  static constexpr int kSmemBytes = kOffQs + 2 * kRows * 4 + 1024;  // + alignment slack
+  // score MMA: bf16 x bf16 (kind::f16), or E4M3 K codes x E4M3 query parts
+  // (kind::f8f6f4, format code 0 for both); P V MMA: bf16, or f16 V and P
   static constexpr uint32_t kIdescS = idesc_16(kCK, kRows, false, false, FP8);
   static constexpr uint32_t kIdescO = idesc_16(128, kRows, true, false, FP8);
   // V^T as an MN-major A operand of 128 rows: the second 64-feature atom is
   // the second box (D = 128) or the first one again (D = 64; rows 64-127 of
   // O^T are then a copy and are never read).
   static constexpr uint32_t kLboV = D == 128 ? kBoxBytes : 0;
+  static constexpr int kMaxSlots = kSlotsK > kSlotsV ? kSlotsK : kSlotsV;
+  static_assert(kMaxSlots <= 8, "barrier arrays");
   static_assert(kSmemBytes + 5120 <= 232448, "shared memory (dynamic + static)");
 };
 
@@ -113,10 +139,11 @@ struct Piece {
 };
 
 struct __align__(8) DecBarriers {
-  uint64_t k_full[6], k_empty[6];
-  uint64_t v_full[6], v_empty[6];
-  uint64_t st_full[2][8];  // FP8 staging rings (K, V): an 8-bit chunk has landed
+  uint64_t k_full[8], k_empty[8];
+  uint64_t v_full[8], v_empty[8];  // FP8: the V staging ring (emptied by the converter warps)
+  uint64_t vo_full[2];             // FP8: an f16 V operand tile is ready (per tile)
   uint64_t q_full[2], q_empty[2];
+  uint64_t qs_full[2], qs_empty[2];  // FP8: a piece's query parts and row scales are ready / read
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], p_empty[2];
   uint64_t o_full[2], o_empty[2];
@@ -301,53 +328,161 @@ __device__ __forceinline__ float2 unpack16x2(uint32_t v) {
   else return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
 }
 
-// One landed 8-bit chunk (128 key rows of D E4M3 codes, row-major) into the
-// 16-bit operand tile (K-major, 128-byte swizzled boxes of 64 features): one
-// warp, out of line.  Every E4M3 value is an f16, so the conversion is exact.
-// Rows r >= nrows (keys at or past the row's length, whose codes may be
-// anything, NaN included) are written as zeros.
+// Two E4M3 codes (low byte = first) as two f16 (low half = first): the
+// hardware conversion, exact (every E4M3 value, NaN included, is an f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(codes));
+  return d;
+}
+
+// Two f32 as E4M3 codes (low byte = lo), rounded to nearest even and
+// saturated to +-448.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t codes) {
+  const uint32_t h = e4m3x2_to_f16x2(codes);
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// Byte offset of 16-byte piece `c` of row r in an 8-bit K-major tile of
+// D-byte rows as the TMA writes it and the MMA reads it: 128-byte swizzle
+// (D = 128: piece c ^ (r % 8)) or 64-byte swizzle (D = 64: c ^ ((r / 2) % 4)).
 template <int D>
-__device__ __noinline__ void convert_e4m3_tile(const uint8_t* src, uint8_t* dst, int lane, int nrows) {
-  constexpr int kChunks = D / 16;  // 16-code pieces per row
-  for (int idx = lane; idx < kCK * kChunks; idx += 32) {
-    const int r = idx / kChunks, c = idx % kChunks;
-    uint4 x = make_uint4(0, 0, 0, 0);
-    if (r < nrows) x = *reinterpret_cast<const uint4*>(src + r * D + c * 16);
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    uint32_t h[8];
+__device__ __forceinline__ int swz8(int r, int c) {
+  return r * D + ((D == 128 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3))) << 4);
+}
+
+// Key row j of a landed E4M3 V chunk (staging tile `st`, rows swizzled as
+// swz8) into row j of the f16 operand tile `vo` (K-major, 128-byte swizzled
+// boxes of 64 features), exact: one thread per row.  A row past the row's
+// length (vis false: its codes may be anything, NaN included) is written as
+// zeros so that 0 * V stays 0 in the P V MMA.
+template <int D>
+__device__ __forceinline__ void convert_v_row(const uint8_t* __restrict__ st, uint8_t* __restrict__ vo, int j,
+                                              bool vis) {
+  constexpr int kC = D / 16;  // 16-code pieces per row
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[e] & 0xffffu), __NV_E4M3);
-      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[e] >> 16), __NV_E4M3);
-      h[2 * e] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
-      h[2 * e + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
-    }
+  for (int c0 = 0; c0 < kC; c0 += 4) {
+    uint4 x[4];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int f = 16 * c + 8 * half;  // first feature of this 16-byte operand piece
-      *reinterpret_cast<uint4*>(dst + (f >> 6) * kBoxBytes + r * 128 + ((((f & 63) >> 3) ^ (r & 7)) << 4)) =
-          make_uint4(h[4 * half], h[4 * half + 1], h[4 * half + 2], h[4 * half + 3]);
+    for (int k = 0; k < 4; ++k)
+      x[k] = vis ? *reinterpret_cast<const uint4*>(st + swz8<D>(j, c0 + k)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
+      uint32_t h[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        h[2 * e] = e4m3x2_to_f16x2((uint16_t)(w[e] & 0xffffu));
+        h[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(w[e] >> 16));
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int f = 16 * (c0 + k) + 8 * half;  // first feature of this 16-byte operand piece
+        *reinterpret_cast<uint4*>(vo + (f >> 6) * kBoxBytes + j * 128 + ((((f & 63) >> 3) ^ (j & 7)) << 4)) =
+            make_uint4(h[4 * half], h[4 * half + 1], h[4 * half + 2], h[4 * half + 3]);
+      }
     }
   }
 }
 
-// A query tile loaded as bf16 rewritten as f16 in place (FP8 caches: the
-// score MMA takes f16 for both operands).  Queries are expected inside the
-// f16 range.
+// A piece's 16 query rows (bf16 tile as loaded: K-major, 128-byte swizzled
+// boxes of 64 features) as three E4M3 part tiles and a scale per row, for
+// the 8-bit score MMA against E4M3 K codes: with s_r = amax_r / 448 and
+// x = q / s_r, h0 = e4m3(x), h1 = e4m3(x - h0), h2 = e4m3(x - h0 - h1), so
+// that q = s_r (h0 + h1 + h2) to about 2^-12 of each element (or 2^-19 of
+// the row's largest, for elements below E4M3's normal range).  All three
+// parts accumulate into the same scores, which the softmax multiplies by
+// s_r.  Rotary queries are rotated first, in f32, at the row's position
+// (pairs i, i + D/2).  One warp, out of line: lane 2r + h makes the features
+// [h D/2, (h + 1) D/2) of row r.
 template <int D>
-__device__ __noinline__ void q_tile_to_f16(uint8_t* qs, int lane) {
-  constexpr int kPieces = kRows * D / 8;  // 16-byte pieces of the tile
-  for (int idx = lane; idx < kPieces; idx += 32) {
-    uint4* p = reinterpret_cast<uint4*>(qs) + idx;
-    uint4 x = *p;
-    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+__device__ __noinline__ void q_tile_to_e4m3_parts(const uint8_t* qt, uint8_t* parts, float* qscale, const Piece& it,
+                                                  const DecodeArgs& a, int lane) {
+  constexpr int H = D / 2;
+  const int r = lane >> 1, hh = lane & 1;
+  auto ld8 = [&](int d) {  // bf16 features d .. d + 7 of row r
+    return *reinterpret_cast<const uint4*>(qt + (d >> 6) * kRowBoxBytes + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4));
+  };
+  auto unpack = [](uint4 v, float* y) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float2 f = unpack16x2<false>(w[e]);
-      w[e] = pack16x2<true>(f.x, f.y);
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+      y[2 * e] = f.x;
+      y[2 * e + 1] = f.y;
     }
-    *p = x;
+  };
+  const bool rope = a.rope_cs != nullptr && r < it.rows;
+  const float* cs = rope ? a.rope_cs + (long)(it.len - a.Tq + (it.r0 + r) % a.Tq) * D : nullptr;
+  // y = the 16 features 16 g .. 16 g + 15 of this lane's half
+  auto load_y = [&](int g, float* y) {
+    const int i0 = 16 * g;  // pair index (feature of the low half)
+    if (!rope) {
+      unpack(ld8(hh * H + i0), y);
+      unpack(ld8(hh * H + i0 + 8), y + 8);
+      return;
+    }
+    float lo[16], hi[16], c[16], sn[16];
+    unpack(ld8(i0), lo);
+    unpack(ld8(i0 + 8), lo + 8);
+    unpack(ld8(H + i0), hi);
+    unpack(ld8(H + i0 + 8), hi + 8);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float4 cv = *reinterpret_cast<const float4*>(cs + i0 + 4 * e);
+      const float4 sv = *reinterpret_cast<const float4*>(cs + H + i0 + 4 * e);
+      c[4 * e] = cv.x, c[4 * e + 1] = cv.y, c[4 * e + 2] = cv.z, c[4 * e + 3] = cv.w;
+      sn[4 * e] = sv.x, sn[4 * e + 1] = sv.y, sn[4 * e + 2] = sv.z, sn[4 * e + 3] = sv.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      y[e] = hh == 0 ? fmaf(lo[e], c[e], -hi[e] * sn[e]) : fmaf(hi[e], c[e], lo[e] * sn[e]);
+  };
+  float amax = 0.f;
+  for (int g = 0; g < H / 16; ++g) {
+    float y[16];
+    load_y(g, y);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(y[e]));
   }
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  const float inv = amax > 0.f ? 448.f / amax : 1.f;
+  for (int g = 0; g < H / 16; ++g) {
+    float y[16];
+    load_y(g, y);
+    uint32_t p[3][4];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float x0 = y[2 * e] * inv, x1 = y[2 * e + 1] * inv;
+      uint32_t code[3];
+#pragma unroll
+      for (int t = 0; t < 3; ++t) {
+        const uint16_t cc = f32x2_to_e4m3x2(x0, x1);
+        code[t] = cc;
+        if (t < 2) {
+          const float2 v = e4m3x2_to_float2(cc);
+          x0 -= v.x;
+          x1 -= v.y;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 3; ++t) {
+        if (e & 1) p[t][e >> 1] |= code[t] << 16;
+        else p[t][e >> 1] = code[t];
+      }
+    }
+    const int off = swz8<D>(r, (hh * H + 16 * g) >> 4);
+#pragma unroll
+    for (int t = 0; t < 3; ++t)
+      *reinterpret_cast<uint4*>(parts + t * kRows * D + off) = make_uint4(p[t][0], p[t][1], p[t][2], p[t][3]);
+  }
+  if (hh == 0) qscale[r] = amax > 0.f ? amax * (1.f / 448.f) : 1.f;
 }
 
 // Rotary embedding of a piece's query rows (one warp, out of line), written
@@ -446,13 +581,12 @@ __device__ __noinline__ void decode_write_out(const DecodeArgs& a, const Piece& 
 }
 
 template <int D, bool PAGED, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
     decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_q, const DecodeArgs a) {
   using C = DecCfg<D, FP8>;
-  constexpr int SL = C::kSlots;
+  constexpr int SK = C::kSlotsK, SV = C::kSlotsV;
   constexpr int NB = C::NB;
-  constexpr int S8 = C::kStage8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ DecBarriers bars;
@@ -480,19 +614,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     bars.abort = 0;
-    for (int i = 0; i < SL; ++i) {
+    for (int i = 0; i < SK; ++i) {
       mbar_init(&bars.k_full[i], 1);
       mbar_init(&bars.k_empty[i], 1);
-      mbar_init(&bars.v_full[i], 1);
-      mbar_init(&bars.v_empty[i], 1);
     }
-    for (int i = 0; i < S8; ++i) {
-      mbar_init(&bars.st_full[0][i], 1);
-      mbar_init(&bars.st_full[1][i], 1);
+    for (int i = 0; i < SV; ++i) {
+      mbar_init(&bars.v_full[i], 1);
+      mbar_init(&bars.v_empty[i], FP8 ? 4 : 1);  // FP8: one arrive per converter warp
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.q_full[i], 1);
       mbar_init(&bars.q_empty[i], 1);
+      mbar_init(&bars.qs_full[i], 1);
+      mbar_init(&bars.qs_empty[i], 4);
+      mbar_init(&bars.vo_full[i], 4);
       mbar_init(&bars.s_full[i], 1);
       mbar_init(&bars.s_empty[i], 4);   // one arrive per softmax warp
       mbar_init(&bars.p_full[i], 4);
@@ -522,24 +657,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 || warp == 6) {
     // ============================== producers: warp 0 K chunks, warp 6 V chunks
+    // into rings of operand tiles (bf16), or of 8-bit tiles (FP8: the K ring
+    // feeds the score MMA, the V ring the softmax warps' conversion)
     const bool is_k = warp == 0;
     const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
     uint64_t* full = is_k ? bars.k_full : bars.v_full;
     uint64_t* empty = is_k ? bars.k_empty : bars.v_empty;
-    uint8_t* ring = smem + (is_k ? 0 : C::kOffV);
-    uint8_t* stage = smem + C::kOffStage + (is_k ? 0 : S8 * C::kTile8);
-    uint64_t* st_full = bars.st_full[is_k ? 0 : 1];
+    uint8_t* ring = smem + (is_k ? 0 : (FP8 ? C::kOffStage : C::kOffV));
+    const int ns = is_k ? SK : SV;
+    const int tile = FP8 ? C::kTile8 : C::kTileBytes;
     if (lane == 0) tma_prefetch_desc(tm);
-    constexpr int NF = FP8 ? S8 : SL;  // TMA destinations: staging slots (FP8) or operand slots
-    int last_fill[NF];
+    int last_fill[C::kMaxSlots];
 #pragma unroll
-    for (int i = 0; i < NF; ++i) last_fill[i] = -1;
-    // TMA of stream chunk cs (piece it, chunk c of it) into `dst` (a tile of
-    // 16-bit operand boxes, or an 8-bit staging tile), completing on `bar`.
-    // Paged: lane i looks up the chunk's i-th page (before the slot wait, so
-    // the lookup's latency overlaps it); pages that hold none of the row's
-    // keys, and invalid entries (reported), get a coordinate past the tensor,
-    // which the TMA fills with zeros.
+    for (int i = 0; i < C::kMaxSlots; ++i) last_fill[i] = -1;
+    // TMA of stream chunk (piece it, chunk c of it) into `dst`, completing on
+    // `bar`.  Paged: lane i looks up the chunk's i-th page (before the slot
+    // wait, so the lookup's latency overlaps it); pages that hold none of the
+    // row's keys, and invalid entries (reported), get a coordinate past the
+    // tensor, which the TMA fills with zeros.
     auto load_chunk = [&](const Piece& it, int c, uint8_t* dst, uint64_t* bar, uint64_t* wait_bar, int wait_parity,
                           int* fill_rec, int fill) {
       const int k0 = it.kbeg + c * kCK;
@@ -587,48 +722,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
-    if constexpr (!FP8) {
-      int cs = 0;
-      for (Cursor cur = begin(); cur.valid; next(cur), ++cs) {
-        const int slot = cs % SL, fill = cs / SL;
-        load_chunk(cur.it, cur.c, ring + slot * C::kTileBytes, &full[slot], fill >= 1 ? &empty[slot] : nullptr,
-                   (fill - 1) & 1, &last_fill[slot], fill);
-      }
-    } else {
-      // FP8: a load cursor runs S8 chunks ahead through the staging ring; the
-      // convert cursor turns each landed 8-bit chunk into the f16 operand
-      // slot (exact: every E4M3 value is an f16) once the MMA that read the
-      // previous one is done, then refills the staging slot it just read
-      Cursor ld = begin();
-      int lcs = 0;
-      for (; lcs < S8 && ld.valid; ++lcs, next(ld))
-        load_chunk(ld.it, ld.c, stage + lcs * C::kTile8, &st_full[lcs], nullptr, 0, &last_fill[lcs], 0);
-      for (Cursor cv = begin(); cv.valid; next(cv)) {
-        const int ci = cv.cs, sg = ci % S8;
-        mbar_wait(&st_full[sg], (ci / S8) & 1, guard);
-        if (ci >= 1) mbar_wait(&empty[0], (ci - 1) & 1, guard);
-        // V rows past the length become zeros here (so that 0 * V stays 0 in
-        // the P V MMA); K rows there only meet masked scores
-        const int nrows = is_k ? kCK : cv.it.len - (cv.it.kbeg + cv.c * kCK);
-        convert_e4m3_tile<D>(stage + sg * C::kTile8, ring, lane, nrows);
-        fence_proxy_async_smem();  // generic writes (operand) and reads (staging) before async-proxy use
-        mbar_arrive_warp(&full[0]);
-        if (ld.valid) {
-          load_chunk(ld.it, ld.c, stage + sg * C::kTile8, &st_full[sg], nullptr, 0, &last_fill[sg], lcs / S8);
-          ++lcs;
-          next(ld);
-        }
+    int slot = 0, fill = 0;
+    for (Cursor cur = begin(); cur.valid; next(cur)) {
+      load_chunk(cur.it, cur.c, ring + slot * tile, &full[slot], fill >= 1 ? &empty[slot] : nullptr, (fill - 1) & 1,
+                 &last_fill[slot], fill);
+      if (++slot == ns) {
+        slot = 0;
+        ++fill;
       }
     }
     // never leave the CTA with copies in flight
     if (lane == 0)
-      for (int i = 0; i < NF; ++i)
-        if (last_fill[i] >= 0) mbar_wait_drain(FP8 ? &st_full[i] : &full[i], (uint32_t)last_fill[i] & 1);
+      for (int i = 0; i < ns; ++i)
+        if (last_fill[i] >= 0) mbar_wait_drain(&full[i], (uint32_t)last_fill[i] & 1);
     __syncwarp();
   } else if (warp == 1) {
     // ===================== score MMA issuer (warp-uniform, one elected lane issues)
     // The query rows of each piece: TMA one piece ahead (the piece's 16 rows,
-    // K-major, 128-byte swizzled, as the score MMA reads them; rows past
+    // K-major, 128-byte swizzled, as the bf16 score MMA reads them; rows past
     // it.rows belong to other heads or lie past the tensor and only fill
     // unused columns of S^T).
     if (lane == 0) tma_prefetch_desc(&tm_q);
@@ -646,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(&bars.q_full[qslot], C::kQBytes);
 #pragma unroll
           for (int x = 0; x < NB; ++x)
-            tma_load_2d(smem + C::kOffQ + qslot * 2 * C::kQBytes + x * kRowBoxBytes, &tm_q, &bars.q_full[qslot],
+            tma_load_2d(smem + C::kOffQ + qslot * C::kQSlot + x * kRowBoxBytes, &tm_q, &bars.q_full[qslot],
                         x * 64, row0);
           last_q[qslot] = (u >> 1) & 1;
         }
@@ -656,37 +767,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < n; ++c) next(qc);
     };
     load_q();
+    int slot = 0, fill = 0;  // K ring position of the current chunk
     for (Cursor cur = begin(); cur.valid; next(cur)) {
-      const int qslot = cur.uses & 1, slot = cur.cs % SL, sb = cur.cs & 1;
+      const int qslot = cur.uses & 1, sb = cur.cs & 1;
       if (cur.c == 0) {
         load_q();  // the next piece's rows
         mbar_wait(&bars.q_full[qslot], (cur.uses >> 1) & 1, guard);
-        uint8_t* qt = smem + C::kOffQ + qslot * 2 * C::kQBytes;
-        if (a.rope_cs != nullptr) rope_rotate_tile<D, FP8>(qt, qt + C::kQBytes, cur.it, a, lane);
-        else if (FP8) q_tile_to_f16<D>(qt, lane);
-        if (FP8 || a.rope_cs != nullptr) {
+        uint8_t* qt = smem + C::kOffQ + qslot * C::kQSlot;
+        if constexpr (FP8) {
+          // the piece's rows as E4M3 parts with row scales (read by the
+          // softmax warps once the previous use of this slot is done)
+          if (cur.uses >= 2) mbar_wait(&bars.qs_empty[qslot], ((cur.uses >> 1) - 1) & 1, guard);
+          q_tile_to_e4m3_parts<D>(qt, smem + C::kOffQ8 + qslot * 3 * C::kQ8Bytes,
+                                  reinterpret_cast<float*>(smem + C::kOffQs) + qslot * kRows, cur.it, a, lane);
+          fence_proxy_async_smem();  // the part tiles are read by the MMAs below
+          mbar_arrive_warp(&bars.qs_full[qslot]);
+        } else if (a.rope_cs != nullptr) {
+          rope_rotate_tile<D, false>(qt, qt + C::kQBytes, cur.it, a, lane);
           fence_proxy_async_smem();  // the rewritten tiles are read by the MMAs below
           __syncwarp();
         }
       }
-      mbar_wait(&bars.k_full[slot], (cur.cs / SL) & 1, guard);
+      mbar_wait(&bars.k_full[slot], fill & 1, guard);
       if (cur.cs >= 2) mbar_wait(&bars.s_empty[sb], ((cur.cs >> 1) - 1) & 1, guard);
       tc_fence_after();
       if (!guard.aborted()) {
-        const uint32_t ka = sbase + slot * C::kTileBytes;
-        const uint32_t qa = sbase + C::kOffQ + qslot * 2 * C::kQBytes;
-        // rotary queries are a bf16 value tile plus a bf16 remainder tile: both accumulate
-        const int tiles = a.rope_cs != nullptr ? 2 : 1;
-        for (int tq = 0; tq < tiles; ++tq)
+        const uint32_t ka = sbase + slot * C::kTileK;
+        if constexpr (FP8) {
+          // E4M3 K codes x the three E4M3 query parts, 32 features per MMA
+          const uint32_t qa = sbase + C::kOffQ8 + qslot * 3 * C::kQ8Bytes;
+          auto desc8 = [](uint32_t addr) { return D == 128 ? sdesc_sw128(addr, 16, 1024) : sdesc_sw64(addr, 16, 512); };
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss_warp(tmem + col_s(sb), sdesc_sw128(ka + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
-                        sdesc_sw128(qa + tq * C::kQBytes + (kk >> 2) * kRowBoxBytes + (kk & 3) * 32, 16, 1024),
-                        C::kIdescS, (tq > 0 || kk > 0) ? 1u : 0u);
+          for (int t = 0; t < 3; ++t)
+#pragma unroll
+            for (int kk = 0; kk < D / 32; ++kk)
+              mma_ss_f8_warp(tmem + col_s(sb), desc8(ka + kk * 32), desc8(qa + t * C::kQ8Bytes + kk * 32), C::kIdescS,
+                             (t > 0 || kk > 0) ? 1u : 0u);
+        } else {
+          const uint32_t qa = sbase + C::kOffQ + qslot * C::kQSlot;
+          // rotary queries are a bf16 value tile plus a bf16 remainder tile: both accumulate
+          const int tiles = a.rope_cs != nullptr ? 2 : 1;
+          for (int tq = 0; tq < tiles; ++tq)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss_warp(tmem + col_s(sb), sdesc_sw128(ka + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                          sdesc_sw128(qa + tq * C::kQBytes + (kk >> 2) * kRowBoxBytes + (kk & 3) * 32, 16, 1024),
+                          C::kIdescS, (tq > 0 || kk > 0) ? 1u : 0u);
+        }
       }
       tc_commit_warp(&bars.s_full[sb]);
       tc_commit_warp(&bars.k_empty[slot]);
       if (cur.c == cur.it.nch - 1) tc_commit_warp(&bars.q_empty[qslot]);
+      if (++slot == SK) {
+        slot = 0;
+        ++fill;
+      }
     }
     // every issued MMA finishes, and no copy is in flight, before TMEM and
     // shared memory are released
@@ -698,15 +833,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 7) {
     // ===================== P V MMA issuer: independent of the score issuer, so
-    // that a V chunk is released as soon as its own P is ready
+    // that a V chunk is released as soon as its own P is ready.  FP8: chunk
+    // i's f16 V is operand tile i % kVop (vo_full, from the converter
+    // warps), released when the P V MMA is done (p_empty).
+    int slot = 0, fill = 0;  // V ring position (bf16)
     for (Cursor cur = begin(); cur.valid; next(cur)) {
-      const int ob = cur.uses & 1, pb = cur.cs & 1, slot = cur.cs % SL;
+      const int ob = cur.uses & 1, pb = cur.cs & 1;
       if (cur.c == 0 && cur.uses >= 2) mbar_wait(&bars.o_empty[ob], ((cur.uses >> 1) - 1) & 1, guard);
-      mbar_wait(&bars.v_full[slot], (cur.cs / SL) & 1, guard);
+      if constexpr (FP8) mbar_wait(&bars.vo_full[cur.cs % C::kVop], (cur.cs / C::kVop) & 1, guard);
+      else mbar_wait(&bars.v_full[slot], fill & 1, guard);
       mbar_wait(&bars.p_full[pb], (cur.cs >> 1) & 1, guard);
       tc_fence_after();
       if (!guard.aborted()) {
-        const uint32_t va = sbase + C::kOffV + slot * C::kTileBytes;
+        const uint32_t va = sbase + C::kOffV + (FP8 ? cur.cs % C::kVop : slot) * C::kTileBytes;
         const uint32_t pa = sbase + C::kOffP + pb * C::kPBytes;
 #pragma unroll
         for (int kk = 0; kk < kCK / 16; ++kk)
@@ -715,8 +854,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (cur.c > 0 || kk > 0) ? 1u : 0u);
       }
       tc_commit_warp(&bars.p_empty[pb]);
-      tc_commit_warp(&bars.v_empty[slot]);
+      if constexpr (!FP8) tc_commit_warp(&bars.v_empty[slot]);
       if (cur.c == cur.it.nch - 1) tc_commit_warp(&bars.o_full[ob]);
+      if (++slot == SV) {
+        slot = 0;
+        ++fill;
+      }
     }
     tc_commit_warp(&bars.teardown[1]);
     mbar_wait_drain(&bars.teardown[1], 0);
@@ -729,6 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* s_sum = reinterpret_cast<float*>(smem + C::kOffSum);
     const float sc_log2 = a.scale_log2;
     float m_used[kRows], lpart[kRows];
+    float sc_row[FP8 ? kRows : 1];  // FP8: score scale times the row's query scale
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
       m_used[r] = -INFINITY;
@@ -751,6 +895,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_used[r] = -INFINITY;
           lpart[r] = 0.f;
         }
+        if constexpr (FP8) {
+          const int qslot = cur.uses & 1;
+          mbar_wait(&bars.qs_full[qslot], (cur.uses >> 1) & 1, guard);
+          const float* qs = reinterpret_cast<const float*>(smem + C::kOffQs) + qslot * kRows;
+#pragma unroll
+          for (int r = 0; r < kRows; ++r) sc_row[r] = qs[r] * sc_log2;
+          mbar_arrive_warp(&bars.qs_empty[qslot]);
+        }
       }
       mbar_wait(&bars.s_full[sb], (i >> 1) & 1, guard);
       tc_fence_after();
@@ -762,14 +914,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_warp(&bars.s_empty[sb]);
 
       // mask: key j (position k0 + j) is visible to the row of position t iff
-      // k0 + j <= len - Tq + t; keys at or past len never are.
+      // k0 + j <= len - Tq + t; keys at or past len never are.  A chunk that
+      // every row sees whole (all but a piece's last one or two) skips it.
       const int k0 = it.kbeg + cur.c * kCK;
       const int lim0 = it.len - a.Tq - k0;
       float s[kRows];
+      if (lim0 >= kCK - 1) {
 #pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        const int t = (it.r0 + r) % a.Tq;
-        s[r] = j <= lim0 + t ? __uint_as_float(sr[r]) * sc_log2 : -INFINITY;
+        for (int r = 0; r < kRows; ++r) s[r] = __uint_as_float(sr[r]) * (FP8 ? sc_row[FP8 ? r : 0] : sc_log2);
+      } else {
+        int t = it.r0 % a.Tq;  // query position of row r, stepped along the rows
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+          s[r] = j <= lim0 + t ? __uint_as_float(sr[r]) * (FP8 ? sc_row[FP8 ? r : 0] : sc_log2) : -INFINITY;
+          t = t + 1 == a.Tq ? 0 : t + 1;
+        }
       }
       // The maximum in use moves only when a score exceeds it by more than
       // 2^8 (or at a piece's first chunk): one barrier-reduction tells
@@ -805,13 +964,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // cache rows at or past len are outside the cache and may hold
       // anything: zero their V (once it has landed) so that 0 * V stays 0
-      // in the MMA.  (FP8: the converter writes those rows as zeros; its
-      // single operand slot can be two fills behind this warp, where a
-      // parity wait on it would not tell the fills apart.)
+      // in the MMA (FP8: the converter warps write them as zeros)
       const int nvis = it.len - k0;
       if (!FP8 && nvis < kCK) {
-        mbar_wait(&bars.v_full[i % SL], (i / SL) & 1, guard);
-        uint8_t* vs = smem + C::kOffV + (i % SL) * C::kTileBytes;
+        mbar_wait(&bars.v_full[i % SV], (i / SV) & 1, guard);
+        uint8_t* vs = smem + C::kOffV + (i % SV) * C::kTileBytes;
         if (j >= nvis) {
 #pragma unroll
           for (int x = 0; x < NB; ++x)
@@ -893,6 +1050,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (pend) write_out();
+  }
+
+  if constexpr (FP8) {
+    if (warp >= 8) {
+      // ================= V converters (FP8): warp 8 + q converts key rows
+      // 32 q .. 32 q + 31 of each landed chunk, one row per thread, into f16
+      // operand tile i % kVop once the P V MMA of chunk i - kVop (its
+      // previous reader; p_empty of that chunk) is done; one converter warp
+      // per SM sub-partition, beside the softmax warp there
+      constexpr int NV = C::kVop;
+      const int j = 32 * (warp - 8) + lane;
+      for (Cursor cur = begin(); cur.valid; next(cur)) {
+        const int i = cur.cs, ot = i % NV;
+        mbar_wait(&bars.v_full[i % SV], (i / SV) & 1, guard);
+        if (i >= NV) mbar_wait(&bars.p_empty[(i - NV) & 1], ((i - NV) >> 1) & 1, guard);
+        const int nvis = cur.it.len - (cur.it.kbeg + cur.c * kCK);
+        convert_v_row<D>(smem + C::kOffStage + (i % SV) * C::kTile8, smem + C::kOffV + ot * C::kTileBytes, j,
+                         j < nvis);
+        fence_proxy_async_smem();  // operand writes and staging reads before async-proxy use
+        mbar_arrive_warp(&bars.v_empty[i % SV]);
+        mbar_arrive_warp(&bars.vo_full[ot]);
+      }
+    }
   }
 
   // ------------------------------------------------------------ teardown
@@ -990,7 +1170,7 @@ static cudaError_t launch_decode_dp(const CUtensorMap& k, const CUtensorMap& v, 
     attr_set[dev] = true;
   }
   prof_begin(kProfDecode, stream);
-  decode_partial_kernel<D, PAGED, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(k, v, q, a);
+  decode_partial_kernel<D, PAGED, FP8><<<grid, FP8 ? kThreads8 : kThreads, C::kSmemBytes, stream>>>(k, v, q, a);
   prof_end(stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.slots <= 1) return e;  // no unit can be cut

@@ -136,3 +136,23 @@ def test_fp8_one_hot_values_keep_chunks_apart(gq):
     assert err < 2e-3 * ro.max() + 1e-4, f"max abs error {err:.3e} (largest feature {ro.max():.3e})"
     check("o", o, ro, TOL_REL_O)
     check_lse(lse, rlse)
+
+
+def test_fp8_nan_codes_inside_the_cache(gq):
+    """An E4M3 NaN code at a visible key makes NaN exactly where the oracle
+    does (V: that feature of the group's rows; K: the whole rows that see
+    it); everything else still matches."""
+    B, Hq, Hkv, Tq, S, D = 2, 8, 2, 1, 700, 128
+    x = W.fp8_decode_inputs(B, Hq, Hkv, Tq, S, D, cache_lens=[700, 300], seed=37)
+    x["v8"][0, 1, 400, 5] = 0x7F
+    x["v8"][1, 0, 17, 100] = 0xFF
+    x["k8"][1, 1, 250, 3] = 0x7F
+    o, lse = run_gpu(gq, x, 0.1)
+    assert gq.get_device_status() == 0
+    ro, rlse = run_oracle(x, 0.1)
+    g, ref = to64(o), ro
+    assert np.isnan(ref).any()
+    np.testing.assert_array_equal(np.isnan(g), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.abs(g[ok] - ref[ok]).max() < 2e-2
+    np.testing.assert_array_equal(np.isnan(to64(lse)), np.isnan(rlse))
