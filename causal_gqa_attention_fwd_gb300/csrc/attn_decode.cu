@@ -152,6 +152,8 @@ struct __align__(8) DecBarriers {
   int abort;
 };
 
+constexpr int kDevBadPages = 11;  // device status: a block-table entry names no page (ATTN_ERR_PAGES)
+
 constexpr int kLenCache = 1024;  // batch rows whose lengths are kept in shared memory
 
 // Chunks of batch row b's cache: ceil(len / 128), 0 for an invalid length.
@@ -326,6 +328,33 @@ template <bool F16>
 __device__ __forceinline__ float2 unpack16x2(uint32_t v) {
   if constexpr (F16) return __half22float2(*reinterpret_cast<const __half2*>(&v));
   else return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+}
+
+// D(tmem) (+)= A(smem) * B(smem)^T   (8-bit A and B, f32 accumulate; 32 K-elements per MMA)
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ss_f8_warp(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if (elect_one()) mma_ss_f8(d, a, b, idesc, acc);
+  __syncwarp();
+}
+// Shared-memory matrix descriptor for a 64-byte-swizzled K-major operand: rows of 64 bytes, 8-row
+// groups `sbo` (512) bytes apart, 512-byte-aligned tile base.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+  d |= (uint64_t)4 << 61;  // 64-byte swizzle
+  return d;
 }
 
 // Two E4M3 codes (low byte = first) as two f16 (low half = first): the

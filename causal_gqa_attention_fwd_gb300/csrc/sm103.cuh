@@ -17,7 +17,7 @@
 namespace gqa {
 
 // Device status word values (mirrors attn_status in include/gqa_attn.h).
-enum : int { kDevOk = 0, kDevTimeout = 9, kDevBadSeqlens = 5, kDevBadPages = 11 };
+enum : int { kDevOk = 0, kDevTimeout = 9, kDevBadSeqlens = 5 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
@@ -183,17 +183,6 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
       : "memory");
 }
 
-// D(tmem) (+)= A(smem) * B(smem)^T   (8-bit A and B, f32 accumulate; 32 K-elements per MMA)
-__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // D(tmem) (+)= A(tmem) * B(smem)^T
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
@@ -221,10 +210,6 @@ __device__ __forceinline__ bool elect_one() {
 // roughly 100 cycles per MMA instead.
 __device__ __forceinline__ void mma_ss_warp(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   if (elect_one()) mma_ss(d, a, b, idesc, acc);
-  __syncwarp();
-}
-__device__ __forceinline__ void mma_ss_f8_warp(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  if (elect_one()) mma_ss_f8(d, a, b, idesc, acc);
   __syncwarp();
 }
 __device__ __forceinline__ void mma_ts_warp(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -264,18 +249,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
   d |= (uint64_t)2 << 61;  // 128-byte swizzle
-  return d;
-}
-
-// The same for a 64-byte-swizzled K-major operand: rows of 64 bytes, 8-row
-// groups `sbo` (512) bytes apart, 512-byte-aligned tile base.
-__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
-  d |= (uint64_t)4 << 61;  // 64-byte swizzle
   return d;
 }
 
