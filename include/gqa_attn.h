@@ -163,7 +163,9 @@ GQA_ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Tq, i
  * sin(p*theta_i).  Each query t of row b is rotated at its position
  * p = cache_lens[b] - Tq + t before the scores: feature i pairs with feature
  * i + D/2, x'_i = x_i cos - x_{i+D/2} sin, x'_{i+D/2} = x_{i+D/2} cos + x_i sin,
- * rounded to bf16.  The cache must hold keys already rotated at their
+ * computed in f32 and carried into the score MMA to about 2^-16 of each
+ * element (a bf16 value plus a bf16 remainder; E4M3 caches: the three E4M3
+ * parts below).  The cache must hold keys already rotated at their
  * positions (as appending them rotated leaves them). */
 GQA_ATTN_API attn_status attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
                                          const int* cache_lens, void* o, float* lse, void* workspace,
@@ -202,10 +204,15 @@ GQA_ATTN_API attn_status attn_decode_paged_fwd(const void* q, const void* k_page
  *   k8, v8           uint8 [B, Hkv, S, D]  (contiguous), or
  *   k8_pages, v8_pages uint8 [num_pages, Hkv, page_size, D]  (paged, as
  *                    attn_decode_paged_fwd)
- * The codes are widened exactly to f16 on the chip; the scores and P V use
- * f16 operands (queries and probabilities included) with f32 accumulation,
- * so the queries must lie inside the f16 range (|q| < 65504).  Workspace,
- * rotary table and errors as attn_decode_fwd. */
+ * The scores are taken on the K codes as stored: each query row q (after
+ * rotation, if any) is split into three E4M3 parts with one f32 scale per
+ * row, q = s (h0 + h1 + h2), s = max|q| / 448, which holds q to about 2^-12
+ * of each element (2^-19 of the row's largest for elements below E4M3's
+ * normal range); the products accumulate in f32.  V is widened exactly to
+ * f16 and P is rounded to f16 for the P V product (f32 accumulation).  NaN
+ * codes at visible keys give NaN where the definition does; codes past
+ * cache_lens[b] are never used.  Workspace, rotary table and errors as
+ * attn_decode_fwd. */
 GQA_ATTN_API attn_status attn_decode_fp8_fwd(const void* q, const void* k8, const void* v8, float k_scale,
                                              float v_scale, const int* cache_lens, void* o, float* lse,
                                              void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Tq,
