@@ -406,7 +406,8 @@ def run_decode(args, world, rank, local):
             "metric": DECODE_METRIC, "value": value, "unit": DECODE_UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "data": "synthetic",
-            "dtype": "E4M3 K/V + bf16 q, f16 MMA operands, f32 arithmetic" if w.fp8 else "bf16 in, f32 arithmetic",
+            "dtype": ("E4M3 K/V, bf16 q: scores E4M3 K x 3-part E4M3 q, P V f16 V x f16 P, f32 accumulation"
+                      if w.fp8 else "bf16 in, f32 arithmetic"),
             "config": decode_config(w, world, flush.describe()),
             "frac_of_peak": value / pk["hbm_gbs"],
             "tokens_per_s": world * w.B * w.Tq * args.steps / (total_ms / 1e3),

@@ -313,23 +313,6 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 }  // namespace
 
-// Two 16-bit floats (low half = first element) from two f32: bf16 or f16.
-template <bool F16>
-__device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
-  if constexpr (F16) {
-    const __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&h);
-  } else {
-    return pack_bf16x2(lo, hi);
-  }
-}
-
-template <bool F16>
-__device__ __forceinline__ float2 unpack16x2(uint32_t v) {
-  if constexpr (F16) return __half22float2(*reinterpret_cast<const __half2*>(&v));
-  else return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
-}
-
 // D(tmem) (+)= A(smem) * B(smem)^T   (8-bit A and B, f32 accumulate; 32 K-elements per MMA)
 __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
@@ -521,7 +504,7 @@ __device__ __noinline__ void q_tile_to_e4m3_parts(const uint8_t* qt, uint8_t* pa
 // x'_i = x_i c - x_{i+D/2} s, x'_{i+D/2} = x_{i+D/2} c + x_i s with c, s from
 // the table row of that position.  The tile is K-major, 128-byte swizzled:
 // feature d of row r sits in box d / 64, 16-byte chunk ((d % 64) / 8) ^ (r % 8).
-template <int D, bool F16>
+template <int D>
 __device__ __noinline__ void rope_rotate_tile(uint8_t* qs, uint8_t* qrem, const Piece& it, const DecodeArgs& a,
                                               int lane) {
   constexpr int H = D / 2;
@@ -548,12 +531,12 @@ __device__ __noinline__ void rope_rotate_tile(uint8_t* qs, uint8_t* qrem, const 
     uint32_t* h32 = reinterpret_cast<uint32_t*>(&hi);
     uint32_t* rl32 = reinterpret_cast<uint32_t*>(&rlo);
     uint32_t* rh32 = reinterpret_cast<uint32_t*>(&rhi);
-    // value = r16(y), remainder = r16(y - value): the pair carries y to well
-    // below the 16-bit format's precision
+    // value = bf16(y), remainder = bf16(y - value): the pair carries y to
+    // about 16 significant bits
     auto split = [](float y0, float y1, uint32_t& v, uint32_t& rm) {
-      v = pack16x2<F16>(y0, y1);
-      const float2 b = unpack16x2<F16>(v);
-      rm = pack16x2<F16>(y0 - b.x, y1 - b.y);
+      v = pack_bf16x2(y0, y1);
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+      rm = pack_bf16x2(y0 - b.x, y1 - b.y);
     };
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -812,7 +795,7 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
           fence_proxy_async_smem();  // the part tiles are read by the MMAs below
           mbar_arrive_warp(&bars.qs_full[qslot]);
         } else if (a.rope_cs != nullptr) {
-          rope_rotate_tile<D, false>(qt, qt + C::kQBytes, cur.it, a, lane);
+          rope_rotate_tile<D>(qt, qt + C::kQBytes, cur.it, a, lane);
           fence_proxy_async_smem();  // the rewritten tiles are read by the MMAs below
           __syncwarp();
         }

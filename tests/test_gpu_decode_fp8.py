@@ -71,8 +71,9 @@ def test_fp8_ignores_nan_codes_past_length(gq):
     check_lse(lse, ref[1])
 
 
-def test_fp8_rope_decode(gq):
-    B, Hq, Hkv, Tq, S, D = 2, 8, 2, 3, 3000, 128
+@pytest.mark.parametrize("D", [128, 64])
+def test_fp8_rope_decode(gq, D):
+    B, Hq, Hkv, Tq, S = 2, 8, 2, 3, 3000
     x = W.fp8_decode_inputs(B, Hq, Hkv, Tq, S, D, cache_lens=[3000, 1500], seed=33)
     tab = W.rope_cos_sin_table(S, D)
     o, lse = run_gpu(gq, x, 0.09, rope_cos_sin=tab.cuda())
@@ -82,9 +83,18 @@ def test_fp8_rope_decode(gq):
     check_lse(lse, rlse)
 
 
-def test_paged_fp8_decode(gq):
-    B, Hq, Hkv, Tq, psz, maxp, D = 3, 8, 2, 1, 32, 30, 128
-    x = W.paged_decode_inputs(B, Hq, Hkv, Tq, psz, maxp, D, cache_lens=[960, 1, 333], spare_pages=2, seed=34)
+PAGED_FP8_CASES = [
+    # B, Hq, Hkv, Tq, page_size, max_pages, D, cache_lens
+    (3, 8, 2, 1, 32, 30, 128, [960, 1, 333]),
+    (3, 14, 2, 2, 16, 40, 64, [640, 2, 301]),   # 64-byte swizzle, 8 page boxes per chunk
+    (2, 8, 8, 1, 128, 5, 64, [640, 129]),      # 64-byte swizzle, chunks inside a page
+]
+
+
+@pytest.mark.parametrize("case", PAGED_FP8_CASES, ids=lambda c: "B%d_Hq%d_Hkv%d_Tq%d_page%d_D%d" % (c[0], c[1], c[2], c[3], c[4], c[6]))
+def test_paged_fp8_decode(gq, case):
+    B, Hq, Hkv, Tq, psz, maxp, D, lens = case
+    x = W.paged_decode_inputs(B, Hq, Hkv, Tq, psz, maxp, D, cache_lens=lens, spare_pages=2, seed=34)
     k8p, ks = W.fp8_cache(x["k_pages"].float())
     v8p, vs = W.fp8_cache(x["v_pages"].float())
     q, bt, ln = x["q"].cuda(), x["block_table"].cuda(), x["cache_lens"].cuda()
