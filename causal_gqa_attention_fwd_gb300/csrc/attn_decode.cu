@@ -94,7 +94,7 @@ struct DecCfg {
   // take microseconds to land under full load, so the shared memory goes to
   // 8-bit slots in flight rather than to a second operand tile.
   static constexpr int kSlotsK = FP8 ? (D == 128 ? 6 : 8) : (D == 128 ? 3 : 6);
-  static constexpr int kSlotsV = FP8 ? (D == 128 ? 3 : 8) : kSlotsK;
+  static constexpr int kSlotsV = FP8 ? (D == 128 ? 4 : 8) : kSlotsK;
   static constexpr int kVop = FP8 ? (D == 128 ? 1 : 2) : 0;
   static constexpr int kTileK = FP8 ? kTile8 : kTileBytes;          // bytes per K ring slot
   static constexpr int kOffV = kSlotsK * kTileK;                    // V ring / FP8 V operand tiles
@@ -123,7 +123,7 @@ struct DecCfg {
   static constexpr uint32_t kLboV = D == 128 ? kBoxBytes : 0;
   static constexpr int kMaxSlots = kSlotsK > kSlotsV ? kSlotsK : kSlotsV;
   static_assert(kMaxSlots <= 8, "barrier arrays");
-  static_assert(kSmemBytes + 5120 <= 232448, "shared memory (dynamic + static)");
+  static_assert(kSmemBytes + 2048 <= 232448, "shared memory (dynamic + static: barriers, lengths)");
 };
 
 __device__ __forceinline__ uint32_t col_s(int b) { return (uint32_t)b * kRows; }
@@ -154,7 +154,7 @@ struct __align__(8) DecBarriers {
 
 constexpr int kDevBadPages = 11;  // device status: a block-table entry names no page (ATTN_ERR_PAGES)
 
-constexpr int kLenCache = 1024;  // batch rows whose lengths are kept in shared memory
+constexpr int kLenCache = 256;  // batch rows whose lengths are kept in shared memory (larger batches read them from global memory)
 
 // Chunks of batch row b's cache: ceil(len / 128), 0 for an invalid length.
 // `lens` is the shared-memory copy of cache_lens (B <= kLenCache) or cache_lens itself.

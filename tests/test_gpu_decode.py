@@ -156,3 +156,15 @@ def test_rope_decode_matches_oracle(gq, case):
     check_lse(lse, rlse)
     plain, _ = run_gpu(gq, x, scale)
     assert not torch.equal(plain, o)
+
+
+def test_decode_many_batch_rows(gq):
+    """More batch rows than the kernel keeps lengths for in shared memory
+    (they are then read from global memory), ragged lengths."""
+    B, Hq, Hkv, Tq, S, D = 300, 4, 2, 1, 300, 64
+    x = W.decode_inputs(B, Hq, Hkv, Tq, S, D, seed=23)
+    o, lse = run_gpu(gq, x, 0.125)
+    assert gq.get_device_status() == 0
+    ro, rlse = run_oracle(x, 0.125)
+    check("o", o, ro, TOL_REL_O)
+    check_lse(lse, rlse)
