@@ -21,17 +21,19 @@
 //   number of chunks whatever the rows' lengths.  A share cuts units into
 //   pieces; a unit processed as one piece writes O / LSE, the pieces of a
 //   cut unit write partials that decode_merge combines.
-//   Roles (256 threads):
+//   Roles (256 threads; 384 for E4M3 caches, below):
 //   warp 0     producer: TMA-loads the share's 128-key K chunks (128-byte
-//              swizzled boxes) into the K ring, running ahead across pieces,
-//              and each piece's 16 query rows (a K-major swizzled tile).
+//              swizzled boxes) into the K ring, running ahead across pieces
+//              (paged caches: one box per page, the pages looked up in the
+//              block table by the warp's lanes before the slot wait).
 //   warp 6     producer of the V ring.  K and V have rings of their own: a
 //              K chunk is released as soon as its score MMA is done, a V
 //              chunk only after P V, so K refills run further ahead.
 //   warp 1     score MMA issuer (S^T into a double buffer, so the softmax of
 //              one chunk overlaps the score MMA of the next); TMEM owner;
-//              with a rotary table it first rotates each piece's query
-//              rows in place at their positions (positions-aware RoPE),
+//              TMA-loads each piece's 16 query rows one piece ahead (a
+//              K-major swizzled tile); with a rotary table it first rotates
+//              them in place at their positions (positions-aware RoPE),
 //              keeping the rounding remainder in a second bf16 tile that a
 //              second set of score MMAs adds in.
 //   warp 7     P V MMA issuer: O^T += V^T P^T as soon as a chunk's P and V
