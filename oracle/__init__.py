@@ -203,6 +203,92 @@ def rope_rotate(x, positions, cos_sin):
     return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
 
 
+def rope_rotate_t(x, positions, cos_sin):
+    """The transpose (= inverse) of ``rope_rotate`` at the same positions:
+    x'_i = x_i c_i + x_{i+D/2} s_i,  x'_{i+D/2} = x_{i+D/2} c_i - x_i s_i.  It takes
+    a gradient with respect to rotated vectors back to the unrotated ones."""
+    x = np.asarray(x, dtype=np.float64)
+    h = x.shape[-1] // 2
+    cs = np.asarray(cos_sin, dtype=np.float64)[np.asarray(positions)]
+    c, s = cs[..., :h], cs[..., h:]
+    lo, hi = x[..., :h], x[..., h:]
+    return np.concatenate([lo * c + hi * s, hi * c - lo * s], axis=-1)
+
+
+def _rope_err_t(e, positions, cos_sin):
+    """Root-sum-square rounding-error scales carried through rope_rotate_t."""
+    e = np.asarray(e, dtype=np.float64)
+    h = e.shape[-1] // 2
+    cs = np.asarray(cos_sin, dtype=np.float64)[np.asarray(positions)]
+    c2, s2 = cs[..., :h] ** 2, cs[..., h:] ** 2
+    lo2, hi2 = e[..., :h] ** 2, e[..., h:] ** 2
+    return np.sqrt(np.concatenate([lo2 * c2 + hi2 * s2, hi2 * c2 + lo2 * s2], axis=-1))
+
+
+def _dense_positions(x):
+    B, H, T = np.asarray(x).shape[:3]
+    return np.broadcast_to(np.arange(T), (B, H, T))
+
+
+def _varlen_positions(x, cu_seqlens):
+    cu = np.asarray(cu_seqlens)
+    total, H = np.asarray(x).shape[:2]
+    pos = np.zeros(total, dtype=np.int64)
+    for a, b in zip(cu[:-1], cu[1:]):
+        pos[a:b] = np.arange(b - a)
+    return np.broadcast_to(pos[:, None], (total, H))
+
+
+def rope_fwd(q, k, v, rope_cos_sin, causal: bool = True, scale: float | None = None, lib=None):
+    """Dense attention with rotary queries and keys (RoPE of
+    MultiHeadAttentionWithRoPE, llm-from-scratch "Project Overview"; the
+    positions-aware RoPE of the microLLM-rocm README): q and k of each row are
+    rotated (rope_rotate) at their positions 0..T-1, then ``fwd``.  Returns
+    (O, LSE) as ``fwd``."""
+    return fwd(rope_rotate(q, _dense_positions(q), rope_cos_sin), rope_rotate(k, _dense_positions(k), rope_cos_sin),
+               v, causal=causal, scale=scale, lib=lib)
+
+
+def rope_bwd(q, k, v, dout, rope_cos_sin, causal: bool = True, scale: float | None = None, lib=None,
+             err_terms: bool = False):
+    """Backward of L = sum(dO * rope_fwd(q, k, v)) with respect to the
+    unrotated q, k and v: ``bwd`` on the rotated q, k, then dq and dk taken
+    back through the rotation (rope_rotate_t).  Returns the same dict as
+    ``bwd`` (error scales carried through the rotation)."""
+    pq, pk = _dense_positions(q), _dense_positions(k)
+    r = bwd(rope_rotate(q, pq, rope_cos_sin), rope_rotate(k, pk, rope_cos_sin), v, dout, causal=causal,
+            scale=scale, lib=lib, err_terms=err_terms)
+    r["dq"] = rope_rotate_t(r["dq"], pq, rope_cos_sin)
+    r["dk"] = rope_rotate_t(r["dk"], pk, rope_cos_sin)
+    if err_terms:
+        r["edq"] = _rope_err_t(r["edq"], pq, rope_cos_sin)
+        r["edk"] = _rope_err_t(r["edk"], pk, rope_cos_sin)
+    return r
+
+
+def rope_varlen_fwd(q, k, v, cu_seqlens, rope_cos_sin, causal: bool = True, scale: float | None = None, lib=None):
+    """``rope_fwd`` for a packed variable-length batch: positions restart at 0
+    in every sequence (only position differences within a sequence reach
+    the result)."""
+    return varlen_fwd(rope_rotate(q, _varlen_positions(q, cu_seqlens), rope_cos_sin),
+                      rope_rotate(k, _varlen_positions(k, cu_seqlens), rope_cos_sin), v, cu_seqlens,
+                      causal=causal, scale=scale, lib=lib)
+
+
+def rope_varlen_bwd(q, k, v, dout, cu_seqlens, rope_cos_sin, causal: bool = True, scale: float | None = None,
+                    lib=None, err_terms: bool = False):
+    """``rope_bwd`` for a packed variable-length batch."""
+    pq, pk = _varlen_positions(q, cu_seqlens), _varlen_positions(k, cu_seqlens)
+    r = varlen_bwd(rope_rotate(q, pq, rope_cos_sin), rope_rotate(k, pk, rope_cos_sin), v, dout, cu_seqlens,
+                   causal=causal, scale=scale, lib=lib, err_terms=err_terms)
+    r["dq"] = rope_rotate_t(r["dq"], pq, rope_cos_sin)
+    r["dk"] = rope_rotate_t(r["dk"], pk, rope_cos_sin)
+    if err_terms:
+        r["edq"] = _rope_err_t(r["edq"], pq, rope_cos_sin)
+        r["edk"] = _rope_err_t(r["edk"], pk, rope_cos_sin)
+    return r
+
+
 def decode_fwd(q, k_cache, v_cache, cache_lens, scale: float | None = None, lib=None, rope_cos_sin=None):
     """Attention of the newest Tq positions over a KV cache.
 

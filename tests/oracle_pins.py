@@ -407,7 +407,65 @@ def pin_fp8_decode(lib):
     np.testing.assert_array_equal(l, l2)
 
 
+def pin_rope_prefill(lib):
+    """Rotary prefill (q and k rotated at positions 0..T-1 before attention):
+    the transpose undoes the rotation; shifting every position by the same
+    amount leaves O and LSE unchanged (the scores depend only on relative
+    position) while dropping the rotation changes them; the backward through
+    the rotation matches central finite differences of L = sum(dO * O) in the
+    unrotated q and k; a packed variable-length batch equals dense runs on
+    its slices (where each sequence's positions start is unobservable: only
+    query-key position differences reach the scores)."""
+    r = _rng(15)
+    D, scale = 8, 0.4
+    tab = _rope_table(64, D)
+    x = r.standard_normal((3, 5, D))
+    pos = r.integers(0, 64, (3, 5))
+    np.testing.assert_allclose(oracle.rope_rotate_t(oracle.rope_rotate(x, pos, tab), pos, tab), x, atol=1e-13)
+    B, Hq, Hkv, T = 2, 4, 2, 6
+    q, do = r.standard_normal((B, Hq, T, D)), r.standard_normal((B, Hq, T, D))
+    k, v = r.standard_normal((B, Hkv, T, D)), r.standard_normal((B, Hkv, T, D))
+    o, l = oracle.rope_fwd(q, k, v, tab, scale=scale, lib=lib)
+    o2, l2 = oracle.rope_fwd(q, k, v, tab[17:], scale=scale, lib=lib)   # every position + 17
+    np.testing.assert_allclose(o2, o, atol=1e-12)
+    np.testing.assert_allclose(l2, l, atol=1e-12)
+    assert np.abs(oracle.fwd(q, k, v, scale=scale, lib=lib)[0] - o).max() > 1e-3
+    g = oracle.rope_bwd(q, k, v, do, tab, scale=scale, lib=lib)
+    np.testing.assert_allclose(g["o"], o, atol=1e-13)
+
+    def loss(qq, kk, vv):
+        return float((do * oracle.rope_fwd(qq, kk, vv, tab, scale=scale, lib=lib)[0]).sum())
+
+    eps = 1e-6
+    for name, which in (("dq", 0), ("dk", 1), ("dv", 2)):
+        base = [q, k, v][which]
+        for idx in list(np.ndindex(base.shape))[::5]:
+            args_p = [q, k, v]
+            a = base.copy()
+            a[idx] += eps
+            args_p[which] = a
+            lp = loss(*args_p)
+            a[idx] -= 2 * eps
+            lm = loss(*args_p)
+            num = (lp - lm) / (2 * eps)
+            assert abs(num - g[name][idx]) <= 1e-6 * (1 + abs(num)), (name, idx, num, g[name][idx])
+    cu = [0, 5, 6, 13]
+    qv, dov = r.standard_normal((13, Hq, D)), r.standard_normal((13, Hq, D))
+    kv, vv = r.standard_normal((13, Hkv, D)), r.standard_normal((13, Hkv, D))
+    ov, lv = oracle.rope_varlen_fwd(qv, kv, vv, cu, tab, scale=scale, lib=lib)
+    gv = oracle.rope_varlen_bwd(qv, kv, vv, dov, cu, tab, scale=scale, lib=lib)
+    dense = lambda t: np.ascontiguousarray(t.transpose(1, 0, 2)[None])
+    for a, b in zip(cu[:-1], cu[1:]):
+        od, ld = oracle.rope_fwd(dense(qv[a:b]), dense(kv[a:b]), dense(vv[a:b]), tab, scale=scale, lib=lib)
+        np.testing.assert_allclose(ov[a:b], od[0].transpose(1, 0, 2), atol=1e-13)
+        np.testing.assert_allclose(lv[:, a:b], ld[0], atol=1e-13)
+        gd = oracle.rope_bwd(dense(qv[a:b]), dense(kv[a:b]), dense(vv[a:b]), dense(dov[a:b]), tab, scale=scale,
+                             lib=lib)
+        for n in ("dq", "dk", "dv"):
+            np.testing.assert_allclose(gv[n][a:b], gd[n][0].transpose(1, 0, 2), atol=1e-12)
+
+
 PINS = [pin_hand_worked, pin_rows_sum_to_one, pin_single_token, pin_constant_keys, pin_shift_invariance,
         pin_gqa_equals_repeated_mha, pin_torch_sdpa, pin_finite_differences, pin_delta_identity,
         pin_varlen_equals_slices, pin_rounding_error_terms, pin_decode_is_dense_suffix,
-        pin_paged_decode_is_contiguous_decode, pin_rope_decode, pin_fp8_decode]
+        pin_paged_decode_is_contiguous_decode, pin_rope_decode, pin_fp8_decode, pin_rope_prefill]
