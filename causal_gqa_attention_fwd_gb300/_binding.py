@@ -25,6 +25,8 @@ STATUS = {
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_fwd_rope_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "attn_fwd_rope": (_I, [_P, _P, _P, _P, _P, _P, _Z, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P]),
     "attn_bwd_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "attn_bwd": (_I, [_P] * 10 + [_Z, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_varlen_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
@@ -147,6 +149,32 @@ def attn_fwd(q, k, v, causal: bool = True, scale=None, o=None, lse=None, stream=
                         _need(lse, "lse", torch.float32), B, Hq, Hkv, T, D, int(causal), _scale(scale, D),
                         _stream(stream))
     _check(st, "attn_fwd")
+    return o, lse
+
+
+def attn_fwd_rope_workspace_size(B, Hq, Hkv, T, D) -> int:
+    return int(lib().attn_fwd_rope_workspace_size(B, Hq, Hkv, T, D))
+
+
+def attn_fwd_rope(q, k, v, rope_cos_sin, causal: bool = True, scale=None, o=None, lse=None, workspace=None,
+                  stream=None):
+    """Dense forward with q and k rotated at positions 0..T-1 (rotary table rope_cos_sin float32
+    [>= T, D] on the device, as attn_decode_fwd) -> (o bf16, lse f32 [B,Hq,T])."""
+    B, Hq, T, D = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, T, D) or v.shape != k.shape:
+        raise ValueError("k, v must be [B, Hkv, T, D] matching q")
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    if workspace is None:
+        workspace = torch.empty(max(attn_fwd_rope_workspace_size(B, Hq, Hkv, T, D), 256), dtype=torch.uint8,
+                                device=q.device)
+    rope_ptr, rope_n = _rope(rope_cos_sin)
+    st = lib().attn_fwd_rope(_need(q, "q"), _need(k, "k"), _need(v, "v"), _need(o, "o"),
+                             _need(lse, "lse", torch.float32), _need(workspace, "workspace", torch.uint8),
+                             workspace.numel(), B, Hq, Hkv, T, D, int(causal), _scale(scale, D), rope_ptr, rope_n,
+                             _stream(stream))
+    _check(st, "attn_fwd_rope")
     return o, lse
 
 

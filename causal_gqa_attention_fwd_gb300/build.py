@@ -19,7 +19,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgqa_attn.so")
 
 SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_decode.cu"]
-HEADERS = ["sm103.cuh", "kernels.h", "tmap.h"]
+HEADERS = ["sm103.cuh", "kernels.h", "tmap.h", "rope.h"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

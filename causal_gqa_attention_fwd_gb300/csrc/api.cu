@@ -9,6 +9,7 @@
 
 #include "gqa_attn.h"
 #include "kernels.h"
+#include "rope.h"
 #include "sm103.cuh"
 #include "tmap.h"
 
@@ -68,13 +69,14 @@ attn_status check_heads(int Hq, int Hkv, int D) {
   return ATTN_OK;
 }
 
-// Dense [N, T, D] bf16 tensor seen as 3-D (D, T, N); box_rows x 64-element boxes.
-bool map_dense(CUtensorMap* m, const void* base, int D, int T, long nheads, int box_rows = 128) {
+// Dense [N, T, D] 16-bit tensor (bf16, or f16 for the rotated copies) seen as
+// 3-D (D, T, N); box_rows x 64-element boxes.
+bool map_dense(CUtensorMap* m, const void* base, int D, int T, long nheads, int box_rows = 128,
+               CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   const uint64_t dims[3] = {(uint64_t)D, (uint64_t)T, (uint64_t)nheads};
   const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)T * D * 2};
   const uint32_t box[3] = {64, (uint32_t)box_rows, 1};
-  return gqa::make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dims, strides, box,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+  return gqa::make_tmap(m, base, dtype, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Packed [total, H, D] bf16 tensor seen as 3-D (D, H, total); boxes of 128 tokens.
@@ -162,7 +164,7 @@ attn_status bwd_common(const void* q, const void* k, const void* v, const void* 
 
 attn_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu,
                        int num_seqs, int T, int total, int max_seqlen, int Hq, int Hkv, int D, int causal,
-                       float scale, void* stream, bool varlen) {
+                       float scale, void* stream, bool varlen, bool f16qk = false) {
   const int rows = varlen ? max_seqlen : T;
   int* status = status_word();
   if (!status) return ATTN_ERR_CUDA;
@@ -192,10 +194,15 @@ attn_status fwd_common(const void* q, const void* k, const void* v, void* o, flo
   if (varlen)
     ok = map_packed(&tq, q, D, Hq, total, 128) && map_packed(&tk, k, D, Hkv, total, 128) &&
          map_packed(&tv, v, D, Hkv, total, 128);
-  else
-    ok = map_dense(&tq, q, D, T, (long)num_seqs * Hq) && map_dense(&tk, k, D, T, (long)num_seqs * Hkv) &&
-         map_dense(&tv, v, D, T, (long)num_seqs * Hkv);
+  else {
+    const CUtensorMapDataType qk_type = f16qk ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    ok = map_dense(&tq, q, D, T, (long)num_seqs * Hq, 128, qk_type) &&
+         map_dense(&tk, k, D, T, (long)num_seqs * Hkv, 128, qk_type) && map_dense(&tv, v, D, T, (long)num_seqs * Hkv);
+  }
   if (!ok) return ATTN_ERR_CUDA;
+  if (f16qk)
+    return launch_status(
+        gqa::launch_attn_fwd_f16qk(tq, tk, tv, a, D, (int)grid, static_cast<cudaStream_t>(stream)));
   return launch_status(gqa::launch_attn_fwd(tq, tk, tv, a, D, (int)grid, static_cast<cudaStream_t>(stream)));
 }
 
@@ -297,6 +304,36 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   if ((long)B * Hq > 0x7fffffffL || !isfinite(scale)) return ATTN_ERR_SHAPE;
   if ((st = check_arch()) != ATTN_OK) return st;
   return fwd_common(q, k, v, o, lse, nullptr, B, T, 0, 0, Hq, Hkv, D, causal, scale, stream, false);
+}
+
+size_t attn_fwd_rope_workspace_size(int B, int Hq, int Hkv, int T, int D) {
+  if (B < 0 || T < 0 || check_heads(Hq, Hkv, D) != ATTN_OK) return 0;
+  return round_up((size_t)B * Hq * T * D * 2, 256) + (size_t)B * Hkv * T * D * 2;
+}
+
+attn_status attn_fwd_rope(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                          size_t workspace_bytes, int B, int Hq, int Hkv, int T, int D, int causal, float scale,
+                          const float* rope_cos_sin, int rope_positions, void* stream) {
+  if (B < 0 || T < 0 || rope_positions < 0) return ATTN_ERR_SHAPE;
+  attn_status st = check_heads(Hq, Hkv, D);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || T == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse || !rope_cos_sin) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(rope_cos_sin))
+    return ATTN_ERR_ALIGN;
+  if ((long)B * Hq > 0x7fffffffL || !isfinite(scale) || rope_positions < T) return ATTN_ERR_SHAPE;
+  const size_t need = attn_fwd_rope_workspace_size(B, Hq, Hkv, T, D);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGN;
+  if ((st = check_arch()) != ATTN_OK) return st;
+  // rotated f16 copies of q and k in the workspace, then the forward on them
+  uint8_t* wq = static_cast<uint8_t*>(workspace);
+  uint8_t* wk = wq + round_up((size_t)B * Hq * T * D * 2, 256);
+  const cudaError_t e = gqa::launch_rope_qk_f16(q, k, wq, wk, (long)B * Hq * T, (long)B * Hkv * T, T, D,
+                                                rope_cos_sin, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  return fwd_common(wq, wk, v, o, lse, nullptr, B, T, 0, 0, Hq, Hkv, D, causal, scale, stream, false, true);
 }
 
 attn_status attn_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse,

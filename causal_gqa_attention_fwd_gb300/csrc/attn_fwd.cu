@@ -21,8 +21,18 @@
 // P (bf16) overwrites the first 64 columns of its S block.
 // Tiles of key blocks past the diagonal are never visited; only the diagonal
 // block and a ragged last block are masked.
+//
+// Rotary prefill (RoPE of MultiHeadAttentionWithRoPE, llm-from-scratch
+// "Project Overview"; positions-aware RoPE of the microLLM-rocm README):
+// rope_qk_f16_kernel rotates Q and K at their positions into f16 copies in
+// one bandwidth-bound pass, and the same kernel (F16QK) takes them as f16
+// operands of the score MMA.  f16 keeps 11 significant bits of the rotated
+// values; rounding them to bf16 would alone put the LSE about 3e-3 off.
+#include <cuda_fp16.h>
+
 #include "sm103.cuh"
 #include "kernels.h"
+#include "rope.h"
 
 namespace gqa {
 
@@ -32,7 +42,7 @@ constexpr int kBM = 128;       // query rows per tile
 constexpr int kBN = 128;       // keys per block
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: lazy O rescale
 
-template <int D>
+template <int D, bool F16QK = false>
 struct FwdCfg {
   static constexpr int kTileBytes = kBM * D * 2;        // one Q / K / V tile
   static constexpr int kBoxes = D / 64;                  // 64-element TMA boxes
@@ -43,7 +53,9 @@ struct FwdCfg {
   static constexpr int kSmemBytes = kSmemQ + kSmemRing + 1024;  // + alignment slack
   __device__ static constexpr uint32_t col_s(int x) { return (uint32_t)x * 128u; }
   __device__ static constexpr uint32_t col_o(int x) { return 256u + (uint32_t)x * D; }
-  static constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false, false);
+  // score MMA: bf16 Q and K, or f16 (rotated copies; A/B format code 0 = f16)
+  static constexpr uint32_t kIdescQK =
+      F16QK ? (idesc_bf16(kBM, kBN, false, false) & ~((7u << 7) | (7u << 10))) : idesc_bf16(kBM, kBN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16(kBM, D, false, true);
 };
 
@@ -68,11 +80,11 @@ struct TileInfo {
 
 }  // namespace
 
-template <int D>
+template <int D, bool F16QK>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, F16QK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                      // 2 tiles
@@ -416,29 +428,94 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <int D>
+template <int D, bool F16QK>
 static cudaError_t launch_fwd_d(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                 const FwdArgs& a, int grid, cudaStream_t stream) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, F16QK>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, F16QK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   prof_begin(kProfFwd, stream);
-  attn_fwd_kernel<D><<<grid, 384, C::kSmemBytes, stream>>>(q, k, v, a);
+  attn_fwd_kernel<D, F16QK><<<grid, 384, C::kSmemBytes, stream>>>(q, k, v, a);
   prof_end(stream);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdArgs& a,
                             int D, int grid, cudaStream_t stream) {
-  if (D == 128) return launch_fwd_d<128>(q, k, v, a, grid, stream);
-  return launch_fwd_d<64>(q, k, v, a, grid, stream);
+  if (D == 128) return launch_fwd_d<128, false>(q, k, v, a, grid, stream);
+  return launch_fwd_d<64, false>(q, k, v, a, grid, stream);
+}
+
+cudaError_t launch_attn_fwd_f16qk(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                  const FwdArgs& a, int D, int grid, cudaStream_t stream) {
+  if (D == 128) return launch_fwd_d<128, true>(q, k, v, a, grid, stream);
+  return launch_fwd_d<64, true>(q, k, v, a, grid, stream);
+}
+
+namespace {
+
+// Eight rotated pairs per thread: features i0..i0+7 of the low half with
+// i0+D/2.. of the high half; D/16 threads per row, rows of q then of k.
+template <int D>
+__global__ void __launch_bounds__(256) rope_qk_f16_kernel(const __nv_bfloat16* __restrict__ q,
+                                                          const __nv_bfloat16* __restrict__ k, __half* __restrict__ qo,
+                                                          __half* __restrict__ ko, long rows_q, long rows_k, int T,
+                                                          const float* __restrict__ cos_sin) {
+  constexpr int H = D / 2, kPer = 8, kThr = H / kPer;
+  const long gid = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long row = gid / kThr;
+  if (row >= rows_q + rows_k) return;
+  const int i0 = (int)(gid % kThr) * kPer;
+  const bool is_q = row < rows_q;
+  const long r = is_q ? row : row - rows_q;
+  const __nv_bfloat16* x = (is_q ? q : k) + r * D;
+  __half* y = (is_q ? qo : ko) + r * D;
+  const float* cs = cos_sin + (r % T) * D;
+  const uint4 lo = *reinterpret_cast<const uint4*>(x + i0), hi = *reinterpret_cast<const uint4*>(x + H + i0);
+  const float4 c0 = *reinterpret_cast<const float4*>(cs + i0), c1 = *reinterpret_cast<const float4*>(cs + i0 + 4);
+  const float4 s0 = *reinterpret_cast<const float4*>(cs + H + i0);
+  const float4 s1 = *reinterpret_cast<const float4*>(cs + H + i0 + 4);
+  const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  const uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w}, wh[4] = {hi.x, hi.y, hi.z, hi.w};
+  uint32_t ol[4], oh[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wl[e]));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wh[e]));
+    const __half2 yl = __floats2half2_rn(fmaf(a.x, c[2 * e], -b.x * sn[2 * e]), fmaf(a.y, c[2 * e + 1], -b.y * sn[2 * e + 1]));
+    const __half2 yh = __floats2half2_rn(fmaf(b.x, c[2 * e], a.x * sn[2 * e]), fmaf(b.y, c[2 * e + 1], a.y * sn[2 * e + 1]));
+    ol[e] = *reinterpret_cast<const uint32_t*>(&yl);
+    oh[e] = *reinterpret_cast<const uint32_t*>(&yh);
+  }
+  *reinterpret_cast<uint4*>(y + i0) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+  *reinterpret_cast<uint4*>(y + H + i0) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+}
+
+}  // namespace
+
+cudaError_t launch_rope_qk_f16(const void* q, const void* k, void* q_out, void* k_out, long rows_q, long rows_k,
+                               int T, int D, const float* cos_sin, cudaStream_t stream) {
+  const long threads = (rows_q + rows_k) * (D / 16);
+  const long blocks = (threads + 255) / 256;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
+  auto qi = static_cast<const __nv_bfloat16*>(q);
+  auto ki = static_cast<const __nv_bfloat16*>(k);
+  auto qo = static_cast<__half*>(q_out);
+  auto ko = static_cast<__half*>(k_out);
+  if (D == 128)
+    rope_qk_f16_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(qi, ki, qo, ko, rows_q, rows_k, T, cos_sin);
+  else
+    rope_qk_f16_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(qi, ki, qo, ko, rows_q, rows_k, T, cos_sin);
+  return cudaGetLastError();
 }
 
 }  // namespace gqa

@@ -122,6 +122,26 @@ GQA_ATTN_API attn_status attn_varlen_fwd(const void* q, const void* k, const voi
 
 GQA_ATTN_API size_t attn_varlen_bwd_workspace_size(int num_seqs, int total_tokens, int Hq, int Hkv, int D);
 
+/* Forward with rotary queries and keys (RoPE of MultiHeadAttentionWithRoPE,
+ * llm-from-scratch "Project Overview"; positions-aware RoPE of the
+ * microLLM-rocm README, section "Why this project exists"): the dense layout
+ * of attn_fwd; q and k of every row are rotated at their positions
+ * 0..T-1 before the attention, with the rotary table of attn_decode_fwd
+ * (rope_cos_sin: DEVICE float32 [rope_positions, D], 16-byte aligned,
+ * rope_positions >= T; row p holds cos(p*theta_i) for i < D/2, then
+ * sin(p*theta_i); feature i pairs with feature i + D/2).  The rotated q and
+ * k are written as f16 (11 significant bits; |rotated value| < 65504) into
+ * the workspace and the score MMA takes them as f16; P V and everything
+ * else is as attn_fwd.
+ * workspace: DEVICE, 256-byte aligned, >= attn_fwd_rope_workspace_size()
+ * bytes (the two rotated copies), no initialisation; errors as attn_fwd,
+ * plus ATTN_ERR_WORKSPACE. */
+GQA_ATTN_API size_t attn_fwd_rope_workspace_size(int B, int Hq, int Hkv, int T, int D);
+GQA_ATTN_API attn_status attn_fwd_rope(const void* q, const void* k, const void* v, void* o, float* lse,
+                                       void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int T,
+                                       int D, int causal, float scale, const float* rope_cos_sin,
+                                       int rope_positions, void* stream);
+
 /* Backward, packed variable-length layout (arguments as attn_bwd plus the
  * sequence description of attn_varlen_fwd). */
 GQA_ATTN_API attn_status attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

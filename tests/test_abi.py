@@ -227,3 +227,26 @@ def test_decode_fp8_validation(lib):
     g = lambda **kw: lib.attn_decode_paged_fp8_fwd(A, A, A, 0.01, 0.01, A, A, A, A, A, 1 << 40, 1, 4, 2, 1,
                                                    kw.get("psz", 64), 8, 8, 64, 0.125, None, 0, None)
     assert g(psz=40) == 2
+
+
+def test_fwd_rope_validation(lib):
+    """Rotary forward: the table and the workspace are checked before any
+    launch (and before the architecture check)."""
+    def f(ptrs=(A, A, A, A, A), ws=A, ws_bytes=1 << 40, tab=A, npos=4096, T=1000, D=128, Hq=4, Hkv=2):
+        return lib.attn_fwd_rope(*ptrs, ws, ws_bytes, 2, Hq, Hkv, T, D, 1, 0.1, tab, npos, None)
+    assert f(D=96) == 3
+    assert f(Hq=3) == 2
+    assert f(tab=NULL) == 1
+    assert f(tab=A + 4) == 4
+    assert f(npos=999) == 2                              # table shorter than T
+    assert f(ws=NULL) == 6
+    assert f(ws_bytes=lib.attn_fwd_rope_workspace_size(2, 4, 2, 1000, 128) - 1) == 6
+    assert f(ws=A + 16) == 4                             # workspace needs 256-byte alignment
+    assert f(ptrs=(NULL,) * 5, T=0, tab=NULL, ws=NULL) == 0    # empty: no-op
+
+
+def test_fwd_rope_workspace_size(lib):
+    # rotated f16 q (256-byte aligned section) then rotated f16 k
+    assert lib.attn_fwd_rope_workspace_size(2, 4, 2, 1000, 128) == 2 * 4 * 1000 * 128 * 2 + 2 * 2 * 1000 * 128 * 2
+    assert lib.attn_fwd_rope_workspace_size(1, 1, 1, 3, 64) == 512 + 3 * 64 * 2
+    assert lib.attn_fwd_rope_workspace_size(1, 4, 2, 100, 96) == 0
