@@ -5,6 +5,7 @@ PyTorch CUDA tensors (PyTorch supplies device memory and the stream):
 
     attn_fwd(q, k, v, causal=True, scale=None) -> (o, lse)
     attn_fwd_rope(q, k, v, rope_cos_sin, causal=True, scale=None) -> (o, lse), q and k rotated
+    attn_varlen_fwd_rope(q, k, v, cu_seqlens, max_seqlen, rope_cos_sin, ...) -> (o, lse)
     attn_bwd(q, k, v, o, lse, dout, causal=True, scale=None) -> (dq, dk, dv)
     attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen, ...) -> (o, lse)
     attn_varlen_bwd(q, k, v, o, lse, dout, cu_seqlens, max_seqlen, ...) -> (dq, dk, dv)
@@ -29,6 +30,7 @@ from ._binding import (  # noqa: F401
     attn_fwd,
     attn_fwd_rope,
     attn_fwd_rope_workspace_size,
+    attn_varlen_fwd_rope,
     attn_varlen_bwd,
     attn_varlen_bwd_workspace_size,
     attn_varlen_fwd,

@@ -27,6 +27,8 @@ SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_fwd_rope_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "attn_fwd_rope": (_I, [_P, _P, _P, _P, _P, _P, _Z, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P]),
+    "attn_varlen_fwd_rope_workspace_size": (_Z, [_I, _I, _I, _I]),
+    "attn_varlen_fwd_rope": (_I, [_P] * 6 + [_I] * 7 + [_F, _P, _I, _P, _Z, _P]),
     "attn_bwd_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "attn_bwd": (_I, [_P] * 10 + [_Z, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_varlen_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
@@ -175,6 +177,30 @@ def attn_fwd_rope(q, k, v, rope_cos_sin, causal: bool = True, scale=None, o=None
                              workspace.numel(), B, Hq, Hkv, T, D, int(causal), _scale(scale, D), rope_ptr, rope_n,
                              _stream(stream))
     _check(st, "attn_fwd_rope")
+    return o, lse
+
+
+def attn_varlen_fwd_rope(q, k, v, cu_seqlens, max_seqlen, rope_cos_sin, causal: bool = True, scale=None, o=None,
+                         lse=None, workspace=None, stream=None):
+    """Packed variable-length forward with q and k rotated at their offsets in their sequences
+    (positions 0..len-1; rotary table as attn_fwd_rope) -> (o, lse [Hq,total])."""
+    total, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (total, Hkv, D) or v.shape != k.shape:
+        raise ValueError("k, v must be [total, Hkv, D] matching q")
+    num_seqs = cu_seqlens.numel() - 1
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((Hq, total), dtype=torch.float32, device=q.device) if lse is None else lse
+    if workspace is None:
+        workspace = torch.empty(max(int(lib().attn_varlen_fwd_rope_workspace_size(total, Hq, Hkv, D)), 256),
+                                dtype=torch.uint8, device=q.device)
+    rope_ptr, rope_n = _rope(rope_cos_sin)
+    st = lib().attn_varlen_fwd_rope(_need(q, "q"), _need(k, "k"), _need(v, "v"), _need(o, "o"),
+                                    _need(lse, "lse", torch.float32), _need(cu_seqlens, "cu_seqlens", torch.int32),
+                                    num_seqs, total, int(max_seqlen), Hq, Hkv, D, int(causal), _scale(scale, D),
+                                    rope_ptr, rope_n, _need(workspace, "workspace", torch.uint8), workspace.numel(),
+                                    _stream(stream))
+    _check(st, "attn_varlen_fwd_rope")
     return o, lse
 
 

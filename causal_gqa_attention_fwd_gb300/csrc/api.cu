@@ -79,13 +79,14 @@ bool map_dense(CUtensorMap* m, const void* base, int D, int T, long nheads, int 
   return gqa::make_tmap(m, base, dtype, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Packed [total, H, D] bf16 tensor seen as 3-D (D, H, total); boxes of 128 tokens.
-bool map_packed(CUtensorMap* m, const void* base, int D, int H, int total, int box_rows) {
+// Packed [total, H, D] 16-bit tensor (bf16, or f16 for the rotated copies)
+// seen as 3-D (D, H, total); boxes of 128 tokens.
+bool map_packed(CUtensorMap* m, const void* base, int D, int H, int total, int box_rows,
+                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   const uint64_t dims[3] = {(uint64_t)D, (uint64_t)H, (uint64_t)total};
   const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)H * D * 2};
   const uint32_t box[3] = {64, 1, (uint32_t)box_rows};
-  return gqa::make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dims, strides, box,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+  return gqa::make_tmap(m, base, dtype, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 attn_status launch_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
@@ -191,11 +192,11 @@ attn_status fwd_common(const void* q, const void* k, const void* v, void* o, flo
   if (grid > 0x7fffffffL) return ATTN_ERR_SHAPE;
   CUtensorMap tq, tk, tv;
   bool ok;
+  const CUtensorMapDataType qk_type = f16qk ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (varlen)
-    ok = map_packed(&tq, q, D, Hq, total, 128) && map_packed(&tk, k, D, Hkv, total, 128) &&
+    ok = map_packed(&tq, q, D, Hq, total, 128, qk_type) && map_packed(&tk, k, D, Hkv, total, 128, qk_type) &&
          map_packed(&tv, v, D, Hkv, total, 128);
   else {
-    const CUtensorMapDataType qk_type = f16qk ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     ok = map_dense(&tq, q, D, T, (long)num_seqs * Hq, 128, qk_type) &&
          map_dense(&tk, k, D, T, (long)num_seqs * Hkv, 128, qk_type) && map_dense(&tv, v, D, T, (long)num_seqs * Hkv);
   }
@@ -328,12 +329,62 @@ attn_status attn_fwd_rope(const void* q, const void* k, const void* v, void* o, 
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGN;
   if ((st = check_arch()) != ATTN_OK) return st;
   // rotated f16 copies of q and k in the workspace, then the forward on them
+  int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
   uint8_t* wq = static_cast<uint8_t*>(workspace);
   uint8_t* wk = wq + round_up((size_t)B * Hq * T * D * 2, 256);
-  const cudaError_t e = gqa::launch_rope_qk_f16(q, k, wq, wk, (long)B * Hq * T, (long)B * Hkv * T, T, D,
-                                                rope_cos_sin, static_cast<cudaStream_t>(stream));
+  gqa::RopeRows rr{};
+  rr.rows_q = (long)B * Hq * T;
+  rr.rows_k = (long)B * Hkv * T;
+  rr.T = T;
+  rr.n_table = rope_positions;
+  rr.status = status;
+  const cudaError_t e =
+      gqa::launch_rope_qk_f16(q, k, wq, wk, rr, D, rope_cos_sin, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return fwd_common(wq, wk, v, o, lse, nullptr, B, T, 0, 0, Hq, Hkv, D, causal, scale, stream, false, true);
+}
+
+size_t attn_varlen_fwd_rope_workspace_size(int total_tokens, int Hq, int Hkv, int D) {
+  if (total_tokens < 0 || check_heads(Hq, Hkv, D) != ATTN_OK) return 0;
+  return round_up((size_t)total_tokens * Hq * D * 2, 256) + (size_t)total_tokens * Hkv * D * 2;
+}
+
+attn_status attn_varlen_fwd_rope(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 const int* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen, int Hq,
+                                 int Hkv, int D, int causal, float scale, const float* rope_cos_sin,
+                                 int rope_positions, void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || rope_positions < 0) return ATTN_ERR_SHAPE;
+  attn_status st = check_heads(Hq, Hkv, D);
+  if (st != ATTN_OK) return st;
+  if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return ATTN_OK;
+  if (max_seqlen > total_tokens || !isfinite(scale) || rope_positions < max_seqlen) return ATTN_ERR_SHAPE;
+  if (!q || !k || !v || !o || !lse || !cu_seqlens || !rope_cos_sin) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(rope_cos_sin))
+    return ATTN_ERR_ALIGN;
+  const size_t need = attn_varlen_fwd_rope_workspace_size(total_tokens, Hq, Hkv, D);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGN;
+  if ((st = check_arch()) != ATTN_OK) return st;
+  int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
+  uint8_t* wq = static_cast<uint8_t*>(workspace);
+  uint8_t* wk = wq + round_up((size_t)total_tokens * Hq * D * 2, 256);
+  gqa::RopeRows rr{};
+  rr.rows_q = (long)total_tokens * Hq;
+  rr.rows_k = (long)total_tokens * Hkv;
+  rr.Hq = Hq;
+  rr.Hkv = Hkv;
+  rr.cu = cu_seqlens;
+  rr.num_seqs = num_seqs;
+  rr.n_table = rope_positions;
+  rr.status = status;
+  const cudaError_t e =
+      gqa::launch_rope_qk_f16(q, k, wq, wk, rr, D, rope_cos_sin, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  return fwd_common(wq, wk, v, o, lse, cu_seqlens, num_seqs, 0, total_tokens, max_seqlen, Hq, Hkv, D, causal,
+                    scale, stream, true, true);
 }
 
 attn_status attn_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse,

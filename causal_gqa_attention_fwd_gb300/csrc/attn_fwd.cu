@@ -463,21 +463,51 @@ namespace {
 
 // Eight rotated pairs per thread: features i0..i0+7 of the low half with
 // i0+D/2.. of the high half; D/16 threads per row, rows of q then of k.
-template <int D>
+// Dense rows ([N, T, D]) are at position row % T.  Packed rows
+// ([total, H, D]: token row / H) are at the token's offset in its sequence,
+// found by a binary search of cu_seqlens; tokens in no sequence get zero
+// rows; a position outside the table (a malformed cu_seqlens) is reported
+// as ATTN_ERR_SEQLENS and the row written as zeros, the table never read
+// out of bounds.
+template <int D, bool PACKED>
 __global__ void __launch_bounds__(256) rope_qk_f16_kernel(const __nv_bfloat16* __restrict__ q,
                                                           const __nv_bfloat16* __restrict__ k, __half* __restrict__ qo,
-                                                          __half* __restrict__ ko, long rows_q, long rows_k, int T,
+                                                          __half* __restrict__ ko, RopeRows rr,
                                                           const float* __restrict__ cos_sin) {
   constexpr int H = D / 2, kPer = 8, kThr = H / kPer;
   const long gid = (long)blockIdx.x * blockDim.x + threadIdx.x;
   const long row = gid / kThr;
-  if (row >= rows_q + rows_k) return;
+  if (row >= rr.rows_q + rr.rows_k) return;
   const int i0 = (int)(gid % kThr) * kPer;
-  const bool is_q = row < rows_q;
-  const long r = is_q ? row : row - rows_q;
+  const bool is_q = row < rr.rows_q;
+  const long r = is_q ? row : row - rr.rows_q;
   const __nv_bfloat16* x = (is_q ? q : k) + r * D;
   __half* y = (is_q ? qo : ko) + r * D;
-  const float* cs = cos_sin + (r % T) * D;
+  long pos;
+  if constexpr (PACKED) {
+    const long tok = r / (is_q ? rr.Hq : rr.Hkv);
+    if (tok < rr.cu[0] || tok >= rr.cu[rr.num_seqs]) {  // in no sequence: never read by the attention
+      *reinterpret_cast<uint4*>(y + i0) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(y + H + i0) = make_uint4(0, 0, 0, 0);
+      return;
+    }
+    int lo = 0, hi = rr.num_seqs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (rr.cu[mid] <= tok) lo = mid;
+      else hi = mid - 1;
+    }
+    pos = tok - rr.cu[lo];
+  } else {
+    pos = r % rr.T;
+  }
+  if (pos < 0 || pos >= rr.n_table) {
+    if (i0 == 0) atomicCAS(rr.status, 0, kDevBadSeqlens);
+    *reinterpret_cast<uint4*>(y + i0) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(y + H + i0) = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const float* cs = cos_sin + pos * D;
   const uint4 lo = *reinterpret_cast<const uint4*>(x + i0), hi = *reinterpret_cast<const uint4*>(x + H + i0);
   const float4 c0 = *reinterpret_cast<const float4*>(cs + i0), c1 = *reinterpret_cast<const float4*>(cs + i0 + 4);
   const float4 s0 = *reinterpret_cast<const float4*>(cs + H + i0);
@@ -501,9 +531,9 @@ __global__ void __launch_bounds__(256) rope_qk_f16_kernel(const __nv_bfloat16* _
 
 }  // namespace
 
-cudaError_t launch_rope_qk_f16(const void* q, const void* k, void* q_out, void* k_out, long rows_q, long rows_k,
-                               int T, int D, const float* cos_sin, cudaStream_t stream) {
-  const long threads = (rows_q + rows_k) * (D / 16);
+cudaError_t launch_rope_qk_f16(const void* q, const void* k, void* q_out, void* k_out, const RopeRows& rr, int D,
+                               const float* cos_sin, cudaStream_t stream) {
+  const long threads = (rr.rows_q + rr.rows_k) * (D / 16);
   const long blocks = (threads + 255) / 256;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
@@ -511,10 +541,15 @@ cudaError_t launch_rope_qk_f16(const void* q, const void* k, void* q_out, void* 
   auto ki = static_cast<const __nv_bfloat16*>(k);
   auto qo = static_cast<__half*>(q_out);
   auto ko = static_cast<__half*>(k_out);
-  if (D == 128)
-    rope_qk_f16_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(qi, ki, qo, ko, rows_q, rows_k, T, cos_sin);
-  else
-    rope_qk_f16_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(qi, ki, qo, ko, rows_q, rows_k, T, cos_sin);
+  const unsigned g = (unsigned)blocks;
+  const bool packed = rr.cu != nullptr;
+  if (D == 128) {
+    if (packed) rope_qk_f16_kernel<128, true><<<g, 256, 0, stream>>>(qi, ki, qo, ko, rr, cos_sin);
+    else rope_qk_f16_kernel<128, false><<<g, 256, 0, stream>>>(qi, ki, qo, ko, rr, cos_sin);
+  } else {
+    if (packed) rope_qk_f16_kernel<64, true><<<g, 256, 0, stream>>>(qi, ki, qo, ko, rr, cos_sin);
+    else rope_qk_f16_kernel<64, false><<<g, 256, 0, stream>>>(qi, ki, qo, ko, rr, cos_sin);
+  }
   return cudaGetLastError();
 }
 

@@ -142,6 +142,20 @@ GQA_ATTN_API attn_status attn_fwd_rope(const void* q, const void* k, const void*
                                        int D, int causal, float scale, const float* rope_cos_sin,
                                        int rope_positions, void* stream);
 
+/* attn_fwd_rope for the packed variable-length layout of attn_varlen_fwd:
+ * every sequence's tokens are at positions 0..len-1 (the offset from
+ * cu_seqlens[s]); rope_positions >= max_seqlen.  A cu_seqlens whose
+ * positions fall outside the table is reported through the device status
+ * word (ATTN_ERR_SEQLENS), as attn_varlen_fwd reports it.
+ * workspace: DEVICE, 256-byte aligned, >= attn_varlen_fwd_rope_workspace_size()
+ * bytes. */
+GQA_ATTN_API size_t attn_varlen_fwd_rope_workspace_size(int total_tokens, int Hq, int Hkv, int D);
+GQA_ATTN_API attn_status attn_varlen_fwd_rope(const void* q, const void* k, const void* v, void* o, float* lse,
+                                              const int* cu_seqlens, int num_seqs, int total_tokens,
+                                              int max_seqlen, int Hq, int Hkv, int D, int causal, float scale,
+                                              const float* rope_cos_sin, int rope_positions, void* workspace,
+                                              size_t workspace_bytes, void* stream);
+
 /* Backward, packed variable-length layout (arguments as attn_bwd plus the
  * sequence description of attn_varlen_fwd). */
 GQA_ATTN_API attn_status attn_varlen_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

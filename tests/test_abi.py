@@ -250,3 +250,16 @@ def test_fwd_rope_workspace_size(lib):
     assert lib.attn_fwd_rope_workspace_size(2, 4, 2, 1000, 128) == 2 * 4 * 1000 * 128 * 2 + 2 * 2 * 1000 * 128 * 2
     assert lib.attn_fwd_rope_workspace_size(1, 1, 1, 3, 64) == 512 + 3 * 64 * 2
     assert lib.attn_fwd_rope_workspace_size(1, 4, 2, 100, 96) == 0
+
+
+def test_varlen_fwd_rope_validation(lib):
+    def f(ptrs=(A,) * 6, n=2, total=10, maxlen=6, tab=A, npos=6, ws=A, ws_bytes=1 << 40, D=128):
+        return lib.attn_varlen_fwd_rope(*ptrs, n, total, maxlen, 4, 2, D, 1, 0.1, tab, npos, ws, ws_bytes, None)
+    assert f(D=96) == 3
+    assert f(tab=NULL) == 1
+    assert f(npos=5) == 2                                # table shorter than max_seqlen
+    assert f(maxlen=11) == 2                             # max_seqlen > total
+    assert f(ws=NULL) == 6
+    assert f(ws=A + 32) == 4
+    assert f(ptrs=(NULL,) * 6, n=0, tab=NULL, ws=NULL) == 0
+    assert lib.attn_varlen_fwd_rope_workspace_size(10, 4, 2, 128) == 10 * 4 * 128 * 2 + 10 * 2 * 128 * 2

@@ -66,3 +66,38 @@ def test_fwd_rope_at_position_zero_is_the_plain_forward(gq):
     # only the MMA's operand format differs
     assert float((o.float() - o2.float()).abs().max()) <= 2.0 ** -7 * float(o2.float().abs().max())
     assert float((lse - lse2).abs().max()) <= 1e-5
+
+
+VARLEN_CASES = [
+    # lengths, Hq, Hkv, D
+    ([1, 300, 129, 64], 4, 2, 128),
+    ([700, 5, 256], 8, 1, 64),
+    ([2048, 17], 6, 2, 128),
+]
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv,D", VARLEN_CASES)
+def test_varlen_fwd_rope_matches_oracle(gq, lens, Hq, Hkv, D):
+    """Packed batch: each sequence's tokens at positions 0..len-1."""
+    x = W.varlen_inputs(lens, Hq, Hkv, D, seed=sum(lens) + 3)
+    cu = x["cu_seqlens"]
+    tab = W.rope_cos_sin_table(max(lens), D)
+    scale = 1.0 / np.sqrt(D)
+    o, lse = gq.attn_varlen_fwd_rope(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), cu.cuda(), x["max_seqlen"],
+                                     tab.cuda(), scale=scale)
+    assert gq.get_device_status() == 0
+    ro, rl = oracle.rope_varlen_fwd(to64(x["q"]), to64(x["k"]), to64(x["v"]), cu.numpy(), tab.double().numpy(),
+                                    scale=scale)
+    check("o", o, ro, TOL_REL_O)
+    check_lse(lse, rl)
+
+
+def test_varlen_fwd_rope_reports_positions_past_the_table(gq):
+    """A sequence longer than max_seqlen (malformed cu_seqlens) would need
+    table rows past rope_positions: reported, nothing read out of bounds."""
+    x = W.varlen_inputs([10, 40], 4, 2, 64, seed=9)
+    cu = x["cu_seqlens"]
+    tab = W.rope_cos_sin_table(16, 64)       # rows for positions 0..15 only
+    gq.attn_varlen_fwd_rope(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), cu.cuda(), 16, tab.cuda(), scale=0.1)
+    assert gq.get_device_status() == 5
+    assert gq.get_device_status() == 0
