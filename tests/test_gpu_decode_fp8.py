@@ -42,6 +42,7 @@ CASES = [
     (2, 16, 2, 4, 640, 128, [640, 385]),
     (2, 4, 4, 1, 300, 64, [300, 129]),
     (4, 32, 8, 1, 4096, 128, None),
+    (8, 32, 8, 1, 16384, 64, None),     # D = 64 with dozens of chunks per CTA: its rings wrap
 ]
 
 
