@@ -10,6 +10,12 @@ with CUDA events on the launching stream.  FLOPs follow the causal convention
 (half of dense): forward 4*D and backward 10*D per visible (query, key) pair,
 i.e. 2*B*Hq*T^2*D and 5*B*Hq*T^2*D.
 
+Before the timed steps, one forward + backward is compared with the fp64
+oracle (the whole workload, or one sampled (batch, kv-head) group of the
+long-context layer) and the figures go into the line's "parity" object.
+Per-kernel times come from a second pass of as many steps with CUDA events
+around every kernel, so the timed steps carry none.
+
 Prints one JSON line.  --impl reference times the fp64 CPU oracle (the only
 reference this method has) on a bounded sample of the same workload.
 
@@ -201,6 +207,66 @@ def oracle_sample(w: W.Workload, x, budget_s: float, t_prefix: int | None = None
     desc = (f"{groups} of {total_groups} (batch, kv-head) groups of {w.name}, {where} "
             f"(G={G} query heads each), forward + backward in fp64, {elapsed:.1f} s")
     return done_flops / elapsed, desc, cores, elapsed
+
+
+# ------------------------------------------------------------- parity leg
+def parity_leg(w: W.Workload, x, out: dict):
+    """Compare one forward + backward of the GPU path with the fp64 oracle,
+    outside the timed region: the whole workload, or for the long-context
+    layer one sampled (batch, kv-head) group (every row of its G query heads
+    and of its K/V head).  Returns every figure of ``oracle.parity`` per
+    output and which elementwise bound it meets."""
+    import numpy as np
+
+    import oracle
+    from oracle import parity as P
+    oracle.build()
+    oracle.set_threads(len(os.sched_getaffinity(0)))
+    f = lambda t: t.detach().float().cpu().numpy().astype(np.float64)
+    t0 = time.perf_counter()
+    G = w.Hq // w.Hkv
+    if w.varlen:
+        # the shortest and the longest packed sequence (sequences are independent)
+        cu = x["cu_seqlens"].tolist()
+        lens = [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+        pick = sorted({min(range(len(lens)), key=lambda i: lens[i]), max(range(len(lens)), key=lambda i: lens[i])})
+        rows = torch.cat([torch.arange(cu[i], cu[i + 1]) for i in pick])
+        sub_cu = np.cumsum([0] + [lens[i] for i in pick]).astype(np.int32)
+        ref = oracle.varlen_bwd(f(x["q"][rows]), f(x["k"][rows]), f(x["v"][rows]), f(x["do"][rows]), sub_cu,
+                                causal=w.causal, scale=w.softmax_scale, err_terms=True)
+        got = {n: f(out[n].cpu()[rows]) for n in ("o", "dq", "dk", "dv")}
+        got["lse"] = f(out["lse"].cpu()[:, rows])
+        sample = (f"packed sequences {pick} of {len(lens)} (lengths {[lens[i] for i in pick]}: the shortest and "
+                  f"the longest), every head, forward and backward")
+    elif w.B * w.T > 4096:
+        b, g = 1, min(5, w.Hkv - 1)
+        hs = slice(g * G, (g + 1) * G)
+        ref = oracle.bwd(f(x["q"][b:b + 1, hs]), f(x["k"][b:b + 1, g:g + 1]), f(x["v"][b:b + 1, g:g + 1]),
+                         f(x["do"][b:b + 1, hs]), causal=w.causal, scale=w.softmax_scale, err_terms=True)
+        got = {n: f(out[n][b:b + 1, hs]) for n in ("o", "lse", "dq")}
+        got.update({n: f(out[n][b:b + 1, g:g + 1]) for n in ("dk", "dv")})
+        sample = f"(batch {b}, kv-head {g}) group: {G} query heads x {w.T} rows, forward and backward"
+    else:
+        ref = oracle.bwd(f(x["q"]), f(x["k"]), f(x["v"]), f(x["do"]), causal=w.causal, scale=w.softmax_scale,
+                         err_terms=True)
+        got = {n: f(out[n]) for n in ("o", "lse", "dq", "dk", "dv")}
+        sample = "whole workload"
+    res = {"o": P.compare("o", got["o"], ref["o"], P.TOL_REL_O)}
+    for n in ("dq", "dk", "dv"):
+        res[n] = P.compare(n, got[n], ref[n], P.TOL_REL_GRAD, ref["e" + n])
+    lse = P.compare_lse(got["lse"], ref["lse"])
+    keep = ("rel_fro", "rel_tol", "max_abs", "flat_excess", "ulp_excess", "widened_excess", "max_ref", "meets")
+    outputs = {n: {k: r[k] for k in keep} for n, r in res.items()}
+    outputs["lse"] = {"max_abs": lse["max_abs"], "tol": lse["tol"]}
+    return {"against": "fp64 CPU oracle", "sample": sample,
+            "tolerances": {"rel_fro_o": P.TOL_REL_O, "rel_fro_grad": P.TOL_REL_GRAD, "abs_flat": P.TOL_ABS,
+                           "lse_abs": P.TOL_LSE,
+                           "abs_widened": "2e-2 + bf16 half-ulp of ref (+ 3 * 2^-8 * e for dq/dk/dv)"},
+            "outputs": outputs,
+            "pass": all(r["ok"] for r in res.values()) and lse["ok"],
+            "flat_pass": all(r["meets"] == "flat" for r in res.values()) and lse["ok"],
+            "half_ulp_pass": all(r["meets"] in ("flat", "half-ulp") for r in res.values()) and lse["ok"],
+            "seconds": time.perf_counter() - t0}
 
 
 # ---------------------------------------------------------------- decode
@@ -512,6 +578,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-parity", action="store_true", help="skip the oracle comparison before the timed steps")
     ap.add_argument("--no-graph", action="store_true", help="decode workloads: time eager calls, not graph replays")
     ap.add_argument("--flush", default="read", choices=["read", "write", "none"],
                     help="L2 eviction between timed steps (see L2Flush)")
@@ -569,11 +636,13 @@ def main():
     torch.cuda.synchronize()
     assert gq.get_device_status() == 0, "device status after warm-up"
 
+    parity = None
+    if rank == 0 and not args.no_parity:
+        parity = parity_leg(w, x, dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv))
+
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    gq.profile_reset()
-    gq.profile_enable(True)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
@@ -588,6 +657,14 @@ def main():
     barrier(world)
     wall = time.perf_counter() - t_wall
     clocks.mark(1)
+    # per-kernel events in a second pass of as many steps, so the timed
+    # steps above carry no event records between their kernels
+    gq.profile_reset()
+    gq.profile_enable(True)
+    for i in range(args.steps):
+        flush(i)
+        step()
+    torch.cuda.synchronize()
     gq.profile_enable(False)
     prof = gq.profile_read()
     clk = clocks.stop()
@@ -671,6 +748,8 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": gpu_launches,
+            "kernel_ms_pass": "second pass, same steps, events per kernel (launches counted there)",
+            "parity": parity,
             "clocks": clk,
             "device_status": status,
             "wall_s_timed_region": wall,

@@ -104,8 +104,12 @@ GQA_ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, c
  * capture.  All calls share the one array and the kernels re-initialise
  * everything they read from it, but calls whose work overlaps on the GPU
  * (other streams, other host threads) race on it: serialise them.
+ * The looked-up address (like the device status word's) stays cached for the
+ * life of the process: after cudaDeviceReset() or anything else that
+ * destroys the device's primary context, do not call this library on that
+ * device again in the same process.
  * Otherwise identical to attn_bwd (same arguments minus the workspace, same
- * results). */
+ * results: dK and dV bit for bit; dQ to f32 addition order). */
 GQA_ATTN_API attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
                                           int B, int Hq, int Hkv, int T, int D, int causal, float scale,

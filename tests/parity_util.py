@@ -1,52 +1,36 @@
 """Comparison helpers for GPU-vs-oracle parity tests.
 
-Tolerances (bf16 inputs, f32 accumulation): relative Frobenius error of O
-<= 5e-3 and of dQ/dK/dV <= 1e-2, elementwise absolute error <= 2e-2, LSE
-absolute error <= 1e-3.  The outputs are stored in bf16, whose rounding alone
-moves a value by up to half a unit in the last place (2^-9 relative: 0.0156
-at |x| = 4..8, 0.031 at 8..16), so the elementwise bound is 2e-2 plus the
-bf16 half-ulp of the reference value.  For the gradients the bound also adds
-3 * u * e (u = 2^-8; e = the oracle's root-sum-square rounding-error scale of
-an output computed from bf16 P, stored-O and dS operands): with large logits
-the dS operand's own rounding reaches ~0.06 on dK elements of magnitude 1..6,
-which no bf16-operand evaluation of the method avoids.  The flat excess is
-still reported.
+The tolerances and both elementwise figures (flat 2e-2, and the widened bound
+that adds the bf16 half-ulp of the reference and, for gradients, 3 u e) are
+defined in ``oracle/parity.py``.  ``check`` asserts the relative Frobenius
+bound and the widened elementwise bound, and records every figure -- the flat
+excess included -- in the JSON-lines file named by GQA_PARITY_RECORD, keyed by
+the running test, so a run leaves a record of which bound each output meets.
 """
+import os
+
 import numpy as np
 import torch
 
-TOL_REL_O = 5e-3
-TOL_REL_GRAD = 1e-2
-TOL_ABS = 2e-2
-TOL_LSE = 1e-3
+from oracle import parity as P
+
+TOL_REL_O = P.TOL_REL_O
+TOL_REL_GRAD = P.TOL_REL_GRAD
+TOL_ABS = P.TOL_ABS
+TOL_LSE = P.TOL_LSE
+rel_fro = P.rel_fro
+bf16_half_ulp = P.bf16_half_ulp
 
 
-def rel_fro(x, ref):
-    x = np.asarray(x, dtype=np.float64)
-    ref = np.asarray(ref, dtype=np.float64)
-    den = np.linalg.norm(ref)
-    return float(np.linalg.norm(x - ref) / (den if den > 0 else 1.0))
-
-
-def bf16_half_ulp(ref):
-    """Half a bf16 unit in the last place at |ref| (8 significant bits)."""
-    a = np.abs(np.asarray(ref, dtype=np.float64))
-    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    return np.where(a > 0, np.exp2(e - 8.0), 0.0)
-
-
-U_BF16 = 2.0 ** -8
-LAMBDA = 3.0
+def _case():
+    return os.environ.get("PYTEST_CURRENT_TEST", "?").split(" (")[0]
 
 
 def abs_excess(x, ref, err=None):
-    """max(|x - ref| - (2e-2 + bf16 half-ulp of ref [+ u * err])); <= 0 passes."""
+    """max(|x - ref| - (2e-2 + bf16 half-ulp of ref [+ 3 u err])); <= 0 passes."""
     x = np.asarray(x, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
-    bound = TOL_ABS + bf16_half_ulp(ref)
-    if err is not None:
-        bound = bound + LAMBDA * U_BF16 * np.asarray(err, dtype=np.float64)
-    return float((np.abs(x - ref) - bound).max()) if x.size else -1.0
+    return float((np.abs(x - ref) - P.rounding_bound(ref, err)).max()) if x.size else -1.0
 
 
 def to64(t):
@@ -54,21 +38,23 @@ def to64(t):
 
 
 def check(name, x, ref, rel_tol, err=None):
-    """Relative Frobenius <= rel_tol and the elementwise bound; returns
+    """Relative Frobenius <= rel_tol and the widened elementwise bound; returns
     (relative Frobenius error, flat elementwise excess)."""
-    x = to64(x) if isinstance(x, torch.Tensor) else x
-    assert np.isfinite(x).all(), f"{name}: non-finite values"
-    rf = rel_fro(x, ref)
-    flat = abs_excess(x, ref)
-    ex = abs_excess(x, ref, err)
-    assert rf <= rel_tol, f"{name}: relative Frobenius error {rf:.3e} > {rel_tol}"
-    assert ex <= 0, f"{name}: elementwise error exceeds bound by {ex:.3e} (flat excess {flat:.3e})"
-    print(f"{name}: rel_fro {rf:.2e}, flat elementwise excess {flat:+.2e}")
-    return rf, flat
+    x = to64(x) if isinstance(x, torch.Tensor) else np.asarray(x, dtype=np.float64)
+    r = P.compare(name, x, ref, rel_tol, err)
+    P.record(_case(), r)
+    assert r["finite"], f"{name}: non-finite values"
+    assert r["rel_fro"] <= rel_tol, f"{name}: relative Frobenius error {r['rel_fro']:.3e} > {rel_tol}"
+    assert r["widened_excess"] <= 0, (f"{name}: elementwise error exceeds bound by {r['widened_excess']:.3e} "
+                                      f"(flat excess {r['flat_excess']:.3e})")
+    print(f"{name}: rel_fro {r['rel_fro']:.2e}, max abs {r['max_abs']:.2e} (flat excess {r['flat_excess']:+.2e}, "
+          f"meets {r['meets']})")
+    return r["rel_fro"], r["flat_excess"]
 
 
 def check_lse(x, ref):
-    x = to64(x) if isinstance(x, torch.Tensor) else x
-    err = float(np.abs(x - ref).max()) if x.size else 0.0
-    assert err <= TOL_LSE, f"lse: max abs error {err:.3e} > {TOL_LSE}"
-    return err
+    x = to64(x) if isinstance(x, torch.Tensor) else np.asarray(x, dtype=np.float64)
+    r = P.compare_lse(x, ref)
+    P.record(_case(), r)
+    assert r["ok"], f"lse: max abs error {r['max_abs']:.3e} > {TOL_LSE}"
+    return r["max_abs"]

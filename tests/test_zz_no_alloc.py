@@ -43,8 +43,10 @@ def test_noalloc_matches_workspace_backward_on_consecutive_calls(shapes):
         ref = g.attn_bwd(q, k, v, o, lse, do, scale=scale)          # caller-provided workspace
         got = _noalloc(g, q, k, v, o, lse, do, scale)
         assert g.get_device_status() == 0
-        for name, a, b in zip(("dq", "dk", "dv"), got, ref):
-            check(name, a, to64(b), TOL_REL_GRAD)
+        # dK and dV are summed in a fixed order inside one CTA: bit for bit
+        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+        # dQ partials are added in f32 in whatever order they arrive
+        check("dq", got[0], to64(ref[0]), TOL_REL_GRAD)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
