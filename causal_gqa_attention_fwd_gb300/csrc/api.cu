@@ -102,13 +102,17 @@ bool map_accum(CUtensorMap* m, const float* base, int D, long rows) {
 
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
-// Backward workspace: Delta [rows], LSE*log2(e) [rows], f32 dQ [rows, D],
-// each section 256-byte aligned.  Dense rows: B*Hq*round_up(T, 128).
-// Packed rows: Hq * total_pad (every sequence gets a 4-aligned base and at
-// least 128 rows of slack before the next one).
+// Backward workspace: Delta [rows], LSE*log2(e) [rows], and for D = 64 the
+// f32 dQ accumulator [rows, D], each section 256-byte aligned (D = 128
+// writes dQ from a query-stationary kernel and needs no accumulator).
+// Dense rows: B*Hq*round_up(T, 128).  Packed rows: Hq * total_pad (every
+// sequence gets a 4-aligned base and at least 128 rows of slack before the
+// next one).
 long varlen_total_pad(int num_seqs, int total) { return (long)round_up((size_t)total + 132L * num_seqs + 256, 128); }
 
-size_t ws_bytes(long rows, int D) { return round_up((size_t)rows * 4, 256) * 2 + (size_t)rows * D * 4; }
+size_t ws_bytes(long rows, int D) {
+  return round_up((size_t)rows * 4, 256) * 2 + (D == 64 ? (size_t)rows * D * 4 : 0);
+}
 
 attn_status bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
                        const void* dout, void* dq, void* dk, void* dv, void* ws, const int* cu, int num_seqs,
@@ -146,11 +150,12 @@ attn_status bwd_common(const void* q, const void* k, const void* v, const void* 
   char* w = static_cast<char*>(ws);
   a.delta = reinterpret_cast<float*>(w);
   a.lse_log2 = reinterpret_cast<float*>(w + round_up((size_t)rows * 4, 256));
-  a.dq_accum = reinterpret_cast<float*>(w + 2 * round_up((size_t)rows * 4, 256));
+  a.dq_accum = D == 64 ? reinterpret_cast<float*>(w + 2 * round_up((size_t)rows * 4, 256)) : nullptr;
+  a.rope_cs = nullptr;
   const long grid = (long)a.n_items * num_seqs * Hkv;
   if (grid > 0x7fffffffL || rows > 0x7fffffffL || (long)a.num_seqs * Hq > 65535L * 65535L) return ATTN_ERR_SHAPE;
   const int bm = gqa::bwd_query_block(D);
-  CUtensorMap tq, tk, tv, tdo, tacc;
+  CUtensorMap tq, tk, tv, tdo, tacc{};
   bool ok;
   if (varlen)
     ok = map_packed(&tq, q, D, Hq, total, bm) && map_packed(&tdo, dout, D, Hq, total, bm) &&
@@ -158,7 +163,7 @@ attn_status bwd_common(const void* q, const void* k, const void* v, const void* 
   else
     ok = map_dense(&tq, q, D, T, (long)num_seqs * Hq, bm) && map_dense(&tdo, dout, D, T, (long)num_seqs * Hq, bm) &&
          map_dense(&tk, k, D, T, (long)num_seqs * Hkv) && map_dense(&tv, v, D, T, (long)num_seqs * Hkv);
-  ok = ok && map_accum(&tacc, a.dq_accum, D, rows);
+  if (D == 64) ok = ok && map_accum(&tacc, a.dq_accum, D, rows);
   if (!ok) return ATTN_ERR_CUDA;
   return launch_status(gqa::launch_attn_bwd(tq, tk, tv, tdo, tacc, a, static_cast<cudaStream_t>(stream)));
 }

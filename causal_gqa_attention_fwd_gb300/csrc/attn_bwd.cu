@@ -26,8 +26,11 @@
 // partials and write dK, dV.
 #include "sm103.cuh"
 #include "kernels.h"
+#include "bwd_common.cuh"
 
 namespace gqa {
+
+using namespace bwd;
 
 namespace {
 
@@ -41,40 +44,6 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const 
                    reinterpret_cast<uint64_t>(map)),
                "r"(smem_u32(src)), "r"(x), "r"(y)
                : "memory");
-}
-
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
-
-// Workspace row of (sequence s, head h, position p).  Dense: s is the batch
-// index and every head owns T_pad rows.  Packed: every head owns total_pad
-// rows and sequence s starts at a 4-aligned base, 132 rows further apart than
-// the tokens before it, so a 128-row tile never reaches the next sequence.
-__device__ __forceinline__ long ws_row(const BwdArgs& a, int s, int tok0, int h, int p) {
-  if (a.varlen) return (long)h * a.total_pad + (long)(((tok0 + 3) & ~3) + 132 * s) + p;
-  return ((long)s * a.Hq + h) * a.T_pad + p;
-}
-
-__device__ __forceinline__ bool seq_bounds(const BwdArgs& a, int s, int& tok0, int& L) {
-  if (!a.varlen) {
-    tok0 = 0;
-    L = a.T;
-    return true;
-  }
-  tok0 = a.cu_seqlens[s];
-  const int tok1 = a.cu_seqlens[s + 1];
-  L = tok1 - tok0;
-  return tok0 >= 0 && L >= 0 && tok1 <= a.total;
-}
-
-// Element offset of row p of head h (of a tensor with H heads) in sequence s.
-__device__ __forceinline__ long row_off(const BwdArgs& a, int s, int tok0, int h, int H, int p, int D) {
-  if (a.varlen) return ((long)(tok0 + p) * H + h) * D;
-  return (((long)s * H + h) * a.T + p) * D;
 }
 
 }  // namespace
@@ -136,10 +105,13 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
         a.delta[w] = dl;
         a.lse_log2[w] = l2;
       }
-      // zero this row of the f32 dQ accumulator (D floats: 2 x 16 bytes per lane)
-      float4* z = reinterpret_cast<float4*>(a.dq_accum + w * D) + part * 2;
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      // zero this row of the f32 dQ accumulator (D floats: 2 x 16 bytes per
+      // lane), where the dQ products are summed in one (D = 64)
+      if (a.dq_accum) {
+        float4* z = reinterpret_cast<float4*>(a.dq_accum + w * D) + part * 2;
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
 }
@@ -638,45 +610,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 template <int D>
-static cudaError_t launch_bwd_d(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                const CUtensorMap& dout, const CUtensorMap& dqacc, const BwdArgs& a,
-                                cudaStream_t stream) {
-  using C = BwdCfg<D>;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+static cudaError_t launch_pre(const BwdArgs& a, cudaStream_t stream) {
   const int rblocks = (a.T + 127) / 128;   // T: dense length, or the longest sequence
   dim3 gpre(rblocks, a.num_seqs * a.Hq);
   prof_begin(kProfBwdPre, stream);
   bwd_pre_kernel<D><<<gpre, 256, 0, stream>>>(a);
   prof_end(stream);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const long grid = (long)a.n_items * a.num_seqs * a.Hkv;
-  prof_begin(kProfBwdMain, stream);
-  bwd_main_kernel<D><<<(unsigned)grid, kBwdThreads, C::kSmemBytes, stream>>>(q, k, v, dout, dqacc, a);
-  prof_end(stream);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  prof_begin(kProfBwdPost, stream);
-  bwd_post_kernel<D><<<gpre, 256, 0, stream>>>(a);
-  prof_end(stream);
   return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
+  return a.D == 128 ? launch_pre<128>(a, stream) : launch_pre<64>(a, stream);
 }
 
 cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& dout, const CUtensorMap& dqacc, const BwdArgs& a,
                             cudaStream_t stream) {
-  if (a.D == 128) return launch_bwd_d<128>(q, k, v, dout, dqacc, a, stream);
-  return launch_bwd_d<64>(q, k, v, dout, dqacc, a, stream);
+  cudaError_t e = launch_bwd_pre(a, stream);
+  if (e != cudaSuccess) return e;
+  if (a.D == 128) return launch_attn_bwd128(q, k, v, dout, a, false, stream);
+  // D = 64: key/value-stationary kernel with dQ partials reduced into f32
+  using C = BwdCfg<64>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(bwd_main_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const long grid = (long)a.n_items * a.num_seqs * a.Hkv;
+  prof_begin(kProfBwdMain, stream);
+  bwd_main_kernel<64><<<(unsigned)grid, kBwdThreads, C::kSmemBytes, stream>>>(q, k, v, dout, dqacc, a);
+  prof_end(stream);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 gpost((a.T + 127) / 128, a.num_seqs * a.Hq);
+  prof_begin(kProfBwdPost, stream);
+  bwd_post_kernel<64><<<gpost, 256, 0, stream>>>(a);
+  prof_end(stream);
+  return cudaGetLastError();
 }
 
-int bwd_query_block(int D) { return D == 128 ? BwdCfg<128>::kBM : BwdCfg<64>::kBM; }
+int bwd_query_block(int D) { return D == 128 ? 128 : BwdCfg<64>::kBM; }
 
 }  // namespace gqa

@@ -1,0 +1,764 @@
+// attn_bwd128.cu -- causal grouped-query attention backward, head dimension
+// 128, for sm_103a.
+//
+// The gradients of L = sum(dO * O) (the causal GQA backward of the
+// microLLM-rocm README, section "Why this project exists"), with P recomputed
+// from the forward's LSE:  P = exp(scale S - LSE), dP = dO V^T,
+// dS = P * (dP - Delta);  dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K.
+// After the preprocess (Delta and -LSE*log2(e) per row, attn_bwd.cu), two
+// kernels, each keeping its accumulators in TMEM for its whole walk, so no
+// partial sum ever leaves the chip:
+//
+//  bwd_dkdv128  key/value-stationary: one CTA per (sequence, K/V head, 128
+//     keys) walks the G query heads of the group and the 128-query blocks
+//     that see its keys.  Per step four 128 x 128 x 128 MMAs:
+//       S^T = K Q^T, dP^T = V dO^T (recomputed), dV += P^T dO, dK += dS^T Q.
+//     Issue order dV(i), S^T(i+1), dK(i), dP^T(i+1): the compute warpgroups
+//     form P^T(i+1) while dK(i) runs and dS^T(i+1) while dV(i+1) runs.
+//  bwd_dq128    query-stationary (the separate dQ pass): one CTA per
+//     (sequence, query head, 128 queries) walks the key blocks its queries
+//     see.  Per step three MMAs:  S = Q K^T, dP = dO V^T (both recomputed),
+//     dQ += dS K.  S is double-buffered in TMEM, so S(j+2) and dP(j+1) run
+//     while the compute warpgroups form dS(j).
+//
+// dQ is therefore written once, complete and bit-reproducible, with no f32
+// accumulator in memory and no conversion pass; the price is recomputing S
+// and dP once more (7 matrix products per (query block, key block) instead
+// of 5).  FLOPs are still counted by the 5 products the method needs.
+//
+// Roles in both kernels (384 threads): warp 0 TMA producer, warp 1 MMA issuer
+// (warp-uniform operands, one elected lane issues; TMEM owner), warps 4-11
+// two compute warpgroups (thread = TMEM lane = key row in bwd_dkdv128, query
+// row in bwd_dq128; warpgroup w takes the step's columns [64w, 64w+64)).
+//
+// F16: Q and K are f16 (the rotated copies of the rotary backward), so every
+// product with Q or K takes f16 operands and dS is packed as f16; the
+// products with V, dO and P stay bf16.
+#include "bwd_common.cuh"
+#include "kernels.h"
+#include "rope.h"
+#include "sm103.cuh"
+
+namespace gqa {
+
+using namespace bwd;
+
+namespace {
+
+constexpr int kTile = 128 * 128 * 2;   // one 128-row, 128-feature tile: two 64-column boxes
+constexpr int kBox = 128 * 128;        // one box: 128 rows x 128 bytes
+constexpr int kStatBytes = 128 * 4;
+constexpr int kThreads = 384;
+constexpr int kCols = 64;              // columns per compute warpgroup
+
+// TMEM column of the packed 16-bit operand for the 16 columns of K-step kk
+// (each warpgroup packs its 64 columns into the first 32 it read them from).
+__device__ constexpr uint32_t packed_col(uint32_t base, int kk) {
+  return base + (uint32_t)((16 * kk) / kCols * kCols + ((16 * kk) % kCols) / 2);
+}
+
+// --------------------------------------------------------------- dK, dV
+struct KvCfg {
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTile;
+  static constexpr int kOffQ = 2 * kTile;       // two stages
+  static constexpr int kOffDO = 4 * kTile;      // two stages
+  static constexpr int kOffStats = 6 * kTile;   // per stage: -LSE*log2(e) [128], then -Delta [128]
+  static constexpr int kOffBars = kOffStats + 2 * 2 * kStatBytes;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 384;
+};
+
+struct __align__(8) KvBars {
+  uint64_t kv_full;
+  uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];
+  uint64_t s_full, dp_full, p_full, ds_full;
+  uint64_t dkdv_done, teardown;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr int kKvSmem = KvCfg::kOffBars + (int)sizeof(KvBars);
+
+// ------------------------------------------------------------------ dQ
+struct QCfg {
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kTile;
+  static constexpr int kOffK = 2 * kTile;       // three K slots
+  static constexpr int kOffV = 5 * kTile;       // two V slots
+  static constexpr int kOffBars = 7 * kTile;
+  static constexpr uint32_t kColS = 0;          // two S buffers: [0,128), [128,256)
+  static constexpr uint32_t kColDP = 256, kColDQ = 384;
+};
+
+struct __align__(8) QBars {
+  uint64_t q_full;
+  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
+  uint64_t s_full[2], dp_full, dp_read, ds_full;
+  uint64_t dq_done, teardown;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr int kQSmem = QCfg::kOffBars + (int)sizeof(QBars);
+static_assert(kKvSmem <= 232448 && kQSmem <= 232448, "shared memory budget");
+
+// Rotary transpose for the gradient of a rotated row at position pos (the
+// rotation took x to x'_i = x_i c - x_{i+64} s, x'_{i+64} = x_{i+64} c + x_i s):
+// g_i = g'_i c + g'_{i+64} s,  g_{i+64} = g'_{i+64} c - g'_i s, for the 32
+// pairs i = i0 .. i0+31 of one thread (lo = columns i, hi = columns i + 64).
+__device__ __forceinline__ void rope_grad_transpose(float* lo, float* hi, const float* cos_sin, int pos, int i0) {
+  const float* cs = cos_sin + (long)pos * 128;
+#pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    const float4 c4 = *reinterpret_cast<const float4*>(cs + i0 + e);
+    const float4 s4 = *reinterpret_cast<const float4*>(cs + 64 + i0 + e);
+    const float c[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float a = lo[e + u], b = hi[e + u];
+      lo[e + u] = fmaf(a, c[u], b * sn[u]);
+      hi[e + u] = fmaf(b, c[u], -a * sn[u]);
+    }
+  }
+}
+
+}  // namespace
+
+// ====================================================================== dK, dV
+template <bool F16>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdArgs a) {
+  using C = KvCfg;
+  constexpr int BM = 128;
+  constexpr uint32_t kIdS = F16 ? idesc_f16(128, 128, false, false) : idesc_bf16(128, 128, false, false);
+  constexpr uint32_t kIdDP = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t kIdDV = idesc_bf16(128, 128, false, true);
+  constexpr uint32_t kIdDK = F16 ? idesc_f16(128, 128, false, true) : idesc_bf16(128, 128, false, true);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ------------------------------------------------------------- decode
+  int item = blockIdx.x;
+  const int hkv = item % a.Hkv;
+  item /= a.Hkv;
+  const int s = item % a.num_seqs;
+  const int nb = item / a.num_seqs;                    // key block; heaviest (0) first
+  int tok0, L;
+  if (!seq_bounds(a, s, tok0, L)) {
+    if (threadIdx.x == 0) atomicCAS(a.status, 0, kDevBadSeqlens);
+    return;
+  }
+  const int k0 = nb * 128;
+  if (k0 >= L) return;
+  if (smem_u32(smem) & 1023u) {      // the swizzled tiles need a 1024-byte-aligned base
+    if (threadIdx.x == 0) atomicCAS(a.status, 0, kDevInternal);
+    return;
+  }
+  const int n_mb = (L + BM - 1) / BM;
+  const int mb0 = a.causal ? nb : 0;
+  const int per_head = n_mb - mb0;
+  const int n_it = a.G * per_head;
+
+  KvBars& bars = *reinterpret_cast<KvBars*>(smem + C::kOffBars);
+  Guard guard{&bars.abort, a.status};
+  if (threadIdx.x == 0) {
+    bars.abort = 0;
+    mbar_init(&bars.kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.q_full[i], 1);
+      mbar_init(&bars.q_empty[i], 1);
+      mbar_init(&bars.do_full[i], 1);
+      mbar_init(&bars.do_empty[i], 1);
+    }
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.p_full, 8);                  // one arrive per compute warp
+    mbar_init(&bars.ds_full, 8);
+    mbar_init(&bars.dkdv_done, 1);
+    mbar_init(&bars.teardown, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  float* stats = reinterpret_cast<float*>(smem + C::kOffStats);   // [stage][2][BM]
+  auto it_head = [&](int i) { return hkv * a.G + i / per_head; };
+  auto it_mb = [&](int i) { return mb0 + i % per_head; };
+
+  if (warp == 0) {
+    // ======================================================== TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      int c1, c2;
+      if (a.varlen) { c1 = hkv; c2 = tok0 + k0; } else { c1 = k0; c2 = s * a.Hkv + hkv; }
+      mbar_expect_tx(&bars.kv_full, 2 * kTile);
+      for (int b = 0; b < 2; ++b) {
+        tma_load_3d(smem + C::kOffK + b * kBox, &tm_k, &bars.kv_full, b * 64, c1, c2);
+        tma_load_3d(smem + C::kOffV + b * kBox, &tm_v, &bars.kv_full, b * 64, c1, c2);
+      }
+      int lastq[2] = {-1, -1}, lastd[2] = {-1, -1};
+      for (int i = 0; i < n_it; ++i) {
+        const int st = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        const int h = it_head(i), mb = it_mb(i);
+        if (a.varlen) { c1 = h; c2 = tok0 + mb * BM; } else { c1 = mb * BM; c2 = s * a.Hq + h; }
+        if (!mbar_wait(&bars.q_empty[st], ph ^ 1, guard)) break;
+        mbar_expect_tx(&bars.q_full[st], kTile + 2 * kStatBytes);
+        for (int b = 0; b < 2; ++b)
+          tma_load_3d(smem + C::kOffQ + st * kTile + b * kBox, &tm_q, &bars.q_full[st], b * 64, c1, c2);
+        const long w = ws_row(a, s, tok0, h, mb * BM);
+        bulk_load(stats + st * 2 * BM, a.lse_log2 + w, kStatBytes, &bars.q_full[st]);
+        bulk_load(stats + st * 2 * BM + BM, a.delta + w, kStatBytes, &bars.q_full[st]);
+        lastq[st] = (int)ph;
+        if (!mbar_wait(&bars.do_empty[st], ph ^ 1, guard)) break;
+        mbar_expect_tx(&bars.do_full[st], kTile);
+        for (int b = 0; b < 2; ++b)
+          tma_load_3d(smem + C::kOffDO + st * kTile + b * kBox, &tm_do, &bars.do_full[st], b * 64, c1, c2);
+        lastd[st] = (int)ph;
+      }
+      // never leave the CTA with copies in flight
+      mbar_wait_drain(&bars.kv_full, 0);
+      for (int st = 0; st < 2; ++st) {
+        if (lastq[st] >= 0) mbar_wait_drain(&bars.q_full[st], (uint32_t)lastq[st]);
+        if (lastd[st] >= 0) mbar_wait_drain(&bars.do_full[st], (uint32_t)lastd[st]);
+      }
+    }
+  } else if (warp == 1) {
+    // ============================ MMA issuer (whole warp, one elected lane issues)
+    const uint32_t aK = smem_u32(smem + C::kOffK), aV = smem_u32(smem + C::kOffV);
+    auto aQ = [&](int st) { return smem_u32(smem + C::kOffQ + st * kTile); };
+    auto aDO = [&](int st) { return smem_u32(smem + C::kOffDO + st * kTile); };
+    // S^T = K Q^T: A = K, B = Q, both K-major, contraction over the 128 features
+    auto mma_s = [&](int st) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+        mma_ss_warp(tmem + C::kColS, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(aQ(st) + off, 16, 1024), kIdS,
+                    kk > 0);
+      }
+    };
+    // dP^T = V dO^T
+    auto mma_dp = [&](int st) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+        mma_ss_warp(tmem + C::kColDP, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(aDO(st) + off, 16, 1024), kIdDP,
+                    kk > 0);
+      }
+    };
+    // dV += P^T dO: A = P^T from TMEM, B = dO [queries x features], MN-major
+    auto mma_dv = [&](int st, bool acc) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts_warp(tmem + C::kColDV, tmem + packed_col(C::kColS, kk), sdesc_sw128(aDO(st) + kk * 2048, kBox, 1024),
+                    kIdDV, (acc || kk > 0) ? 1u : 0u);
+    };
+    // dK += dS^T Q
+    auto mma_dk = [&](int st, bool acc) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts_warp(tmem + C::kColDK, tmem + packed_col(C::kColDP, kk), sdesc_sw128(aQ(st) + kk * 2048, kBox, 1024),
+                    kIdDK, (acc || kk > 0) ? 1u : 0u);
+    };
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full, 0, guard));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_full[0], 0, guard));
+    if (ok) {
+      tc_fence_after();
+      mma_s(0);
+      tc_commit_warp(&bars.s_full);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.do_full[0], 0, guard));
+    }
+    if (ok) {
+      tc_fence_after();
+      mma_dp(0);
+      tc_commit_warp(&bars.dp_full);
+    }
+    for (int i = 0; i < n_it && ok; ++i) {
+      const int st = i & 1, st1 = (i + 1) & 1;
+      const uint32_t ph1 = ((i + 1) >> 1) & 1;
+      const bool more = i + 1 < n_it;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_full, i & 1, guard)))) break;
+      tc_fence_after();
+      mma_dv(st, i > 0);
+      tc_commit_warp(&bars.do_empty[st]);
+      if (more) {   // the S^T columns are free once dV(i) has read P^T(i): in-order issue
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_full[st1], ph1, guard)))) break;
+        tc_fence_after();
+        mma_s(st1);
+        tc_commit_warp(&bars.s_full);
+      }
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.ds_full, i & 1, guard)))) break;
+      tc_fence_after();
+      mma_dk(st, i > 0);
+      tc_commit_warp(&bars.q_empty[st]);
+      if (more) {   // the dP^T columns are free once dK(i) has read dS^T(i)
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.do_full[st1], ph1, guard)))) break;
+        tc_fence_after();
+        mma_dp(st1);
+        tc_commit_warp(&bars.dp_full);
+      }
+    }
+    if (ok) tc_commit_warp(&bars.dkdv_done);
+    tc_commit_warp(&bars.teardown);
+    mbar_wait_drain(&bars.teardown, 0);
+  } else if (warp >= 4) {
+    // ============================================ compute warpgroups
+    const int wg = (warp - 4) >> 2;
+    const int c0 = wg * kCols;                          // first query column of this warpgroup
+    const int r = threadIdx.x & 127;                    // key row = TMEM lane
+    const int key = k0 + r;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const float c = a.scale_log2;
+    bool ok = true;
+    float p[kCols];                                     // P^T row segment of the current step
+    for (int i = 0; i < n_it; ++i) {
+      const int st = i & 1;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_full[st], (i >> 1) & 1, guard)))) break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, i & 1, guard)))) break;
+      tc_fence_after();
+      const float* nlse2 = stats + st * 2 * BM + c0;       // -LSE*log2(e) per query column
+      const float* ndl = stats + st * 2 * BM + BM + c0;     // -Delta per query column
+      const int q0 = it_mb(i) * BM + c0;
+      const bool need_mask = (a.causal && q0 <= k0 + 127) || (k0 + 128 > L) || (q0 + kCols > L);
+      const int qmin = a.causal ? key : 0;               // smallest visible query index
+      {
+        uint32_t* pv = reinterpret_cast<uint32_t*>(p);
+        tmem_ld_x32(tmem + lane_base + C::kColS + c0, pv);
+        tmem_ld_x32(tmem + lane_base + C::kColS + c0 + 32, pv + 32);
+        tmem_ld_wait();
+        reg_fence<kCols>(pv);
+      }
+      const uint64_t c2 = f2(c, c);
+#pragma unroll
+      for (int j = 0; j < kCols; j += 2) {
+        const uint64_t nl = *reinterpret_cast<const uint64_t*>(nlse2 + j);
+        f2_split(fma2(f2(p[j], p[j + 1]), c2, nl), p[j], p[j + 1]);
+        p[j] = ex2_approx(p[j]);
+        p[j + 1] = ex2_approx(p[j + 1]);
+      }
+      if (need_mask) {
+        const bool krow_ok = key < L;
+#pragma unroll
+        for (int j = 0; j < kCols; ++j) {
+          const int qi = q0 + j;
+          if (!krow_ok || qi >= L || qi < qmin) p[j] = 0.f;
+        }
+      }
+      // P^T (bf16) over this warpgroup's first 32 S^T columns: A of dV += P^T dO
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(p[32 * q + 2 * e], p[32 * q + 2 * e + 1]);
+        tmem_st_x16(tmem + lane_base + C::kColS + c0 + q * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive_warp(&bars.p_full);
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, i & 1, guard)))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t dv[32];
+        tmem_ld_x32(tmem + lane_base + C::kColDP + c0 + q * 32, dv);
+        tmem_ld_wait();
+        reg_fence<32>(dv);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int j = q * 32 + 2 * e;
+          const uint64_t nd = *reinterpret_cast<const uint64_t*>(ndl + j);
+          float d0, d1;
+          f2_split(mul2(f2(p[j], p[j + 1]), add2(f2(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])), nd)),
+                   d0, d1);                                  // P (dP - Delta)
+          w[e] = F16 ? pack_f16x2(d0, d1) : pack_bf16x2(d0, d1);
+        }
+        // dS^T over this warpgroup's dP^T columns: A of dK += dS^T Q
+        tmem_st_x16(tmem + lane_base + C::kColDP + c0 + q * 16, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive_warp(&bars.ds_full);
+    }
+    // ------------------------------------------------ dK (wg 0), dV (wg 1)
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.dkdv_done, 0, guard));
+    if (ok) {
+      tc_fence_after();
+      const uint32_t col = wg == 0 ? C::kColDK : C::kColDV;
+      uint8_t* tile = smem + (wg == 0 ? C::kOffK : C::kOffV);   // dead: every MMA has completed
+      const uint32_t srow = smem_u32(tile) + r * 256;
+      // Each half-row pair (features i, i + 64) together, so the rotary
+      // backward can undo the key rotation of dK at the key's position.
+#pragma unroll 1
+      for (int q = 0; q < 2; ++q) {
+        float lo[32], hi[32];
+        tmem_ld_x32(tmem + lane_base + col + q * 32, reinterpret_cast<uint32_t*>(lo));
+        tmem_ld_x32(tmem + lane_base + col + 64 + q * 32, reinterpret_cast<uint32_t*>(hi));
+        tmem_ld_wait();
+        reg_fence<32>(reinterpret_cast<uint32_t*>(lo));
+        reg_fence<32>(reinterpret_cast<uint32_t*>(hi));
+        if (wg == 0) {
+          if (F16 && key < L) rope_grad_transpose(lo, hi, a.rope_cs, key, q * 32);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            lo[e] *= a.scale;
+            hi[e] *= a.scale;
+          }
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const float* x = half == 0 ? lo : hi;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int ch = half * 8 + q * 4 + cc;
+            st_shared_v4(srow + ((ch ^ (r & 7)) << 4), pack_bf16x2(x[8 * cc], x[8 * cc + 1]),
+                         pack_bf16x2(x[8 * cc + 2], x[8 * cc + 3]), pack_bf16x2(x[8 * cc + 4], x[8 * cc + 5]),
+                         pack_bf16x2(x[8 * cc + 6], x[8 * cc + 7]));
+          }
+        }
+      }
+      __syncwarp();
+      // this warp's 32 rows, coalesced 16-byte stores (rows inside the sequence)
+      const int rows_valid = min(128, L - k0);
+      const int row0 = (warp & 3) * 32;
+      __nv_bfloat16* dst = wg == 0 ? a.dk : a.dv;
+      const uint32_t sb = smem_u32(tile);
+      for (int idx = lane; idx < 32 * 16; idx += 32) {
+        const int row = row0 + idx / 16, cch = idx % 16;
+        if (row < rows_valid) {
+          const uint4 val = ld_shared_v4(sb + row * 256 + ((cch ^ (row & 7)) << 4));
+          *reinterpret_cast<uint4*>(dst + row_off(a, s, tok0, hkv, a.Hkv, k0 + row, 128) + cch * 8) = val;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ========================================================================= dQ
+template <bool F16>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const BwdArgs a) {
+  using C = QCfg;
+  constexpr int BM = 128;
+  constexpr uint32_t kIdS = F16 ? idesc_f16(128, 128, false, false) : idesc_bf16(128, 128, false, false);
+  constexpr uint32_t kIdDP = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t kIdDQ = F16 ? idesc_f16(128, 128, false, true) : idesc_bf16(128, 128, false, true);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ------------------------------------------------------------- decode
+  // blockIdx.x -> (query head, sequence, query block); heaviest (last) block first
+  int item = blockIdx.x;
+  const int h = item % a.Hq;
+  item /= a.Hq;
+  const int s = item % a.num_seqs;
+  const int mb = a.n_items - 1 - item / a.num_seqs;
+  int tok0, L;
+  if (!seq_bounds(a, s, tok0, L)) {
+    if (threadIdx.x == 0) atomicCAS(a.status, 0, kDevBadSeqlens);
+    return;
+  }
+  const int q0 = mb * BM;
+  if (q0 >= L) return;
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicCAS(a.status, 0, kDevInternal);
+    return;
+  }
+  const int hkv = h / a.G;
+  const int n_kb = a.causal ? mb + 1 : (L + 127) / 128;   // key blocks these queries see
+
+  QBars& bars = *reinterpret_cast<QBars*>(smem + C::kOffBars);
+  Guard guard{&bars.abort, a.status};
+  if (threadIdx.x == 0) {
+    bars.abort = 0;
+    mbar_init(&bars.q_full, 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&bars.k_full[i], 1);
+      mbar_init(&bars.k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.v_full[i], 1);
+      mbar_init(&bars.v_empty[i], 1);
+      mbar_init(&bars.s_full[i], 1);
+    }
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.dp_read, 8);
+    mbar_init(&bars.ds_full, 8);
+    mbar_init(&bars.dq_done, 1);
+    mbar_init(&bars.teardown, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  if (warp == 0) {
+    // ======================================================== TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int c1, c2;
+      if (a.varlen) { c1 = h; c2 = tok0 + q0; } else { c1 = q0; c2 = s * a.Hq + h; }
+      mbar_expect_tx(&bars.q_full, 2 * kTile);
+      for (int b = 0; b < 2; ++b) {
+        tma_load_3d(smem + C::kOffQ + b * kBox, &tm_q, &bars.q_full, b * 64, c1, c2);
+        tma_load_3d(smem + C::kOffDO + b * kBox, &tm_do, &bars.q_full, b * 64, c1, c2);
+      }
+      int lastk[3] = {-1, -1, -1}, lastv[2] = {-1, -1};
+      for (int j = 0; j < n_kb; ++j) {
+        if (a.varlen) { c1 = hkv; c2 = tok0 + j * 128; } else { c1 = j * 128; c2 = s * a.Hkv + hkv; }
+        const int ks = j % 3, vs = j & 1;
+        const uint32_t kph = (j / 3) & 1, vph = (j >> 1) & 1;
+        if (!mbar_wait(&bars.k_empty[ks], kph ^ 1, guard)) break;
+        mbar_expect_tx(&bars.k_full[ks], kTile);
+        for (int b = 0; b < 2; ++b)
+          tma_load_3d(smem + C::kOffK + ks * kTile + b * kBox, &tm_k, &bars.k_full[ks], b * 64, c1, c2);
+        lastk[ks] = (int)kph;
+        if (!mbar_wait(&bars.v_empty[vs], vph ^ 1, guard)) break;
+        mbar_expect_tx(&bars.v_full[vs], kTile);
+        for (int b = 0; b < 2; ++b)
+          tma_load_3d(smem + C::kOffV + vs * kTile + b * kBox, &tm_v, &bars.v_full[vs], b * 64, c1, c2);
+        lastv[vs] = (int)vph;
+      }
+      mbar_wait_drain(&bars.q_full, 0);
+      for (int i = 0; i < 3; ++i)
+        if (lastk[i] >= 0) mbar_wait_drain(&bars.k_full[i], (uint32_t)lastk[i]);
+      for (int i = 0; i < 2; ++i)
+        if (lastv[i] >= 0) mbar_wait_drain(&bars.v_full[i], (uint32_t)lastv[i]);
+    }
+  } else if (warp == 1) {
+    // ============================ MMA issuer (whole warp, one elected lane issues)
+    const uint32_t aQ = smem_u32(smem + C::kOffQ), aDO = smem_u32(smem + C::kOffDO);
+    auto aK = [&](int j) { return smem_u32(smem + C::kOffK + (j % 3) * kTile); };
+    auto aV = [&](int j) { return smem_u32(smem + C::kOffV + (j & 1) * kTile); };
+    auto wait_k = [&](int j) { return __all_sync(0xffffffffu, mbar_wait(&bars.k_full[j % 3], (j / 3) & 1, guard)); };
+    auto wait_v = [&](int j) { return __all_sync(0xffffffffu, mbar_wait(&bars.v_full[j & 1], (j >> 1) & 1, guard)); };
+    // S(j) = Q K_j^T into S buffer j & 1: A = Q, B = K_j, both K-major
+    auto mma_s = [&](int j) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+        mma_ss_warp(tmem + C::kColS + (j & 1) * 128, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK(j) + off, 16, 1024),
+                    kIdS, kk > 0);
+      }
+    };
+    // dP(j) = dO V_j^T
+    auto mma_dp = [&](int j) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+        mma_ss_warp(tmem + C::kColDP, sdesc_sw128(aDO + off, 16, 1024), sdesc_sw128(aV(j) + off, 16, 1024), kIdDP,
+                    kk > 0);
+      }
+    };
+    // dQ += dS(j) K_j: A = dS from TMEM (packed over S buffer j & 1), B = K_j [keys x features], MN-major
+    auto mma_dq = [&](int j) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts_warp(tmem + C::kColDQ, tmem + packed_col(C::kColS + (j & 1) * 128, kk),
+                    sdesc_sw128(aK(j) + kk * 2048, kBox, 1024), kIdDQ, (j > 0 || kk > 0) ? 1u : 0u);
+    };
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_full, 0, guard));
+    if (ok && (ok = wait_k(0))) {
+      tc_fence_after();
+      mma_s(0);
+      tc_commit_warp(&bars.s_full[0]);
+    }
+    if (ok && (ok = wait_v(0))) {
+      tc_fence_after();
+      mma_dp(0);
+      tc_commit_warp(&bars.dp_full);
+      tc_commit_warp(&bars.v_empty[0]);
+    }
+    if (ok && n_kb > 1 && (ok = wait_k(1))) {
+      tc_fence_after();
+      mma_s(1);
+      tc_commit_warp(&bars.s_full[1]);
+    }
+    for (int j = 0; j < n_kb && ok; ++j) {
+      if (j + 1 < n_kb) {   // the dP columns are free once the compute warps have read dP(j)
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_read, j & 1, guard)))) break;
+        if (!(ok = wait_v(j + 1))) break;
+        tc_fence_after();
+        mma_dp(j + 1);
+        tc_commit_warp(&bars.dp_full);
+        tc_commit_warp(&bars.v_empty[(j + 1) & 1]);
+      }
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.ds_full, j & 1, guard)))) break;
+      tc_fence_after();
+      mma_dq(j);
+      tc_commit_warp(&bars.k_empty[j % 3]);
+      if (j + 2 < n_kb) {   // S buffer j & 1 is free once dQ(j) has read dS(j)
+        if (!(ok = wait_k(j + 2))) break;
+        tc_fence_after();
+        mma_s(j + 2);
+        tc_commit_warp(&bars.s_full[j & 1]);
+      }
+    }
+    if (ok) tc_commit_warp(&bars.dq_done);
+    tc_commit_warp(&bars.teardown);
+    mbar_wait_drain(&bars.teardown, 0);
+  } else if (warp >= 4) {
+    // ============================================ compute warpgroups
+    const int wg = (warp - 4) >> 2;
+    const int c0 = wg * kCols;                          // first key column of this warpgroup
+    const int r = threadIdx.x & 127;                    // query row = TMEM lane
+    const int qi = q0 + r;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const float c = a.scale_log2;
+    const long wrow = ws_row(a, s, tok0, h, qi);
+    const float nlse2 = a.lse_log2[wrow];              // -LSE*log2(e) (-inf past the sequence)
+    const float ndl = a.delta[wrow];                   // -Delta
+    const uint64_t c2 = f2(c, c), nl2 = f2(nlse2, nlse2), nd2 = f2(ndl, ndl);
+    bool ok = true;
+    for (int j = 0; j < n_kb; ++j) {
+      const uint32_t sb = C::kColS + (j & 1) * 128;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[j & 1], (j >> 1) & 1, guard)))) break;
+      tc_fence_after();
+      float p[kCols];
+      {
+        uint32_t* pv = reinterpret_cast<uint32_t*>(p);
+        tmem_ld_x32(tmem + lane_base + sb + c0, pv);
+        tmem_ld_x32(tmem + lane_base + sb + c0 + 32, pv + 32);
+        tmem_ld_wait();
+        reg_fence<kCols>(pv);
+      }
+#pragma unroll
+      for (int e = 0; e < kCols; e += 2) {
+        f2_split(fma2(f2(p[e], p[e + 1]), c2, nl2), p[e], p[e + 1]);
+        p[e] = ex2_approx(p[e]);
+        p[e + 1] = ex2_approx(p[e + 1]);
+      }
+      const int kbase = j * 128 + c0;                   // key index of this warpgroup's column 0
+      if ((a.causal && j == mb) || kbase + kCols > L || q0 + 128 > L) {
+        const int lim = a.causal ? min(qi + 1, L) : L;   // visible keys: k < lim (none past the sequence)
+#pragma unroll
+        for (int e = 0; e < kCols; ++e)
+          if (kbase + e >= lim || qi >= L) p[e] = 0.f;
+      }
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, j & 1, guard)))) break;
+      tc_fence_after();
+      uint32_t dv[kCols];
+      tmem_ld_x32(tmem + lane_base + C::kColDP + c0, dv);
+      tmem_ld_x32(tmem + lane_base + C::kColDP + c0 + 32, dv + 32);
+      tmem_ld_wait();
+      reg_fence<kCols>(dv);
+      tc_fence_before();
+      mbar_arrive_warp(&bars.dp_read);                  // dP(j+1) may overwrite the dP columns
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int x = q * 32 + 2 * e;
+          float d0, d1;
+          f2_split(mul2(f2(p[x], p[x + 1]), add2(f2(__uint_as_float(dv[x]), __uint_as_float(dv[x + 1])), nd2)), d0,
+                   d1);                                   // P (dP - Delta)
+          w[e] = F16 ? pack_f16x2(d0, d1) : pack_bf16x2(d0, d1);
+        }
+        // dS over this warpgroup's first 32 columns of S buffer j & 1: A of dQ += dS K
+        tmem_st_x16(tmem + lane_base + sb + c0 + q * 16, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive_warp(&bars.ds_full);
+    }
+    // ------------------------------------------------------- dQ epilogue
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_done, 0, guard));
+    if (ok) {
+      tc_fence_after();
+      // warpgroup wg: feature pairs (i, i + 64) for i in [32 wg, 32 wg + 32)
+      float lo[32], hi[32];
+      tmem_ld_x32(tmem + lane_base + C::kColDQ + 32 * wg, reinterpret_cast<uint32_t*>(lo));
+      tmem_ld_x32(tmem + lane_base + C::kColDQ + 64 + 32 * wg, reinterpret_cast<uint32_t*>(hi));
+      tmem_ld_wait();
+      reg_fence<32>(reinterpret_cast<uint32_t*>(lo));
+      reg_fence<32>(reinterpret_cast<uint32_t*>(hi));
+      if (F16 && qi < L) rope_grad_transpose(lo, hi, a.rope_cs, qi, 32 * wg);
+      const uint32_t srow = smem_u32(smem + C::kOffQ) + r * 256;   // the Q tile is dead: every MMA has completed
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const float* x = half == 0 ? lo : hi;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int ch = half * 8 + wg * 4 + cc;
+          st_shared_v4(srow + ((ch ^ (r & 7)) << 4), pack_bf16x2(x[8 * cc] * a.scale, x[8 * cc + 1] * a.scale),
+                       pack_bf16x2(x[8 * cc + 2] * a.scale, x[8 * cc + 3] * a.scale),
+                       pack_bf16x2(x[8 * cc + 4] * a.scale, x[8 * cc + 5] * a.scale),
+                       pack_bf16x2(x[8 * cc + 6] * a.scale, x[8 * cc + 7] * a.scale));
+        }
+      }
+      __syncwarp();
+      // this warp's 32 rows, the 8 chunks this warpgroup wrote in each
+      const int rows_valid = min(128, L - q0);
+      const int row0 = (warp & 3) * 32;
+      const uint32_t sbase = smem_u32(smem + C::kOffQ);
+      for (int idx = lane; idx < 32 * 8; idx += 32) {
+        const int row = row0 + idx / 8, k8 = idx % 8;
+        const int cch = (k8 >> 2) * 8 + wg * 4 + (k8 & 3);
+        if (row < rows_valid) {
+          const uint4 val = ld_shared_v4(sbase + row * 256 + ((cch ^ (row & 7)) << 4));
+          *reinterpret_cast<uint4*>(a.dq + row_off(a, s, tok0, h, a.Hq, q0 + row, 128) + cch * 8) = val;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ==================================================================== launch
+template <bool F16>
+static cudaError_t launch128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                             const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(bwd_dkdv128_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(bwd_dq128_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const long kv_grid = (long)a.n_items * a.num_seqs * a.Hkv;
+  prof_begin(kProfBwdMain, stream);
+  bwd_dkdv128_kernel<F16><<<(unsigned)kv_grid, kThreads, kKvSmem, stream>>>(q, k, v, dout, a);
+  prof_end(stream);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long q_grid = (long)a.n_items * a.num_seqs * a.Hq;
+  prof_begin(kProfBwdDq, stream);
+  bwd_dq128_kernel<F16><<<(unsigned)q_grid, kThreads, kQSmem, stream>>>(q, k, v, dout, a);
+  prof_end(stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const CUtensorMap& dout, const BwdArgs& a, bool f16qk, cudaStream_t stream) {
+  return f16qk ? launch128<true>(q, k, v, dout, a, stream) : launch128<false>(q, k, v, dout, a, stream);
+}
+
+}  // namespace gqa

@@ -31,8 +31,9 @@ struct FwdArgs {
 cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdArgs& a,
                             int D, int grid, cudaStream_t stream);
 
-// Backward.  Same layouts; dQ is accumulated in f32 (dq_accum, row-padded)
-// and converted by a final pass.
+// Backward.  Same layouts.  D = 64: dQ is accumulated in f32 (dq_accum,
+// row-padded) and converted by a final pass; D = 128: a query-stationary
+// kernel writes dQ directly (dq_accum unused).
 struct BwdArgs {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
@@ -45,7 +46,7 @@ struct BwdArgs {
   __nv_bfloat16* dv;
   float* delta;           // workspace: -Delta, [B,Hq,T_pad] or [Hq,total_pad]
   float* lse_log2;        // workspace: -LSE * log2(e), same layout as delta
-  float* dq_accum;        // workspace: f32 dQ, [B,Hq,T_pad,D] or [Hq,total_pad,D]
+  float* dq_accum;        // workspace: f32 dQ, [B,Hq,T_pad,D] or [Hq,total_pad,D] (D = 64 only)
   const int* cu_seqlens;
   int* status;
   int num_seqs;
@@ -60,6 +61,9 @@ struct BwdArgs {
   int n_items;            // key-block items per sequence (max)
   float scale;
   float scale_log2;
+  // rotary backward (D = 128, f16 Q/K copies): [positions, D] cos/sin table;
+  // dK and dQ rows get the transposed rotation at their positions
+  const float* rope_cs;
 };
 
 // dqacc: 2-D f32 map over the dQ accumulator (D, rows), 32 x 128 boxes,
@@ -67,6 +71,15 @@ struct BwdArgs {
 cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& dout, const CUtensorMap& dqacc, const BwdArgs& a,
                             cudaStream_t stream);
+
+// D = 128 after the preprocess: the key/value-stationary dK/dV kernel and the
+// query-stationary dQ kernel (attn_bwd128.cu).  f16qk: q and k are the f16
+// rotated copies (the rotary backward).
+cudaError_t launch_attn_bwd128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const CUtensorMap& dout, const BwdArgs& a, bool f16qk, cudaStream_t stream);
+
+// The preprocess alone (Delta, -LSE*log2(e); zeroes dq_accum when set).
+cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream);
 
 // Query rows per step of the backward main kernel for head dimension D.
 int bwd_query_block(int D);
@@ -121,7 +134,8 @@ enum ProfKind {
   kProfBwdPost = 3,
   kProfDecode = 4,
   kProfDecodeMerge = 5,
-  kProfKinds = 6
+  kProfBwdDq = 6,
+  kProfKinds = 7
 };
 void prof_begin(int kind, cudaStream_t s);
 void prof_end(cudaStream_t s);

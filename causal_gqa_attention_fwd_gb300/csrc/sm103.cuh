@@ -17,7 +17,8 @@
 namespace gqa {
 
 // Device status word values (mirrors attn_status in include/gqa_attn.h).
-enum : int { kDevOk = 0, kDevTimeout = 9, kDevBadSeqlens = 5 };
+// kDevInternal (ATTN_ERR_CUDA): a kernel's own layout check failed.
+enum : int { kDevOk = 0, kDevTimeout = 9, kDevBadSeqlens = 5, kDevInternal = 8 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
@@ -340,6 +341,23 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two f32 -> f16x2 (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Instruction descriptor for kind::f16 with f16 (not bf16) A and B.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_bf16(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10));
+}
+
+// Fire-and-forget f32 add into global memory (performed at L2).
+__device__ __forceinline__ void red_add_f32(float* gaddr, float v) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(gaddr), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {

@@ -81,8 +81,10 @@ GQA_ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int T, int D
 /* Backward, dense layout.  Reads Q, K, V, the forward's O and LSE, and dO;
  * writes dQ, dK, dV (bf16).  workspace: device memory of at least
  * attn_bwd_workspace_size() bytes, 256-byte aligned, owned by the caller; it
- * holds Delta, LSE*log2(e) and the float32 dQ accumulator and needs no
- * initialisation. */
+ * holds Delta and LSE*log2(e) per query row (and, for D = 64, the float32 dQ
+ * accumulator) and needs no initialisation.  D = 128 computes dQ in a
+ * query-stationary pass of its own, so its dQ is bit-reproducible; for
+ * D = 64 the dQ partials are added in f32 in arrival order. */
 GQA_ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                      const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                      int B, int Hq, int Hkv, int T, int D, int causal, float scale, void* stream);
@@ -284,8 +286,9 @@ GQA_ATTN_API attn_status attn_selftest_wait_timeout(int limit_ms, void* stream);
 /* Kernel timing (instrumentation; not thread-safe).  While enabled, every
  * kernel launch is bracketed by a CUDA event pair recorded on the caller's
  * stream.  attn_profile_read synchronises those events and returns, for one
- * kernel kind (0 forward, 1 backward preprocess, 2 backward main,
- * 3 backward dQ conversion, 4 decode partial, 5 decode split merge), the
+ * kernel kind (0 forward, 1 backward preprocess, 2 backward main (D = 128:
+ * the dK/dV kernel), 3 backward dQ conversion (D = 64), 4 decode partial,
+ * 5 decode split merge, 6 backward dQ kernel (D = 128)), the
  * number of launches and their summed device
  * time in milliseconds since the last attn_profile_reset.  At most 65536
  * launches are recorded between resets.  Off by default. */
