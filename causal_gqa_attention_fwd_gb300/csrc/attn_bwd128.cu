@@ -19,7 +19,8 @@
 //     (sequence, query head, 128 queries) walks the key blocks its queries
 //     see.  Per step three MMAs:  S = Q K^T, dP = dO V^T (both recomputed),
 //     dQ += dS K.  S is double-buffered in TMEM, so S(j+2) and dP(j+1) run
-//     while the compute warpgroups form dS(j).
+//     while the compute warpgroups form dS(j); dP is issued by a second warp,
+//     so its stream fills the tensor pipe while the S / dQ issuer waits.
 //
 // dQ is therefore written once, complete and bit-reproducible, with no f32
 // accumulator in memory and no conversion pass; the price is recomputing S
@@ -27,8 +28,9 @@
 // of 5).  FLOPs are still counted by the 5 products the method needs.
 //
 // Roles in both kernels (384 threads): warp 0 TMA producer, warp 1 MMA issuer
-// (warp-uniform operands, one elected lane issues; TMEM owner), warps 4-11
-// two compute warpgroups (thread = TMEM lane = key row in bwd_dkdv128, query
+// (warp-uniform operands, one elected lane issues; TMEM owner) -- in
+// bwd_dq128 warp 2 issues the dP stream beside it --, warps 4-11 two compute
+// warpgroups (thread = TMEM lane = key row in bwd_dkdv128, query
 // row in bwd_dq128; warpgroup w takes the step's columns [64w, 64w+64)).
 //
 // F16: Q and K are f16 (the rotated copies of the rotary backward), so every
@@ -231,40 +233,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ============================ MMA issuer (whole warp, one elected lane issues)
-    const uint32_t aK = smem_u32(smem + C::kOffK), aV = smem_u32(smem + C::kOffV);
-    auto aQ = [&](int st) { return smem_u32(smem + C::kOffQ + st * kTile); };
-    auto aDO = [&](int st) { return smem_u32(smem + C::kOffDO + st * kTile); };
+    // Issue order dV(i), S^T(i+1), dK(i), dP^T(i+1).  (Two issuers, one per
+    // path, measured slower here: their interleaving delays S^T(i+1) and so
+    // the compute warpgroups' P^T(i+1).)
+    // K-major operand descriptors (contraction over features, 64 per box) and
+    // MN-major ones (contraction over the 128 rows, 16 per step), per stage
+    const uint64_t dK = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
+    const uint64_t dQk = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+    const uint64_t dDOk = sdesc_sw128(smem_u32(smem + C::kOffDO), 16, 1024);
+    const uint64_t dQm = sdesc_sw128(smem_u32(smem + C::kOffQ), kBox, 1024);
+    const uint64_t dDOm = sdesc_sw128(smem_u32(smem + C::kOffDO), kBox, 1024);
     // S^T = K Q^T: A = K, B = Q, both K-major, contraction over the 128 features
     auto mma_s = [&](int st) {
+      const uint64_t q = sdesc_add(dQk, st * kTile);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-        mma_ss_warp(tmem + C::kColS, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(aQ(st) + off, 16, 1024), kIdS,
-                    kk > 0);
+        mma_ss_warp(tmem + C::kColS, sdesc_add(dK, off), sdesc_add(q, off), kIdS, kk > 0);
       }
     };
     // dP^T = V dO^T
     auto mma_dp = [&](int st) {
+      const uint64_t g = sdesc_add(dDOk, st * kTile);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-        mma_ss_warp(tmem + C::kColDP, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(aDO(st) + off, 16, 1024), kIdDP,
-                    kk > 0);
+        mma_ss_warp(tmem + C::kColDP, sdesc_add(dV, off), sdesc_add(g, off), kIdDP, kk > 0);
       }
     };
     // dV += P^T dO: A = P^T from TMEM, B = dO [queries x features], MN-major
     auto mma_dv = [&](int st, bool acc) {
+      const uint64_t g = sdesc_add(dDOm, st * kTile);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts_warp(tmem + C::kColDV, tmem + packed_col(C::kColS, kk), sdesc_sw128(aDO(st) + kk * 2048, kBox, 1024),
-                    kIdDV, (acc || kk > 0) ? 1u : 0u);
+        mma_ts_warp(tmem + C::kColDV, tmem + packed_col(C::kColS, kk), sdesc_add(g, kk * 2048), kIdDV,
+                    (acc || kk > 0) ? 1u : 0u);
     };
     // dK += dS^T Q
     auto mma_dk = [&](int st, bool acc) {
+      const uint64_t q = sdesc_add(dQm, st * kTile);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts_warp(tmem + C::kColDK, tmem + packed_col(C::kColDP, kk), sdesc_sw128(aQ(st) + kk * 2048, kBox, 1024),
-                    kIdDK, (acc || kk > 0) ? 1u : 0u);
+        mma_ts_warp(tmem + C::kColDK, tmem + packed_col(C::kColDP, kk), sdesc_add(q, kk * 2048), kIdDK,
+                    (acc || kk > 0) ? 1u : 0u);
     };
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full, 0, guard));
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_full[0], 0, guard));
@@ -498,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.dp_read, 8);
     mbar_init(&bars.ds_full, 8);
     mbar_init(&bars.dq_done, 1);
-    mbar_init(&bars.teardown, 1);
+    mbar_init(&bars.teardown, 2);                // one commit from each issuer
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -544,76 +556,69 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 2; ++i)
         if (lastv[i] >= 0) mbar_wait_drain(&bars.v_full[i], (uint32_t)lastv[i]);
     }
-  } else if (warp == 1) {
-    // ============================ MMA issuer (whole warp, one elected lane issues)
-    const uint32_t aQ = smem_u32(smem + C::kOffQ), aDO = smem_u32(smem + C::kOffDO);
-    auto aK = [&](int j) { return smem_u32(smem + C::kOffK + (j % 3) * kTile); };
-    auto aV = [&](int j) { return smem_u32(smem + C::kOffV + (j & 1) * kTile); };
-    auto wait_k = [&](int j) { return __all_sync(0xffffffffu, mbar_wait(&bars.k_full[j % 3], (j / 3) & 1, guard)); };
-    auto wait_v = [&](int j) { return __all_sync(0xffffffffu, mbar_wait(&bars.v_full[j & 1], (j >> 1) & 1, guard)); };
-    // S(j) = Q K_j^T into S buffer j & 1: A = Q, B = K_j, both K-major
-    auto mma_s = [&](int j) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-        mma_ss_warp(tmem + C::kColS + (j & 1) * 128, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK(j) + off, 16, 1024),
-                    kIdS, kk > 0);
-      }
-    };
-    // dP(j) = dO V_j^T
-    auto mma_dp = [&](int j) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-        mma_ss_warp(tmem + C::kColDP, sdesc_sw128(aDO + off, 16, 1024), sdesc_sw128(aV(j) + off, 16, 1024), kIdDP,
-                    kk > 0);
-      }
-    };
-    // dQ += dS(j) K_j: A = dS from TMEM (packed over S buffer j & 1), B = K_j [keys x features], MN-major
-    auto mma_dq = [&](int j) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ts_warp(tmem + C::kColDQ, tmem + packed_col(C::kColS + (j & 1) * 128, kk),
-                    sdesc_sw128(aK(j) + kk * 2048, kBox, 1024), kIdDQ, (j > 0 || kk > 0) ? 1u : 0u);
-    };
+  } else if (warp == 1 || warp == 2) {
+    // ============ two MMA issuers (whole warps, one elected lane issues):
+    // warp 1 S(j) and dQ += dS(j) K_j, warp 2 dP(j); disjoint TMEM columns.
+    const uint64_t dQ = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+    const uint64_t dDO = sdesc_sw128(smem_u32(smem + C::kOffDO), 16, 1024);
+    const uint64_t dKk = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+    const uint64_t dKm = sdesc_sw128(smem_u32(smem + C::kOffK), kBox, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_full, 0, guard));
-    if (ok && (ok = wait_k(0))) {
-      tc_fence_after();
-      mma_s(0);
-      tc_commit_warp(&bars.s_full[0]);
-    }
-    if (ok && (ok = wait_v(0))) {
-      tc_fence_after();
-      mma_dp(0);
-      tc_commit_warp(&bars.dp_full);
-      tc_commit_warp(&bars.v_empty[0]);
-    }
-    if (ok && n_kb > 1 && (ok = wait_k(1))) {
-      tc_fence_after();
-      mma_s(1);
-      tc_commit_warp(&bars.s_full[1]);
-    }
-    for (int j = 0; j < n_kb && ok; ++j) {
-      if (j + 1 < n_kb) {   // the dP columns are free once the compute warps have read dP(j)
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_read, j & 1, guard)))) break;
-        if (!(ok = wait_v(j + 1))) break;
+    if (warp == 1) {
+      auto wait_k = [&](int j) { return __all_sync(0xffffffffu, mbar_wait(&bars.k_full[j % 3], (j / 3) & 1, guard)); };
+      // S(j) = Q K_j^T into S buffer j & 1: A = Q, B = K_j, both K-major
+      auto mma_s = [&](int j) {
+        const uint64_t k = sdesc_add(dKk, (j % 3) * kTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          mma_ss_warp(tmem + C::kColS + (j & 1) * 128, sdesc_add(dQ, off), sdesc_add(k, off), kIdS, kk > 0);
+        }
+      };
+      // dQ += dS(j) K_j: A = dS from TMEM (packed over S buffer j & 1), B = K_j [keys x features], MN-major
+      auto mma_dq = [&](int j) {
+        const uint64_t k = sdesc_add(dKm, (j % 3) * kTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts_warp(tmem + C::kColDQ, tmem + packed_col(C::kColS + (j & 1) * 128, kk), sdesc_add(k, kk * 2048),
+                      kIdDQ, (j > 0 || kk > 0) ? 1u : 0u);
+      };
+      for (int j = 0; j < 2 && j < n_kb && ok; ++j) {
+        if (!(ok = wait_k(j))) break;
         tc_fence_after();
-        mma_dp(j + 1);
+        mma_s(j);
+        tc_commit_warp(&bars.s_full[j]);
+      }
+      for (int j = 0; j < n_kb && ok; ++j) {
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.ds_full, j & 1, guard)))) break;
+        tc_fence_after();
+        mma_dq(j);
+        tc_commit_warp(&bars.k_empty[j % 3]);
+        if (j + 2 < n_kb) {   // S buffer j & 1 is free once dQ(j) has read dS(j): in-order issue
+          if (!(ok = wait_k(j + 2))) break;
+          tc_fence_after();
+          mma_s(j + 2);
+          tc_commit_warp(&bars.s_full[j & 1]);
+        }
+      }
+      if (ok) tc_commit_warp(&bars.dq_done);
+    } else {
+      // dP(j) = dO V_j^T; the dP columns are free once the compute warps have read dP(j-1)
+      for (int j = 0; j < n_kb && ok; ++j) {
+        if (j > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_read, (j - 1) & 1, guard)))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.v_full[j & 1], (j >> 1) & 1, guard)))) break;
+        tc_fence_after();
+        const uint64_t v = sdesc_add(dV, (j & 1) * kTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          mma_ss_warp(tmem + C::kColDP, sdesc_add(dDO, off), sdesc_add(v, off), kIdDP, kk > 0);
+        }
         tc_commit_warp(&bars.dp_full);
-        tc_commit_warp(&bars.v_empty[(j + 1) & 1]);
-      }
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.ds_full, j & 1, guard)))) break;
-      tc_fence_after();
-      mma_dq(j);
-      tc_commit_warp(&bars.k_empty[j % 3]);
-      if (j + 2 < n_kb) {   // S buffer j & 1 is free once dQ(j) has read dS(j)
-        if (!(ok = wait_k(j + 2))) break;
-        tc_fence_after();
-        mma_s(j + 2);
-        tc_commit_warp(&bars.s_full[j & 1]);
+        tc_commit_warp(&bars.v_empty[j & 1]);
       }
     }
-    if (ok) tc_commit_warp(&bars.dq_done);
     tc_commit_warp(&bars.teardown);
     mbar_wait_drain(&bars.teardown, 0);
   } else if (warp >= 4) {

@@ -253,6 +253,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The descriptor of an operand `bytes` further on (16-byte multiple): shared
+// memory addresses stay below 2^18, so the 14-bit start-address field never
+// carries into the next field.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // ---- TMEM <-> registers.  32x32b shape: thread t of a warp reads/writes TMEM
 // lane (32 * (warp % 4) + t); the lane offset is encoded in taddr[31:16].
 #define GQA_R8(p) "=r"(p[0]), "=r"(p[1]), "=r"(p[2]), "=r"(p[3]), "=r"(p[4]), "=r"(p[5]), "=r"(p[6]), "=r"(p[7])
