@@ -676,26 +676,24 @@ def main():
     value = whole_job_tflops(world, f_fwd + f_bwd, args.steps, total_ms)
     n_fwd, t_fwd = prof["attn_fwd"]
     n_main, t_main = prof["bwd_main"]
-    bwd_ms = sum(prof[k][1] for k in ("bwd_pre", "bwd_main", "bwd_post", "bwd_dq")) / args.steps
+    bwd_ms = sum(prof[k][1] for k in ("bwd_pre", "bwd_main", "bwd_dq")) / args.steps
     fwd_ms = t_fwd / max(n_fwd, 1)
     pk = peaks()
     gpu_launches = sum(prof[k][0] for k in prof)
 
-    # roofline of the dominant kernel, the backward main kernel.  D = 128: the
-    # key/value-stationary dK/dV kernel, whose algorithmic work is its four
-    # products per visible (query, key) pair (S^T, dP^T, dV, dK: 8*D FLOPs; the
-    # separate dQ kernel does the fifth and recomputes S and dP).  D = 64: the
-    # fused kernel with all five products (10*D).
+    # roofline of the dominant kernel, the key/value-stationary dK/dV kernel,
+    # whose algorithmic work is its four products per visible (query, key)
+    # pair (S^T, dP^T, dV, dK: 8*D FLOPs; the separate dQ kernel does the
+    # fifth and recomputes S and dP).
     main_ms = t_main / max(n_main, 1)
-    main_flops = f_bwd * (0.8 if w.D == 128 else 1.0)
+    main_flops = f_bwd * 0.8
     achieved = main_flops / (main_ms / 1e3) / 1e12
     roofline_traffic = measured_traffic(w.name, "bwd_main")
-    roofline = {"kernel": "bwd_dkdv" if w.D == 128 else "bwd_main", "bound": "tensor", "achieved": achieved,
+    roofline = {"kernel": "bwd_dkdv", "bound": "tensor", "achieved": achieved,
                 "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
                 "traffic": roofline_traffic, "peak_source": pk["source"] + " (burst bf16)",
                 "flops_per_launch": main_flops,
-                "flops_per_launch_basis": ("8*D per visible (query, key) pair: S^T, dP^T, dV, dK" if w.D == 128
-                                           else "10*D per visible (query, key) pair: all five products")}
+                "flops_per_launch_basis": "8*D per visible (query, key) pair: S^T, dP^T, dV, dK"}
 
     # end to end through the public API with host buffers
     e2e = None

@@ -7,6 +7,8 @@ PyTorch CUDA tensors (PyTorch supplies device memory and the stream):
     attn_fwd_rope(q, k, v, rope_cos_sin, causal=True, scale=None) -> (o, lse), q and k rotated
     attn_varlen_fwd_rope(q, k, v, cu_seqlens, max_seqlen, rope_cos_sin, ...) -> (o, lse)
     attn_bwd(q, k, v, o, lse, dout, causal=True, scale=None) -> (dq, dk, dv)
+    attn_bwd_rope(q, k, v, o, lse, dout, rope_cos_sin, ...) -> (dq, dk, dv), the backward of attn_fwd_rope
+    attn_varlen_bwd_rope(q, k, v, o, lse, dout, cu_seqlens, max_seqlen, rope_cos_sin, ...) -> (dq, dk, dv)
     attn_varlen_fwd(q, k, v, cu_seqlens, max_seqlen, ...) -> (o, lse)
     attn_varlen_bwd(q, k, v, o, lse, dout, cu_seqlens, max_seqlen, ...) -> (dq, dk, dv)
     attn_decode_fwd(q, k_cache, v_cache, cache_lens, scale=None) -> (o, lse)
@@ -21,6 +23,7 @@ from ._binding import (  # noqa: F401
     AttnError,
     attn_bwd,
     attn_bwd_noalloc,
+    attn_bwd_rope,
     attn_bwd_workspace_size,
     attn_decode_fp8_fwd,
     attn_decode_fwd,
@@ -32,6 +35,7 @@ from ._binding import (  # noqa: F401
     attn_fwd_rope_workspace_size,
     attn_varlen_fwd_rope,
     attn_varlen_bwd,
+    attn_varlen_bwd_rope,
     attn_varlen_bwd_workspace_size,
     attn_varlen_fwd,
     get_device_status,

@@ -30,6 +30,10 @@ SIGNATURES = {
     "attn_varlen_fwd_rope_workspace_size": (_Z, [_I, _I, _I, _I]),
     "attn_varlen_fwd_rope": (_I, [_P] * 6 + [_I] * 7 + [_F, _P, _I, _P, _Z, _P]),
     "attn_bwd_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "attn_bwd_rope_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "attn_bwd_rope": (_I, [_P] * 10 + [_Z, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P]),
+    "attn_varlen_bwd_rope_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "attn_varlen_bwd_rope": (_I, [_P] * 10 + [_Z, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P]),
     "attn_bwd": (_I, [_P] * 10 + [_Z, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_varlen_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_varlen_bwd_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
@@ -49,8 +53,7 @@ SIGNATURES = {
     "attn_decode_paged_fp8_fwd": (_I, [_P, _P, _P, _F, _F] + [_P] * 5 + [_Z] + [_I] * 8 + [_F, _P, _I, _P]),
 }
 
-PROFILE_KINDS = {"attn_fwd": 0, "bwd_pre": 1, "bwd_main": 2, "bwd_post": 3, "decode": 4, "decode_merge": 5,
-                 "bwd_dq": 6}
+PROFILE_KINDS = {"attn_fwd": 0, "bwd_pre": 1, "bwd_main": 2, "decode": 4, "decode_merge": 5, "bwd_dq": 6}
 
 _lib = None
 
@@ -225,6 +228,50 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = True, scale=None, dq=None, dk
                         _need(dv, "dv"), _need(workspace, "workspace", torch.uint8), workspace.numel(),
                         B, Hq, Hkv, T, D, int(causal), _scale(scale, D), _stream(stream))
     _check(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_rope(q, k, v, o, lse, dout, rope_cos_sin, causal: bool = True, scale=None, dq=None, dk=None, dv=None,
+                  workspace=None, stream=None):
+    """Backward of attn_fwd_rope -> (dq, dk, dv) bf16, gradients with respect to the unrotated q, k, v
+    (rotary table as attn_fwd_rope; o, lse from attn_fwd_rope)."""
+    B, Hq, T, D = q.shape
+    Hkv = k.shape[1]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(max(int(lib().attn_bwd_rope_workspace_size(B, Hq, Hkv, T, D)), 256),
+                                dtype=torch.uint8, device=q.device)
+    rope_ptr, rope_n = _rope(rope_cos_sin)
+    st = lib().attn_bwd_rope(_need(q, "q"), _need(k, "k"), _need(v, "v"), _need(o, "o"),
+                             _need(lse, "lse", torch.float32), _need(dout, "dout"), _need(dq, "dq"), _need(dk, "dk"),
+                             _need(dv, "dv"), _need(workspace, "workspace", torch.uint8), workspace.numel(),
+                             B, Hq, Hkv, T, D, int(causal), _scale(scale, D), rope_ptr, rope_n, _stream(stream))
+    _check(st, "attn_bwd_rope")
+    return dq, dk, dv
+
+
+def attn_varlen_bwd_rope(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, rope_cos_sin, causal: bool = True,
+                         scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward of attn_varlen_fwd_rope -> (dq, dk, dv)."""
+    total, Hq, D = q.shape
+    Hkv = k.shape[1]
+    n = cu_seqlens.numel() - 1
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(max(int(lib().attn_varlen_bwd_rope_workspace_size(n, total, Hq, Hkv, D)), 256),
+                                dtype=torch.uint8, device=q.device)
+    rope_ptr, rope_n = _rope(rope_cos_sin)
+    st = lib().attn_varlen_bwd_rope(_need(q, "q"), _need(k, "k"), _need(v, "v"), _need(o, "o"),
+                                    _need(lse, "lse", torch.float32), _need(dout, "dout"), _need(dq, "dq"),
+                                    _need(dk, "dk"), _need(dv, "dv"), _need(workspace, "workspace", torch.uint8),
+                                    workspace.numel(), _need(cu_seqlens, "cu_seqlens", torch.int32), n, total,
+                                    int(max_seqlen), Hq, Hkv, D, int(causal), _scale(scale, D), rope_ptr, rope_n,
+                                    _stream(stream))
+    _check(st, "attn_varlen_bwd_rope")
     return dq, dk, dv
 
 

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgqa_attn.so")
 
-SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd128.cu", "attn_decode.cu"]
+SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_split.cu", "attn_decode.cu"]
 HEADERS = ["sm103.cuh", "kernels.h", "tmap.h", "rope.h", "bwd_common.cuh"]
 
 NVCC_FLAGS = [

@@ -91,33 +91,28 @@ bool map_packed(CUtensorMap* m, const void* base, int D, int H, int total, int b
 
 attn_status launch_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
-// f32 dQ accumulator [rows, D] seen as 2-D (D, rows); 32 x 128 boxes, 128-byte swizzle.
-bool map_accum(CUtensorMap* m, const float* base, int D, long rows) {
-  const uint64_t dims[2] = {(uint64_t)D, (uint64_t)rows};
-  const uint64_t strides[1] = {(uint64_t)D * 4};
-  const uint32_t box[2] = {32, 128};
-  return gqa::make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dims, strides, box,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
-// Backward workspace: Delta [rows], LSE*log2(e) [rows], and for D = 64 the
-// f32 dQ accumulator [rows, D], each section 256-byte aligned (D = 128
-// writes dQ from a query-stationary kernel and needs no accumulator).
-// Dense rows: B*Hq*round_up(T, 128).  Packed rows: Hq * total_pad (every
+// Backward workspace: Delta [rows], LSE*log2(e) [rows], each section
+// 256-byte aligned (dQ comes from a query-stationary kernel and needs no
+// accumulator).  Dense rows: B*Hq*round_up(T, 128).  Packed rows: Hq * total_pad (every
 // sequence gets a 4-aligned base and at least 128 rows of slack before the
 // next one).
 long varlen_total_pad(int num_seqs, int total) { return (long)round_up((size_t)total + 132L * num_seqs + 256, 128); }
 
 size_t ws_bytes(long rows, int D) {
-  return round_up((size_t)rows * 4, 256) * 2 + (D == 64 ? (size_t)rows * D * 4 : 0);
+  (void)D;
+  return round_up((size_t)rows * 4, 256) * 2;
 }
 
 attn_status bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
                        const void* dout, void* dq, void* dk, void* dv, void* ws, const int* cu, int num_seqs,
                        int T, int total, int max_seqlen, int Hq, int Hkv, int D, int causal, float scale,
-                       void* stream, bool varlen) {
+                       void* stream, bool varlen, const float* rope_cs = nullptr) {
+  // rope_cs: q and k are the f16 copies rotated at their positions by the
+  // rotary table rope_cs; dQ and dK are taken back through the rotation
+  const bool f16qk = rope_cs != nullptr;
+  const CUtensorMapDataType qk_type = f16qk ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   int* status = status_word();
   if (!status) return ATTN_ERR_CUDA;
   BwdArgs a{};
@@ -150,22 +145,21 @@ attn_status bwd_common(const void* q, const void* k, const void* v, const void* 
   char* w = static_cast<char*>(ws);
   a.delta = reinterpret_cast<float*>(w);
   a.lse_log2 = reinterpret_cast<float*>(w + round_up((size_t)rows * 4, 256));
-  a.dq_accum = D == 64 ? reinterpret_cast<float*>(w + 2 * round_up((size_t)rows * 4, 256)) : nullptr;
-  a.rope_cs = nullptr;
+  a.rope_cs = rope_cs;
   const long grid = (long)a.n_items * num_seqs * Hkv;
   if (grid > 0x7fffffffL || rows > 0x7fffffffL || (long)a.num_seqs * Hq > 65535L * 65535L) return ATTN_ERR_SHAPE;
-  const int bm = gqa::bwd_query_block(D);
-  CUtensorMap tq, tk, tv, tdo, tacc{};
+  const int bm = 128;   // query rows per step of both backward kernels
+  CUtensorMap tq, tk, tv, tdo;
   bool ok;
   if (varlen)
-    ok = map_packed(&tq, q, D, Hq, total, bm) && map_packed(&tdo, dout, D, Hq, total, bm) &&
-         map_packed(&tk, k, D, Hkv, total, 128) && map_packed(&tv, v, D, Hkv, total, 128);
+    ok = map_packed(&tq, q, D, Hq, total, bm, qk_type) && map_packed(&tdo, dout, D, Hq, total, bm) &&
+         map_packed(&tk, k, D, Hkv, total, 128, qk_type) && map_packed(&tv, v, D, Hkv, total, 128);
   else
-    ok = map_dense(&tq, q, D, T, (long)num_seqs * Hq, bm) && map_dense(&tdo, dout, D, T, (long)num_seqs * Hq, bm) &&
-         map_dense(&tk, k, D, T, (long)num_seqs * Hkv) && map_dense(&tv, v, D, T, (long)num_seqs * Hkv);
-  if (D == 64) ok = ok && map_accum(&tacc, a.dq_accum, D, rows);
+    ok = map_dense(&tq, q, D, T, (long)num_seqs * Hq, bm, qk_type) &&
+         map_dense(&tdo, dout, D, T, (long)num_seqs * Hq, bm) &&
+         map_dense(&tk, k, D, T, (long)num_seqs * Hkv, 128, qk_type) && map_dense(&tv, v, D, T, (long)num_seqs * Hkv);
   if (!ok) return ATTN_ERR_CUDA;
-  return launch_status(gqa::launch_attn_bwd(tq, tk, tv, tdo, tacc, a, static_cast<cudaStream_t>(stream)));
+  return launch_status(gqa::launch_attn_bwd(tq, tk, tv, tdo, a, static_cast<cudaStream_t>(stream), f16qk));
 }
 
 attn_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu,
@@ -458,6 +452,92 @@ attn_status attn_varlen_bwd(const void* q, const void* k, const void* v, const v
                     max_seqlen, Hq, Hkv, D, causal, scale, stream, true);
 }
 
+size_t attn_bwd_rope_workspace_size(int B, int Hq, int Hkv, int T, int D) {
+  if (B < 0 || T < 0 || check_heads(Hq, Hkv, D) != ATTN_OK) return 0;
+  return round_up(attn_fwd_rope_workspace_size(B, Hq, Hkv, T, D), 256) + attn_bwd_workspace_size(B, Hq, Hkv, T, D);
+}
+
+attn_status attn_bwd_rope(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                          int B, int Hq, int Hkv, int T, int D, int causal, float scale, const float* rope_cos_sin,
+                          int rope_positions, void* stream) {
+  if (B < 0 || T < 0 || rope_positions < 0) return ATTN_ERR_SHAPE;
+  attn_status st = check_heads(Hq, Hkv, D);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || T == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !rope_cos_sin) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(rope_cos_sin))
+    return ATTN_ERR_ALIGN;
+  if ((long)B * Hq > 0x7fffffffL || !isfinite(scale) || rope_positions < T) return ATTN_ERR_SHAPE;
+  if (!workspace || workspace_bytes < attn_bwd_rope_workspace_size(B, Hq, Hkv, T, D) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_WORKSPACE;
+  if ((st = check_arch()) != ATTN_OK) return st;
+  int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
+  // rotated f16 copies of q and k, then the backward on them
+  uint8_t* wq = static_cast<uint8_t*>(workspace);
+  uint8_t* wk = wq + round_up((size_t)B * Hq * T * D * 2, 256);
+  uint8_t* wb = wq + round_up(attn_fwd_rope_workspace_size(B, Hq, Hkv, T, D), 256);
+  gqa::RopeRows rr{};
+  rr.rows_q = (long)B * Hq * T;
+  rr.rows_k = (long)B * Hkv * T;
+  rr.T = T;
+  rr.n_table = rope_positions;
+  rr.status = status;
+  if (gqa::launch_rope_qk_f16(q, k, wq, wk, rr, D, rope_cos_sin, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return bwd_common(wq, wk, v, o, lse, dout, dq, dk, dv, wb, nullptr, B, T, 0, 0, Hq, Hkv, D, causal, scale, stream,
+                    false, rope_cos_sin);
+}
+
+size_t attn_varlen_bwd_rope_workspace_size(int num_seqs, int total_tokens, int Hq, int Hkv, int D) {
+  if (num_seqs < 0 || total_tokens < 0 || check_heads(Hq, Hkv, D) != ATTN_OK) return 0;
+  return round_up(attn_varlen_fwd_rope_workspace_size(total_tokens, Hq, Hkv, D), 256) +
+         attn_varlen_bwd_workspace_size(num_seqs, total_tokens, Hq, Hkv, D);
+}
+
+attn_status attn_varlen_bwd_rope(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                 const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                                 size_t workspace_bytes, const int* cu_seqlens, int num_seqs, int total_tokens,
+                                 int max_seqlen, int Hq, int Hkv, int D, int causal, float scale,
+                                 const float* rope_cos_sin, int rope_positions, void* stream) {
+  if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || rope_positions < 0) return ATTN_ERR_SHAPE;
+  attn_status st = check_heads(Hq, Hkv, D);
+  if (st != ATTN_OK) return st;
+  if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return ATTN_OK;
+  if (max_seqlen > total_tokens || !isfinite(scale) || rope_positions < max_seqlen) return ATTN_ERR_SHAPE;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !cu_seqlens || !rope_cos_sin)
+    return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(rope_cos_sin))
+    return ATTN_ERR_ALIGN;
+  if (!workspace ||
+      workspace_bytes < attn_varlen_bwd_rope_workspace_size(num_seqs, total_tokens, Hq, Hkv, D) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_WORKSPACE;
+  if ((st = check_arch()) != ATTN_OK) return st;
+  int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
+  uint8_t* wq = static_cast<uint8_t*>(workspace);
+  uint8_t* wk = wq + round_up((size_t)total_tokens * Hq * D * 2, 256);
+  uint8_t* wb = wq + round_up(attn_varlen_fwd_rope_workspace_size(total_tokens, Hq, Hkv, D), 256);
+  gqa::RopeRows rr{};
+  rr.rows_q = (long)total_tokens * Hq;
+  rr.rows_k = (long)total_tokens * Hkv;
+  rr.Hq = Hq;
+  rr.Hkv = Hkv;
+  rr.cu = cu_seqlens;
+  rr.num_seqs = num_seqs;
+  rr.n_table = rope_positions;
+  rr.status = status;
+  if (gqa::launch_rope_qk_f16(q, k, wq, wk, rr, D, rope_cos_sin, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return bwd_common(wq, wk, v, o, lse, dout, dq, dk, dv, wb, cu_seqlens, num_seqs, 0, total_tokens, max_seqlen, Hq,
+                    Hkv, D, causal, scale, stream, true, rope_cos_sin);
+}
+
 }  // extern "C"
 
 // ------------------------------------------------------ cached (decode) attention
@@ -715,7 +795,7 @@ attn_status attn_decode_paged_fp8_fwd(const void* q, const void* k8_pages, const
 // Scratch for attn_bwd_noalloc: a file-scope device array, so the library
 // never has to allocate device memory for it.  Every device that loads the
 // library holds these bytes until the process exits.
-#define GQA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+#define GQA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 static __device__ __align__(256) unsigned char g_bwd_scratch[GQA_NOALLOC_SCRATCH_BYTES];
 
 // Device address of g_bwd_scratch on the current device.  The name is only a

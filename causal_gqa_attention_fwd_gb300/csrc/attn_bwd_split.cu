@@ -1,5 +1,5 @@
-// attn_bwd128.cu -- causal grouped-query attention backward, head dimension
-// 128, for sm_103a.
+// attn_bwd_split.cu -- causal grouped-query attention backward for sm_103a,
+// head dimension 64 or 128.
 //
 // The gradients of L = sum(dO * O) (the causal GQA backward of the
 // microLLM-rocm README, section "Why this project exists"), with P recomputed
@@ -9,13 +9,13 @@
 // kernels, each keeping its accumulators in TMEM for its whole walk, so no
 // partial sum ever leaves the chip:
 //
-//  bwd_dkdv128  key/value-stationary: one CTA per (sequence, K/V head, 128
+//  bwd_dkdv     key/value-stationary: one CTA per (sequence, K/V head, 128
 //     keys) walks the G query heads of the group and the 128-query blocks
-//     that see its keys.  Per step four 128 x 128 x 128 MMAs:
+//     that see its keys.  Per step four MMAs (128 x 128 x D, 128 x D x 128):
 //       S^T = K Q^T, dP^T = V dO^T (recomputed), dV += P^T dO, dK += dS^T Q.
 //     Issue order dV(i), S^T(i+1), dK(i), dP^T(i+1): the compute warpgroups
 //     form P^T(i+1) while dK(i) runs and dS^T(i+1) while dV(i+1) runs.
-//  bwd_dq128    query-stationary (the separate dQ pass): one CTA per
+//  bwd_dq       query-stationary (the separate dQ pass): one CTA per
 //     (sequence, query head, 128 queries) walks the key blocks its queries
 //     see.  Per step three MMAs:  S = Q K^T, dP = dO V^T (both recomputed),
 //     dQ += dS K.  S is double-buffered in TMEM, so S(j+2) and dP(j+1) run
@@ -29,9 +29,9 @@
 //
 // Roles in both kernels (384 threads): warp 0 TMA producer, warp 1 MMA issuer
 // (warp-uniform operands, one elected lane issues; TMEM owner) -- in
-// bwd_dq128 warp 2 issues the dP stream beside it --, warps 4-11 two compute
-// warpgroups (thread = TMEM lane = key row in bwd_dkdv128, query
-// row in bwd_dq128; warpgroup w takes the step's columns [64w, 64w+64)).
+// bwd_dq warp 2 issues the dP stream beside it --, warps 4-11 two compute
+// warpgroups (thread = TMEM lane = key row in bwd_dkdv, query
+// row in bwd_dq; warpgroup w takes the step's columns [64w, 64w+64)).
 //
 // F16: Q and K are f16 (the rotated copies of the rotary backward), so every
 // product with Q or K takes f16 operands and dS is packed as f16; the
@@ -47,8 +47,9 @@ using namespace bwd;
 
 namespace {
 
-constexpr int kTile = 128 * 128 * 2;   // one 128-row, 128-feature tile: two 64-column boxes
-constexpr int kBox = 128 * 128;        // one box: 128 rows x 128 bytes
+constexpr int kBox = 128 * 128;        // one 64-feature box: 128 rows x 128 bytes
+template <int D>
+constexpr int kTileOf = 128 * D * 2;   // one 128-row tile: D / 64 boxes
 constexpr int kStatBytes = 128 * 4;
 constexpr int kThreads = 384;
 constexpr int kCols = 64;              // columns per compute warpgroup
@@ -60,14 +61,16 @@ __device__ constexpr uint32_t packed_col(uint32_t base, int kk) {
 }
 
 // --------------------------------------------------------------- dK, dV
+template <int D>
 struct KvCfg {
+  static constexpr int kTile = kTileOf<D>;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTile;
   static constexpr int kOffQ = 2 * kTile;       // two stages
   static constexpr int kOffDO = 4 * kTile;      // two stages
   static constexpr int kOffStats = 6 * kTile;   // per stage: -LSE*log2(e) [128], then -Delta [128]
   static constexpr int kOffBars = kOffStats + 2 * 2 * kStatBytes;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 384;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 256 + D;
 };
 
 struct __align__(8) KvBars {
@@ -78,10 +81,13 @@ struct __align__(8) KvBars {
   uint32_t tmem_base;
   int abort;
 };
-constexpr int kKvSmem = KvCfg::kOffBars + (int)sizeof(KvBars);
+template <int D>
+constexpr int kKvSmem = KvCfg<D>::kOffBars + (int)sizeof(KvBars);
 
 // ------------------------------------------------------------------ dQ
+template <int D>
 struct QCfg {
+  static constexpr int kTile = kTileOf<D>;
   static constexpr int kOffQ = 0;
   static constexpr int kOffDO = kTile;
   static constexpr int kOffK = 2 * kTile;       // three K slots
@@ -99,19 +105,21 @@ struct __align__(8) QBars {
   uint32_t tmem_base;
   int abort;
 };
-constexpr int kQSmem = QCfg::kOffBars + (int)sizeof(QBars);
-static_assert(kKvSmem <= 232448 && kQSmem <= 232448, "shared memory budget");
+template <int D>
+constexpr int kQSmem = QCfg<D>::kOffBars + (int)sizeof(QBars);
+static_assert(kKvSmem<128> <= 232448 && kQSmem<128> <= 232448, "shared memory budget");
 
 // Rotary transpose for the gradient of a rotated row at position pos (the
-// rotation took x to x'_i = x_i c - x_{i+64} s, x'_{i+64} = x_{i+64} c + x_i s):
-// g_i = g'_i c + g'_{i+64} s,  g_{i+64} = g'_{i+64} c - g'_i s, for the 32
-// pairs i = i0 .. i0+31 of one thread (lo = columns i, hi = columns i + 64).
+// rotation took x to x'_i = x_i c - x_{i+D/2} s, x'_{i+D/2} = x_{i+D/2} c + x_i s):
+// g_i = g'_i c + g'_{i+D/2} s,  g_{i+D/2} = g'_{i+D/2} c - g'_i s, for the NP
+// pairs i = i0 .. i0+NP-1 of one thread (lo = columns i, hi = columns i + D/2).
+template <int D, int NP>
 __device__ __forceinline__ void rope_grad_transpose(float* lo, float* hi, const float* cos_sin, int pos, int i0) {
-  const float* cs = cos_sin + (long)pos * 128;
+  const float* cs = cos_sin + (long)pos * D;
 #pragma unroll
-  for (int e = 0; e < 32; e += 4) {
+  for (int e = 0; e < NP; e += 4) {
     const float4 c4 = *reinterpret_cast<const float4*>(cs + i0 + e);
-    const float4 s4 = *reinterpret_cast<const float4*>(cs + 64 + i0 + e);
+    const float4 s4 = *reinterpret_cast<const float4*>(cs + D / 2 + i0 + e);
     const float c[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -122,20 +130,29 @@ __device__ __forceinline__ void rope_grad_transpose(float* lo, float* hi, const 
   }
 }
 
+// N TMEM columns (16 or 32) of this thread's lane into registers.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
+  if constexpr (N == 32) tmem_ld_x32(taddr, r);
+  else tmem_ld_x16(taddr, r);
+}
+
 }  // namespace
 
 // ====================================================================== dK, dV
-template <bool F16>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_dkdv128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const BwdArgs a) {
-  using C = KvCfg;
+  using C = KvCfg<D>;
   constexpr int BM = 128;
+  constexpr int kTile = C::kTile;
+  constexpr int NB = D / 64;                   // 64-feature boxes per tile
   constexpr uint32_t kIdS = F16 ? idesc_f16(128, 128, false, false) : idesc_bf16(128, 128, false, false);
   constexpr uint32_t kIdDP = idesc_bf16(128, 128, false, false);
-  constexpr uint32_t kIdDV = idesc_bf16(128, 128, false, true);
-  constexpr uint32_t kIdDK = F16 ? idesc_f16(128, 128, false, true) : idesc_bf16(128, 128, false, true);
+  constexpr uint32_t kIdDV = idesc_bf16(128, D, false, true);
+  constexpr uint32_t kIdDK = F16 ? idesc_f16(128, D, false, true) : idesc_bf16(128, D, false, true);
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -200,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int c1, c2;
       if (a.varlen) { c1 = hkv; c2 = tok0 + k0; } else { c1 = k0; c2 = s * a.Hkv + hkv; }
       mbar_expect_tx(&bars.kv_full, 2 * kTile);
-      for (int b = 0; b < 2; ++b) {
+      for (int b = 0; b < NB; ++b) {
         tma_load_3d(smem + C::kOffK + b * kBox, &tm_k, &bars.kv_full, b * 64, c1, c2);
         tma_load_3d(smem + C::kOffV + b * kBox, &tm_v, &bars.kv_full, b * 64, c1, c2);
       }
@@ -212,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a.varlen) { c1 = h; c2 = tok0 + mb * BM; } else { c1 = mb * BM; c2 = s * a.Hq + h; }
         if (!mbar_wait(&bars.q_empty[st], ph ^ 1, guard)) break;
         mbar_expect_tx(&bars.q_full[st], kTile + 2 * kStatBytes);
-        for (int b = 0; b < 2; ++b)
+        for (int b = 0; b < NB; ++b)
           tma_load_3d(smem + C::kOffQ + st * kTile + b * kBox, &tm_q, &bars.q_full[st], b * 64, c1, c2);
         const long w = ws_row(a, s, tok0, h, mb * BM);
         bulk_load(stats + st * 2 * BM, a.lse_log2 + w, kStatBytes, &bars.q_full[st]);
@@ -220,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         lastq[st] = (int)ph;
         if (!mbar_wait(&bars.do_empty[st], ph ^ 1, guard)) break;
         mbar_expect_tx(&bars.do_full[st], kTile);
-        for (int b = 0; b < 2; ++b)
+        for (int b = 0; b < NB; ++b)
           tma_load_3d(smem + C::kOffDO + st * kTile + b * kBox, &tm_do, &bars.do_full[st], b * 64, c1, c2);
         lastd[st] = (int)ph;
       }
@@ -244,11 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dDOk = sdesc_sw128(smem_u32(smem + C::kOffDO), 16, 1024);
     const uint64_t dQm = sdesc_sw128(smem_u32(smem + C::kOffQ), kBox, 1024);
     const uint64_t dDOm = sdesc_sw128(smem_u32(smem + C::kOffDO), kBox, 1024);
-    // S^T = K Q^T: A = K, B = Q, both K-major, contraction over the 128 features
+    // S^T = K Q^T: A = K, B = Q, both K-major, contraction over the D features
     auto mma_s = [&](int st) {
       const uint64_t q = sdesc_add(dQk, st * kTile);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
         mma_ss_warp(tmem + C::kColS, sdesc_add(dK, off), sdesc_add(q, off), kIdS, kk > 0);
       }
@@ -257,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto mma_dp = [&](int st) {
       const uint64_t g = sdesc_add(dDOk, st * kTile);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
         mma_ss_warp(tmem + C::kColDP, sdesc_add(dV, off), sdesc_add(g, off), kIdDP, kk > 0);
       }
@@ -404,19 +421,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t col = wg == 0 ? C::kColDK : C::kColDV;
       uint8_t* tile = smem + (wg == 0 ? C::kOffK : C::kOffV);   // dead: every MMA has completed
-      const uint32_t srow = smem_u32(tile) + r * 256;
-      // Each half-row pair (features i, i + 64) together, so the rotary
+      const uint32_t srow = smem_u32(tile) + r * (2 * D);
+      // Each half-row pair (features i, i + D/2) together, so the rotary
       // backward can undo the key rotation of dK at the key's position.
 #pragma unroll 1
-      for (int q = 0; q < 2; ++q) {
+      for (int q = 0; q < D / 64; ++q) {
         float lo[32], hi[32];
         tmem_ld_x32(tmem + lane_base + col + q * 32, reinterpret_cast<uint32_t*>(lo));
-        tmem_ld_x32(tmem + lane_base + col + 64 + q * 32, reinterpret_cast<uint32_t*>(hi));
+        tmem_ld_x32(tmem + lane_base + col + D / 2 + q * 32, reinterpret_cast<uint32_t*>(hi));
         tmem_ld_wait();
         reg_fence<32>(reinterpret_cast<uint32_t*>(lo));
         reg_fence<32>(reinterpret_cast<uint32_t*>(hi));
         if (wg == 0) {
-          if (F16 && key < L) rope_grad_transpose(lo, hi, a.rope_cs, key, q * 32);
+          if (F16 && key < L) rope_grad_transpose<D, 32>(lo, hi, a.rope_cs, key, q * 32);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             lo[e] *= a.scale;
@@ -428,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float* x = half == 0 ? lo : hi;
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
-            const int ch = half * 8 + q * 4 + cc;
+            const int ch = half * (D / 16) + q * 4 + cc;
             st_shared_v4(srow + ((ch ^ (r & 7)) << 4), pack_bf16x2(x[8 * cc], x[8 * cc + 1]),
                          pack_bf16x2(x[8 * cc + 2], x[8 * cc + 3]), pack_bf16x2(x[8 * cc + 4], x[8 * cc + 5]),
                          pack_bf16x2(x[8 * cc + 6], x[8 * cc + 7]));
@@ -437,15 +454,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       // this warp's 32 rows, coalesced 16-byte stores (rows inside the sequence)
+      constexpr int kChunks = D / 8;                 // 16-byte chunks per row
       const int rows_valid = min(128, L - k0);
       const int row0 = (warp & 3) * 32;
       __nv_bfloat16* dst = wg == 0 ? a.dk : a.dv;
       const uint32_t sb = smem_u32(tile);
-      for (int idx = lane; idx < 32 * 16; idx += 32) {
-        const int row = row0 + idx / 16, cch = idx % 16;
+      for (int idx = lane; idx < 32 * kChunks; idx += 32) {
+        const int row = row0 + idx / kChunks, cch = idx % kChunks;
         if (row < rows_valid) {
-          const uint4 val = ld_shared_v4(sb + row * 256 + ((cch ^ (row & 7)) << 4));
-          *reinterpret_cast<uint4*>(dst + row_off(a, s, tok0, hkv, a.Hkv, k0 + row, 128) + cch * 8) = val;
+          const uint4 val = ld_shared_v4(sb + row * (2 * D) + ((cch ^ (row & 7)) << 4));
+          *reinterpret_cast<uint4*>(dst + row_off(a, s, tok0, hkv, a.Hkv, k0 + row, D) + cch * 8) = val;
         }
       }
     }
@@ -458,16 +476,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ========================================================================= dQ
-template <bool F16>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_dq128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const BwdArgs a) {
-  using C = QCfg;
+  using C = QCfg<D>;
   constexpr int BM = 128;
+  constexpr int kTile = C::kTile;
+  constexpr int NB = D / 64;                   // 64-feature boxes per tile
   constexpr uint32_t kIdS = F16 ? idesc_f16(128, 128, false, false) : idesc_bf16(128, 128, false, false);
   constexpr uint32_t kIdDP = idesc_bf16(128, 128, false, false);
-  constexpr uint32_t kIdDQ = F16 ? idesc_f16(128, 128, false, true) : idesc_bf16(128, 128, false, true);
+  constexpr uint32_t kIdDQ = F16 ? idesc_f16(128, D, false, true) : idesc_bf16(128, D, false, true);
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -530,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int c1, c2;
       if (a.varlen) { c1 = h; c2 = tok0 + q0; } else { c1 = q0; c2 = s * a.Hq + h; }
       mbar_expect_tx(&bars.q_full, 2 * kTile);
-      for (int b = 0; b < 2; ++b) {
+      for (int b = 0; b < NB; ++b) {
         tma_load_3d(smem + C::kOffQ + b * kBox, &tm_q, &bars.q_full, b * 64, c1, c2);
         tma_load_3d(smem + C::kOffDO + b * kBox, &tm_do, &bars.q_full, b * 64, c1, c2);
       }
@@ -541,12 +561,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kph = (j / 3) & 1, vph = (j >> 1) & 1;
         if (!mbar_wait(&bars.k_empty[ks], kph ^ 1, guard)) break;
         mbar_expect_tx(&bars.k_full[ks], kTile);
-        for (int b = 0; b < 2; ++b)
+        for (int b = 0; b < NB; ++b)
           tma_load_3d(smem + C::kOffK + ks * kTile + b * kBox, &tm_k, &bars.k_full[ks], b * 64, c1, c2);
         lastk[ks] = (int)kph;
         if (!mbar_wait(&bars.v_empty[vs], vph ^ 1, guard)) break;
         mbar_expect_tx(&bars.v_full[vs], kTile);
-        for (int b = 0; b < 2; ++b)
+        for (int b = 0; b < NB; ++b)
           tma_load_3d(smem + C::kOffV + vs * kTile + b * kBox, &tm_v, &bars.v_full[vs], b * 64, c1, c2);
         lastv[vs] = (int)vph;
       }
@@ -571,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto mma_s = [&](int j) {
         const uint64_t k = sdesc_add(dKk, (j % 3) * kTile);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
           mma_ss_warp(tmem + C::kColS + (j & 1) * 128, sdesc_add(dQ, off), sdesc_add(k, off), kIdS, kk > 0);
         }
@@ -611,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint64_t v = sdesc_add(dV, (j & 1) * kTile);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
           mma_ss_warp(tmem + C::kColDP, sdesc_add(dDO, off), sdesc_add(v, off), kIdDP, kk > 0);
         }
@@ -690,21 +710,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_done, 0, guard));
     if (ok) {
       tc_fence_after();
-      // warpgroup wg: feature pairs (i, i + 64) for i in [32 wg, 32 wg + 32)
-      float lo[32], hi[32];
-      tmem_ld_x32(tmem + lane_base + C::kColDQ + 32 * wg, reinterpret_cast<uint32_t*>(lo));
-      tmem_ld_x32(tmem + lane_base + C::kColDQ + 64 + 32 * wg, reinterpret_cast<uint32_t*>(hi));
+      // warpgroup wg: feature pairs (i, i + D/2) for i in [NP wg, NP wg + NP)
+      constexpr int NP = D / 4;
+      float lo[NP], hi[NP];
+      tmem_ld_cols<NP>(tmem + lane_base + C::kColDQ + NP * wg, reinterpret_cast<uint32_t*>(lo));
+      tmem_ld_cols<NP>(tmem + lane_base + C::kColDQ + D / 2 + NP * wg, reinterpret_cast<uint32_t*>(hi));
       tmem_ld_wait();
-      reg_fence<32>(reinterpret_cast<uint32_t*>(lo));
-      reg_fence<32>(reinterpret_cast<uint32_t*>(hi));
-      if (F16 && qi < L) rope_grad_transpose(lo, hi, a.rope_cs, qi, 32 * wg);
-      const uint32_t srow = smem_u32(smem + C::kOffQ) + r * 256;   // the Q tile is dead: every MMA has completed
+      reg_fence<NP>(reinterpret_cast<uint32_t*>(lo));
+      reg_fence<NP>(reinterpret_cast<uint32_t*>(hi));
+      if (F16 && qi < L) rope_grad_transpose<D, NP>(lo, hi, a.rope_cs, qi, NP * wg);
+      const uint32_t srow = smem_u32(smem + C::kOffQ) + r * (2 * D);   // the Q tile is dead: every MMA has completed
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const float* x = half == 0 ? lo : hi;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const int ch = half * 8 + wg * 4 + cc;
+        for (int cc = 0; cc < NP / 8; ++cc) {
+          const int ch = half * (D / 16) + wg * (NP / 8) + cc;
           st_shared_v4(srow + ((ch ^ (r & 7)) << 4), pack_bf16x2(x[8 * cc] * a.scale, x[8 * cc + 1] * a.scale),
                        pack_bf16x2(x[8 * cc + 2] * a.scale, x[8 * cc + 3] * a.scale),
                        pack_bf16x2(x[8 * cc + 4] * a.scale, x[8 * cc + 5] * a.scale),
@@ -712,16 +733,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      // this warp's 32 rows, the 8 chunks this warpgroup wrote in each
+      // this warp's 32 rows, the 2 NP / 8 chunks this warpgroup wrote in each
+      constexpr int kMine = 2 * (NP / 8);
       const int rows_valid = min(128, L - q0);
       const int row0 = (warp & 3) * 32;
       const uint32_t sbase = smem_u32(smem + C::kOffQ);
-      for (int idx = lane; idx < 32 * 8; idx += 32) {
-        const int row = row0 + idx / 8, k8 = idx % 8;
-        const int cch = (k8 >> 2) * 8 + wg * 4 + (k8 & 3);
+      for (int idx = lane; idx < 32 * kMine; idx += 32) {
+        const int row = row0 + idx / kMine, k8 = idx % kMine;
+        const int cch = (k8 / (NP / 8)) * (D / 16) + wg * (NP / 8) + k8 % (NP / 8);
         if (row < rows_valid) {
-          const uint4 val = ld_shared_v4(sbase + row * 256 + ((cch ^ (row & 7)) << 4));
-          *reinterpret_cast<uint4*>(a.dq + row_off(a, s, tok0, h, a.Hq, q0 + row, 128) + cch * 8) = val;
+          const uint4 val = ld_shared_v4(sbase + row * (2 * D) + ((cch ^ (row & 7)) << 4));
+          *reinterpret_cast<uint4*>(a.dq + row_off(a, s, tok0, h, a.Hq, q0 + row, D) + cch * 8) = val;
         }
       }
     }
@@ -734,36 +756,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ==================================================================== launch
-template <bool F16>
-static cudaError_t launch128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                             const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream) {
+template <int D, bool F16>
+static cudaError_t launch_split(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
     cudaError_t e =
-        cudaFuncSetAttribute(bwd_dkdv128_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmem);
+        cudaFuncSetAttribute(bwd_dkdv_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmem<D>);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(bwd_dq128_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+    e = cudaFuncSetAttribute(bwd_dq_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem<D>);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const long kv_grid = (long)a.n_items * a.num_seqs * a.Hkv;
   prof_begin(kProfBwdMain, stream);
-  bwd_dkdv128_kernel<F16><<<(unsigned)kv_grid, kThreads, kKvSmem, stream>>>(q, k, v, dout, a);
+  bwd_dkdv_kernel<D, F16><<<(unsigned)kv_grid, kThreads, kKvSmem<D>, stream>>>(q, k, v, dout, a);
   prof_end(stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long q_grid = (long)a.n_items * a.num_seqs * a.Hq;
   prof_begin(kProfBwdDq, stream);
-  bwd_dq128_kernel<F16><<<(unsigned)q_grid, kThreads, kQSmem, stream>>>(q, k, v, dout, a);
+  bwd_dq_kernel<D, F16><<<(unsigned)q_grid, kThreads, kQSmem<D>, stream>>>(q, k, v, dout, a);
   prof_end(stream);
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_bwd128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                               const CUtensorMap& dout, const BwdArgs& a, bool f16qk, cudaStream_t stream) {
-  return f16qk ? launch128<true>(q, k, v, dout, a, stream) : launch128<false>(q, k, v, dout, a, stream);
+cudaError_t launch_attn_bwd_split(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                  const CUtensorMap& dout, const BwdArgs& a, bool f16qk, cudaStream_t stream) {
+  if (a.D == 128)
+    return f16qk ? launch_split<128, true>(q, k, v, dout, a, stream) : launch_split<128, false>(q, k, v, dout, a, stream);
+  return f16qk ? launch_split<64, true>(q, k, v, dout, a, stream) : launch_split<64, false>(q, k, v, dout, a, stream);
 }
 
 }  // namespace gqa

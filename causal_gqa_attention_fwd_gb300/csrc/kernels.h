@@ -31,9 +31,8 @@ struct FwdArgs {
 cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdArgs& a,
                             int D, int grid, cudaStream_t stream);
 
-// Backward.  Same layouts.  D = 64: dQ is accumulated in f32 (dq_accum,
-// row-padded) and converted by a final pass; D = 128: a query-stationary
-// kernel writes dQ directly (dq_accum unused).
+// Backward.  Same layouts; the workspace holds -Delta and -LSE*log2(e) per
+// query row (row-padded to whole 128-row tiles).
 struct BwdArgs {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
@@ -46,7 +45,6 @@ struct BwdArgs {
   __nv_bfloat16* dv;
   float* delta;           // workspace: -Delta, [B,Hq,T_pad] or [Hq,total_pad]
   float* lse_log2;        // workspace: -LSE * log2(e), same layout as delta
-  float* dq_accum;        // workspace: f32 dQ, [B,Hq,T_pad,D] or [Hq,total_pad,D] (D = 64 only)
   const int* cu_seqlens;
   int* status;
   int num_seqs;
@@ -66,23 +64,17 @@ struct BwdArgs {
   const float* rope_cs;
 };
 
-// dqacc: 2-D f32 map over the dQ accumulator (D, rows), 32 x 128 boxes,
-// 128-byte swizzle (used for D = 64).
-cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& dout, const CUtensorMap& dqacc, const BwdArgs& a,
-                            cudaStream_t stream);
-
-// D = 128 after the preprocess: the key/value-stationary dK/dV kernel and the
-// query-stationary dQ kernel (attn_bwd128.cu).  f16qk: q and k are the f16
+// The preprocess, then the dK/dV and dQ kernels.  f16qk: q and k are the f16
 // rotated copies (the rotary backward).
-cudaError_t launch_attn_bwd128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                               const CUtensorMap& dout, const BwdArgs& a, bool f16qk, cudaStream_t stream);
+cudaError_t launch_attn_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& dout, const BwdArgs& a, cudaStream_t stream, bool f16qk = false);
 
-// The preprocess alone (Delta, -LSE*log2(e); zeroes dq_accum when set).
-cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream);
+// After the preprocess: the key/value-stationary dK/dV kernel and the
+// query-stationary dQ kernel (attn_bwd_split.cu).  f16qk: q and k are the
+// f16 rotated copies (the rotary backward).
+cudaError_t launch_attn_bwd_split(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                  const CUtensorMap& dout, const BwdArgs& a, bool f16qk, cudaStream_t stream);
 
-// Query rows per step of the backward main kernel for head dimension D.
-int bwd_query_block(int D);
 
 // Cached (decode) attention.  Q, O [B,Hq,Tq,D]; K/V cache [B,Hkv,S,D];
 // LSE [B,Hq,Tq]; cache_lens [B].  The R = G*Tq query rows of a (row, K/V
@@ -131,7 +123,7 @@ enum ProfKind {
   kProfFwd = 0,
   kProfBwdPre = 1,
   kProfBwdMain = 2,
-  kProfBwdPost = 3,
+  kProfUnused3 = 3,
   kProfDecode = 4,
   kProfDecodeMerge = 5,
   kProfBwdDq = 6,

@@ -81,10 +81,10 @@ GQA_ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int T, int D
 /* Backward, dense layout.  Reads Q, K, V, the forward's O and LSE, and dO;
  * writes dQ, dK, dV (bf16).  workspace: device memory of at least
  * attn_bwd_workspace_size() bytes, 256-byte aligned, owned by the caller; it
- * holds Delta and LSE*log2(e) per query row (and, for D = 64, the float32 dQ
- * accumulator) and needs no initialisation.  D = 128 computes dQ in a
- * query-stationary pass of its own, so its dQ is bit-reproducible; for
- * D = 64 the dQ partials are added in f32 in arrival order. */
+ * holds Delta and LSE*log2(e) per query row and needs no initialisation.
+ * dK and dV come from a key/value-stationary kernel, dQ from a
+ * query-stationary one; each sums its products in a fixed order, so the
+ * results are bit-reproducible. */
 GQA_ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                      const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                      int B, int Hq, int Hkv, int T, int D, int causal, float scale, void* stream);
@@ -98,8 +98,9 @@ GQA_ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, c
  * tensors it must read and write, or a stream that is being captured into a
  * CUDA graph, during which cudaMalloc is not permitted.
  * The scratch is a static device array of attn_bwd_noalloc_scratch_bytes()
- * bytes (64 MiB) inside the library; every GPU that loads the library holds
- * it until the process exits.  Sizes whose attn_bwd_workspace_size() exceeds
+ * bytes (16 MiB: 8 bytes per query row, so up to 2^21 rows B*Hq*T, T rounded
+ * up to 128) inside the library; every GPU that loads the library holds it
+ * until the process exits.  Sizes whose attn_bwd_workspace_size() exceeds
  * it return ATTN_ERR_SCRATCH_LIMIT before anything is launched.  The first
  * call on a device looks up the array's device address (once per device,
  * with that device current), so make that first call before any stream
@@ -111,7 +112,7 @@ GQA_ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, c
  * destroys the device's primary context, do not call this library on that
  * device again in the same process.
  * Otherwise identical to attn_bwd (same arguments minus the workspace, same
- * results: dK and dV bit for bit; dQ to f32 addition order). */
+ * results bit for bit). */
 GQA_ATTN_API attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
                                           int B, int Hq, int Hkv, int T, int D, int causal, float scale,
@@ -161,6 +162,38 @@ GQA_ATTN_API attn_status attn_varlen_fwd_rope(const void* q, const void* k, cons
                                               int max_seqlen, int Hq, int Hkv, int D, int causal, float scale,
                                               const float* rope_cos_sin, int rope_positions, void* workspace,
                                               size_t workspace_bytes, void* stream);
+
+/* Backward of attn_fwd_rope (rotary queries and keys; RoPE of
+ * MultiHeadAttentionWithRoPE, llm-from-scratch "Project Overview";
+ * positions-aware RoPE of the microLLM-rocm README, section "Why this project
+ * exists"): the gradients of L = sum(dO * O) with respect to the UNROTATED
+ * q and k (and v).  Arguments as attn_bwd, plus the rotary table of
+ * attn_fwd_rope (rope_cos_sin DEVICE float32 [rope_positions, D], 16-byte
+ * aligned, rope_positions >= T); o and lse are attn_fwd_rope's outputs.
+ * The kernels rotate q and k at positions 0..T-1 into f16 copies (as the
+ * forward does), run the backward with f16 Q/K operands and an f16 dS, and
+ * take dQ and dK back through the rotation (x -> R^T x at each row's
+ * position) before rounding them to bf16.
+ * workspace: DEVICE, 256-byte aligned, >= attn_bwd_rope_workspace_size()
+ * bytes (the rotated copies and attn_bwd's workspace), no initialisation. */
+GQA_ATTN_API size_t attn_bwd_rope_workspace_size(int B, int Hq, int Hkv, int T, int D);
+GQA_ATTN_API attn_status attn_bwd_rope(const void* q, const void* k, const void* v, const void* o,
+                                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                       void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int T,
+                                       int D, int causal, float scale, const float* rope_cos_sin,
+                                       int rope_positions, void* stream);
+
+/* attn_bwd_rope for the packed variable-length layout (attn_varlen_bwd's
+ * arguments plus the table; positions 0..len-1 in every sequence,
+ * rope_positions >= max_seqlen).  workspace >=
+ * attn_varlen_bwd_rope_workspace_size() bytes. */
+GQA_ATTN_API size_t attn_varlen_bwd_rope_workspace_size(int num_seqs, int total_tokens, int Hq, int Hkv, int D);
+GQA_ATTN_API attn_status attn_varlen_bwd_rope(const void* q, const void* k, const void* v, const void* o,
+                                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                              void* workspace, size_t workspace_bytes, const int* cu_seqlens,
+                                              int num_seqs, int total_tokens, int max_seqlen, int Hq, int Hkv, int D,
+                                              int causal, float scale, const float* rope_cos_sin,
+                                              int rope_positions, void* stream);
 
 /* Backward, packed variable-length layout (arguments as attn_bwd plus the
  * sequence description of attn_varlen_fwd). */
@@ -286,9 +319,9 @@ GQA_ATTN_API attn_status attn_selftest_wait_timeout(int limit_ms, void* stream);
 /* Kernel timing (instrumentation; not thread-safe).  While enabled, every
  * kernel launch is bracketed by a CUDA event pair recorded on the caller's
  * stream.  attn_profile_read synchronises those events and returns, for one
- * kernel kind (0 forward, 1 backward preprocess, 2 backward main (D = 128:
- * the dK/dV kernel), 3 backward dQ conversion (D = 64), 4 decode partial,
- * 5 decode split merge, 6 backward dQ kernel (D = 128)), the
+ * kernel kind (0 forward, 1 backward preprocess, 2 backward dK/dV kernel,
+ * 3 unused, 4 decode partial, 5 decode split merge, 6 backward dQ kernel),
+ * the
  * number of launches and their summed device
  * time in milliseconds since the last attn_profile_reset.  At most 65536
  * launches are recorded between resets.  Off by default. */

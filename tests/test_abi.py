@@ -108,24 +108,27 @@ def test_noalloc_validation(lib):
     # returns before any CUDA call: shape, scratch limit, NULL pointers
     args = (A,) * 9
     assert lib.attn_bwd_noalloc(*args, 1, 3, 2, 16, 64, 1, 0.1, None) == 2
-    assert lib.attn_bwd_noalloc(*args, 1, 64, 8, 8192, 64, 1, 0.1, None) == 10
+    assert lib.attn_bwd_noalloc(*args, 2, 1024, 8, 2048, 64, 1, 0.1, None) == 10
     assert lib.attn_bwd_noalloc(*((NULL,) * 9), 1, 4, 2, 0, 64, 1, 0.1, None) == 0
     assert lib.attn_bwd_noalloc(*((NULL,) * 9), 1, 4, 2, 16, 64, 1, 0.1, None) == 1
-    assert lib.attn_bwd_noalloc_scratch_bytes() == 64 << 20
+    assert lib.attn_bwd_noalloc_scratch_bytes() == 16 << 20
 
 
 def test_workspace_sizes(lib):
-    # Delta + LSE*log2e (256-aligned f32 rows each), plus f32 dQ rows for D = 64;
-    # rows = B*Hq*roundup(T,128)
+    # Delta + LSE*log2e: 256-aligned f32 rows each; rows = B*Hq*roundup(T,128)
     rows = 2 * 32 * 4096
     assert lib.attn_bwd_workspace_size(2, 32, 8, 4096, 128) == 2 * rows * 4
     rows = 1 * 4 * 256
-    assert lib.attn_bwd_workspace_size(1, 4, 2, 129, 64) == 2 * rows * 4 + rows * 64 * 4
+    assert lib.attn_bwd_workspace_size(1, 4, 2, 129, 64) == 2 * rows * 4
     assert lib.attn_bwd_workspace_size(1, 3, 2, 16, 64) == 0
     pad = -(-(17000 + 132 * 16 + 256) // 128) * 128        # packed rows per head
     assert lib.attn_varlen_bwd_workspace_size(16, 17000, 16, 8, 128) == 2 * (-(-16 * pad * 4 // 256) * 256)
-    assert lib.attn_varlen_bwd_workspace_size(16, 17000, 16, 8, 64) > 16 * 17000 * 64 * 4
+    assert lib.attn_varlen_bwd_workspace_size(16, 17000, 16, 8, 64) == 2 * (-(-16 * pad * 4 // 256) * 256)
     assert lib.attn_varlen_bwd_workspace_size(2, 10, 4, 2, 96) == 0
+    # rotary backward: the two rotated f16 copies (256-aligned) before attn_bwd's workspace
+    qk = -(-(2 * 32 * 4096 * 128 * 2) // 256) * 256 + 2 * 8 * 4096 * 128 * 2
+    assert lib.attn_bwd_rope_workspace_size(2, 32, 8, 4096, 128) == (-(-qk // 256) * 256 +
+                                                                     lib.attn_bwd_workspace_size(2, 32, 8, 4096, 128))
 
 
 def test_status_strings(lib):

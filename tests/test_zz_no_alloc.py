@@ -14,7 +14,6 @@ import numpy as np
 import pytest
 import torch
 
-from parity_util import TOL_REL_GRAD, check, to64
 from causal_gqa_attention_fwd_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -43,21 +42,17 @@ def test_noalloc_matches_workspace_backward_on_consecutive_calls(shapes):
         ref = g.attn_bwd(q, k, v, o, lse, do, scale=scale)          # caller-provided workspace
         got = _noalloc(g, q, k, v, o, lse, do, scale)
         assert g.get_device_status() == 0
-        # dK and dV are summed in a fixed order inside one CTA: bit for bit;
-        # so is dQ at D = 128 (a query-stationary pass)
-        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
-        if D == 128:
-            assert torch.equal(got[0], ref[0])
-        # at D = 64 the dQ partials are added in f32 in whatever order they arrive
-        check("dq", got[0], to64(ref[0]), TOL_REL_GRAD)
+        # every gradient is summed in a fixed order: bit for bit
+        for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+            assert torch.equal(a, b), name
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     import causal_gqa_attention_fwd_gb300 as g
     lib = g.lib()
     cap = lib.attn_bwd_noalloc_scratch_bytes()
-    assert cap == 64 << 20
-    B, Hq, Hkv, T, D = 1, 64, 8, 8192, 64
+    assert cap == 16 << 20
+    B, Hq, Hkv, T, D = 2, 1024, 8, 2048, 64
     assert lib.attn_bwd_workspace_size(B, Hq, Hkv, T, D) > cap
     p = 256      # aligned placeholder address: the call must return before touching it
     st = lib.attn_bwd_noalloc(p, p, p, p, p, p, p, p, p, B, Hq, Hkv, T, D, 1, 0.088, None)
