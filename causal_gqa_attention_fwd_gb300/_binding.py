@@ -43,6 +43,7 @@ SIGNATURES = {
     "attn_bwd_noalloc": (_I, [_P] * 9 + [_I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_noalloc_scratch_bytes": (_Z, []),
     "attn_selftest_wait_timeout": (_I, [_I, _P]),
+    "attn_test_inject_timeout": (_I, [_I, _I]),
     "attn_profile_enable": (_I, [_I]),
     "attn_profile_reset": (_I, []),
     "attn_profile_read": (_I, [_I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)]),

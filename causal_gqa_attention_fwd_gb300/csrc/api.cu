@@ -91,6 +91,15 @@ bool map_packed(CUtensorMap* m, const void* base, int D, int H, int total, int b
 
 attn_status launch_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
+// Failure-path test (attn_test_inject_timeout): one armed injection, consumed
+// by the next launch of the named kernel (1 forward, 2 backward dK/dV,
+// 3 backward dQ); 0 = none.
+struct Inject {
+  int kernel = 0;
+  uint64_t wait_ns = 0;
+};
+Inject g_inject;
+
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
 // Backward workspace: Delta [rows], LSE*log2(e) [rows], each section
@@ -146,6 +155,14 @@ attn_status bwd_common(const void* q, const void* k, const void* v, const void* 
   a.delta = reinterpret_cast<float*>(w);
   a.lse_log2 = reinterpret_cast<float*>(w + round_up((size_t)rows * 4, 256));
   a.rope_cs = rope_cs;
+  a.inject_kernel = 0;
+  a.inject_step = -1;
+  if (g_inject.kernel == 2 || g_inject.kernel == 3) {
+    a.inject_kernel = g_inject.kernel - 1;   // 1 dK/dV, 2 dQ
+    a.inject_step = 1;
+    a.wait_ns = g_inject.wait_ns;
+    g_inject.kernel = 0;
+  }
   const long grid = (long)a.n_items * num_seqs * Hkv;
   if (grid > 0x7fffffffL || rows > 0x7fffffffL || (long)a.num_seqs * Hq > 65535L * 65535L) return ATTN_ERR_SHAPE;
   const int bm = 128;   // query rows per step of both backward kernels
@@ -186,6 +203,12 @@ attn_status fwd_common(const void* q, const void* k, const void* v, void* o, flo
   const int mblocks = (rows + 127) / 128;
   a.m_items = a.pair_heads ? mblocks : (mblocks + 1) / 2;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.inject_step = -1;
+  if (g_inject.kernel == 1) {
+    a.inject_step = 1;
+    a.wait_ns = g_inject.wait_ns;
+    g_inject.kernel = 0;
+  }
   const long grid = (long)a.m_items * num_seqs * a.pairs_per_seq;
   if (grid <= 0) return ATTN_OK;
   if (grid > 0x7fffffffL) return ATTN_ERR_SHAPE;
@@ -828,6 +851,13 @@ attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const 
   if (!scratch) return ATTN_ERR_CUDA;
   return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, scratch, GQA_NOALLOC_SCRATCH_BYTES, B, Hq, Hkv, T, D, causal,
                   scale, stream);
+}
+
+attn_status attn_test_inject_timeout(int kernel, int limit_ms) {
+  if (kernel < 0 || kernel > 3 || limit_ms < 1 || limit_ms > 5000) return ATTN_ERR_SHAPE;
+  g_inject.kernel = kernel;
+  g_inject.wait_ns = (uint64_t)limit_ms * 1000000ull;
+  return ATTN_OK;
 }
 
 attn_status attn_selftest_wait_timeout(int limit_ms, void* stream) {

@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_it = a.G * per_head;
 
   KvBars& bars = *reinterpret_cast<KvBars*>(smem + C::kOffBars);
-  Guard guard{&bars.abort, a.status};
+  Guard guard{&bars.abort, a.status, a.inject_kernel == 1 ? a.wait_ns : kWaitLimitNs};
   if (threadIdx.x == 0) {
     bars.abort = 0;
     mbar_init(&bars.kv_full, 1);
@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int lastq[2] = {-1, -1}, lastd[2] = {-1, -1};
       for (int i = 0; i < n_it; ++i) {
+        if (a.inject_kernel == 1 && blockIdx.x == 0 && i == a.inject_step) break;   // failure-path test
         const int st = i & 1;
         const uint32_t ph = (i >> 1) & 1;
         const int h = it_head(i), mb = it_mb(i);
@@ -513,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_kb = a.causal ? mb + 1 : (L + 127) / 128;   // key blocks these queries see
 
   QBars& bars = *reinterpret_cast<QBars*>(smem + C::kOffBars);
-  Guard guard{&bars.abort, a.status};
+  Guard guard{&bars.abort, a.status, a.inject_kernel == 2 ? a.wait_ns : kWaitLimitNs};
   if (threadIdx.x == 0) {
     bars.abort = 0;
     mbar_init(&bars.q_full, 1);
@@ -556,6 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int lastk[3] = {-1, -1, -1}, lastv[2] = {-1, -1};
       for (int j = 0; j < n_kb; ++j) {
+        if (a.inject_kernel == 2 && blockIdx.x == 0 && j == a.inject_step) break;   // failure-path test
         if (a.varlen) { c1 = hkv; c2 = tok0 + j * 128; } else { c1 = j * 128; c2 = s * a.Hkv + hkv; }
         const int ks = j % 3, vs = j & 1;
         const uint32_t kph = (j / 3) & 1, vph = (j >> 1) & 1;

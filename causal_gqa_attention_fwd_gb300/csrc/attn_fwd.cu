@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  Guard guard{&bars.abort, args.status};
+  Guard guard{&bars.abort, args.status, args.inject_step >= 0 ? args.wait_ns : kWaitLimitNs};
 
   // ---------------------------------------------------------- work decode
   // blockIdx.x -> (row-block item, sequence/batch, head pair); heaviest
@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(384, 1)
       int idx = 0;
       bool ok = true;
       for (int j = 0; j < nkv && ok; ++j) {
+        if (blockIdx.x == 0 && j == args.inject_step) break;   // failure-path test: a load never issued
         for (int kv = 0; kv < 2 && ok; ++kv, ++idx) {
           const int st = idx % C::kStages;
           const uint32_t ph = (idx / C::kStages) & 1;

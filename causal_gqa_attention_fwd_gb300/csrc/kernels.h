@@ -26,6 +26,11 @@ struct FwdArgs {
   int pairs_per_seq;      // head pairs (pair_heads) or heads
   int m_items;            // row-block items per sequence
   float scale_log2;       // scale * log2(e)
+  // failure-path test only (attn_test_inject_timeout): when inject_step >= 0,
+  // CTA 0's producer stops before the load of that step and every wait of
+  // the launch gives up after wait_ns
+  int inject_step;
+  uint64_t wait_ns;
 };
 
 cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdArgs& a,
@@ -59,9 +64,15 @@ struct BwdArgs {
   int n_items;            // key-block items per sequence (max)
   float scale;
   float scale_log2;
-  // rotary backward (D = 128, f16 Q/K copies): [positions, D] cos/sin table;
-  // dK and dQ rows get the transposed rotation at their positions
+  // rotary backward (f16 Q/K copies): [positions, D] cos/sin table; dK and
+  // dQ rows get the transposed rotation at their positions
   const float* rope_cs;
+  // failure-path test only (attn_test_inject_timeout): in the kernel named by
+  // inject_kernel (1 dK/dV, 2 dQ), CTA 0's producer stops before the load of
+  // step inject_step and every wait gives up after wait_ns
+  int inject_kernel;
+  int inject_step;
+  uint64_t wait_ns;
 };
 
 // The preprocess, then the dK/dV and dQ kernels.  f16qk: q and k are the f16

@@ -69,8 +69,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Per-CTA failure state: a shared abort flag every role polls while waiting,
 // and the library's global status word (first failure code wins).
 struct Guard {
-  volatile int* abort;  // shared memory
-  int* status;          // global memory
+  volatile int* abort;                 // shared memory
+  int* status;                         // global memory
+  uint64_t limit_ns = kWaitLimitNs;    // per wait (shortened by the failure-path test only)
   __device__ __forceinline__ bool aborted() const { return *abort != 0; }
   __device__ void fail(int code) const {
     *abort = 1;
@@ -79,10 +80,10 @@ struct Guard {
 };
 
 // Wait for phase `parity` of `bar` to complete.  Returns false (after
-// flagging a timeout) if it does not within kWaitLimitNs, or if another role
-// of the CTA already gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Guard& g,
-                                          uint64_t limit_ns = kWaitLimitNs) {
+// flagging a timeout) if it does not within limit_ns (the guard's limit when
+// 0), or if another role of the CTA already gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Guard& g, uint64_t limit_ns = 0) {
+  if (limit_ns == 0) limit_ns = g.limit_ns;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {

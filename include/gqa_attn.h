@@ -316,6 +316,21 @@ GQA_ATTN_API attn_status attn_get_device_status(void* stream, int* out, int clea
  * faulted, and attn_get_device_status() then reports the timeout. */
 GQA_ATTN_API attn_status attn_selftest_wait_timeout(int limit_ms, void* stream);
 
+/* Failure-path test of the production kernels (no counterpart in the pages;
+ * not thread-safe).  Arms one injected failure for the next launch of one
+ * kernel: 1 the forward (attn_fwd and attn_fwd_rope), 2 the backward's dK/dV
+ * kernel, 3 the backward's dQ kernel (attn_bwd and its variants); 0 disarms.
+ * In that launch every bounded wait gives up after limit_ms (1..5000) instead
+ * of the usual 2 s, and the first CTA's TMA producer stops before the loads
+ * of its second step, so one of that CTA's waits expires.  The kernel then
+ * records ATTN_ERR_TIMEOUT in the device status word, its other roles see
+ * the CTA's abort flag and stop, the issued copies and MMAs are drained,
+ * TMEM is freed and the kernel returns: the GPU is neither hung nor faulted
+ * and the next call runs normally.  The failing CTA's outputs are left
+ * unwritten or partial; every other CTA completes.  The injection is
+ * consumed by the launch that takes it. */
+GQA_ATTN_API attn_status attn_test_inject_timeout(int kernel, int limit_ms);
+
 /* Kernel timing (instrumentation; not thread-safe).  While enabled, every
  * kernel launch is bracketed by a CUDA event pair recorded on the caller's
  * stream.  attn_profile_read synchronises those events and returns, for one

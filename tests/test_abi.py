@@ -131,6 +131,16 @@ def test_workspace_sizes(lib):
                                                                      lib.attn_bwd_workspace_size(2, 32, 8, 4096, 128))
 
 
+def test_inject_timeout_validation(lib):
+    # test-only failure injection: kernel 0 (none) .. 3, limit 1..5000 ms; arming is host state only
+    assert lib.attn_test_inject_timeout(4, 50) == 2
+    assert lib.attn_test_inject_timeout(-1, 50) == 2
+    assert lib.attn_test_inject_timeout(1, 0) == 2
+    assert lib.attn_test_inject_timeout(1, 6000) == 2
+    assert lib.attn_test_inject_timeout(2, 50) == 0
+    assert lib.attn_test_inject_timeout(0, 1) == 0            # disarm
+
+
 def test_status_strings(lib):
     import causal_gqa_attention_fwd_gb300 as g
     for code in range(12):

@@ -41,3 +41,35 @@ def test_selftest_rejects_bad_limits():
     lib = g.lib()
     assert lib.attn_selftest_wait_timeout(0, None) == 2
     assert lib.attn_selftest_wait_timeout(6000, None) == 2
+
+
+@pytest.mark.parametrize("kernel,name", [(1, "forward"), (2, "backward dK/dV"), (3, "backward dQ")])
+def test_production_kernel_wait_expires_and_next_call_is_clean(kernel, name):
+    """attn_test_inject_timeout makes one wait of a production kernel run out
+    (its first CTA's producer stops before its second step, waits limited to
+    50 ms): the launch must record ATTN_ERR_TIMEOUT and return -- drained and
+    with its TMEM freed, or the next launch on that SM could not allocate --
+    and the next normal call must reproduce a clean run bit for bit."""
+    import causal_gqa_attention_fwd_gb300 as g
+    from causal_gqa_attention_fwd_gb300 import workloads as W
+    lib = g.lib()
+    x = W.dense_inputs(1, 4, 2, 1024, 128, seed=kernel)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    scale = 1.0 / np.sqrt(128)
+
+    def run():
+        o, lse = g.attn_fwd(q, k, v, scale=scale)
+        dq, dk, dv = g.attn_bwd(q, k, v, o, lse, do, scale=scale)
+        return [t.clone() for t in (o, lse, dq, dk, dv)]
+
+    assert g.get_device_status() in (0, 9)             # clear anything earlier
+    ref = run()
+    assert g.get_device_status() == 0
+    assert lib.attn_test_inject_timeout(kernel, 50) == 0
+    run()
+    code = g.get_device_status(clear=True)
+    assert code == 9, f"{name}: {g.status_string(code)}"   # ATTN_ERR_TIMEOUT
+    again = run()
+    assert g.get_device_status() == 0
+    for a, b in zip(again, ref):
+        assert torch.equal(a, b), name
