@@ -206,6 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   float* stats = reinterpret_cast<float*>(smem + C::kOffStats);   // [stage][2][BM]
+  // the dQ kernel (launched next, programmatic dependent launch) reads
+  // nothing this grid writes: let its CTAs take SMs as this grid's finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   auto it_head = [&](int i) { return hkv * a.G + i / per_head; };
   auto it_mb = [&](int i) { return mb0 + i % per_head; };
 
@@ -778,10 +781,25 @@ static cudaError_t launch_split(const CUtensorMap& q, const CUtensorMap& k, cons
   prof_end(stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // dQ kernel: programmatic dependent launch.  It reads only the inputs and
+  // the preprocess's rows (complete before the dK/dV grid started) and
+  // writes only dQ, so it never waits on the dK/dV grid: its CTAs fill the
+  // SMs that grid leaves idle (its tail; all of a small grid's spare SMs).
   const long q_grid = (long)a.n_items * a.num_seqs * a.Hq;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)q_grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kQSmem<D>;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   prof_begin(kProfBwdDq, stream);
-  bwd_dq_kernel<D, F16><<<(unsigned)q_grid, kThreads, kQSmem<D>, stream>>>(q, k, v, dout, a);
+  e = cudaLaunchKernelEx(&cfg, bwd_dq_kernel<D, F16>, q, k, v, dout, a);
   prof_end(stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
