@@ -38,6 +38,7 @@ from ._binding import (  # noqa: F401
     attn_varlen_bwd_rope,
     attn_varlen_bwd_workspace_size,
     attn_varlen_fwd,
+    get_check_line,
     get_device_status,
     lib,
     profile_enable,

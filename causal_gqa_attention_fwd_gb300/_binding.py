@@ -14,11 +14,12 @@ import os
 import torch
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgqa_attn.so")
+DEBUG_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgqa_attn_debug.so")
 
 STATUS = {
     0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_SHAPE", 3: "ATTN_ERR_HEADDIM", 4: "ATTN_ERR_ALIGN",
     5: "ATTN_ERR_SEQLENS", 6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_ARCH", 8: "ATTN_ERR_CUDA",
-    9: "ATTN_ERR_TIMEOUT", 10: "ATTN_ERR_SCRATCH_LIMIT", 11: "ATTN_ERR_PAGES",
+    9: "ATTN_ERR_TIMEOUT", 10: "ATTN_ERR_SCRATCH_LIMIT", 11: "ATTN_ERR_PAGES", 12: "ATTN_ERR_CHECK",
 }
 
 # name -> (restype, argtypes)
@@ -40,6 +41,8 @@ SIGNATURES = {
     "attn_varlen_bwd": (_I, [_P] * 10 + [_Z, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_get_device_status": (_I, [_P, ctypes.POINTER(_I), _I]),
+    "attn_get_check_line": (_I, [_P, ctypes.POINTER(_I), _I]),
+    "attn_is_debug_build": (_I, []),
     "attn_bwd_noalloc": (_I, [_P] * 9 + [_I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_noalloc_scratch_bytes": (_Z, []),
     "attn_selftest_wait_timeout": (_I, [_I, _P]),
@@ -115,6 +118,13 @@ def _need(t: torch.Tensor, name: str, dtype=torch.bfloat16):
 
 def _scale(scale, D):
     return float(scale) if scale is not None else 1.0 / float(D) ** 0.5
+
+
+def get_check_line(clear: bool = True, stream=None) -> int:
+    """Debug build: synchronise and return (and clear) the source line of the first failed bounds check."""
+    out = ctypes.c_int(0)
+    _check(lib().attn_get_check_line(_stream(stream), ctypes.byref(out), int(clear)), "attn_get_check_line")
+    return out.value
 
 
 def get_device_status(clear: bool = True, stream=None) -> int:

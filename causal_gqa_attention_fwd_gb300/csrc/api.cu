@@ -18,8 +18,10 @@ namespace {
 using gqa::BwdArgs;
 using gqa::FwdArgs;
 
-// Per-device status word (first device-detected error since last cleared).
+// Per-device status word (first device-detected error since last cleared),
+// and, in debug builds, the source line of the first failed bounds check.
 __device__ int g_attn_status;
+__device__ int g_attn_check_line;
 
 constexpr int kMaxDevices = 64;
 
@@ -30,6 +32,17 @@ int* status_word() {
   if (dev < kMaxDevices && cache[dev]) return cache[dev];
   void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_attn_status) != cudaSuccess) return nullptr;
+  if (dev < kMaxDevices) cache[dev] = static_cast<int*>(p);
+  return static_cast<int*>(p);
+}
+
+int* check_line_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  static int* cache[kMaxDevices] = {};
+  if (dev < kMaxDevices && cache[dev]) return cache[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_attn_check_line) != cudaSuccess) return nullptr;
   if (dev < kMaxDevices) cache[dev] = static_cast<int*>(p);
   return static_cast<int*>(p);
 }
@@ -117,7 +130,7 @@ size_t ws_bytes(long rows, int D) {
 attn_status bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
                        const void* dout, void* dq, void* dk, void* dv, void* ws, const int* cu, int num_seqs,
                        int T, int total, int max_seqlen, int Hq, int Hkv, int D, int causal, float scale,
-                       void* stream, bool varlen, const float* rope_cs = nullptr) {
+                       void* stream, bool varlen, const float* rope_cs = nullptr, int n_table = 0) {
   // rope_cs: q and k are the f16 copies rotated at their positions by the
   // rotary table rope_cs; dQ and dK are taken back through the rotation
   const bool f16qk = rope_cs != nullptr;
@@ -151,10 +164,13 @@ attn_status bwd_common(const void* q, const void* k, const void* v, const void* 
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   const long rows = varlen ? (long)Hq * a.total_pad : (long)num_seqs * Hq * a.T_pad;
+  a.ws_rows = rows;
   char* w = static_cast<char*>(ws);
   a.delta = reinterpret_cast<float*>(w);
   a.lse_log2 = reinterpret_cast<float*>(w + round_up((size_t)rows * 4, 256));
   a.rope_cs = rope_cs;
+  a.n_table = n_table;
+  a.dbg_line = check_line_word();
   a.inject_kernel = 0;
   a.inject_step = -1;
   if (g_inject.kernel == 2 || g_inject.kernel == 3) {
@@ -203,6 +219,7 @@ attn_status fwd_common(const void* q, const void* k, const void* v, void* o, flo
   const int mblocks = (rows + 127) / 128;
   a.m_items = a.pair_heads ? mblocks : (mblocks + 1) / 2;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.dbg_line = check_line_word();
   a.inject_step = -1;
   if (g_inject.kernel == 1) {
     a.inject_step = 1;
@@ -512,7 +529,7 @@ attn_status attn_bwd_rope(const void* q, const void* k, const void* v, const voi
   if (gqa::launch_rope_qk_f16(q, k, wq, wk, rr, D, rope_cos_sin, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
   return bwd_common(wq, wk, v, o, lse, dout, dq, dk, dv, wb, nullptr, B, T, 0, 0, Hq, Hkv, D, causal, scale, stream,
-                    false, rope_cos_sin);
+                    false, rope_cos_sin, rope_positions);
 }
 
 size_t attn_varlen_bwd_rope_workspace_size(int num_seqs, int total_tokens, int Hq, int Hkv, int D) {
@@ -558,7 +575,7 @@ attn_status attn_varlen_bwd_rope(const void* q, const void* k, const void* v, co
   if (gqa::launch_rope_qk_f16(q, k, wq, wk, rr, D, rope_cos_sin, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
   return bwd_common(wq, wk, v, o, lse, dout, dq, dk, dv, wb, cu_seqlens, num_seqs, 0, total_tokens, max_seqlen, Hq,
-                    Hkv, D, causal, scale, stream, true, rope_cos_sin);
+                    Hkv, D, causal, scale, stream, true, rope_cos_sin, rope_positions);
 }
 
 }  // extern "C"
@@ -886,8 +903,32 @@ const char* attn_status_string(attn_status s) {
     case ATTN_ERR_SCRATCH_LIMIT:
       return "the problem needs more backward scratch than attn_bwd_noalloc's built-in array holds";
     case ATTN_ERR_PAGES: return "a block-table entry names no page of the pool";
+    case ATTN_ERR_CHECK: return "a bounds check of the debug build failed (attn_get_check_line gives its line)";
   }
   return "unknown status";
+}
+
+attn_status attn_get_check_line(void* stream, int* out, int clear) {
+  if (!out) return ATTN_ERR_NULL;
+  int* w = check_line_word();
+  if (!w) return ATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (clear && v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(w, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  *out = v;
+  return ATTN_OK;
+}
+
+int attn_is_debug_build(void) {
+#ifdef GQA_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 attn_status attn_get_device_status(void* stream, int* out, int clear) {

@@ -47,8 +47,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
       const int p = blockIdx.x * 128 + base + u * kRowsPerPass + sub;
       prow[u] = p;
       acc[u] = 0.f;
-      if (p < L) {
-        const long off = row_off(a, s, tok0, h, a.Hq, p, D) + part * 8;
+      const long off = row_off(a, s, tok0, h, a.Hq, p, D) + part * 8;
+      if (p < L && GQA_CHECK(off >= 0 && off + 8 <= elems(a, a.Hq), a.status, a.dbg_line)) {
         const uint4 ov = *reinterpret_cast<const uint4*>(a.o + off);
         const uint4 gv = *reinterpret_cast<const uint4*>(a.dout + off);
         const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
@@ -68,10 +68,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
       const int p = prow[u];
       if (p >= Lr) continue;
       const long w = ws_row(a, s, tok0, h, p);
-      if (part == 0) {
+      if (part == 0 && GQA_CHECK(w >= 0 && w < a.ws_rows, a.status, a.dbg_line)) {
         float dl = 0.f, l2 = -INFINITY;       // stored negated: -Delta, -LSE*log2(e)
-        if (p < L) {
-          const long li = a.varlen ? (long)h * a.total + tok0 + p : ((long)s * a.Hq + h) * a.T + p;
+        const long li = a.varlen ? (long)h * a.total + tok0 + p : ((long)s * a.Hq + h) * a.T + p;
+        if (p < L && GQA_CHECK(li >= 0 && li < elems(a, a.Hq) / a.D, a.status, a.dbg_line)) {
           dl = -acc[u];
           l2 = -a.lse[li] * 1.4426950408889634f;
         }

@@ -220,10 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int c1, c2;
       if (a.varlen) { c1 = hkv; c2 = tok0 + k0; } else { c1 = k0; c2 = s * a.Hkv + hkv; }
       mbar_expect_tx(&bars.kv_full, 2 * kTile);
-      for (int b = 0; b < NB; ++b) {
-        tma_load_3d(smem + C::kOffK + b * kBox, &tm_k, &bars.kv_full, b * 64, c1, c2);
-        tma_load_3d(smem + C::kOffV + b * kBox, &tm_v, &bars.kv_full, b * 64, c1, c2);
-      }
+      if (GQA_CHECK(tile_ok(a, a.Hkv, c1, c2), a.status, a.dbg_line))
+        for (int b = 0; b < NB; ++b) {
+          tma_load_3d(smem + C::kOffK + b * kBox, &tm_k, &bars.kv_full, b * 64, c1, c2);
+          tma_load_3d(smem + C::kOffV + b * kBox, &tm_v, &bars.kv_full, b * 64, c1, c2);
+        }
       int lastq[2] = {-1, -1}, lastd[2] = {-1, -1};
       for (int i = 0; i < n_it; ++i) {
         if (a.inject_kernel == 1 && blockIdx.x == 0 && i == a.inject_step) break;   // failure-path test
@@ -233,11 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a.varlen) { c1 = h; c2 = tok0 + mb * BM; } else { c1 = mb * BM; c2 = s * a.Hq + h; }
         if (!mbar_wait(&bars.q_empty[st], ph ^ 1, guard)) break;
         mbar_expect_tx(&bars.q_full[st], kTile + 2 * kStatBytes);
-        for (int b = 0; b < NB; ++b)
-          tma_load_3d(smem + C::kOffQ + st * kTile + b * kBox, &tm_q, &bars.q_full[st], b * 64, c1, c2);
         const long w = ws_row(a, s, tok0, h, mb * BM);
-        bulk_load(stats + st * 2 * BM, a.lse_log2 + w, kStatBytes, &bars.q_full[st]);
-        bulk_load(stats + st * 2 * BM + BM, a.delta + w, kStatBytes, &bars.q_full[st]);
+        if (GQA_CHECK(tile_ok(a, a.Hq, c1, c2) && w >= 0 && w + BM <= a.ws_rows, a.status, a.dbg_line)) {
+          for (int b = 0; b < NB; ++b)
+            tma_load_3d(smem + C::kOffQ + st * kTile + b * kBox, &tm_q, &bars.q_full[st], b * 64, c1, c2);
+          bulk_load(stats + st * 2 * BM, a.lse_log2 + w, kStatBytes, &bars.q_full[st]);
+          bulk_load(stats + st * 2 * BM + BM, a.delta + w, kStatBytes, &bars.q_full[st]);
+        }
         lastq[st] = (int)ph;
         if (!mbar_wait(&bars.do_empty[st], ph ^ 1, guard)) break;
         mbar_expect_tx(&bars.do_full[st], kTile);
@@ -437,7 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence<32>(reinterpret_cast<uint32_t*>(lo));
         reg_fence<32>(reinterpret_cast<uint32_t*>(hi));
         if (wg == 0) {
-          if (F16 && key < L) rope_grad_transpose<D, 32>(lo, hi, a.rope_cs, key, q * 32);
+          if (F16 && key < L && GQA_CHECK(key < a.n_table, a.status, a.dbg_line))
+            rope_grad_transpose<D, 32>(lo, hi, a.rope_cs, key, q * 32);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             lo[e] *= a.scale;
@@ -465,9 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sb = smem_u32(tile);
       for (int idx = lane; idx < 32 * kChunks; idx += 32) {
         const int row = row0 + idx / kChunks, cch = idx % kChunks;
-        if (row < rows_valid) {
+        const long off = row_off(a, s, tok0, hkv, a.Hkv, k0 + row, D) + cch * 8;
+        if (row < rows_valid && GQA_CHECK(off >= 0 && off + 8 <= elems(a, a.Hkv), a.status, a.dbg_line)) {
           const uint4 val = ld_shared_v4(sb + row * (2 * D) + ((cch ^ (row & 7)) << 4));
-          *reinterpret_cast<uint4*>(dst + row_off(a, s, tok0, hkv, a.Hkv, k0 + row, D) + cch * 8) = val;
+          *reinterpret_cast<uint4*>(dst + off) = val;
         }
       }
     }
@@ -554,10 +559,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int c1, c2;
       if (a.varlen) { c1 = h; c2 = tok0 + q0; } else { c1 = q0; c2 = s * a.Hq + h; }
       mbar_expect_tx(&bars.q_full, 2 * kTile);
-      for (int b = 0; b < NB; ++b) {
-        tma_load_3d(smem + C::kOffQ + b * kBox, &tm_q, &bars.q_full, b * 64, c1, c2);
-        tma_load_3d(smem + C::kOffDO + b * kBox, &tm_do, &bars.q_full, b * 64, c1, c2);
-      }
+      if (GQA_CHECK(tile_ok(a, a.Hq, c1, c2), a.status, a.dbg_line))
+        for (int b = 0; b < NB; ++b) {
+          tma_load_3d(smem + C::kOffQ + b * kBox, &tm_q, &bars.q_full, b * 64, c1, c2);
+          tma_load_3d(smem + C::kOffDO + b * kBox, &tm_do, &bars.q_full, b * 64, c1, c2);
+        }
       int lastk[3] = {-1, -1, -1}, lastv[2] = {-1, -1};
       for (int j = 0; j < n_kb; ++j) {
         if (a.inject_kernel == 2 && blockIdx.x == 0 && j == a.inject_step) break;   // failure-path test
@@ -566,13 +572,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kph = (j / 3) & 1, vph = (j >> 1) & 1;
         if (!mbar_wait(&bars.k_empty[ks], kph ^ 1, guard)) break;
         mbar_expect_tx(&bars.k_full[ks], kTile);
-        for (int b = 0; b < NB; ++b)
-          tma_load_3d(smem + C::kOffK + ks * kTile + b * kBox, &tm_k, &bars.k_full[ks], b * 64, c1, c2);
+        const bool kv_ok = GQA_CHECK(tile_ok(a, a.Hkv, c1, c2), a.status, a.dbg_line);
+        if (kv_ok)
+          for (int b = 0; b < NB; ++b)
+            tma_load_3d(smem + C::kOffK + ks * kTile + b * kBox, &tm_k, &bars.k_full[ks], b * 64, c1, c2);
         lastk[ks] = (int)kph;
         if (!mbar_wait(&bars.v_empty[vs], vph ^ 1, guard)) break;
         mbar_expect_tx(&bars.v_full[vs], kTile);
-        for (int b = 0; b < NB; ++b)
-          tma_load_3d(smem + C::kOffV + vs * kTile + b * kBox, &tm_v, &bars.v_full[vs], b * 64, c1, c2);
+        if (kv_ok)
+          for (int b = 0; b < NB; ++b)
+            tma_load_3d(smem + C::kOffV + vs * kTile + b * kBox, &tm_v, &bars.v_full[vs], b * 64, c1, c2);
         lastv[vs] = (int)vph;
       }
       mbar_wait_drain(&bars.q_full, 0);
@@ -655,8 +664,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float c = a.scale_log2;
     const long wrow = ws_row(a, s, tok0, h, qi);
-    const float nlse2 = a.lse_log2[wrow];              // -LSE*log2(e) (-inf past the sequence)
-    const float ndl = a.delta[wrow];                   // -Delta
+    const bool wrow_ok = GQA_CHECK(wrow >= 0 && wrow < a.ws_rows, a.status, a.dbg_line);
+    const float nlse2 = wrow_ok ? a.lse_log2[wrow] : -INFINITY;   // -LSE*log2(e) (-inf past the sequence)
+    const float ndl = wrow_ok ? a.delta[wrow] : 0.f;              // -Delta
     const uint64_t c2 = f2(c, c), nl2 = f2(nlse2, nlse2), nd2 = f2(ndl, ndl);
     bool ok = true;
     for (int j = 0; j < n_kb; ++j) {
@@ -723,7 +733,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       reg_fence<NP>(reinterpret_cast<uint32_t*>(lo));
       reg_fence<NP>(reinterpret_cast<uint32_t*>(hi));
-      if (F16 && qi < L) rope_grad_transpose<D, NP>(lo, hi, a.rope_cs, qi, NP * wg);
+      if (F16 && qi < L && GQA_CHECK(qi < a.n_table, a.status, a.dbg_line))
+        rope_grad_transpose<D, NP>(lo, hi, a.rope_cs, qi, NP * wg);
       const uint32_t srow = smem_u32(smem + C::kOffQ) + r * (2 * D);   // the Q tile is dead: every MMA has completed
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -746,9 +757,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int idx = lane; idx < 32 * kMine; idx += 32) {
         const int row = row0 + idx / kMine, k8 = idx % kMine;
         const int cch = (k8 / (NP / 8)) * (D / 16) + wg * (NP / 8) + k8 % (NP / 8);
-        if (row < rows_valid) {
+        const long off = row_off(a, s, tok0, h, a.Hq, q0 + row, D) + cch * 8;
+        if (row < rows_valid && GQA_CHECK(off >= 0 && off + 8 <= elems(a, a.Hq), a.status, a.dbg_line)) {
           const uint4 val = ld_shared_v4(sbase + row * (2 * D) + ((cch ^ (row & 7)) << 4));
-          *reinterpret_cast<uint4*>(a.dq + row_off(a, s, tok0, h, a.Hq, q0 + row, D) + cch * 8) = val;
+          *reinterpret_cast<uint4*>(a.dq + off) = val;
         }
       }
     }

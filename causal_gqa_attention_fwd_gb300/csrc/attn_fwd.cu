@@ -168,6 +168,12 @@ __global__ void __launch_bounds__(384, 1)
       c2 = seq * nheads_b + head;
     }
   };
+  // debug builds: a tile's start lies inside its tensor map
+  auto tile_ok = [&](int nheads_b, int c1, int c2) {
+    return args.varlen ? (c1 >= 0 && c1 < nheads_b && c2 >= 0 && c2 < args.total)
+                       : (c1 >= 0 && c1 < args.T && c2 >= 0 && c2 < args.num_seqs * nheads_b);
+  };
+  (void)tile_ok;
 
   if (warp == 0) {
     // ======================================================== TMA producer
@@ -180,8 +186,9 @@ __global__ void __launch_bounds__(384, 1)
         int c1, c2;
         coords(ti[x].hq, args.Hq, ti[x].mb * kBM, c1, c2);
         mbar_expect_tx(&bars.q_full[x], C::kTileBytes);
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(sQ + x * C::kTileBytes + b * C::kBoxBytes, &tm_q, &bars.q_full[x], b * 64, c1, c2);
+        if (GQA_CHECK(tile_ok(args.Hq, c1, c2), args.status, args.dbg_line))
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(sQ + x * C::kTileBytes + b * C::kBoxBytes, &tm_q, &bars.q_full[x], b * 64, c1, c2);
       }
       int last_phase[8];
       for (int s = 0; s < 8; ++s) last_phase[s] = -1;
@@ -198,8 +205,9 @@ __global__ void __launch_bounds__(384, 1)
           uint8_t* dst = sRing + st * C::kTileBytes;
           mbar_expect_tx(&bars.kv_full[st], C::kTileBytes);
           const CUtensorMap* tm = kv == 0 ? &tm_k : &tm_v;
-          for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(dst + b * C::kBoxBytes, tm, &bars.kv_full[st], b * 64, c1, c2);
+          if (GQA_CHECK(tile_ok(args.Hkv, c1, c2), args.status, args.dbg_line))
+            for (int b = 0; b < C::kBoxes; ++b)
+              tma_load_3d(dst + b * C::kBoxBytes, tm, &bars.kv_full[st], b * 64, c1, c2);
           last_phase[st] = (int)ph;
         }
       }
@@ -394,7 +402,8 @@ __global__ void __launch_bounds__(384, 1)
           const float lse = (m_run + __log2f(l_run)) * 0.69314718055994531f;
           const long li = args.varlen ? (long)t.hq * args.total + tok0 + qi
                                       : ((long)seq * args.Hq + t.hq) * args.T + qi;
-          args.lse[li] = lse;
+          const long n_lse = args.varlen ? (long)args.Hq * args.total : (long)args.num_seqs * args.Hq * args.T;
+          if (GQA_CHECK(li >= 0 && li < n_lse, args.status, args.dbg_line)) args.lse[li] = lse;
         }
         __syncwarp();
         // coalesced copy of this warp's 32 rows (those inside the sequence)
@@ -413,7 +422,10 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll 4
         for (int idx = lane; idx < 32 * kChunks; idx += 32) {
           const int row = row0 + idx / kChunks, cch = idx % kChunks;
-          if (row < rows_valid) {
+          const long n_o = (args.varlen ? (long)args.total : (long)args.num_seqs * args.T) * args.Hq * D;
+          if (row < rows_valid &&
+              GQA_CHECK(obase + row * ors + cch * 8 >= args.o && obase + row * ors + cch * 8 + 8 <= args.o + n_o,
+                        args.status, args.dbg_line)) {
             const uint4 v = ld_shared_v4(sbase + row * (D * 2) + ((cch ^ (row & 7)) << 4));
             *reinterpret_cast<uint4*>(obase + row * ors + cch * 8) = v;
           }

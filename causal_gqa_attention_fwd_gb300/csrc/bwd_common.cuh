@@ -44,5 +44,16 @@ __device__ __forceinline__ long row_off(const BwdArgs& a, int s, int tok0, int h
 }
 
 
+// Bounds used by the debug build's checks: elements of a [.., H, .., D]
+// tensor, and whether a tile's start coordinates (c1, c2) lie inside its
+// tensor map (dense (D, T, num_seqs*H); packed (D, H, total)).
+__device__ __forceinline__ long elems(const BwdArgs& a, int H) {
+  return a.varlen ? (long)a.total * H * a.D : (long)a.num_seqs * H * a.T * a.D;
+}
+__device__ __forceinline__ bool tile_ok(const BwdArgs& a, int H, int c1, int c2) {
+  return a.varlen ? (c1 >= 0 && c1 < H && c2 >= 0 && c2 < a.total)
+                  : (c1 >= 0 && c1 < a.T && c2 >= 0 && c2 < a.num_seqs * H);
+}
+
 }  // namespace bwd
 }  // namespace gqa

@@ -31,6 +31,7 @@ struct FwdArgs {
   // the launch gives up after wait_ns
   int inject_step;
   uint64_t wait_ns;
+  int* dbg_line;          // debug builds: source line of the first failed bounds check
 };
 
 cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdArgs& a,
@@ -73,6 +74,9 @@ struct BwdArgs {
   int inject_kernel;
   int inject_step;
   uint64_t wait_ns;
+  long ws_rows;           // rows of each workspace section (bounds of the debug build)
+  int n_table;            // rows of rope_cs
+  int* dbg_line;          // debug builds: source line of the first failed bounds check
 };
 
 // The preprocess, then the dK/dV and dQ kernels.  f16qk: q and k are the f16

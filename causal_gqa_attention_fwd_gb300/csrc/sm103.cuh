@@ -17,8 +17,25 @@
 namespace gqa {
 
 // Device status word values (mirrors attn_status in include/gqa_attn.h).
-// kDevInternal (ATTN_ERR_CUDA): a kernel's own layout check failed.
-enum : int { kDevOk = 0, kDevTimeout = 9, kDevBadSeqlens = 5, kDevInternal = 8 };
+// kDevInternal (ATTN_ERR_CUDA): a kernel's own layout check failed;
+// kDevCheck (ATTN_ERR_CHECK): a bounds check of the debug build failed.
+enum : int { kDevOk = 0, kDevTimeout = 9, kDevBadSeqlens = 5, kDevInternal = 8, kDevCheck = 12 };
+
+// Debug builds (-DGQA_DEBUG): explicit bounds checks of computed global,
+// shared-memory and tensor-map indices, GQA_CHECK(cond, status, line_word).
+// A failed check records ATTN_ERR_CHECK in the status word and the source
+// line in the debug line word, and the guarded access is skipped; nothing
+// traps.  Release builds compile every check to `true` (cond unevaluated).
+#ifdef GQA_DEBUG
+__device__ __noinline__ inline bool debug_check_failed(int* status, int* where, int line) {
+  if (where) atomicCAS(where, 0, line);
+  atomicCAS(status, 0, kDevCheck);
+  return false;
+}
+#define GQA_CHECK(cond, status, where) ((cond) || ::gqa::debug_check_failed((status), (where), __LINE__))
+#else
+#define GQA_CHECK(cond, status, where) true
+#endif
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 

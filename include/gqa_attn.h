@@ -68,7 +68,8 @@ typedef enum {
     ATTN_ERR_CUDA = 8,       /* a CUDA runtime call failed (launch, tensor map, attribute) */
     ATTN_ERR_TIMEOUT = 9,    /* device-detected: a bounded in-kernel wait expired */
     ATTN_ERR_SCRATCH_LIMIT = 10, /* attn_bwd_noalloc: sizes need more than its built-in scratch */
-    ATTN_ERR_PAGES = 11      /* device-detected: a block-table entry names no page of the pool */
+    ATTN_ERR_PAGES = 11,     /* device-detected: a block-table entry names no page of the pool */
+    ATTN_ERR_CHECK = 12      /* device-detected, debug build only: a bounds check of a computed index failed */
 } attn_status;
 
 /* Forward, dense layout.  Writes O (bf16) and LSE (float32). */
@@ -307,6 +308,17 @@ GQA_ATTN_API const char* attn_status_string(attn_status status);
  * cleared); clears it when clear != 0.  Returns ATTN_ERR_CUDA if the copy
  * fails (e.g. a sticky CUDA error), else ATTN_OK. */
 GQA_ATTN_API attn_status attn_get_device_status(void* stream, int* out, int clear);
+
+/* Debug build (libgqa_attn_debug.so, compiled with -DGQA_DEBUG; no
+ * counterpart in the pages): the kernels check every computed tensor-map
+ * coordinate, global row offset, workspace row and rotary-table row against
+ * its bounds before the access; a failed check skips the access, records
+ * ATTN_ERR_CHECK in the status word and its source line in a second word.
+ * attn_get_check_line synchronises `stream` and reads (and clears when
+ * clear != 0) that line: 0 when no check failed, always 0 in the release
+ * build.  attn_is_debug_build returns 1 in the debug build, 0 otherwise. */
+GQA_ATTN_API attn_status attn_get_check_line(void* stream, int* out, int clear);
+GQA_ATTN_API int attn_is_debug_build(void);
 
 /* Failure-path self-test (no counterpart in the pages).  Launches one small
  * kernel that waits, through the library's bounded in-kernel wait, on a

@@ -141,9 +141,19 @@ def test_inject_timeout_validation(lib):
     assert lib.attn_test_inject_timeout(0, 1) == 0            # disarm
 
 
+def test_debug_build_exports_the_same_symbols(lib):
+    from causal_gqa_attention_fwd_gb300 import build
+    dbg = ctypes.CDLL(build.build(debug=True))
+    for n in declared_functions():
+        assert hasattr(dbg, n), f"{n} not exported by the debug build"
+    dbg.attn_is_debug_build.restype = ctypes.c_int
+    assert dbg.attn_is_debug_build() == 1
+    assert lib.attn_is_debug_build() == 0
+
+
 def test_status_strings(lib):
     import causal_gqa_attention_fwd_gb300 as g
-    for code in range(12):
+    for code in range(13):
         s = g.status_string(code)
         assert s and s != "unknown status"
     assert g.status_string(99) == "unknown status"
