@@ -108,6 +108,13 @@ struct __align__(8) QBars {
 template <int D>
 constexpr int kQSmem = QCfg<D>::kOffBars + (int)sizeof(QBars);
 static_assert(kKvSmem<128> <= 232448 && kQSmem<128> <= 232448, "shared memory budget");
+// TMEM layouts fit the 512 columns the kernels allocate
+static_assert(KvCfg<128>::kColDV + 128 <= 512 && KvCfg<64>::kColDV + 64 <= 512, "dK/dV TMEM layout");
+static_assert(QCfg<128>::kColDQ + 128 <= 512 && QCfg<64>::kColDQ + 64 <= 512, "dQ TMEM layout");
+static_assert(KvCfg<128>::kColDP + 128 <= KvCfg<128>::kColDK && QCfg<128>::kColS + 256 <= QCfg<128>::kColDP,
+              "TMEM regions do not overlap");
+// shared-memory tiles stay 1024-byte aligned (the 128-byte swizzle is address-based)
+static_assert(kTileOf<64> % 1024 == 0 && kBox % 1024 == 0 && KvCfg<128>::kOffStats % 1024 == 0, "tile alignment");
 
 // Rotary transpose for the gradient of a rotated row at position pos (the
 // rotation took x to x'_i = x_i c - x_{i+D/2} s, x'_{i+D/2} = x_{i+D/2} c + x_i s):

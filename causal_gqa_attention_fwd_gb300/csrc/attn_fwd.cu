@@ -59,6 +59,9 @@ struct FwdCfg {
   static constexpr uint32_t kIdescPV = idesc_bf16(kBM, D, false, true);
 };
 
+// TMEM layout (S_A, S_B, O_A, O_B) fits the 512 columns the kernel allocates
+static_assert(256 + 2 * 128 <= 512, "forward TMEM layout");
+
 struct __align__(8) FwdBarriers {
   uint64_t q_full[2];
   uint64_t kv_full[8];
