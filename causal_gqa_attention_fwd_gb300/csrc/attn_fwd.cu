@@ -160,6 +160,11 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
+  // Register split (launched 384 x 168 = 64512), set at the top of each
+  // role: the control warpgroup (warps 0-3) keeps 64, the two softmax
+  // warpgroups take 216 each, so a softmax thread holds its whole 128-column
+  // score row without spilling: 128*64 + 256*216 = 63488 <= 64512, and per
+  // sub-partition (warps w, w+4, w+8) 32*(64 + 216 + 216) = 15872 <= 16384.
 
   // Coordinates of a 128-row tile in a Q / K / V tensor map.
   auto coords = [&](int head, int nheads_b, int row0, int& c1, int& c2) {
@@ -180,6 +185,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0) {
     // ======================================================== TMA producer
+    regs_dec<64>();
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -222,6 +228,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     // ============================================ MMA issuer (whole warp, one lane issues)
+    regs_dec<64>();
     {
       bool ok = true;
       for (int x = 0; x < 2 && ok; ++x)
@@ -288,8 +295,11 @@ __global__ void __launch_bounds__(384, 1)
       tc_commit_warp(&bars.teardown);
       mbar_wait_drain(&bars.teardown, 0);
     }
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
+    regs_dec<64>();                         // idle: registers go to the softmax warpgroups
+  } else {
     // ============================================================ softmax
+    regs_inc<216>();
     const int x = (warp - 4) >> 2;          // tile
     const int r = threadIdx.x & 127;        // row within the tile
     const TileInfo t = ti[x];

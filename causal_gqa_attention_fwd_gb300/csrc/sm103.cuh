@@ -276,6 +276,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 // carries into the next field.
 __device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
 
+// Warpgroup register reallocation (all 128 threads of a warpgroup execute it
+// together).  The kernels that use it launch 384 threads at 168 registers
+// (64512 in all) and move registers from the control warpgroup to the two
+// compute warpgroups; each use states the split it takes against that total.
+template <int N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+
 // ---- TMEM <-> registers.  32x32b shape: thread t of a warp reads/writes TMEM
 // lane (32 * (warp % 4) + t); the lane offset is encoded in taddr[31:16].
 #define GQA_R8(p) "=r"(p[0]), "=r"(p[1]), "=r"(p[2]), "=r"(p[3]), "=r"(p[4]), "=r"(p[5]), "=r"(p[6]), "=r"(p[7])
