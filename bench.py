@@ -675,8 +675,8 @@ def main():
     ms_per_step = total_ms / args.steps
     value = whole_job_tflops(world, f_fwd + f_bwd, args.steps, total_ms)
     n_fwd, t_fwd = prof["attn_fwd"]
-    n_main, t_main = prof["bwd_main"]
-    bwd_ms = sum(prof[k][1] for k in ("bwd_pre", "bwd_main", "bwd_dq")) / args.steps
+    n_main, t_main = prof["bwd_dkdv"]
+    bwd_ms = sum(prof[k][1] for k in ("bwd_pre", "bwd_dkdv", "bwd_dq")) / args.steps
     fwd_ms = t_fwd / max(n_fwd, 1)
     pk = peaks()
     gpu_launches = sum(prof[k][0] for k in prof)
@@ -688,7 +688,7 @@ def main():
     main_ms = t_main / max(n_main, 1)
     main_flops = f_bwd * 0.8
     achieved = main_flops / (main_ms / 1e3) / 1e12
-    roofline_traffic = measured_traffic(w.name, "bwd_main")
+    roofline_traffic = measured_traffic(w.name, "bwd_dkdv")
     roofline = {"kernel": "bwd_dkdv", "bound": "tensor", "achieved": achieved,
                 "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
                 "traffic": roofline_traffic, "peak_source": pk["source"] + " (burst bf16)",

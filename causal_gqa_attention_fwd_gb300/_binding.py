@@ -57,7 +57,7 @@ SIGNATURES = {
     "attn_decode_paged_fp8_fwd": (_I, [_P, _P, _P, _F, _F] + [_P] * 5 + [_Z] + [_I] * 8 + [_F, _P, _I, _P]),
 }
 
-PROFILE_KINDS = {"attn_fwd": 0, "bwd_pre": 1, "bwd_main": 2, "decode": 4, "decode_merge": 5, "bwd_dq": 6}
+PROFILE_KINDS = {"attn_fwd": 0, "bwd_pre": 1, "bwd_dkdv": 2, "decode": 4, "decode_merge": 5, "bwd_dq": 6}
 
 _lib = None
 

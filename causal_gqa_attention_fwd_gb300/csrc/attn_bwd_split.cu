@@ -795,7 +795,7 @@ static cudaError_t launch_split(const CUtensorMap& q, const CUtensorMap& k, cons
     attr_set[dev] = true;
   }
   const long kv_grid = (long)a.n_items * a.num_seqs * a.Hkv;
-  prof_begin(kProfBwdMain, stream);
+  prof_begin(kProfBwdDkdv, stream);
   bwd_dkdv_kernel<D, F16><<<(unsigned)kv_grid, kThreads, kKvSmem<D>, stream>>>(q, k, v, dout, a);
   prof_end(stream);
   cudaError_t e = cudaGetLastError();

@@ -137,7 +137,7 @@ cudaError_t launch_attn_decode(const CUtensorMap& k, const CUtensorMap& v, const
 enum ProfKind {
   kProfFwd = 0,
   kProfBwdPre = 1,
-  kProfBwdMain = 2,
+  kProfBwdDkdv = 2,
   kProfUnused3 = 3,
   kProfDecode = 4,
   kProfDecodeMerge = 5,
