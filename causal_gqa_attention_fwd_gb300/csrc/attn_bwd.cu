@@ -24,12 +24,18 @@ using namespace bwd;
 // ================================================================ preprocess
 // grid: (row blocks of 128, num_seqs * Hq); 256 threads.  A row is handled by
 // D/8 lanes (16 bytes of O and of dO each); a warp covers 32/(D/8) rows per
-// pass and keeps four passes of loads in flight.
-template <int D>
+// pass and issues all P passes' loads before it uses any.  P = 4 (31
+// registers, eight CTAs per SM) suits grids of several waves; a grid that
+// fits in one wave at two CTAs per SM takes P = 8 at D = 128 (one sweep of
+// the CTA's 128 rows, 256 bytes in flight per thread), so that its few CTAs
+// per SM still keep enough bytes in flight.
+template <int D, int P>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
   constexpr int kLanesPerRow = D / 8;
   constexpr int kRowsPerPass = 32 / kLanesPerRow;            // per warp
-  constexpr int kPasses = 4;
+  static_assert(128 % (8 * kRowsPerPass * P) == 0, "sweeps tile the row block");
+  griddep_wait();      // O (and dO) may come from the previous grid
+  griddep_launch();
   const int s = blockIdx.y / a.Hq, h = blockIdx.y % a.Hq;
   int tok0, L;
   if (!seq_bounds(a, s, tok0, L)) {
@@ -39,40 +45,40 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
   const int Lr = (L + 127) & ~127;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane / kLanesPerRow, part = lane % kLanesPerRow;
-  for (int base = warp * kRowsPerPass * kPasses; base < 128; base += 8 * kRowsPerPass * kPasses) {
-    float acc[kPasses];
-    int prow[kPasses];
+  for (int base = warp * kRowsPerPass * P; base < 128; base += 8 * kRowsPerPass * P) {
+    uint4 ov[P], gv[P];
 #pragma unroll
-    for (int u = 0; u < kPasses; ++u) {
+    for (int u = 0; u < P; ++u) {
       const int p = blockIdx.x * 128 + base + u * kRowsPerPass + sub;
-      prow[u] = p;
-      acc[u] = 0.f;
+      ov[u] = make_uint4(0, 0, 0, 0);
+      gv[u] = make_uint4(0, 0, 0, 0);
       const long off = row_off(a, s, tok0, h, a.Hq, p, D) + part * 8;
       if (p < L && GQA_CHECK(off >= 0 && off + 8 <= elems(a, a.Hq), a.status, a.dbg_line)) {
-        const uint4 ov = *reinterpret_cast<const uint4*>(a.o + off);
-        const uint4 gv = *reinterpret_cast<const uint4*>(a.dout + off);
-        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 of = __bfloat1622float2(o2[e]), gf = __bfloat1622float2(g2[e]);
-          acc[u] = fmaf(of.x, gf.x, acc[u]);
-          acc[u] = fmaf(of.y, gf.y, acc[u]);
-        }
+        ov[u] = *reinterpret_cast<const uint4*>(a.o + off);
+        gv[u] = *reinterpret_cast<const uint4*>(a.dout + off);
       }
     }
 #pragma unroll
-    for (int u = 0; u < kPasses; ++u) {
+    for (int u = 0; u < P; ++u) {
+      float acc = 0.f;
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[u]);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv[u]);
 #pragma unroll
-      for (int m = kLanesPerRow / 2; m > 0; m >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], m);
-      const int p = prow[u];
+      for (int e = 0; e < 4; ++e) {
+        const float2 of = __bfloat1622float2(o2[e]), gf = __bfloat1622float2(g2[e]);
+        acc = fmaf(of.x, gf.x, acc);
+        acc = fmaf(of.y, gf.y, acc);
+      }
+#pragma unroll
+      for (int m = kLanesPerRow / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+      const int p = blockIdx.x * 128 + base + u * kRowsPerPass + sub;
       if (p >= Lr) continue;
       const long w = ws_row(a, s, tok0, h, p);
       if (part == 0 && GQA_CHECK(w >= 0 && w < a.ws_rows, a.status, a.dbg_line)) {
         float dl = 0.f, l2 = -INFINITY;       // stored negated: -Delta, -LSE*log2(e)
         const long li = a.varlen ? (long)h * a.total + tok0 + p : ((long)s * a.Hq + h) * a.T + p;
         if (p < L && GQA_CHECK(li >= 0 && li < elems(a, a.Hq) / a.D, a.status, a.dbg_line)) {
-          dl = -acc[u];
+          dl = -acc;
           l2 = -a.lse[li] * 1.4426950408889634f;
         }
         a.delta[w] = dl;
@@ -84,11 +90,27 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
 
 template <int D>
 static cudaError_t launch_pre(const BwdArgs& a, cudaStream_t stream) {
+  static int sms[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return cudaErrorUnknown;
+    sms[dev] = n;
+  }
+  const int n_sm = dev < 64 ? sms[dev] : 148;
   const int rblocks = (a.T + 127) / 128;   // T: dense length, or the longest sequence
   dim3 gpre(rblocks, a.num_seqs * a.Hq);
+  const bool one_wave = (long)rblocks * a.num_seqs * a.Hq <= 2L * n_sm;
   prof_begin(kProfBwdPre, stream);
-  bwd_pre_kernel<D><<<gpre, 256, 0, stream>>>(a);
+  cudaError_t e;
+  if constexpr (D == 128)
+    e = one_wave ? launch_programmatic(bwd_pre_kernel<D, 8>, gpre, dim3(256), 0, stream, a)
+                 : launch_programmatic(bwd_pre_kernel<D, 4>, gpre, dim3(256), 0, stream, a);
+  else
+    e = launch_programmatic(bwd_pre_kernel<D, 4>, gpre, dim3(256), 0, stream, a);
   prof_end(stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

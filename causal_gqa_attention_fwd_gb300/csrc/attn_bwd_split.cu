@@ -163,6 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // A packed batch's decode reads cu_seqlens: wait for the preprocess grid
+  // first.  A dense one reads no memory before the set-up below.
+  if (a.varlen) griddep_wait();
+
   // ------------------------------------------------------------- decode
   int item = blockIdx.x;
   const int hkv = item % a.Hkv;
@@ -213,9 +217,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   float* stats = reinterpret_cast<float*>(smem + C::kOffStats);   // [stage][2][BM]
-  // the dQ kernel (launched next, programmatic dependent launch) reads
-  // nothing this grid writes: let its CTAs take SMs as this grid's finish
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // The preprocess grid's rows are complete and visible past this wait.
+  if (!a.varlen) griddep_wait();
+  // The dQ kernel (launched next, programmatic dependent launch) reads
+  // nothing this grid writes, only the preprocess's rows, which are complete
+  // once every CTA of this grid has passed the wait above (or exited without
+  // reading anything): let its CTAs take SMs as this grid's finish.
+  griddep_launch();
   auto it_head = [&](int i) { return hkv * a.G + i / per_head; };
   auto it_mb = [&](int i) { return mb0 + i % per_head; };
 
@@ -796,27 +804,21 @@ static cudaError_t launch_split(const CUtensorMap& q, const CUtensorMap& k, cons
   }
   const long kv_grid = (long)a.n_items * a.num_seqs * a.Hkv;
   prof_begin(kProfBwdDkdv, stream);
-  bwd_dkdv_kernel<D, F16><<<(unsigned)kv_grid, kThreads, kKvSmem<D>, stream>>>(q, k, v, dout, a);
+  cudaError_t e = launch_programmatic(bwd_dkdv_kernel<D, F16>, dim3((unsigned)kv_grid), dim3(kThreads), kKvSmem<D>,
+                                      stream, q, k, v, dout, a);
   prof_end(stream);
-  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // dQ kernel: programmatic dependent launch.  It reads only the inputs and
-  // the preprocess's rows (complete before the dK/dV grid started) and
-  // writes only dQ, so it never waits on the dK/dV grid: its CTAs fill the
-  // SMs that grid leaves idle (its tail; all of a small grid's spare SMs).
+  // the preprocess's rows (complete once every dK/dV CTA has passed its
+  // griddep_wait, which is when that grid lets this one start) and writes
+  // only dQ, so it never waits on the dK/dV grid: its CTAs fill the SMs that
+  // grid leaves idle (its tail; all of a small grid's spare SMs).
   const long q_grid = (long)a.n_items * a.num_seqs * a.Hq;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)q_grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kQSmem<D>;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   prof_begin(kProfBwdDq, stream);
-  e = cudaLaunchKernelEx(&cfg, bwd_dq_kernel<D, F16>, q, k, v, dout, a);
+  e = launch_programmatic(bwd_dq_kernel<D, F16>, dim3((unsigned)q_grid), dim3(kThreads), kQSmem<D>, stream, q, k, v,
+                          dout, a);
   prof_end(stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

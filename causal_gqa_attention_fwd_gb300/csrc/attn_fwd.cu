@@ -98,6 +98,10 @@ __global__ void __launch_bounds__(384, 1)
   const int lane = threadIdx.x & 31;
   Guard guard{&bars.abort, args.status, args.inject_step >= 0 ? args.wait_ns : kWaitLimitNs};
 
+  // A packed batch's decode reads cu_seqlens: wait for the previous grid
+  // first.  A dense one reads no memory before the set-up below.
+  if (args.varlen) griddep_wait();
+
   // ---------------------------------------------------------- work decode
   // blockIdx.x -> (row-block item, sequence/batch, head pair); heaviest
   // (largest row block) first.
@@ -160,6 +164,8 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
+  if (!args.varlen) griddep_wait();   // the inputs may come from the previous grid
+  griddep_launch();
   // Register split (launched 384 x 168 = 64512), set at the top of each
   // role: the control warpgroup (warps 0-3) keeps 64, the two softmax
   // warpgroups take 216 each, so a softmax thread holds its whole 128-column
@@ -468,8 +474,10 @@ static cudaError_t launch_fwd_d(const CUtensorMap& q, const CUtensorMap& k, cons
     attr_set[dev] = true;
   }
   prof_begin(kProfFwd, stream);
-  attn_fwd_kernel<D, F16QK><<<grid, 384, C::kSmemBytes, stream>>>(q, k, v, a);
+  cudaError_t e = launch_programmatic(attn_fwd_kernel<D, F16QK>, dim3(grid), dim3(384), C::kSmemBytes, stream, q, k,
+                                      v, a);
   prof_end(stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

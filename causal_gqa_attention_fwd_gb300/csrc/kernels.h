@@ -144,6 +144,25 @@ enum ProfKind {
   kProfBwdDq = 6,
   kProfKinds = 7
 };
+// Launch with programmatic stream serialization (see griddep_wait in
+// sm103.cuh): the kernel's CTAs may be scheduled, and run their set-up, while
+// the previous kernel in the stream drains.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 void prof_begin(int kind, cudaStream_t s);
 void prof_end(cudaStream_t s);
 

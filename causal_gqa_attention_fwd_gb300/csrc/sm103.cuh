@@ -215,6 +215,15 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 
 // One lane of a converged warp (the lowest); every lane gets the same answer
 // pattern on every call, so the same lane issues all of a warp's tcgen05 work.
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream is still
+// running: it calls griddep_wait() before it touches global memory that
+// kernel may write or read, and griddep_launch() once its own dependents may
+// be scheduled (the next grid starts when every CTA of this one has called it
+// or exited).  Both are no-ops for a kernel launched the ordinary way.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ bool elect_one() {
   uint32_t p;
   asm volatile(
