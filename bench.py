@@ -176,16 +176,34 @@ class ClockSampler:
 # ------------------------------------------------------------- CPU oracle
 def oracle_sample(w: W.Workload, x, budget_s: float, t_prefix: int | None = None):
     """Time the fp64 oracle on whole (batch, kv-head) groups of the workload
-    until about budget_s seconds of CPU work (at least one group).  With
-    t_prefix, each group is cut to its first t_prefix positions (a causal
-    prefix is itself a complete causal problem).  Returns (FLOP/s, sample
-    description, cores, seconds)."""
+    (packed batches: whole sequences, every head) until about budget_s
+    seconds of CPU work (at least one group).  With t_prefix, each group is
+    cut to its first t_prefix positions (a causal prefix is itself a complete
+    causal problem).  Returns (FLOP/s, sample description, cores, seconds)."""
     import numpy as np
 
     import oracle
     oracle.build()
     cores = len(os.sched_getaffinity(0))
     oracle.set_threads(cores)
+    if w.varlen:
+        f = lambda t: t.float().numpy().astype(np.float64)
+        cu = x["cu_seqlens"].tolist()
+        nseq = len(cu) - 1
+        done_flops, elapsed, seqs = 0.0, 0.0, 0
+        while seqs == 0 or (elapsed < budget_s and seqs < nseq):
+            a, b = cu[seqs], cu[seqs + 1]
+            sub_cu = np.array([0, b - a], dtype=np.int32)
+            q, k, v, do = (f(x[n][a:b]) for n in ("q", "k", "v", "do"))
+            t0 = time.perf_counter()
+            oracle.varlen_bwd(q, k, v, do, sub_cu, causal=w.causal, scale=w.softmax_scale)  # forward + backward
+            elapsed += time.perf_counter() - t0
+            seqs += 1
+            ff, fb = flops(W.Workload("s", B=1, Hq=w.Hq, Hkv=w.Hkv, T=b - a, D=w.D, causal=w.causal))
+            done_flops += ff + fb
+        desc = (f"the first {seqs} of {nseq} packed sequences of {w.name} (lengths {[cu[i + 1] - cu[i] for i in range(seqs)]}), "
+                f"every head, forward + backward in fp64, {elapsed:.1f} s")
+        return done_flops / elapsed, desc, cores, elapsed
     G = w.Hq // w.Hkv
     T = min(w.T, t_prefix) if t_prefix else w.T
     done_flops, elapsed, groups = 0.0, 0.0, 0

@@ -24,15 +24,18 @@ using namespace bwd;
 // ================================================================ preprocess
 // grid: (row blocks of 128, num_seqs * Hq); 256 threads.  A row is handled by
 // D/8 lanes (16 bytes of O and of dO each); a warp covers 32/(D/8) rows per
-// pass and issues all P passes' loads before it uses any.  P = 4 (31
-// registers, eight CTAs per SM) suits grids of several waves; a grid that
-// fits in one wave at two CTAs per SM takes P = 8 at D = 128 (one sweep of
-// the CTA's 128 rows, 256 bytes in flight per thread), so that its few CTAs
-// per SM still keep enough bytes in flight.
-template <int D, int P>
+// pass.  Two forms:
+//   SWEEP = false  four passes per sweep, each used as it lands (about 31
+//                  registers, eight CTAs per SM): grids of several waves;
+//   SWEEP = true   (D = 128) one sweep of the CTA's 128 rows whose eight
+//                  passes are all issued before any is used (256 bytes in
+//                  flight per thread): a grid of one wave at two CTAs per SM,
+//                  whose few CTAs must each keep many bytes in flight.
+template <int D, bool SWEEP>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
   constexpr int kLanesPerRow = D / 8;
   constexpr int kRowsPerPass = 32 / kLanesPerRow;            // per warp
+  constexpr int P = SWEEP ? 128 / (8 * kRowsPerPass) : 4;    // passes per sweep
   static_assert(128 % (8 * kRowsPerPass * P) == 0, "sweeps tile the row block");
   griddep_wait();      // O (and dO) may come from the previous grid
   griddep_launch();
@@ -45,45 +48,64 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
   const int Lr = (L + 127) & ~127;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane / kLanesPerRow, part = lane % kLanesPerRow;
-  for (int base = warp * kRowsPerPass * P; base < 128; base += 8 * kRowsPerPass * P) {
-    uint4 ov[P], gv[P];
+  // Delta of row p from its 16-byte pieces of O and dO (this lane's part),
+  // reduced over the row's lanes; written with -LSE*log2(e) by lane part 0
+  auto finish = [&](float acc, int p) {
 #pragma unroll
-    for (int u = 0; u < P; ++u) {
-      const int p = blockIdx.x * 128 + base + u * kRowsPerPass + sub;
-      ov[u] = make_uint4(0, 0, 0, 0);
-      gv[u] = make_uint4(0, 0, 0, 0);
-      const long off = row_off(a, s, tok0, h, a.Hq, p, D) + part * 8;
-      if (p < L && GQA_CHECK(off >= 0 && off + 8 <= elems(a, a.Hq), a.status, a.dbg_line)) {
-        ov[u] = *reinterpret_cast<const uint4*>(a.o + off);
-        gv[u] = *reinterpret_cast<const uint4*>(a.dout + off);
+    for (int m = kLanesPerRow / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (p >= Lr) return;
+    const long w = ws_row(a, s, tok0, h, p);
+    if (part == 0 && GQA_CHECK(w >= 0 && w < a.ws_rows, a.status, a.dbg_line)) {
+      float dl = 0.f, l2 = -INFINITY;       // stored negated: -Delta, -LSE*log2(e)
+      const long li = a.varlen ? (long)h * a.total + tok0 + p : ((long)s * a.Hq + h) * a.T + p;
+      if (p < L && GQA_CHECK(li >= 0 && li < elems(a, a.Hq) / a.D, a.status, a.dbg_line)) {
+        dl = -acc;
+        l2 = -a.lse[li] * 1.4426950408889634f;
       }
+      a.delta[w] = dl;
+      a.lse_log2[w] = l2;
     }
+  };
+  auto dot8 = [](const uint4& ov, const uint4& gv) {
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+    float acc = 0.f;
 #pragma unroll
-    for (int u = 0; u < P; ++u) {
-      float acc = 0.f;
-      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[u]);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv[u]);
+    for (int e = 0; e < 4; ++e) {
+      const float2 of = __bfloat1622float2(o2[e]), gf = __bfloat1622float2(g2[e]);
+      acc = fmaf(of.x, gf.x, acc);
+      acc = fmaf(of.y, gf.y, acc);
+    }
+    return acc;
+  };
+  for (int base = warp * kRowsPerPass * P; base < 128; base += 8 * kRowsPerPass * P) {
+    if constexpr (SWEEP) {
+      uint4 ov[P], gv[P];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 of = __bfloat1622float2(o2[e]), gf = __bfloat1622float2(g2[e]);
-        acc = fmaf(of.x, gf.x, acc);
-        acc = fmaf(of.y, gf.y, acc);
-      }
-#pragma unroll
-      for (int m = kLanesPerRow / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-      const int p = blockIdx.x * 128 + base + u * kRowsPerPass + sub;
-      if (p >= Lr) continue;
-      const long w = ws_row(a, s, tok0, h, p);
-      if (part == 0 && GQA_CHECK(w >= 0 && w < a.ws_rows, a.status, a.dbg_line)) {
-        float dl = 0.f, l2 = -INFINITY;       // stored negated: -Delta, -LSE*log2(e)
-        const long li = a.varlen ? (long)h * a.total + tok0 + p : ((long)s * a.Hq + h) * a.T + p;
-        if (p < L && GQA_CHECK(li >= 0 && li < elems(a, a.Hq) / a.D, a.status, a.dbg_line)) {
-          dl = -acc;
-          l2 = -a.lse[li] * 1.4426950408889634f;
+      for (int u = 0; u < P; ++u) {
+        const int p = blockIdx.x * 128 + base + u * kRowsPerPass + sub;
+        ov[u] = make_uint4(0, 0, 0, 0);
+        gv[u] = make_uint4(0, 0, 0, 0);
+        const long off = row_off(a, s, tok0, h, a.Hq, p, D) + part * 8;
+        if (p < L && GQA_CHECK(off >= 0 && off + 8 <= elems(a, a.Hq), a.status, a.dbg_line)) {
+          ov[u] = *reinterpret_cast<const uint4*>(a.o + off);
+          gv[u] = *reinterpret_cast<const uint4*>(a.dout + off);
         }
-        a.delta[w] = dl;
-        a.lse_log2[w] = l2;
       }
+#pragma unroll
+      for (int u = 0; u < P; ++u) finish(dot8(ov[u], gv[u]), blockIdx.x * 128 + base + u * kRowsPerPass + sub);
+    } else {
+      float acc[P];
+#pragma unroll
+      for (int u = 0; u < P; ++u) {
+        const int p = blockIdx.x * 128 + base + u * kRowsPerPass + sub;
+        acc[u] = 0.f;
+        const long off = row_off(a, s, tok0, h, a.Hq, p, D) + part * 8;
+        if (p < L && GQA_CHECK(off >= 0 && off + 8 <= elems(a, a.Hq), a.status, a.dbg_line))
+          acc[u] = dot8(*reinterpret_cast<const uint4*>(a.o + off), *reinterpret_cast<const uint4*>(a.dout + off));
+      }
+#pragma unroll
+      for (int u = 0; u < P; ++u) finish(acc[u], blockIdx.x * 128 + base + u * kRowsPerPass + sub);
     }
   }
 }
@@ -105,10 +127,10 @@ static cudaError_t launch_pre(const BwdArgs& a, cudaStream_t stream) {
   prof_begin(kProfBwdPre, stream);
   cudaError_t e;
   if constexpr (D == 128)
-    e = one_wave ? launch_programmatic(bwd_pre_kernel<D, 8>, gpre, dim3(256), 0, stream, a)
-                 : launch_programmatic(bwd_pre_kernel<D, 4>, gpre, dim3(256), 0, stream, a);
+    e = one_wave ? launch_programmatic(bwd_pre_kernel<D, true>, gpre, dim3(256), 0, stream, a)
+                 : launch_programmatic(bwd_pre_kernel<D, false>, gpre, dim3(256), 0, stream, a);
   else
-    e = launch_programmatic(bwd_pre_kernel<D, 4>, gpre, dim3(256), 0, stream, a);
+    e = launch_programmatic(bwd_pre_kernel<D, false>, gpre, dim3(256), 0, stream, a);
   prof_end(stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

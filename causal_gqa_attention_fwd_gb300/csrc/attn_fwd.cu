@@ -18,7 +18,12 @@
 //               form); allocates TMEM.
 //   warps 4-7   softmax for tile A, warps 8-11 for tile B; thread = row.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A, O_B (D columns each).
-// P (bf16) overwrites the first 64 columns of its S block.
+// D = 128: P (bf16) overwrites the first 64 columns of its S block, so a
+// tile's next S = Q K^T waits for its P V.  D = 64: P_A [384,448) and P_B
+// [448,512) have their own columns, so the next S is issued as soon as the
+// softmax has read the current one into registers (s_free) and is computed
+// while that softmax runs; the softmax waits for the previous P V (pv_done)
+// before it writes P or rescales O.
 // Tiles of key blocks past the diagonal are never visited; only the diagonal
 // block and a ragged last block are masked.
 //
@@ -51,16 +56,21 @@ struct FwdCfg {
   static constexpr int kSmemQ = 2 * kTileBytes;
   static constexpr int kSmemRing = kStages * kTileBytes;
   static constexpr int kSmemBytes = kSmemQ + kSmemRing + 1024;  // + alignment slack
+  // D = 64 leaves TMEM room for P columns of its own (see the layout above)
+  static constexpr bool kSepP = D == 64;
   __device__ static constexpr uint32_t col_s(int x) { return (uint32_t)x * 128u; }
   __device__ static constexpr uint32_t col_o(int x) { return 256u + (uint32_t)x * D; }
+  __device__ static constexpr uint32_t col_p(int x) { return kSepP ? 384u + (uint32_t)x * 64u : col_s(x); }
   // score MMA: bf16 Q and K, or f16 (rotated copies; A/B format code 0 = f16)
   static constexpr uint32_t kIdescQK =
       F16QK ? (idesc_bf16(kBM, kBN, false, false) & ~((7u << 7) | (7u << 10))) : idesc_bf16(kBM, kBN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16(kBM, D, false, true);
 };
 
-// TMEM layout (S_A, S_B, O_A, O_B) fits the 512 columns the kernel allocates
+// TMEM layout (S_A, S_B, O_A, O_B; at D = 64 also P_A, P_B) fits the 512
+// columns the kernel allocates
 static_assert(256 + 2 * 128 <= 512, "forward TMEM layout");
+static_assert(256 + 2 * 64 + 2 * 64 <= 512, "forward TMEM layout with P columns (D = 64)");
 
 struct __align__(8) FwdBarriers {
   uint64_t q_full[2];
@@ -69,6 +79,8 @@ struct __align__(8) FwdBarriers {
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
+  uint64_t s_free[2];    // D = 64: the softmax has read S into registers
+  uint64_t pv_done[2];   // D = 64: a tile's P V has completed
   uint64_t teardown;
   uint32_t tmem_base;
   int abort;
@@ -148,6 +160,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bars.s_full[i], 1);
       mbar_init(&bars.p_full[i], kBM / 32);      // one arrive per softmax warp
       mbar_init(&bars.o_done[i], 1);
+      mbar_init(&bars.s_free[i], kBM / 32);
+      mbar_init(&bars.pv_done[i], 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars.kv_full[s], 1);
@@ -255,7 +269,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t va = ring_addr + st * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          mma_ts_warp(tmem + C::col_o(x), tmem + C::col_s(x) + kk * 8, sdesc_sw128(va + kk * 2048, C::kBoxBytes, 1024),
+          mma_ts_warp(tmem + C::col_o(x), tmem + C::col_p(x) + kk * 8, sdesc_sw128(va + kk * 2048, C::kBoxBytes, 1024),
                  C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
         }
       };
@@ -274,7 +288,39 @@ __global__ void __launch_bounds__(384, 1)
           tc_commit_warp(&bars.kv_empty[stage_of(0)]);
         }
       }
-      for (int j = 0; j < nkv && ok; ++j) {
+      if constexpr (C::kSepP) {
+        // Per step j: the next scores of each tile as soon as its softmax has
+        // read S_j (K_{j+1}), then each tile's P_j V_j once P_j is written.
+        for (int j = 0; j < nkv && ok; ++j) {
+          const int vi = 2 * j + 1, ki = 2 * j + 2;
+          if (j + 1 < nkv) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full[stage_of(ki)], phase_of(ki), guard));
+            for (int x = 0; x < 2 && ok; ++x) {
+              if (j + 1 >= ti[x].nkv) continue;
+              ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_free[x], j & 1, guard));
+              if (!ok) break;
+              tc_fence_after();
+              issue_qk(x, stage_of(ki));
+              tc_commit_warp(&bars.s_full[x]);
+            }
+            if (!ok) break;
+            tc_commit_warp(&bars.kv_empty[stage_of(ki)]);
+          }
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full[stage_of(vi)], phase_of(vi), guard));
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (j >= ti[x].nkv) continue;
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_full[x], j & 1, guard));
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(x, stage_of(vi), j > 0);
+            tc_commit_warp(&bars.pv_done[x]);
+            if (j + 1 == ti[x].nkv) tc_commit_warp(&bars.o_done[x]);
+          }
+          if (!ok) break;
+          tc_commit_warp(&bars.kv_empty[stage_of(vi)]);
+        }
+      }
+      for (int j = 0; j < nkv && ok && !C::kSepP; ++j) {
         const int vi = 2 * j + 1, ki = 2 * j + 2;
         ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full[stage_of(vi)], phase_of(vi), guard));
         if (ok && j + 1 < nkv) ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full[stage_of(ki)], phase_of(ki), guard));
@@ -312,6 +358,7 @@ __global__ void __launch_bounds__(384, 1)
     if (t.valid) {
       const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
       const uint32_t tS = tmem + lane_base + C::col_s(x);
+      const uint32_t tP = tmem + lane_base + C::col_p(x);
       const uint32_t tO = tmem + lane_base + C::col_o(x);
       const float c = args.scale_log2;
       const int qi = t.mb * kBM + r;        // query index within the sequence
@@ -327,6 +374,10 @@ __global__ void __launch_bounds__(384, 1)
         for (int q = 0; q < kBN / 32; ++q) tmem_ld_x32(tS + q * 32, s + q * 32);
         tmem_ld_wait();
         reg_fence<kBN>(s);
+        if constexpr (C::kSepP) {
+          tc_fence_before();
+          mbar_arrive_warp(&bars.s_free[x]);   // S_j is in registers: the next S may overwrite it
+        }
         float* sf = reinterpret_cast<float*>(s);
         const int k0 = j * kBN;
         const bool need_mask = (args.causal && j == t.mb) || (k0 + kBN > L);
@@ -356,6 +407,14 @@ __global__ void __launch_bounds__(384, 1)
           resc = true;
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        if constexpr (C::kSepP) {
+          // P_{j-1} V_{j-1} has read the P columns and finished adding into O
+          if (j > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.pv_done[x], (j - 1) & 1, guard));
+            if (!ok) break;
+            tc_fence_after();
+          }
+        }
         // p = 2^(s c - m): exponent arguments and the row sum in paired f32
         const uint64_t c2 = f2(c, c), nm2 = f2(-m_use, -m_use);
         uint64_t acc[4] = {0, 0, 0, 0};
@@ -370,7 +429,7 @@ __global__ void __launch_bounds__(384, 1)
             acc[i & 3] = add2(acc[i & 3], f2(p0, p1));
             pk[i] = pack_bf16x2(p0, p1);
           }
-          tmem_st_x16(tS + q * 16, pk);
+          tmem_st_x16(tP + q * 16, pk);
         }
         float rs0, rs1;
         f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), rs0, rs1);
