@@ -287,6 +287,76 @@ def parity_leg(w: W.Workload, x, out: dict):
             "seconds": time.perf_counter() - t0}
 
 
+def decode_parity_leg(w, x, o, lse):
+    """Compare one decode call with the fp64 oracle on two batch rows (the
+    shortest and the longest cache; rows are independent), every head and
+    query position.  Paged caches: only the pages those rows use are handed
+    to the oracle, with the block table renumbered.  Returns O's figures of
+    ``oracle.parity`` and the LSE error, as the prefill leg does."""
+    import numpy as np
+
+    import oracle
+    from oracle import parity as P
+    oracle.build()
+    oracle.set_threads(len(os.sched_getaffinity(0)))
+    t0 = time.perf_counter()
+    f = lambda t: t.float().numpy().astype(np.float64)
+    lens = x["cache_lens"]
+    rows = sorted({int(lens.argmin()), int(lens.argmax())})
+    q, ln = f(x["q"][rows]), lens[rows].numpy()
+    if w.fp8:
+        ro, rlse = oracle.fp8_decode_fwd(q, x["k8"][rows].numpy(), x["v8"][rows].numpy(), x["k_scale"], x["v_scale"],
+                                         ln, scale=w.softmax_scale)
+    elif w.page_size:
+        bt = x["block_table"][rows]
+        used = sorted({int(e) for r, n in zip(bt, ln) for e in r[: (int(n) + w.page_size - 1) // w.page_size]})
+        remap = {e: i for i, e in enumerate(used)}
+        bt_sub = np.array([[remap.get(int(e), 0) for e in r] for r in bt], dtype=np.int32)
+        idx = torch.tensor(used, dtype=torch.int64)
+        ro, rlse = oracle.paged_decode_fwd(q, f(x["k_pages"][idx]), f(x["v_pages"][idx]), bt_sub, ln,
+                                           scale=w.softmax_scale)
+    else:
+        ro, rlse = oracle.decode_fwd(q, f(x["k_cache"][rows]), f(x["v_cache"][rows]), ln, scale=w.softmax_scale)
+    res = P.compare("o", f(o.cpu()[rows]), ro, P.TOL_REL_O)
+    le = P.compare_lse(f(lse.cpu()[rows]), rlse)
+    keep = ("rel_fro", "rel_tol", "max_abs", "flat_excess", "ulp_excess", "widened_excess", "max_ref", "meets")
+    return {"against": "fp64 CPU oracle",
+            "sample": f"batch rows {rows} (cache lengths {[int(v) for v in ln]}: the shortest and the longest), "
+                      f"every head and query position",
+            "tolerances": {"rel_fro_o": P.TOL_REL_O, "abs_flat": P.TOL_ABS, "lse_abs": P.TOL_LSE},
+            "outputs": {"o": {k: res[k] for k in keep}, "lse": {"max_abs": le["max_abs"], "tol": le["tol"]}},
+            "pass": res["ok"] and le["ok"], "flat_pass": res["meets"] == "flat" and le["ok"],
+            "seconds": time.perf_counter() - t0}
+
+
+def graph_launch_floor_us(stream, reps: int = 50) -> float:
+    """Median time of replaying a CUDA graph of two minimal kernels (one-element
+    writes): the launch floor under any two-kernel call such as a decode
+    (partial + merge)."""
+    t = torch.zeros(1, device="cuda")
+    with torch.cuda.stream(stream):
+        t.add_(1.0)
+        t.add_(1.0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        t.add_(1.0)
+        t.add_(1.0)
+    for _ in range(5):
+        g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    ms = sorted(a.elapsed_time(b) for a, b in ts)
+    return ms[len(ms) // 2] * 1e3
+
+
 # ---------------------------------------------------------------- decode
 DECODE_METRIC = "cached GQA decode attention: algorithmic HBM GB/s and % of GB300 copy bandwidth"
 DECODE_UNIT = "GB/s"
@@ -412,6 +482,11 @@ def run_decode(args, world, rank, local):
     torch.cuda.synchronize()
     assert gq.get_device_status() == 0, "device status after warm-up"
 
+    parity = None
+    if rank == 0 and not args.no_parity:
+        parity = decode_parity_leg(w, x, o, lse)
+    floor_us = graph_launch_floor_us(stream)
+
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -497,6 +572,9 @@ def run_decode(args, world, rank, local):
             "tokens_per_s": world * w.B * w.Tq * args.steps / (total_ms / 1e3),
             "kernel_ms": {k: (t / n if n else None) for k, (n, t) in prof.items() if n},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "parity": parity,
+            "launch_floor_us": floor_us,
+            "launch_floor": "median replay of a CUDA graph of two one-element kernels (a decode call launches two)",
             "gpu_launches": sum(prof[k][0] for k in prof), "kernel_ms_pass": "second pass, same steps, events per kernel",
             "launch": "CUDA graph replay of the call" if graph is not None else "eager calls",
             "clocks": clk, "device_status": status,
