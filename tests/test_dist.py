@@ -35,7 +35,7 @@ def _worker(rank, world, port, out):
 
 def test_replica_coordination_gloo_two_ranks():
     world = 2
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:   # no fork of a threaded process
         out = mgr.dict()
         mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
         assert out[0] == out[1] == 20.0          # both ranks see the slowest rank's time
