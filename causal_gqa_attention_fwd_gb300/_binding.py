@@ -20,6 +20,7 @@ STATUS = {
     0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_SHAPE", 3: "ATTN_ERR_HEADDIM", 4: "ATTN_ERR_ALIGN",
     5: "ATTN_ERR_SEQLENS", 6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_ARCH", 8: "ATTN_ERR_CUDA",
     9: "ATTN_ERR_TIMEOUT", 10: "ATTN_ERR_SCRATCH_LIMIT", 11: "ATTN_ERR_PAGES", 12: "ATTN_ERR_CHECK",
+    13: "ATTN_ERR_RANGE",
 }
 
 # name -> (restype, argtypes)

@@ -904,6 +904,7 @@ const char* attn_status_string(attn_status s) {
       return "the problem needs more backward scratch than attn_bwd_noalloc's built-in array holds";
     case ATTN_ERR_PAGES: return "a block-table entry names no page of the pool";
     case ATTN_ERR_CHECK: return "a bounds check of the debug build failed (attn_get_check_line gives its line)";
+    case ATTN_ERR_RANGE: return "a rotated q or k value is not finite or does not fit f16 (|x| >= 65520)";
   }
   return "unknown status";
 }

@@ -609,15 +609,23 @@ __global__ void __launch_bounds__(256) rope_qk_f16_kernel(const __nv_bfloat16* _
   const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
   const uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w}, wh[4] = {hi.x, hi.y, hi.z, hi.w};
   uint32_t ol[4], oh[4];
+  // f16 holds magnitudes below 65520 (larger ones round to infinity): a
+  // value outside that, or not finite, is reported (ATTN_ERR_RANGE) and
+  // written as f16 rounds it
+  bool fits = true;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wl[e]));
     const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wh[e]));
-    const __half2 yl = __floats2half2_rn(fmaf(a.x, c[2 * e], -b.x * sn[2 * e]), fmaf(a.y, c[2 * e + 1], -b.y * sn[2 * e + 1]));
-    const __half2 yh = __floats2half2_rn(fmaf(b.x, c[2 * e], a.x * sn[2 * e]), fmaf(b.y, c[2 * e + 1], a.y * sn[2 * e + 1]));
+    const float l0 = fmaf(a.x, c[2 * e], -b.x * sn[2 * e]), l1 = fmaf(a.y, c[2 * e + 1], -b.y * sn[2 * e + 1]);
+    const float h0 = fmaf(b.x, c[2 * e], a.x * sn[2 * e]), h1 = fmaf(b.y, c[2 * e + 1], a.y * sn[2 * e + 1]);
+    fits = fits && fabsf(l0) < 65520.f && fabsf(l1) < 65520.f && fabsf(h0) < 65520.f && fabsf(h1) < 65520.f;
+    const __half2 yl = __floats2half2_rn(l0, l1);
+    const __half2 yh = __floats2half2_rn(h0, h1);
     ol[e] = *reinterpret_cast<const uint32_t*>(&yl);
     oh[e] = *reinterpret_cast<const uint32_t*>(&yh);
   }
+  if (!fits) atomicCAS(rr.status, 0, kDevRange);
   *reinterpret_cast<uint4*>(y + i0) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
   *reinterpret_cast<uint4*>(y + H + i0) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
 }

@@ -19,7 +19,8 @@ namespace gqa {
 // Device status word values (mirrors attn_status in include/gqa_attn.h).
 // kDevInternal (ATTN_ERR_CUDA): a kernel's own layout check failed;
 // kDevCheck (ATTN_ERR_CHECK): a bounds check of the debug build failed.
-enum : int { kDevOk = 0, kDevTimeout = 9, kDevBadSeqlens = 5, kDevInternal = 8, kDevCheck = 12 };
+// kDevRange (ATTN_ERR_RANGE): a rotated q or k value does not fit f16.
+enum : int { kDevOk = 0, kDevTimeout = 9, kDevBadSeqlens = 5, kDevInternal = 8, kDevCheck = 12, kDevRange = 13 };
 
 // Debug builds (-DGQA_DEBUG): explicit bounds checks of computed global,
 // shared-memory and tensor-map indices, GQA_CHECK(cond, status, line_word).

@@ -69,7 +69,8 @@ typedef enum {
     ATTN_ERR_TIMEOUT = 9,    /* device-detected: a bounded in-kernel wait expired */
     ATTN_ERR_SCRATCH_LIMIT = 10, /* attn_bwd_noalloc: sizes need more than its built-in scratch */
     ATTN_ERR_PAGES = 11,     /* device-detected: a block-table entry names no page of the pool */
-    ATTN_ERR_CHECK = 12      /* device-detected, debug build only: a bounds check of a computed index failed */
+    ATTN_ERR_CHECK = 12,     /* device-detected, debug build only: a bounds check of a computed index failed */
+    ATTN_ERR_RANGE = 13      /* device-detected: a rotated q or k value is not finite or does not fit f16 */
 } attn_status;
 
 /* Forward, dense layout.  Writes O (bf16) and LSE (float32). */
@@ -138,9 +139,13 @@ GQA_ATTN_API size_t attn_varlen_bwd_workspace_size(int num_seqs, int total_token
  * (rope_cos_sin: DEVICE float32 [rope_positions, D], 16-byte aligned,
  * rope_positions >= T; row p holds cos(p*theta_i) for i < D/2, then
  * sin(p*theta_i); feature i pairs with feature i + D/2).  The rotated q and
- * k are written as f16 (11 significant bits; |rotated value| < 65504) into
- * the workspace and the score MMA takes them as f16; P V and everything
- * else is as attn_fwd.
+ * k are written as f16 (11 significant bits) into the workspace and the
+ * score MMA takes them as f16; P V and everything else is as attn_fwd.
+ * A rotated value that is not finite or has |value| >= 65520 (beyond f16;
+ * it becomes infinite there) is recorded in the device status word as
+ * ATTN_ERR_RANGE; the call still completes, and its outputs for the rows
+ * that meet that value are then not meaningful.  The rotary backward
+ * (attn_bwd_rope, attn_varlen_bwd_rope) reports the same way.
  * workspace: DEVICE, 256-byte aligned, >= attn_fwd_rope_workspace_size()
  * bytes (the two rotated copies), no initialisation; errors as attn_fwd,
  * plus ATTN_ERR_WORKSPACE. */

@@ -153,7 +153,7 @@ def test_debug_build_exports_the_same_symbols(lib):
 
 def test_status_strings(lib):
     import causal_gqa_attention_fwd_gb300 as g
-    for code in range(13):
+    for code in range(14):
         s = g.status_string(code)
         assert s and s != "unknown status"
     assert g.status_string(99) == "unknown status"

@@ -101,3 +101,24 @@ def test_varlen_fwd_rope_reports_positions_past_the_table(gq):
     gq.attn_varlen_fwd_rope(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), cu.cuda(), 16, tab.cuda(), scale=0.1)
     assert gq.get_device_status() == 5
     assert gq.get_device_status() == 0
+
+
+def test_fwd_rope_reports_rotated_values_beyond_f16(gq):
+    """The rotated copies are f16: a rotated value that does not fit (here a
+    q element of 70144 at position 0, where the rotation leaves it as is) is
+    recorded as ATTN_ERR_RANGE (13); one that fits (59904) is not; the next
+    call on ordinary inputs reports nothing."""
+    B, Hq, Hkv, T, D = 1, 2, 1, 128, 128
+    x = W.dense_inputs(B, Hq, Hkv, T, D, seed=21)
+    tab = W.rope_cos_sin_table(T, D).cuda()
+    k, v = x["k"].cuda(), x["v"].cuda()
+    q = x["q"].clone()
+    q[0, 1, 0, 0] = 60000.0                     # bf16 59904: fits f16
+    gq.attn_fwd_rope(q.cuda(), k, v, tab, scale=0.1)
+    assert gq.get_device_status() == 0
+    q[0, 1, 0, 0] = 70000.0                     # bf16 70144: beyond f16
+    gq.attn_fwd_rope(q.cuda(), k, v, tab, scale=0.1)
+    assert gq.get_device_status() == 13
+    o, lse = gq.attn_fwd_rope(x["q"].cuda(), k, v, tab, scale=0.1)
+    assert gq.get_device_status() == 0
+    assert torch.isfinite(o.float()).all()
