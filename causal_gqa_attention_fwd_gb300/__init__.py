@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     attn_bwd,
     attn_bwd_noalloc,
     attn_bwd_rope,
+    attn_bwd_rope_workspace_size,
     attn_bwd_workspace_size,
     attn_decode_fp8_fwd,
     attn_decode_fwd,
@@ -34,8 +35,10 @@ from ._binding import (  # noqa: F401
     attn_fwd_rope,
     attn_fwd_rope_workspace_size,
     attn_varlen_fwd_rope,
+    attn_varlen_fwd_rope_workspace_size,
     attn_varlen_bwd,
     attn_varlen_bwd_rope,
+    attn_varlen_bwd_rope_workspace_size,
     attn_varlen_bwd_workspace_size,
     attn_varlen_fwd,
     get_check_line,

@@ -208,7 +208,7 @@ def attn_varlen_fwd_rope(q, k, v, cu_seqlens, max_seqlen, rope_cos_sin, causal: 
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((Hq, total), dtype=torch.float32, device=q.device) if lse is None else lse
     if workspace is None:
-        workspace = torch.empty(max(int(lib().attn_varlen_fwd_rope_workspace_size(total, Hq, Hkv, D)), 256),
+        workspace = torch.empty(max(attn_varlen_fwd_rope_workspace_size(total, Hq, Hkv, D), 256),
                                 dtype=torch.uint8, device=q.device)
     rope_ptr, rope_n = _rope(rope_cos_sin)
     st = lib().attn_varlen_fwd_rope(_need(q, "q"), _need(k, "k"), _need(v, "v"), _need(o, "o"),
@@ -220,8 +220,20 @@ def attn_varlen_fwd_rope(q, k, v, cu_seqlens, max_seqlen, rope_cos_sin, causal: 
     return o, lse
 
 
+def attn_varlen_fwd_rope_workspace_size(total, Hq, Hkv, D) -> int:
+    return int(lib().attn_varlen_fwd_rope_workspace_size(total, Hq, Hkv, D))
+
+
 def attn_bwd_workspace_size(B, Hq, Hkv, T, D) -> int:
     return int(lib().attn_bwd_workspace_size(B, Hq, Hkv, T, D))
+
+
+def attn_bwd_rope_workspace_size(B, Hq, Hkv, T, D) -> int:
+    return int(lib().attn_bwd_rope_workspace_size(B, Hq, Hkv, T, D))
+
+
+def attn_varlen_bwd_rope_workspace_size(num_seqs, total, Hq, Hkv, D) -> int:
+    return int(lib().attn_varlen_bwd_rope_workspace_size(num_seqs, total, Hq, Hkv, D))
 
 
 def attn_bwd(q, k, v, o, lse, dout, causal: bool = True, scale=None, dq=None, dk=None, dv=None,
@@ -253,7 +265,7 @@ def attn_bwd_rope(q, k, v, o, lse, dout, rope_cos_sin, causal: bool = True, scal
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     if workspace is None:
-        workspace = torch.empty(max(int(lib().attn_bwd_rope_workspace_size(B, Hq, Hkv, T, D)), 256),
+        workspace = torch.empty(max(attn_bwd_rope_workspace_size(B, Hq, Hkv, T, D), 256),
                                 dtype=torch.uint8, device=q.device)
     rope_ptr, rope_n = _rope(rope_cos_sin)
     st = lib().attn_bwd_rope(_need(q, "q"), _need(k, "k"), _need(v, "v"), _need(o, "o"),
@@ -274,7 +286,7 @@ def attn_varlen_bwd_rope(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, rop
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     if workspace is None:
-        workspace = torch.empty(max(int(lib().attn_varlen_bwd_rope_workspace_size(n, total, Hq, Hkv, D)), 256),
+        workspace = torch.empty(max(attn_varlen_bwd_rope_workspace_size(n, total, Hq, Hkv, D), 256),
                                 dtype=torch.uint8, device=q.device)
     rope_ptr, rope_n = _rope(rope_cos_sin)
     st = lib().attn_varlen_bwd_rope(_need(q, "q"), _need(k, "k"), _need(v, "v"), _need(o, "o"),

@@ -289,3 +289,21 @@ def test_varlen_fwd_rope_validation(lib):
     assert f(ws=A + 32) == 4
     assert f(ptrs=(NULL,) * 6, n=0, tab=NULL, ws=NULL) == 0
     assert lib.attn_varlen_fwd_rope_workspace_size(10, 4, 2, 128) == 10 * 4 * 128 * 2 + 10 * 2 * 128 * 2
+
+
+def test_python_binding_exposes_every_workspace_size():
+    """Each *_workspace_size entry point of the header has a same-named
+    Python function in the package, returning what the C call returns."""
+    import causal_gqa_attention_fwd_gb300 as g
+    lib = g.lib()
+    cases = {
+        "attn_fwd_rope_workspace_size": (2, 4, 2, 1000, 128),
+        "attn_varlen_fwd_rope_workspace_size": (1000, 4, 2, 128),
+        "attn_bwd_workspace_size": (2, 4, 2, 1000, 128),
+        "attn_bwd_rope_workspace_size": (2, 4, 2, 1000, 128),
+        "attn_varlen_bwd_workspace_size": (3, 1000, 4, 2, 128),
+        "attn_varlen_bwd_rope_workspace_size": (3, 1000, 4, 2, 128),
+        "attn_decode_workspace_size": (2, 8, 2, 1, 4096, 128),
+    }
+    for name, args in cases.items():
+        assert getattr(g, name)(*args) == int(getattr(lib, name)(*args)) > 0, name
