@@ -124,7 +124,7 @@ long varlen_total_pad(int num_seqs, int total) { return (long)round_up((size_t)t
 
 size_t ws_bytes(long rows, int D) {
   (void)D;
-  return round_up((size_t)rows * 4, 256) * 2;
+  return round_up((size_t)rows * 4, 256) * 2 + 256;   // -Delta, -LSE*log2(e), the dQ kernel's tile counter
 }
 
 attn_status bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -168,6 +168,7 @@ attn_status bwd_common(const void* q, const void* k, const void* v, const void* 
   char* w = static_cast<char*>(ws);
   a.delta = reinterpret_cast<float*>(w);
   a.lse_log2 = reinterpret_cast<float*>(w + round_up((size_t)rows * 4, 256));
+  a.tile_counter = reinterpret_cast<int*>(w + 2 * round_up((size_t)rows * 4, 256));
   a.rope_cs = rope_cs;
   a.n_table = n_table;
   a.dbg_line = check_line_word();

@@ -39,6 +39,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
   static_assert(128 % (8 * kRowsPerPass * P) == 0, "sweeps tile the row block");
   griddep_wait();      // O (and dO) may come from the previous grid
   griddep_launch();
+  // the dQ kernel's tile counter (the previous call's dQ grid has completed:
+  // it preceded this grid in the stream)
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.tile_counter = 0;
   const int s = blockIdx.y / a.Hq, h = blockIdx.y % a.Hq;
   int tok0, L;
   if (!seq_bounds(a, s, tok0, L)) {

@@ -98,10 +98,12 @@ struct QCfg {
 };
 
 struct __align__(8) QBars {
-  uint64_t q_full;
+  uint64_t q_full, q_empty, do_full, do_empty;
   uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
   uint64_t s_full[2], dp_full, dp_read, ds_full;
-  uint64_t dq_done, teardown;
+  uint64_t dq_done, dq_free, teardown;
+  uint64_t tile_full[2], tile_empty[2];   // the mailbox of claimed tiles
+  int tile[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -500,6 +502,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ========================================================================= dQ
+// Persistent: one CTA per SM takes (query head, sequence, 128-query block)
+// tiles, heaviest first, until none is left: CTA c starts with tile c, and
+// every later tile comes from a counter in the workspace (zeroed by the
+// preprocess).  Warp 3 claims the tiles and loads each tile's
+// Q and dO; the other roles read the claimed tile from a two-slot mailbox.
+// The K/V rings, the S buffers and every barrier run on across tiles (step
+// counters continue), so a tile's first loads and its first S MMAs overlap
+// the previous tile's last steps: Q(e+1) is loaded once the last S of tile e
+// is done (q_empty), dO(e+1) once tile e's epilogue has read its staging
+// area, the dO tile (do_empty), and the first dQ MMA of tile e+1 waits until
+// tile e's accumulator has been read out (dq_free).
 template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -512,35 +525,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kIdS = F16 ? idesc_f16(128, 128, false, false) : idesc_bf16(128, 128, false, false);
   constexpr uint32_t kIdDP = idesc_bf16(128, 128, false, false);
   constexpr uint32_t kIdDQ = F16 ? idesc_f16(128, D, false, true) : idesc_bf16(128, D, false, true);
+  constexpr int kReaders = 11;                 // mailbox readers: warps 0, 1, 2 and the 8 compute warps
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // ------------------------------------------------------------- decode
-  // blockIdx.x -> (query head, sequence, query block); heaviest (last) block first
-  int item = blockIdx.x;
-  const int h = item % a.Hq;
-  item /= a.Hq;
-  const int s = item % a.num_seqs;
-  const int mb = a.n_items - 1 - item / a.num_seqs;
-  int tok0, L;
-  if (!seq_bounds(a, s, tok0, L)) {
-    if (threadIdx.x == 0) atomicCAS(a.status, 0, kDevBadSeqlens);
-    return;
-  }
-  const int q0 = mb * BM;
-  if (q0 >= L) return;
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) atomicCAS(a.status, 0, kDevInternal);
     return;
   }
-  const int hkv = h / a.G;
-  const int n_kb = a.causal ? mb + 1 : (L + 127) / 128;   // key blocks these queries see
+  const int n_tiles = a.n_items * a.num_seqs * a.Hq;
 
   QBars& bars = *reinterpret_cast<QBars*>(smem + C::kOffBars);
   Guard guard{&bars.abort, a.status, a.inject_kernel == 2 ? a.wait_ns : kWaitLimitNs};
   if (threadIdx.x == 0) {
     bars.abort = 0;
     mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.q_empty, 1);
+    mbar_init(&bars.do_full, 1);
+    mbar_init(&bars.do_empty, 8);                // one arrive per compute warp, after its epilogue
     for (int i = 0; i < 3; ++i) {
       mbar_init(&bars.k_full[i], 1);
       mbar_init(&bars.k_empty[i], 1);
@@ -549,11 +550,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.v_full[i], 1);
       mbar_init(&bars.v_empty[i], 1);
       mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.tile_full[i], 1);
+      mbar_init(&bars.tile_empty[i], kReaders);
     }
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.dp_read, 8);
     mbar_init(&bars.ds_full, 8);
     mbar_init(&bars.dq_done, 1);
+    mbar_init(&bars.dq_free, 8);
     mbar_init(&bars.teardown, 2);                // one commit from each issuer
     fence_barrier_init();
   }
@@ -566,45 +570,129 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
 
-  if (warp == 0) {
-    // ======================================================== TMA producer
+  // A tile's coordinates; empty when its queries lie past its sequence (or
+  // the sequence's bounds are invalid, which the fetcher reports).
+  struct Tile {
+    int h, s, mb, tok0, L, q0, n_kb;
+    bool empty;
+  };
+  auto decode = [&](int t, bool report) {
+    Tile x;
+    x.h = t % a.Hq;
+    t /= a.Hq;
+    x.s = t % a.num_seqs;
+    x.mb = a.n_items - 1 - t / a.num_seqs;
+    x.empty = !seq_bounds(a, x.s, x.tok0, x.L);
+    if (x.empty && report) atomicCAS(a.status, 0, kDevBadSeqlens);
+    x.q0 = x.mb * BM;
+    x.empty = x.empty || x.q0 >= x.L;
+    x.n_kb = a.causal ? x.mb + 1 : (x.L + 127) / 128;   // key blocks these queries see
+    return x;
+  };
+  // The k-th claimed tile (-1: none left), read from the mailbox by every
+  // role except the fetcher; false if the wait gave up.
+  auto read_tile = [&](int k, int& t) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&bars.tile_full[k & 1], (k >> 1) & 1, guard))) return false;
+    t = *reinterpret_cast<volatile int*>(&bars.tile[k & 1]);
+    mbar_arrive_warp(&bars.tile_empty[k & 1]);
+    return true;
+  };
+
+  if (warp == 3) {
+    // ================================= tile fetcher and Q / dO loads
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      int e = 0;                                 // non-empty tiles loaded
+      for (int k = 0;; ++k) {
+        const int slot = k & 1;
+        if (k >= 2 && !mbar_wait(&bars.tile_empty[slot], ((k >> 1) - 1) & 1, guard)) break;
+        // the first tile of each CTA is its own index (the grid is no larger
+        // than the tile count), so its loads start without a round trip to
+        // the counter; later tiles come from the counter, after the first
+        // gridDim.x
+        int t = k == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.tile_counter, 1);
+        if (t >= n_tiles) t = -1;
+        bars.tile[slot] = t;
+        mbar_arrive(&bars.tile_full[slot]);
+        if (t < 0) break;
+        const Tile x = decode(t, true);
+        if (x.empty) continue;
+        int c1, c2;
+        if (a.varlen) { c1 = x.h; c2 = x.tok0 + x.q0; } else { c1 = x.q0; c2 = x.s * a.Hq + x.h; }
+        const bool ok_tile = GQA_CHECK(tile_ok(a, a.Hq, c1, c2), a.status, a.dbg_line);
+        if (e >= 1 && !mbar_wait(&bars.q_empty, (e - 1) & 1, guard)) break;
+        mbar_expect_tx(&bars.q_full, kTile);
+        if (ok_tile)
+          for (int b = 0; b < NB; ++b) tma_load_3d(smem + C::kOffQ + b * kBox, &tm_q, &bars.q_full, b * 64, c1, c2);
+        if (e >= 1 && !mbar_wait(&bars.do_empty, (e - 1) & 1, guard)) {
+          ++e;                                   // Q(e) was issued: drain it below
+          break;
+        }
+        mbar_expect_tx(&bars.do_full, kTile);
+        if (ok_tile)
+          for (int b = 0; b < NB; ++b)
+            tma_load_3d(smem + C::kOffDO + b * kBox, &tm_do, &bars.do_full, b * 64, c1, c2);
+        ++e;
+      }
+      // never leave the CTA with copies in flight
+      if (e >= 1) {
+        mbar_wait_drain(&bars.q_full, (uint32_t)(e - 1) & 1);
+        mbar_wait_drain(&bars.do_full, (uint32_t)(e - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 0) {
+    // ================================================ K / V TMA producer
+    int lastk[3] = {-1, -1, -1}, lastv[2] = {-1, -1};
+    int g = 0;                                   // steps of the tiles before this one
+    bool stop = false;
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int c1, c2;
-      if (a.varlen) { c1 = h; c2 = tok0 + q0; } else { c1 = q0; c2 = s * a.Hq + h; }
-      mbar_expect_tx(&bars.q_full, 2 * kTile);
-      if (GQA_CHECK(tile_ok(a, a.Hq, c1, c2), a.status, a.dbg_line))
-        for (int b = 0; b < NB; ++b) {
-          tma_load_3d(smem + C::kOffQ + b * kBox, &tm_q, &bars.q_full, b * 64, c1, c2);
-          tma_load_3d(smem + C::kOffDO + b * kBox, &tm_do, &bars.q_full, b * 64, c1, c2);
+    }
+    for (int k = 0; !stop; ++k) {
+      int t;
+      if (!read_tile(k, t) || t < 0) break;
+      const Tile x = decode(t, false);
+      if (x.empty) continue;
+      const int hkv = x.h / a.G;
+      if (lane == 0) {
+        for (int j = 0; j < x.n_kb; ++j) {
+          const int gs = g + j;
+          if (a.inject_kernel == 2 && t == 0 && j == a.inject_step) {   // failure-path test: the first tile
+            stop = true;
+            break;
+          }
+          int c1, c2;
+          if (a.varlen) { c1 = hkv; c2 = x.tok0 + j * 128; } else { c1 = j * 128; c2 = x.s * a.Hkv + hkv; }
+          const int ks = gs % 3, vs = gs & 1;
+          const uint32_t kph = (gs / 3) & 1, vph = (gs >> 1) & 1;
+          if (!mbar_wait(&bars.k_empty[ks], kph ^ 1, guard)) { stop = true; break; }
+          mbar_expect_tx(&bars.k_full[ks], kTile);
+          const bool kv_ok = GQA_CHECK(tile_ok(a, a.Hkv, c1, c2), a.status, a.dbg_line);
+          if (kv_ok)
+            for (int b = 0; b < NB; ++b)
+              tma_load_3d(smem + C::kOffK + ks * kTile + b * kBox, &tm_k, &bars.k_full[ks], b * 64, c1, c2);
+          lastk[ks] = (int)kph;
+          if (!mbar_wait(&bars.v_empty[vs], vph ^ 1, guard)) { stop = true; break; }
+          mbar_expect_tx(&bars.v_full[vs], kTile);
+          if (kv_ok)
+            for (int b = 0; b < NB; ++b)
+              tma_load_3d(smem + C::kOffV + vs * kTile + b * kBox, &tm_v, &bars.v_full[vs], b * 64, c1, c2);
+          lastv[vs] = (int)vph;
         }
-      int lastk[3] = {-1, -1, -1}, lastv[2] = {-1, -1};
-      for (int j = 0; j < n_kb; ++j) {
-        if (a.inject_kernel == 2 && blockIdx.x == 0 && j == a.inject_step) break;   // failure-path test
-        if (a.varlen) { c1 = hkv; c2 = tok0 + j * 128; } else { c1 = j * 128; c2 = s * a.Hkv + hkv; }
-        const int ks = j % 3, vs = j & 1;
-        const uint32_t kph = (j / 3) & 1, vph = (j >> 1) & 1;
-        if (!mbar_wait(&bars.k_empty[ks], kph ^ 1, guard)) break;
-        mbar_expect_tx(&bars.k_full[ks], kTile);
-        const bool kv_ok = GQA_CHECK(tile_ok(a, a.Hkv, c1, c2), a.status, a.dbg_line);
-        if (kv_ok)
-          for (int b = 0; b < NB; ++b)
-            tma_load_3d(smem + C::kOffK + ks * kTile + b * kBox, &tm_k, &bars.k_full[ks], b * 64, c1, c2);
-        lastk[ks] = (int)kph;
-        if (!mbar_wait(&bars.v_empty[vs], vph ^ 1, guard)) break;
-        mbar_expect_tx(&bars.v_full[vs], kTile);
-        if (kv_ok)
-          for (int b = 0; b < NB; ++b)
-            tma_load_3d(smem + C::kOffV + vs * kTile + b * kBox, &tm_v, &bars.v_full[vs], b * 64, c1, c2);
-        lastv[vs] = (int)vph;
       }
-      mbar_wait_drain(&bars.q_full, 0);
+      stop = __shfl_sync(0xffffffffu, stop, 0);
+      g += x.n_kb;
+    }
+    if (lane == 0) {
       for (int i = 0; i < 3; ++i)
         if (lastk[i] >= 0) mbar_wait_drain(&bars.k_full[i], (uint32_t)lastk[i]);
       for (int i = 0; i < 2; ++i)
         if (lastv[i] >= 0) mbar_wait_drain(&bars.v_full[i], (uint32_t)lastv[i]);
     }
+    __syncwarp();
   } else if (warp == 1 || warp == 2) {
     // ============ two MMA issuers (whole warps, one elected lane issues):
     // warp 1 S(j) and dQ += dS(j) K_j, warp 2 dP(j); disjoint TMEM columns.
@@ -613,59 +701,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dKk = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
     const uint64_t dKm = sdesc_sw128(smem_u32(smem + C::kOffK), kBox, 1024);
     const uint64_t dV = sdesc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_full, 0, guard));
+    bool ok = true;
+    int g = 0, e = 0;                            // steps and non-empty tiles before this one
     if (warp == 1) {
-      auto wait_k = [&](int j) { return __all_sync(0xffffffffu, mbar_wait(&bars.k_full[j % 3], (j / 3) & 1, guard)); };
-      // S(j) = Q K_j^T into S buffer j & 1: A = Q, B = K_j, both K-major
-      auto mma_s = [&](int j) {
-        const uint64_t k = sdesc_add(dKk, (j % 3) * kTile);
+      auto wait_k = [&](int gs) {
+        return __all_sync(0xffffffffu, mbar_wait(&bars.k_full[gs % 3], (gs / 3) & 1, guard));
+      };
+      // S(gs) = Q K^T into S buffer gs & 1: A = Q, B = K, both K-major
+      auto mma_s = [&](int gs) {
+        const uint64_t kd = sdesc_add(dKk, (gs % 3) * kTile);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_ss_warp(tmem + C::kColS + (j & 1) * 128, sdesc_add(dQ, off), sdesc_add(k, off), kIdS, kk > 0);
+          mma_ss_warp(tmem + C::kColS + (gs & 1) * 128, sdesc_add(dQ, off), sdesc_add(kd, off), kIdS, kk > 0);
         }
       };
-      // dQ += dS(j) K_j: A = dS from TMEM (packed over S buffer j & 1), B = K_j [keys x features], MN-major
-      auto mma_dq = [&](int j) {
-        const uint64_t k = sdesc_add(dKm, (j % 3) * kTile);
+      // dQ += dS(gs) K: A = dS from TMEM (packed over S buffer gs & 1), B = K [keys x features], MN-major
+      auto mma_dq = [&](int gs, bool first) {
+        const uint64_t kd = sdesc_add(dKm, (gs % 3) * kTile);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts_warp(tmem + C::kColDQ, tmem + packed_col(C::kColS + (j & 1) * 128, kk), sdesc_add(k, kk * 2048),
-                      kIdDQ, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_warp(tmem + C::kColDQ, tmem + packed_col(C::kColS + (gs & 1) * 128, kk), sdesc_add(kd, kk * 2048),
+                      kIdDQ, (!first || kk > 0) ? 1u : 0u);
       };
-      for (int j = 0; j < 2 && j < n_kb && ok; ++j) {
-        if (!(ok = wait_k(j))) break;
-        tc_fence_after();
-        mma_s(j);
-        tc_commit_warp(&bars.s_full[j]);
-      }
-      for (int j = 0; j < n_kb && ok; ++j) {
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.ds_full, j & 1, guard)))) break;
-        tc_fence_after();
-        mma_dq(j);
-        tc_commit_warp(&bars.k_empty[j % 3]);
-        if (j + 2 < n_kb) {   // S buffer j & 1 is free once dQ(j) has read dS(j): in-order issue
-          if (!(ok = wait_k(j + 2))) break;
+      for (int k = 0; ok; ++k) {
+        int t;
+        if (!(ok = read_tile(k, t)) || t < 0) break;
+        const Tile x = decode(t, false);
+        if (x.empty) continue;
+        const int n = x.n_kb;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_full, e & 1, guard)))) break;
+        for (int j = 0; j < 2 && j < n && ok; ++j) {
+          if (!(ok = wait_k(g + j))) break;
           tc_fence_after();
-          mma_s(j + 2);
-          tc_commit_warp(&bars.s_full[j & 1]);
+          mma_s(g + j);
+          tc_commit_warp(&bars.s_full[(g + j) & 1]);
+          if (j == n - 1) tc_commit_warp(&bars.q_empty);   // the tile's last S: Q may be replaced
         }
+        for (int j = 0; j < n && ok; ++j) {
+          const int gs = g + j;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.ds_full, gs & 1, guard)))) break;
+          if (j == 0 && e >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_free, (e - 1) & 1, guard))))
+            break;                               // the previous tile's dQ has left TMEM
+          tc_fence_after();
+          mma_dq(gs, j == 0);
+          tc_commit_warp(&bars.k_empty[gs % 3]);
+          if (j + 2 < n) {   // S buffer gs & 1 is free once dQ(gs) has read dS(gs): in-order issue
+            if (!(ok = wait_k(gs + 2))) break;
+            tc_fence_after();
+            mma_s(gs + 2);
+            tc_commit_warp(&bars.s_full[gs & 1]);
+            if (j + 2 == n - 1) tc_commit_warp(&bars.q_empty);
+          }
+        }
+        if (ok) tc_commit_warp(&bars.dq_done);
+        g += n;
+        ++e;
       }
-      if (ok) tc_commit_warp(&bars.dq_done);
     } else {
-      // dP(j) = dO V_j^T; the dP columns are free once the compute warps have read dP(j-1)
-      for (int j = 0; j < n_kb && ok; ++j) {
-        if (j > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_read, (j - 1) & 1, guard)))) break;
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.v_full[j & 1], (j >> 1) & 1, guard)))) break;
-        tc_fence_after();
-        const uint64_t v = sdesc_add(dV, (j & 1) * kTile);
+      // dP(gs) = dO V^T; the dP columns are free once the compute warps have read dP(gs-1)
+      for (int k = 0; ok; ++k) {
+        int t;
+        if (!(ok = read_tile(k, t)) || t < 0) break;
+        const Tile x = decode(t, false);
+        if (x.empty) continue;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.do_full, e & 1, guard)))) break;
+        for (int j = 0; j < x.n_kb && ok; ++j) {
+          const int gs = g + j;
+          if (gs > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_read, (gs - 1) & 1, guard)))) break;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.v_full[gs & 1], (gs >> 1) & 1, guard)))) break;
+          tc_fence_after();
+          const uint64_t vd = sdesc_add(dV, (gs & 1) * kTile);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_ss_warp(tmem + C::kColDP, sdesc_add(dDO, off), sdesc_add(v, off), kIdDP, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+            mma_ss_warp(tmem + C::kColDP, sdesc_add(dDO, off), sdesc_add(vd, off), kIdDP, kk > 0);
+          }
+          tc_commit_warp(&bars.dp_full);
+          tc_commit_warp(&bars.v_empty[gs & 1]);
         }
-        tc_commit_warp(&bars.dp_full);
-        tc_commit_warp(&bars.v_empty[j & 1]);
+        g += x.n_kb;
+        ++e;
       }
     }
     tc_commit_warp(&bars.teardown);
@@ -675,70 +791,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wg = (warp - 4) >> 2;
     const int c0 = wg * kCols;                          // first key column of this warpgroup
     const int r = threadIdx.x & 127;                    // query row = TMEM lane
-    const int qi = q0 + r;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float c = a.scale_log2;
-    const long wrow = ws_row(a, s, tok0, h, qi);
-    const bool wrow_ok = GQA_CHECK(wrow >= 0 && wrow < a.ws_rows, a.status, a.dbg_line);
-    const float nlse2 = wrow_ok ? a.lse_log2[wrow] : -INFINITY;   // -LSE*log2(e) (-inf past the sequence)
-    const float ndl = wrow_ok ? a.delta[wrow] : 0.f;              // -Delta
-    const uint64_t c2 = f2(c, c), nl2 = f2(nlse2, nlse2), nd2 = f2(ndl, ndl);
     bool ok = true;
-    for (int j = 0; j < n_kb; ++j) {
-      const uint32_t sb = C::kColS + (j & 1) * 128;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[j & 1], (j >> 1) & 1, guard)))) break;
-      tc_fence_after();
-      float p[kCols];
-      {
-        uint32_t* pv = reinterpret_cast<uint32_t*>(p);
-        tmem_ld_x32(tmem + lane_base + sb + c0, pv);
-        tmem_ld_x32(tmem + lane_base + sb + c0 + 32, pv + 32);
-        tmem_ld_wait();
-        reg_fence<kCols>(pv);
-      }
-#pragma unroll
-      for (int e = 0; e < kCols; e += 2) {
-        f2_split(fma2(f2(p[e], p[e + 1]), c2, nl2), p[e], p[e + 1]);
-        p[e] = ex2_approx(p[e]);
-        p[e + 1] = ex2_approx(p[e + 1]);
-      }
-      const int kbase = j * 128 + c0;                   // key index of this warpgroup's column 0
-      if ((a.causal && j == mb) || kbase + kCols > L || q0 + 128 > L) {
-        const int lim = a.causal ? min(qi + 1, L) : L;   // visible keys: k < lim (none past the sequence)
-#pragma unroll
-        for (int e = 0; e < kCols; ++e)
-          if (kbase + e >= lim || qi >= L) p[e] = 0.f;
-      }
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, j & 1, guard)))) break;
-      tc_fence_after();
-      uint32_t dv[kCols];
-      tmem_ld_x32(tmem + lane_base + C::kColDP + c0, dv);
-      tmem_ld_x32(tmem + lane_base + C::kColDP + c0 + 32, dv + 32);
-      tmem_ld_wait();
-      reg_fence<kCols>(dv);
-      tc_fence_before();
-      mbar_arrive_warp(&bars.dp_read);                  // dP(j+1) may overwrite the dP columns
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int x = q * 32 + 2 * e;
-          float d0, d1;
-          f2_split(mul2(f2(p[x], p[x + 1]), add2(f2(__uint_as_float(dv[x]), __uint_as_float(dv[x + 1])), nd2)), d0,
-                   d1);                                   // P (dP - Delta)
-          w[e] = F16 ? pack_f16x2(d0, d1) : pack_bf16x2(d0, d1);
+    int g = 0, e = 0;                                   // steps and non-empty tiles before this one
+    for (int k = 0; ok; ++k) {
+      int t;
+      if (!(ok = read_tile(k, t)) || t < 0) break;
+      const Tile x = decode(t, false);
+      if (x.empty) continue;
+      const int qi = x.q0 + r;
+      const long wrow = ws_row(a, x.s, x.tok0, x.h, qi);
+      const bool wrow_ok = GQA_CHECK(wrow >= 0 && wrow < a.ws_rows, a.status, a.dbg_line);
+      const float nlse2 = wrow_ok ? a.lse_log2[wrow] : -INFINITY;   // -LSE*log2(e) (-inf past the sequence)
+      const float ndl = wrow_ok ? a.delta[wrow] : 0.f;              // -Delta
+      const uint64_t c2 = f2(c, c), nl2 = f2(nlse2, nlse2), nd2 = f2(ndl, ndl);
+      for (int j = 0; j < x.n_kb; ++j) {
+        const int gs = g + j;
+        const uint32_t sb = C::kColS + (gs & 1) * 128;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[gs & 1], (gs >> 1) & 1, guard)))) break;
+        tc_fence_after();
+        float p[kCols];
+        {
+          uint32_t* pv = reinterpret_cast<uint32_t*>(p);
+          tmem_ld_x32(tmem + lane_base + sb + c0, pv);
+          tmem_ld_x32(tmem + lane_base + sb + c0 + 32, pv + 32);
+          tmem_ld_wait();
+          reg_fence<kCols>(pv);
         }
-        // dS over this warpgroup's first 32 columns of S buffer j & 1: A of dQ += dS K
-        tmem_st_x16(tmem + lane_base + sb + c0 + q * 16, w);
+#pragma unroll
+        for (int e2 = 0; e2 < kCols; e2 += 2) {
+          f2_split(fma2(f2(p[e2], p[e2 + 1]), c2, nl2), p[e2], p[e2 + 1]);
+          p[e2] = ex2_approx(p[e2]);
+          p[e2 + 1] = ex2_approx(p[e2 + 1]);
+        }
+        const int kbase = j * 128 + c0;                   // key index of this warpgroup's column 0
+        if ((a.causal && j == x.mb) || kbase + kCols > x.L || x.q0 + 128 > x.L) {
+          const int lim = a.causal ? min(qi + 1, x.L) : x.L;   // visible keys: k < lim (none past the sequence)
+#pragma unroll
+          for (int e2 = 0; e2 < kCols; ++e2)
+            if (kbase + e2 >= lim || qi >= x.L) p[e2] = 0.f;
+        }
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, gs & 1, guard)))) break;
+        tc_fence_after();
+        uint32_t dv[kCols];
+        tmem_ld_x32(tmem + lane_base + C::kColDP + c0, dv);
+        tmem_ld_x32(tmem + lane_base + C::kColDP + c0 + 32, dv + 32);
+        tmem_ld_wait();
+        reg_fence<kCols>(dv);
+        tc_fence_before();
+        mbar_arrive_warp(&bars.dp_read);                  // dP(gs+1) may overwrite the dP columns
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e2 = 0; e2 < 16; ++e2) {
+            const int xx = q * 32 + 2 * e2;
+            float d0, d1;
+            f2_split(mul2(f2(p[xx], p[xx + 1]), add2(f2(__uint_as_float(dv[xx]), __uint_as_float(dv[xx + 1])), nd2)),
+                     d0, d1);                               // P (dP - Delta)
+            w[e2] = F16 ? pack_f16x2(d0, d1) : pack_bf16x2(d0, d1);
+          }
+          // dS over this warpgroup's first 32 columns of S buffer gs & 1: A of dQ += dS K
+          tmem_st_x16(tmem + lane_base + sb + c0 + q * 16, w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_warp(&bars.ds_full);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive_warp(&bars.ds_full);
-    }
-    // ------------------------------------------------------- dQ epilogue
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_done, 0, guard));
-    if (ok) {
+      if (!ok) break;
+      // ----------------------------------------------------- dQ epilogue
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.dq_done, e & 1, guard)))) break;
       tc_fence_after();
       // warpgroup wg: feature pairs (i, i + D/2) for i in [NP wg, NP wg + NP)
       constexpr int NP = D / 4;
@@ -748,39 +871,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       reg_fence<NP>(reinterpret_cast<uint32_t*>(lo));
       reg_fence<NP>(reinterpret_cast<uint32_t*>(hi));
-      if (F16 && qi < L && GQA_CHECK(qi < a.n_table, a.status, a.dbg_line))
+      tc_fence_before();
+      mbar_arrive_warp(&bars.dq_free);                  // the next tile's dQ may overwrite the accumulator
+      if (F16 && qi < x.L && GQA_CHECK(qi < a.n_table, a.status, a.dbg_line))
         rope_grad_transpose<D, NP>(lo, hi, a.rope_cs, qi, NP * wg);
-      const uint32_t srow = smem_u32(smem + C::kOffQ) + r * (2 * D);   // the Q tile is dead: every MMA has completed
+      // staged through the dO tile: every dP of this tile has completed (its
+      // dS came before dq_done), and the next dO waits for do_empty
+      const uint32_t srow = smem_u32(smem + C::kOffDO) + r * (2 * D);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        const float* x = half == 0 ? lo : hi;
+        const float* xv = half == 0 ? lo : hi;
 #pragma unroll
         for (int cc = 0; cc < NP / 8; ++cc) {
           const int ch = half * (D / 16) + wg * (NP / 8) + cc;
-          st_shared_v4(srow + ((ch ^ (r & 7)) << 4), pack_bf16x2(x[8 * cc] * a.scale, x[8 * cc + 1] * a.scale),
-                       pack_bf16x2(x[8 * cc + 2] * a.scale, x[8 * cc + 3] * a.scale),
-                       pack_bf16x2(x[8 * cc + 4] * a.scale, x[8 * cc + 5] * a.scale),
-                       pack_bf16x2(x[8 * cc + 6] * a.scale, x[8 * cc + 7] * a.scale));
+          st_shared_v4(srow + ((ch ^ (r & 7)) << 4), pack_bf16x2(xv[8 * cc] * a.scale, xv[8 * cc + 1] * a.scale),
+                       pack_bf16x2(xv[8 * cc + 2] * a.scale, xv[8 * cc + 3] * a.scale),
+                       pack_bf16x2(xv[8 * cc + 4] * a.scale, xv[8 * cc + 5] * a.scale),
+                       pack_bf16x2(xv[8 * cc + 6] * a.scale, xv[8 * cc + 7] * a.scale));
         }
       }
       __syncwarp();
       // this warp's 32 rows, the 2 NP / 8 chunks this warpgroup wrote in each
       constexpr int kMine = 2 * (NP / 8);
-      const int rows_valid = min(128, L - q0);
+      const int rows_valid = min(128, x.L - x.q0);
       const int row0 = (warp & 3) * 32;
-      const uint32_t sbase = smem_u32(smem + C::kOffQ);
+      const uint32_t sbase = smem_u32(smem + C::kOffDO);
       for (int idx = lane; idx < 32 * kMine; idx += 32) {
         const int row = row0 + idx / kMine, k8 = idx % kMine;
         const int cch = (k8 / (NP / 8)) * (D / 16) + wg * (NP / 8) + k8 % (NP / 8);
-        const long off = row_off(a, s, tok0, h, a.Hq, q0 + row, D) + cch * 8;
+        const long off = row_off(a, x.s, x.tok0, x.h, a.Hq, x.q0 + row, D) + cch * 8;
         if (row < rows_valid && GQA_CHECK(off >= 0 && off + 8 <= elems(a, a.Hq), a.status, a.dbg_line)) {
           const uint4 val = ld_shared_v4(sbase + row * (2 * D) + ((cch ^ (row & 7)) << 4));
           *reinterpret_cast<uint4*>(a.dq + off) = val;
         }
       }
+      mbar_arrive_warp(&bars.do_empty);                 // the staging area may take the next dO
+      g += x.n_kb;
+      ++e;
     }
   }
 
+  // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -815,7 +946,16 @@ static cudaError_t launch_split(const CUtensorMap& q, const CUtensorMap& k, cons
   // griddep_wait, which is when that grid lets this one start) and writes
   // only dQ, so it never waits on the dK/dV grid: its CTAs fill the SMs that
   // grid leaves idle (its tail; all of a small grid's spare SMs).
-  const long q_grid = (long)a.n_items * a.num_seqs * a.Hq;
+  // persistent: at most one CTA per SM, each taking tiles until none is left
+  static int sms[64] = {};
+  if (dev < 64 && sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return cudaErrorUnknown;
+    sms[dev] = n;
+  }
+  const long n_sm = dev < 64 ? sms[dev] : 148;
+  const long q_tiles = (long)a.n_items * a.num_seqs * a.Hq;
+  const long q_grid = q_tiles < n_sm ? q_tiles : n_sm;
   prof_begin(kProfBwdDq, stream);
   e = launch_programmatic(bwd_dq_kernel<D, F16>, dim3((unsigned)q_grid), dim3(kThreads), kQSmem<D>, stream, q, k, v,
                           dout, a);

@@ -51,6 +51,7 @@ struct BwdArgs {
   __nv_bfloat16* dv;
   float* delta;           // workspace: -Delta, [B,Hq,T_pad] or [Hq,total_pad]
   float* lse_log2;        // workspace: -LSE * log2(e), same layout as delta
+  int* tile_counter;      // workspace: the dQ kernel's next tile (zeroed by the preprocess)
   const int* cu_seqlens;
   int* status;
   int num_seqs;
@@ -69,8 +70,9 @@ struct BwdArgs {
   // dQ rows get the transposed rotation at their positions
   const float* rope_cs;
   // failure-path test only (attn_test_inject_timeout): in the kernel named by
-  // inject_kernel (1 dK/dV, 2 dQ), CTA 0's producer stops before the load of
-  // step inject_step and every wait gives up after wait_ns
+  // inject_kernel (1 dK/dV, 2 dQ), the producer of CTA 0 (dK/dV) or of the
+  // CTA that takes the first tile (dQ) stops before the load of step
+  // inject_step, and every wait gives up after wait_ns
   int inject_kernel;
   int inject_step;
   uint64_t wait_ns;

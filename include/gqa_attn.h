@@ -83,10 +83,12 @@ GQA_ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int T, int D
 /* Backward, dense layout.  Reads Q, K, V, the forward's O and LSE, and dO;
  * writes dQ, dK, dV (bf16).  workspace: device memory of at least
  * attn_bwd_workspace_size() bytes, 256-byte aligned, owned by the caller; it
- * holds Delta and LSE*log2(e) per query row and needs no initialisation.
- * dK and dV come from a key/value-stationary kernel, dQ from a
- * query-stationary one; each sums its products in a fixed order, so the
- * results are bit-reproducible. */
+ * holds Delta and LSE*log2(e) per query row and the dQ kernel's tile counter,
+ * and needs no initialisation (the call writes all of it first); two calls
+ * in flight at once need two workspaces.  dK and dV come from a
+ * key/value-stationary kernel, dQ from a persistent query-stationary one
+ * that takes its tiles from that counter; each tile's gradient is summed in
+ * a fixed order inside one CTA, so the results are bit-reproducible. */
 GQA_ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                      const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                      int B, int Hq, int Hkv, int T, int D, int causal, float scale, void* stream);
@@ -338,8 +340,10 @@ GQA_ATTN_API attn_status attn_selftest_wait_timeout(int limit_ms, void* stream);
  * kernel: 1 the forward (attn_fwd and attn_fwd_rope), 2 the backward's dK/dV
  * kernel, 3 the backward's dQ kernel (attn_bwd and its variants); 0 disarms.
  * In that launch every bounded wait gives up after limit_ms (1..5000) instead
- * of the usual 2 s, and the first CTA's TMA producer stops before the loads
- * of its second step, so one of that CTA's waits expires.  The kernel then
+ * of the usual 2 s, and one CTA's TMA producer stops before the loads of
+ * its second step (the forward's and the dK/dV kernel's first CTA; for the
+ * persistent dQ kernel, the CTA that takes its first tile), so one of that
+ * CTA's waits expires.  The kernel then
  * records ATTN_ERR_TIMEOUT in the device status word, its other roles see
  * the CTA's abort flag and stop, the issued copies and MMAs are drained,
  * TMEM is freed and the kernel returns: the GPU is neither hung nor faulted

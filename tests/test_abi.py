@@ -115,15 +115,16 @@ def test_noalloc_validation(lib):
 
 
 def test_workspace_sizes(lib):
-    # Delta + LSE*log2e: 256-aligned f32 rows each; rows = B*Hq*roundup(T,128)
+    # Delta + LSE*log2e: 256-aligned f32 rows each; rows = B*Hq*roundup(T,128);
+    # then 256 bytes for the dQ kernel's tile counter
     rows = 2 * 32 * 4096
-    assert lib.attn_bwd_workspace_size(2, 32, 8, 4096, 128) == 2 * rows * 4
+    assert lib.attn_bwd_workspace_size(2, 32, 8, 4096, 128) == 2 * rows * 4 + 256
     rows = 1 * 4 * 256
-    assert lib.attn_bwd_workspace_size(1, 4, 2, 129, 64) == 2 * rows * 4
+    assert lib.attn_bwd_workspace_size(1, 4, 2, 129, 64) == 2 * rows * 4 + 256
     assert lib.attn_bwd_workspace_size(1, 3, 2, 16, 64) == 0
     pad = -(-(17000 + 132 * 16 + 256) // 128) * 128        # packed rows per head
-    assert lib.attn_varlen_bwd_workspace_size(16, 17000, 16, 8, 128) == 2 * (-(-16 * pad * 4 // 256) * 256)
-    assert lib.attn_varlen_bwd_workspace_size(16, 17000, 16, 8, 64) == 2 * (-(-16 * pad * 4 // 256) * 256)
+    assert lib.attn_varlen_bwd_workspace_size(16, 17000, 16, 8, 128) == 2 * (-(-16 * pad * 4 // 256) * 256) + 256
+    assert lib.attn_varlen_bwd_workspace_size(16, 17000, 16, 8, 64) == 2 * (-(-16 * pad * 4 // 256) * 256) + 256
     assert lib.attn_varlen_bwd_workspace_size(2, 10, 4, 2, 96) == 0
     # rotary backward: the two rotated f16 copies (256-aligned) before attn_bwd's workspace
     qk = -(-(2 * 32 * 4096 * 128 * 2) // 256) * 256 + 2 * 8 * 4096 * 128 * 2
