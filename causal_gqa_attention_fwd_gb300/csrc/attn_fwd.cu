@@ -78,6 +78,7 @@ struct __align__(8) FwdBarriers {
   uint64_t kv_empty[8];
   uint64_t s_full[2];
   uint64_t p_full[2];
+  uint64_t p_half[2];    // D = 128: keys 0-63 of P are in TMEM (p_full: all of P)
   uint64_t o_done[2];
   uint64_t s_free[2];    // D = 64: the softmax has read S into registers
   uint64_t pv_done[2];   // D = 64: a tile's P V has completed
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bars.q_full[i], 1);
       mbar_init(&bars.s_full[i], 1);
       mbar_init(&bars.p_full[i], kBM / 32);      // one arrive per softmax warp
+      mbar_init(&bars.p_half[i], kBM / 32);
       mbar_init(&bars.o_done[i], 1);
       mbar_init(&bars.s_free[i], kBM / 32);
       mbar_init(&bars.pv_done[i], 1);
@@ -265,14 +267,16 @@ __global__ void __launch_bounds__(384, 1)
                  C::kIdescQK, kk > 0);
         }
       };
-      auto issue_pv = [&](int x, int st, int acc) {
+      // P V over the keys [16 kk0, 16 kk1) of the block (P packed in TMEM)
+      auto issue_pv_part = [&](int x, int st, int acc, int kk0, int kk1) {
         const uint32_t va = ring_addr + st * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
+        for (int kk = kk0; kk < kk1; ++kk) {
           mma_ts_warp(tmem + C::col_o(x), tmem + C::col_p(x) + kk * 8, sdesc_sw128(va + kk * 2048, C::kBoxBytes, 1024),
                  C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
         }
       };
+      auto issue_pv = [&](int x, int st, int acc) { issue_pv_part(x, st, acc, 0, kBN / 16); };
       // K_j sits at ring index 2j, V_j at 2j + 1.
       auto stage_of = [&](int idx) { return idx % C::kStages; };
       auto phase_of = [&](int idx) { return (uint32_t)((idx / C::kStages) & 1); };
@@ -328,10 +332,16 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         for (int x = 0; x < 2 && ok; ++x) {
           if (j >= ti[x].nkv) continue;
+          // P_j arrives in two halves (keys 0-63, then 64-127): the first
+          // half's P V runs while the softmax forms the second half
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_half[x], j & 1, guard));
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv_part(x, stage_of(vi), j > 0, 0, kBN / 32);
           ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_full[x], j & 1, guard));
           if (!ok) break;
           tc_fence_after();
-          issue_pv(x, stage_of(vi), j > 0);
+          issue_pv_part(x, stage_of(vi), 1, kBN / 32, kBN / 16);
           if (j + 1 < ti[x].nkv) {
             issue_qk(x, stage_of(ki));
             tc_commit_warp(&bars.s_full[x]);
@@ -415,6 +425,24 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_after();
           }
         }
+        // Split P (D = 128): O is rescaled first (P_{j-1} V_{j-1} has
+        // completed: the commit of S_j covered it), then P goes out in two
+        // halves, signalled on p_half and p_full (each completes once per
+        // step), so the first half's P V overlaps the second half's
+        // exponentials.
+        constexpr bool kSplitP = !C::kSepP;
+        if (kSplitP && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld_x32(tO + q * 32, o);
+            tmem_ld_wait();
+            reg_fence<32>(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st_x32(tO + q * 32, o);
+          }
+        }
         // p = 2^(s c - m): exponent arguments and the row sum in paired f32
         const uint64_t c2 = f2(c, c), nm2 = f2(-m_use, -m_use);
         uint64_t acc[4] = {0, 0, 0, 0};
@@ -430,12 +458,17 @@ __global__ void __launch_bounds__(384, 1)
             pk[i] = pack_bf16x2(p0, p1);
           }
           tmem_st_x16(tP + q * 16, pk);
+          if (kSplitP && q == kBN / 64 - 1) {
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive_warp(&bars.p_half[x]);   // keys 0-63 of P_j are in TMEM
+          }
         }
         float rs0, rs1;
         f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), rs0, rs1);
         const float rs = rs0 + rs1;
         l_run = l_run * alpha + rs;
-        if (__any_sync(0xffffffffu, resc)) {
+        if (!kSplitP && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
           for (int q = 0; q < D / 32; ++q) {
             uint32_t o[32];
