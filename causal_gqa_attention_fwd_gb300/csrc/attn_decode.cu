@@ -75,7 +75,6 @@ constexpr int kBoxBytes = kCK * 128;      // 64 features x 128 keys, bf16
 constexpr int kRowBoxBytes = kRows * 128; // 64 features (or keys) x 16 rows, bf16
 constexpr int kThreads = 256;             // 16-bit caches: 8 warps
 constexpr int kThreads8 = 384;            // E4M3 caches: 8 warps + 4 V converter warps
-constexpr uint32_t kTmemCols = 64;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // kind::f16 instruction descriptor with f32 accumulation and bf16 (f16 = false)
@@ -83,6 +82,19 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 __host__ __device__ constexpr uint32_t idesc_16(int M, int N, bool a_mn, bool b_mn, bool f16) {
   return f16 ? (idesc_bf16(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10))) : idesc_bf16(M, N, a_mn, b_mn);
 }
+
+// TMEM columns (lane = key of the chunk for S^T, feature for O^T): two S^T
+// buffers, then two O^T buffers of kRows columns.  An E4M3 score MMA stacks
+// the three query part tiles along N, so its S^T buffers are 3 kRows wide
+// and the softmax adds the three column groups.
+template <bool FP8>
+constexpr int kSCols = (FP8 ? 3 : 1) * kRows;
+template <bool FP8>
+constexpr uint32_t kTmemCols = FP8 ? 128 : 64;
+template <bool FP8>
+__device__ __forceinline__ uint32_t col_s(int b) { return (uint32_t)(b * kSCols<FP8>); }
+template <bool FP8>
+__device__ __forceinline__ uint32_t col_o(int b) { return (uint32_t)(2 * kSCols<FP8> + b * kRows); }
 
 template <int D, bool FP8>
 struct DecCfg {
@@ -117,7 +129,7 @@ struct DecCfg {
   static constexpr int kSmemBytes = kOffQs + 2 * kRows * 4 + 1024;  // + alignment slack
   // score MMA: bf16 x bf16 (kind::f16), or E4M3 K codes x E4M3 query parts
   // (kind::f8f6f4, format code 0 for both); P V MMA: bf16, or f16 V and P
-  static constexpr uint32_t kIdescS = idesc_16(kCK, kRows, false, false, FP8);
+  static constexpr uint32_t kIdescS = idesc_16(kCK, kSCols<FP8>, false, false, FP8);
   static constexpr uint32_t kIdescO = idesc_16(128, kRows, true, false, FP8);
   // V^T as an MN-major A operand of 128 rows: the second 64-feature atom is
   // the second box (D = 128) or the first one again (D = 64; rows 64-127 of
@@ -127,9 +139,6 @@ struct DecCfg {
   static_assert(kMaxSlots <= 8, "barrier arrays");
   static_assert(kSmemBytes + 2048 <= 232448, "shared memory (dynamic + static: barriers, lengths)");
 };
-
-__device__ __forceinline__ uint32_t col_s(int b) { return (uint32_t)b * kRows; }
-__device__ __forceinline__ uint32_t col_o(int b) { return 32u + (uint32_t)b * kRows; }
 
 // One piece: a run of a unit's chunks inside one CTA's share.
 struct Piece {
@@ -561,7 +570,7 @@ __device__ __noinline__ void rope_rotate_tile(uint8_t* qs, uint8_t* qrem, const 
 // its O^T, read this thread's feature row of it, release the buffer and
 // write O / LSE (one-split unit) or the unnormalised partial and its
 // (max, sum) -- the row statistics wait in shared memory (s_fin).
-template <int D>
+template <int D, bool FP8>
 __device__ __noinline__ void decode_write_out(const DecodeArgs& a, const Piece& it, int uses, uint32_t tmem_lane,
                                               uint64_t* o_full, uint64_t* o_empty, const float2* s_fin, int j,
                                               const Guard& guard) {
@@ -569,7 +578,7 @@ __device__ __noinline__ void decode_write_out(const DecodeArgs& a, const Piece& 
   mbar_wait(&o_full[ob], (uses >> 1) & 1, guard);
   tc_fence_after();
   uint32_t ov[kRows];
-  tmem_ld_x16(tmem_lane + col_o(ob), ov);
+  tmem_ld_x16(tmem_lane + col_o<FP8>(ob), ov);
   tmem_ld_wait();
   reg_fence<kRows>(ov);
   tc_fence_before();
@@ -654,7 +663,7 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bars.tmem_base, kTmemCols);
+    tmem_alloc(&bars.tmem_base, kTmemCols<FP8>);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -808,15 +817,15 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
       if (!guard.aborted()) {
         const uint32_t ka = sbase + slot * C::kTileK;
         if constexpr (FP8) {
-          // E4M3 K codes x the three E4M3 query parts, 32 features per MMA
+          // E4M3 K codes x the three E4M3 query parts, 32 features per MMA:
+          // the part tiles lie back to back (row 16 t + r of a 48-row K-major
+          // operand is row r of part t), so one N = 48 MMA covers all three
           const uint32_t qa = sbase + C::kOffQ8 + qslot * 3 * C::kQ8Bytes;
           auto desc8 = [](uint32_t addr) { return D == 128 ? sdesc_sw128(addr, 16, 1024) : sdesc_sw64(addr, 16, 512); };
 #pragma unroll
-          for (int t = 0; t < 3; ++t)
-#pragma unroll
-            for (int kk = 0; kk < D / 32; ++kk)
-              mma_ss_f8_warp(tmem + col_s(sb), desc8(ka + kk * 32), desc8(qa + t * C::kQ8Bytes + kk * 32), C::kIdescS,
-                             (t > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < D / 32; ++kk)
+            mma_ss_f8_warp(tmem + col_s<FP8>(sb), desc8(ka + kk * 32), desc8(qa + kk * 32), C::kIdescS,
+                           kk > 0 ? 1u : 0u);
         } else {
           const uint32_t qa = sbase + C::kOffQ + qslot * C::kQSlot;
           // rotary queries are a bf16 value tile plus a bf16 remainder tile: both accumulate
@@ -824,7 +833,7 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
           for (int tq = 0; tq < tiles; ++tq)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss_warp(tmem + col_s(sb), sdesc_sw128(ka + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+              mma_ss_warp(tmem + col_s<FP8>(sb), sdesc_sw128(ka + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
                           sdesc_sw128(qa + tq * C::kQBytes + (kk >> 2) * kRowBoxBytes + (kk & 3) * 32, 16, 1024),
                           C::kIdescS, (tq > 0 || kk > 0) ? 1u : 0u);
         }
@@ -863,7 +872,7 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
         const uint32_t pa = sbase + C::kOffP + pb * C::kPBytes;
 #pragma unroll
         for (int kk = 0; kk < kCK / 16; ++kk)
-          mma_ss_warp(tmem + col_o(ob), sdesc_sw128(va + kk * 2048, C::kLboV, 1024),
+          mma_ss_warp(tmem + col_o<FP8>(ob), sdesc_sw128(va + kk * 2048, C::kLboV, 1024),
                       sdesc_sw128(pa + (kk >> 2) * kRowBoxBytes + (kk & 3) * 32, 16, 1024), C::kIdescO,
                       (cur.c > 0 || kk > 0) ? 1u : 0u);
       }
@@ -898,7 +907,7 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
     int pend_uses = 0;
     auto write_out = [&]() {
       pend = false;
-      decode_write_out<D>(a, pend_it, pend_uses, tmem + lane_off, bars.o_full, bars.o_empty, s_fin, j, guard);
+      decode_write_out<D, FP8>(a, pend_it, pend_uses, tmem + lane_off, bars.o_full, bars.o_empty, s_fin, j, guard);
     };
     for (Cursor cur = begin(); cur.valid; next(cur)) {
       const Piece& it = cur.it;
@@ -921,9 +930,24 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
       mbar_wait(&bars.s_full[sb], (i >> 1) & 1, guard);
       tc_fence_after();
       uint32_t sr[kRows];
-      tmem_ld_x16(tmem + lane_off + col_s(sb), sr);
-      tmem_ld_wait();
-      reg_fence<kRows>(sr);
+      if constexpr (FP8) {
+        // the three query parts' scores, summed in order
+        uint32_t s1[kRows], s2[kRows];
+        tmem_ld_x16(tmem + lane_off + col_s<FP8>(sb), sr);
+        tmem_ld_x16(tmem + lane_off + col_s<FP8>(sb) + kRows, s1);
+        tmem_ld_x16(tmem + lane_off + col_s<FP8>(sb) + 2 * kRows, s2);
+        tmem_ld_wait();
+        reg_fence<kRows>(sr);
+        reg_fence<kRows>(s1);
+        reg_fence<kRows>(s2);
+#pragma unroll
+        for (int r = 0; r < kRows; ++r)
+          sr[r] = __float_as_uint((__uint_as_float(sr[r]) + __uint_as_float(s1[r])) + __uint_as_float(s2[r]));
+      } else {
+        tmem_ld_x16(tmem + lane_off + col_s<FP8>(sb), sr);
+        tmem_ld_wait();
+        reg_fence<kRows>(sr);
+      }
       tc_fence_before();
       mbar_arrive_warp(&bars.s_empty[sb]);
 
@@ -1012,7 +1036,7 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
         const int pp = (i - 1) & 1;
         mbar_wait(&bars.p_empty[pp], ((i - 1) >> 1) & 1, guard);
         tc_fence_after();
-        const uint32_t to = tmem + lane_off + col_o(cur.uses & 1);
+        const uint32_t to = tmem + lane_off + col_o<FP8>(cur.uses & 1);
         uint32_t ov[kRows];
         tmem_ld_x16(to, ov);
         tmem_ld_wait();
@@ -1093,7 +1117,7 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols<FP8>);
 }
 
 // One CTA per output row (b, h, t) of a cut unit (rows of units processed
