@@ -304,9 +304,10 @@ def decode_parity_leg(w, x, o, lse):
     lens = x["cache_lens"]
     rows = sorted({int(lens.argmin()), int(lens.argmax())})
     q, ln = f(x["q"][rows]), lens[rows].numpy()
+    rope = x["rope_cs"].double().numpy() if w.rope else None
     if w.fp8:
         ro, rlse = oracle.fp8_decode_fwd(q, x["k8"][rows].numpy(), x["v8"][rows].numpy(), x["k_scale"], x["v_scale"],
-                                         ln, scale=w.softmax_scale)
+                                         ln, scale=w.softmax_scale, rope_cos_sin=rope)
     elif w.page_size:
         bt = x["block_table"][rows]
         used = sorted({int(e) for r, n in zip(bt, ln) for e in r[: (int(n) + w.page_size - 1) // w.page_size]})
@@ -314,9 +315,10 @@ def decode_parity_leg(w, x, o, lse):
         bt_sub = np.array([[remap.get(int(e), 0) for e in r] for r in bt], dtype=np.int32)
         idx = torch.tensor(used, dtype=torch.int64)
         ro, rlse = oracle.paged_decode_fwd(q, f(x["k_pages"][idx]), f(x["v_pages"][idx]), bt_sub, ln,
-                                           scale=w.softmax_scale)
+                                           scale=w.softmax_scale, rope_cos_sin=rope)
     else:
-        ro, rlse = oracle.decode_fwd(q, f(x["k_cache"][rows]), f(x["v_cache"][rows]), ln, scale=w.softmax_scale)
+        ro, rlse = oracle.decode_fwd(q, f(x["k_cache"][rows]), f(x["v_cache"][rows]), ln, scale=w.softmax_scale,
+                                     rope_cos_sin=rope)
     res = P.compare("o", f(o.cpu()[rows]), ro, P.TOL_REL_O)
     le = P.compare_lse(f(lse.cpu()[rows]), rlse)
     keep = ("rel_fro", "rel_tol", "max_abs", "flat_excess", "ulp_excess", "widened_excess", "max_ref", "meets")
@@ -366,12 +368,14 @@ def decode_bytes(w: W.DecodeWorkload, lens) -> int:
     """Algorithmic bytes of one decode call: K and V rows inside each row's
     cache (2 bytes each, 1 for E4M3 caches), Q read, O written (bf16), LSE
     written (f32), the lengths (paged: and the block-table entries of the
-    pages that hold keys)."""
+    pages that hold keys; rotary queries: the f32 table row of each query
+    position)."""
     lens = torch.as_tensor(lens, dtype=torch.int64)
     kv = 2 * w.Hkv * w.D * (1 if w.fp8 else 2) * int(lens.sum())
     qo = 2 * w.B * w.Hq * w.Tq * w.D * 2
     table = 4 * int(((lens + w.page_size - 1) // w.page_size).sum()) if w.page_size else 0
-    return kv + qo + w.B * w.Hq * w.Tq * 4 + w.B * 4 + table
+    rope = 4 * w.D * w.B * w.Tq if w.rope else 0
+    return kv + qo + w.B * w.Hq * w.Tq * 4 + w.B * 4 + table + rope
 
 
 def oracle_decode_sample(w: W.DecodeWorkload, x, budget_s: float):
@@ -389,6 +393,7 @@ def oracle_decode_sample(w: W.DecodeWorkload, x, budget_s: float):
     kp = vp = None
     if w.page_size:
         kp, vp = f(x["k_pages"]), f(x["v_pages"])
+    rope = x["rope_cs"].double().numpy() if w.rope else None
     while rows == 0 or (elapsed < budget_s and rows < w.B):
         b = rows
         lens = x["cache_lens"][b:b + 1]
@@ -403,11 +408,11 @@ def oracle_decode_sample(w: W.DecodeWorkload, x, budget_s: float):
             args = (f(x["q"][b:b + 1]), f(x["k_cache"][b:b + 1]), f(x["v_cache"][b:b + 1]), lens.numpy())
             fn = oracle.decode_fwd
         t0 = time.perf_counter()
-        fn(*args, scale=w.softmax_scale)
+        fn(*args, scale=w.softmax_scale, rope_cos_sin=rope)
         elapsed += time.perf_counter() - t0
         rows += 1
         one = W.DecodeWorkload("s", B=1, Hq=w.Hq, Hkv=w.Hkv, Tq=w.Tq, S=w.S, D=w.D, min_len=0, max_len=0,
-                               page_size=w.page_size, fp8=w.fp8)
+                               page_size=w.page_size, fp8=w.fp8, rope=w.rope)
         done += decode_bytes(one, lens)
     desc = f"{rows} of {w.B} batch rows of {w.name} (whole caches), fp64, {elapsed:.1f} s"
     return done / elapsed, desc, cores, elapsed
@@ -421,6 +426,8 @@ def decode_config(w: W.DecodeWorkload, world: int, l2: str):
         c["paged"] = f"pages of {w.page_size} positions, [num_pages, Hkv, page, D], shuffled over the pool"
     if w.fp8:
         c["kv_cache"] = "E4M3 codes with one scale per cache (amax -> 448), N(0,1) source values"
+    if w.rope:
+        c["rope"] = "queries rotated in the kernel at their positions (rotate-half, base 10000, f32 table)"
     return c
 
 
@@ -437,8 +444,11 @@ def run_decode(args, world, rank, local):
         names = ("q", "k_pages", "v_pages", "block_table", "cache_lens")
     else:
         names = ("q", "k_cache", "v_cache", "cache_lens")
+    if w.rope:
+        names = names + ("rope_cs",)
     dx = {n: x[n].to(dev) for n in names}
     q, lens = dx["q"], dx["cache_lens"]
+    rcs = dx.get("rope_cs")
     scale = w.softmax_scale
     ws_bytes = gq.attn_decode_workspace_size(w.B, w.Hq, w.Hkv, w.Tq, w.S, w.D)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
@@ -448,12 +458,13 @@ def run_decode(args, world, rank, local):
     def step():
         if w.fp8:
             gq.attn_decode_fp8_fwd(q, dx["k8"], dx["v8"], x["k_scale"], x["v_scale"], lens, scale=scale, o=o,
-                                   lse=lse, workspace=ws)
+                                   lse=lse, workspace=ws, rope_cos_sin=rcs)
         elif w.page_size:
             gq.attn_decode_paged_fwd(q, dx["k_pages"], dx["v_pages"], dx["block_table"], lens, scale=scale, o=o,
-                                     lse=lse, workspace=ws)
+                                     lse=lse, workspace=ws, rope_cos_sin=rcs)
         else:
-            gq.attn_decode_fwd(q, dx["k_cache"], dx["v_cache"], lens, scale=scale, o=o, lse=lse, workspace=ws)
+            gq.attn_decode_fwd(q, dx["k_cache"], dx["v_cache"], lens, scale=scale, o=o, lse=lse, workspace=ws,
+                               rope_cos_sin=rcs)
 
     step()
 

@@ -84,11 +84,12 @@ __host__ __device__ constexpr uint32_t idesc_16(int M, int N, bool a_mn, bool b_
 }
 
 // TMEM columns (lane = key of the chunk for S^T, feature for O^T): two S^T
-// buffers, then two O^T buffers of kRows columns.  An E4M3 score MMA stacks
-// the three query part tiles along N, so its S^T buffers are 3 kRows wide
-// and the softmax adds the three column groups.
+// buffers, then two O^T buffers of kRows columns.  A score MMA stacks the
+// query operand's parts along N -- the three E4M3 part tiles, or a rotary
+// query's bf16 value and remainder rows -- so the S^T buffers are 3 (2)
+// kRows wide and the softmax adds the column groups.
 template <bool FP8>
-constexpr int kSCols = (FP8 ? 3 : 1) * kRows;
+constexpr int kSCols = (FP8 ? 3 : 2) * kRows;
 template <bool FP8>
 constexpr uint32_t kTmemCols = FP8 ? 128 : 64;
 template <bool FP8>
@@ -115,9 +116,12 @@ struct DecCfg {
   static constexpr int kOffStage = kOffV + (FP8 ? kVop : kSlotsV) * kTileBytes;  // FP8 V staging ring
   static constexpr int kOffQ = kOffStage + (FP8 ? kSlotsV * kTile8 : 0);
   static constexpr int kQBytes = NB * kRowBoxBytes;       // 16 query rows, bf16, K-major
-  // query slots (one per piece, two pieces): bf16 [value tile, remainder
-  // tile]; FP8 [bf16 tile] followed by [three E4M3 part tiles] per slot
-  static constexpr int kQSlot = (FP8 ? 1 : 2) * kQBytes;
+  // query slots (one per piece, two pieces): bf16 caches, per 64-feature box
+  // the 16 value rows then the 16 remainder rows (rotary queries), so that
+  // one 32-row K-major operand covers both; FP8 [bf16 tile] followed by
+  // [three E4M3 part tiles] per slot
+  static constexpr int kQBoxStride = (FP8 ? 1 : 2) * kRowBoxBytes;
+  static constexpr int kQSlot = NB * kQBoxStride;
   static constexpr int kQ8Bytes = kRows * D;              // one E4M3 part: 16 rows of D bytes, K-major
   static constexpr int kOffQ8 = kOffQ + 2 * kQSlot;
   static constexpr int kPBytes = 2 * kRowBoxBytes;        // 16 rows x 128 keys, K-major
@@ -130,6 +134,7 @@ struct DecCfg {
   // score MMA: bf16 x bf16 (kind::f16), or E4M3 K codes x E4M3 query parts
   // (kind::f8f6f4, format code 0 for both); P V MMA: bf16, or f16 V and P
   static constexpr uint32_t kIdescS = idesc_16(kCK, kSCols<FP8>, false, false, FP8);
+  static constexpr uint32_t kIdescS1 = idesc_16(kCK, kRows, false, false, FP8);   // bf16, plain queries
   static constexpr uint32_t kIdescO = idesc_16(128, kRows, true, false, FP8);
   // V^T as an MN-major A operand of 128 rows: the second 64-feature atom is
   // the second box (D = 128) or the first one again (D = 64; rows 64-127 of
@@ -509,20 +514,24 @@ __device__ __noinline__ void q_tile_to_e4m3_parts(const uint8_t* qt, uint8_t* pa
 }
 
 // Rotary embedding of a piece's query rows (one warp, out of line), written
-// back as bf16 value (over the loaded rows) plus bf16 remainder (qrem):
-// row r is query position t = (r0 + r) % Tq of its head, at position
-// len - Tq + t of the row; feature i pairs with i + D/2 (rotate-half),
-// x'_i = x_i c - x_{i+D/2} s, x'_{i+D/2} = x_{i+D/2} c + x_i s with c, s from
-// the table row of that position.  The tile is K-major, 128-byte swizzled:
-// feature d of row r sits in box d / 64, 16-byte chunk ((d % 64) / 8) ^ (r % 8).
+// back as bf16 value (over the loaded rows) plus bf16 remainder (the 16 rows
+// under them in the same box): row r is query position t = (r0 + r) % Tq of
+// its head, at position len - Tq + t of the row; feature i pairs with
+// i + D/2 (rotate-half), x'_i = x_i c - x_{i+D/2} s,
+// x'_{i+D/2} = x_{i+D/2} c + x_i s with c, s from the table row of that
+// position.  The slot is K-major, 128-byte swizzled, one 4 KB box per 64
+// features (value rows 0-15, remainder rows 16-31): feature d of row r sits
+// in box d / 64, row r (value) or 16 + r (remainder), 16-byte chunk
+// ((d % 64) / 8) ^ (r % 8).
 template <int D>
-__device__ __noinline__ void rope_rotate_tile(uint8_t* qs, uint8_t* qrem, const Piece& it, const DecodeArgs& a,
-                                              int lane) {
+__device__ __noinline__ void rope_rotate_tile(uint8_t* qs, const Piece& it, const DecodeArgs& a, int lane) {
   constexpr int H = D / 2;
   constexpr int kChunks = H / 8;  // 8-feature chunks of the low half
-  auto off = [&](int r, int d) { return (d >> 6) * kRowBoxBytes + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4); };
+  auto off = [&](int r, int d) {
+    return (d >> 6) * (2 * kRowBoxBytes) + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4);
+  };
   auto at = [&](int r, int d) -> uint4* { return reinterpret_cast<uint4*>(qs + off(r, d)); };
-  auto rem = [&](int r, int d) -> uint4* { return reinterpret_cast<uint4*>(qrem + off(r, d)); };
+  auto rem = [&](int r, int d) -> uint4* { return reinterpret_cast<uint4*>(qs + kRowBoxBytes + off(r, d)); };
   for (int idx = lane; idx < kRows * kChunks; idx += 32) {
     const int r = idx / kChunks, d0 = (idx % kChunks) * 8;
     if (r >= it.rows) {  // unused rows: no remainder
@@ -780,7 +789,7 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
           mbar_expect_tx(&bars.q_full[qslot], C::kQBytes);
 #pragma unroll
           for (int x = 0; x < NB; ++x)
-            tma_load_2d(smem + C::kOffQ + qslot * C::kQSlot + x * kRowBoxBytes, &tm_q, &bars.q_full[qslot],
+            tma_load_2d(smem + C::kOffQ + qslot * C::kQSlot + x * C::kQBoxStride, &tm_q, &bars.q_full[qslot],
                         x * 64, row0);
           last_q[qslot] = (u >> 1) & 1;
         }
@@ -806,7 +815,7 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
           fence_proxy_async_smem();  // the part tiles are read by the MMAs below
           mbar_arrive_warp(&bars.qs_full[qslot]);
         } else if (a.rope_cs != nullptr) {
-          rope_rotate_tile<D>(qt, qt + C::kQBytes, cur.it, a, lane);
+          rope_rotate_tile<D>(qt, cur.it, a, lane);
           fence_proxy_async_smem();  // the rewritten tiles are read by the MMAs below
           __syncwarp();
         }
@@ -828,14 +837,14 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
                            kk > 0 ? 1u : 0u);
         } else {
           const uint32_t qa = sbase + C::kOffQ + qslot * C::kQSlot;
-          // rotary queries are a bf16 value tile plus a bf16 remainder tile: both accumulate
-          const int tiles = a.rope_cs != nullptr ? 2 : 1;
-          for (int tq = 0; tq < tiles; ++tq)
+          // rotary queries: the value rows and the remainder rows under them,
+          // one N = 32 operand (columns [0, 16) and [16, 32) of S^T)
+          const uint32_t idesc = a.rope_cs != nullptr ? C::kIdescS : C::kIdescS1;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss_warp(tmem + col_s<FP8>(sb), sdesc_sw128(ka + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
-                          sdesc_sw128(qa + tq * C::kQBytes + (kk >> 2) * kRowBoxBytes + (kk & 3) * 32, 16, 1024),
-                          C::kIdescS, (tq > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss_warp(tmem + col_s<FP8>(sb), sdesc_sw128(ka + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                        sdesc_sw128(qa + (kk >> 2) * C::kQBoxStride + (kk & 3) * 32, 16, 1024), idesc,
+                        kk > 0 ? 1u : 0u);
         }
       }
       tc_commit_warp(&bars.s_full[sb]);
@@ -943,6 +952,16 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
 #pragma unroll
         for (int r = 0; r < kRows; ++r)
           sr[r] = __float_as_uint((__uint_as_float(sr[r]) + __uint_as_float(s1[r])) + __uint_as_float(s2[r]));
+      } else if (a.rope_cs != nullptr) {
+        // a rotary query's value and remainder scores
+        uint32_t s1[kRows];
+        tmem_ld_x16(tmem + lane_off + col_s<FP8>(sb), sr);
+        tmem_ld_x16(tmem + lane_off + col_s<FP8>(sb) + kRows, s1);
+        tmem_ld_wait();
+        reg_fence<kRows>(sr);
+        reg_fence<kRows>(s1);
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) sr[r] = __float_as_uint(__uint_as_float(sr[r]) + __uint_as_float(s1[r]));
       } else {
         tmem_ld_x16(tmem + lane_off + col_s<FP8>(sb), sr);
         tmem_ld_wait();

@@ -78,6 +78,7 @@ class DecodeWorkload:
     scale: float = field(default=0.0)
     page_size: int = 0      # > 0: paged cache of S / page_size pages per row
     fp8: bool = False       # E4M3 caches with per-tensor scales
+    rope: bool = False      # queries rotated at their positions (rotary table of S rows)
 
     @property
     def softmax_scale(self) -> float:
@@ -102,6 +103,9 @@ DECODE_WORKLOADS["decode_paged_long_gqa_s32k_p16"] = DecodeWorkload(
 
 DECODE_WORKLOADS["decode_fp8_long_gqa_s32k"] = DecodeWorkload(
     "decode_fp8_long_gqa_s32k", B=8, Hq=32, Hkv=8, Tq=1, S=32768, D=128, min_len=16384, max_len=32768, fp8=True)
+
+DECODE_WORKLOADS["decode_rope_long_gqa_s32k"] = DecodeWorkload(
+    "decode_rope_long_gqa_s32k", B=8, Hq=32, Hkv=8, Tq=1, S=32768, D=128, min_len=16384, max_len=32768, rope=True)
 
 DECODE_HEADLINE = "decode_long_gqa_s32k"
 
@@ -193,12 +197,18 @@ def paged_decode_inputs(B, Hq, Hkv, Tq, page_size, max_pages, D, cache_lens=None
 
 
 def make_decode_inputs(w: DecodeWorkload, seed=0):
+    """The workload's inputs (CPU); with ``rope`` also ``rope_cs``, the
+    rotary table of the cache's S positions."""
     if w.fp8:
-        return fp8_decode_inputs(w.B, w.Hq, w.Hkv, w.Tq, w.S, w.D, min_len=w.min_len, max_len=w.max_len, seed=seed)
-    if w.page_size:
-        return paged_decode_inputs(w.B, w.Hq, w.Hkv, w.Tq, w.page_size, w.S // w.page_size, w.D, min_len=w.min_len,
-                                   max_len=w.max_len, seed=seed)
-    return decode_inputs(w.B, w.Hq, w.Hkv, w.Tq, w.S, w.D, min_len=w.min_len, max_len=w.max_len, seed=seed)
+        x = fp8_decode_inputs(w.B, w.Hq, w.Hkv, w.Tq, w.S, w.D, min_len=w.min_len, max_len=w.max_len, seed=seed)
+    elif w.page_size:
+        x = paged_decode_inputs(w.B, w.Hq, w.Hkv, w.Tq, w.page_size, w.S // w.page_size, w.D, min_len=w.min_len,
+                                max_len=w.max_len, seed=seed)
+    else:
+        x = decode_inputs(w.B, w.Hq, w.Hkv, w.Tq, w.S, w.D, min_len=w.min_len, max_len=w.max_len, seed=seed)
+    if w.rope:
+        x["rope_cs"] = rope_cos_sin_table(w.S, w.D)
+    return x
 
 
 def rope_cos_sin_table(positions: int, D: int, base: float = 10000.0):
