@@ -288,36 +288,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S^T = K Q^T: A = K, B = Q, both K-major, contraction over the D features
     auto mma_s = [&](int st) {
       const uint64_t q = sdesc_add(dQk, st * kTile);
+      if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-        mma_ss_warp(tmem + C::kColS, sdesc_add(dK, off), sdesc_add(q, off), kIdS, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          mma_ss(tmem + C::kColS, sdesc_add(dK, off), sdesc_add(q, off), kIdS, kk > 0);
+        }
       }
+      __syncwarp();
     };
     // dP^T = V dO^T
     auto mma_dp = [&](int st) {
       const uint64_t g = sdesc_add(dDOk, st * kTile);
+      if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-        mma_ss_warp(tmem + C::kColDP, sdesc_add(dV, off), sdesc_add(g, off), kIdDP, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          mma_ss(tmem + C::kColDP, sdesc_add(dV, off), sdesc_add(g, off), kIdDP, kk > 0);
+        }
       }
+      __syncwarp();
     };
     // dV += P^T dO: A = P^T from TMEM, B = dO [queries x features], MN-major
     auto mma_dv = [&](int st, bool acc) {
       const uint64_t g = sdesc_add(dDOm, st * kTile);
+      if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ts_warp(tmem + C::kColDV, tmem + packed_col(C::kColS, kk), sdesc_add(g, kk * 2048), kIdDV,
-                    (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + C::kColDV, tmem + packed_col(C::kColS, kk), sdesc_add(g, kk * 2048), kIdDV,
+                      (acc || kk > 0) ? 1u : 0u);
+      }
+      __syncwarp();
     };
     // dK += dS^T Q
     auto mma_dk = [&](int st, bool acc) {
       const uint64_t q = sdesc_add(dQm, st * kTile);
+      if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ts_warp(tmem + C::kColDK, tmem + packed_col(C::kColDP, kk), sdesc_add(q, kk * 2048), kIdDK,
-                    (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + C::kColDK, tmem + packed_col(C::kColDP, kk), sdesc_add(q, kk * 2048), kIdDK,
+                      (acc || kk > 0) ? 1u : 0u);
+      }
+      __syncwarp();
     };
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.kv_full, 0, guard));
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_full[0], 0, guard));
@@ -710,19 +722,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S(gs) = Q K^T into S buffer gs & 1: A = Q, B = K, both K-major
       auto mma_s = [&](int gs) {
         const uint64_t kd = sdesc_add(dKk, (gs % 3) * kTile);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_ss_warp(tmem + C::kColS + (gs & 1) * 128, sdesc_add(dQ, off), sdesc_add(kd, off), kIdS, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+            mma_ss(tmem + C::kColS + (gs & 1) * 128, sdesc_add(dQ, off), sdesc_add(kd, off), kIdS, kk > 0);
+          }
         }
+        __syncwarp();
       };
       // dQ += dS(gs) K: A = dS from TMEM (packed over S buffer gs & 1), B = K [keys x features], MN-major
       auto mma_dq = [&](int gs, bool first) {
         const uint64_t kd = sdesc_add(dKm, (gs % 3) * kTile);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts_warp(tmem + C::kColDQ, tmem + packed_col(C::kColS + (gs & 1) * 128, kk), sdesc_add(kd, kk * 2048),
-                      kIdDQ, (!first || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::kColDQ, tmem + packed_col(C::kColS + (gs & 1) * 128, kk), sdesc_add(kd, kk * 2048),
+                        kIdDQ, (!first || kk > 0) ? 1u : 0u);
+        }
+        __syncwarp();
       };
       for (int k = 0; ok; ++k) {
         int t;
@@ -772,11 +790,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.v_full[gs & 1], (gs >> 1) & 1, guard)))) break;
           tc_fence_after();
           const uint64_t vd = sdesc_add(dV, (gs & 1) * kTile);
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-            mma_ss_warp(tmem + C::kColDP, sdesc_add(dDO, off), sdesc_add(vd, off), kIdDP, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+              mma_ss(tmem + C::kColDP, sdesc_add(dDO, off), sdesc_add(vd, off), kIdDP, kk > 0);
+            }
           }
+          __syncwarp();
           tc_commit_warp(&bars.dp_full);
           tc_commit_warp(&bars.v_empty[gs & 1]);
         }

@@ -340,10 +340,6 @@ __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
-__device__ __forceinline__ void mma_ss_f8_warp(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  if (elect_one()) mma_ss_f8(d, a, b, idesc, acc);
-  __syncwarp();
-}
 // Shared-memory matrix descriptor for a 64-byte-swizzled K-major operand: rows of 64 bytes, 8-row
 // groups `sbo` (512) bytes apart, 512-byte-aligned tile base.
 __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -831,20 +827,26 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
           // operand is row r of part t), so one N = 48 MMA covers all three
           const uint32_t qa = sbase + C::kOffQ8 + qslot * 3 * C::kQ8Bytes;
           auto desc8 = [](uint32_t addr) { return D == 128 ? sdesc_sw128(addr, 16, 1024) : sdesc_sw64(addr, 16, 512); };
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < D / 32; ++kk)
-            mma_ss_f8_warp(tmem + col_s<FP8>(sb), desc8(ka + kk * 32), desc8(qa + kk * 32), C::kIdescS,
-                           kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 32; ++kk)
+              mma_ss_f8(tmem + col_s<FP8>(sb), desc8(ka + kk * 32), desc8(qa + kk * 32), C::kIdescS,
+                             kk > 0 ? 1u : 0u);
+          }
+          __syncwarp();
         } else {
           const uint32_t qa = sbase + C::kOffQ + qslot * C::kQSlot;
           // rotary queries: the value rows and the remainder rows under them,
           // one N = 32 operand (columns [0, 16) and [16, 32) of S^T)
           const uint32_t idesc = a.rope_cs != nullptr ? C::kIdescS : C::kIdescS1;
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss_warp(tmem + col_s<FP8>(sb), sdesc_sw128(ka + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
-                        sdesc_sw128(qa + (kk >> 2) * C::kQBoxStride + (kk & 3) * 32, 16, 1024), idesc,
-                        kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tmem + col_s<FP8>(sb), sdesc_sw128(ka + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                          sdesc_sw128(qa + (kk >> 2) * C::kQBoxStride + (kk & 3) * 32, 16, 1024), idesc,
+                          kk > 0 ? 1u : 0u);
+          }
+          __syncwarp();
         }
       }
       tc_commit_warp(&bars.s_full[sb]);
@@ -879,11 +881,14 @@ __global__ void __launch_bounds__(FP8 ? kThreads8 : kThreads, 1)
       if (!guard.aborted()) {
         const uint32_t va = sbase + C::kOffV + (FP8 ? cur.cs % C::kVop : slot) * C::kTileBytes;
         const uint32_t pa = sbase + C::kOffP + pb * C::kPBytes;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kCK / 16; ++kk)
-          mma_ss_warp(tmem + col_o<FP8>(ob), sdesc_sw128(va + kk * 2048, C::kLboV, 1024),
-                      sdesc_sw128(pa + (kk >> 2) * kRowBoxBytes + (kk & 3) * 32, 16, 1024), C::kIdescO,
-                      (cur.c > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kCK / 16; ++kk)
+            mma_ss(tmem + col_o<FP8>(ob), sdesc_sw128(va + kk * 2048, C::kLboV, 1024),
+                        sdesc_sw128(pa + (kk >> 2) * kRowBoxBytes + (kk & 3) * 32, 16, 1024), C::kIdescO,
+                        (cur.c > 0 || kk > 0) ? 1u : 0u);
+        }
+        __syncwarp();
       }
       tc_commit_warp(&bars.p_empty[pb]);
       if constexpr (!FP8) tc_commit_warp(&bars.v_empty[slot]);

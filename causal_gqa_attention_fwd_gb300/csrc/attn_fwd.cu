@@ -260,21 +260,27 @@ __global__ void __launch_bounds__(384, 1)
       auto issue_qk = [&](int x, int st) {
         const uint32_t qa = sq_addr + x * C::kTileBytes;
         const uint32_t ka = ring_addr + st * C::kTileBytes;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          mma_ss_warp(tmem + C::col_s(x), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                 C::kIdescQK, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+            mma_ss(tmem + C::col_s(x), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                   C::kIdescQK, kk > 0);
+          }
         }
+        __syncwarp();
       };
       // P V over the keys [16 kk0, 16 kk1) of the block (P packed in TMEM)
       auto issue_pv_part = [&](int x, int st, int acc, int kk0, int kk1) {
         const uint32_t va = ring_addr + st * C::kTileBytes;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = kk0; kk < kk1; ++kk) {
-          mma_ts_warp(tmem + C::col_o(x), tmem + C::col_p(x) + kk * 8, sdesc_sw128(va + kk * 2048, C::kBoxBytes, 1024),
-                 C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+          for (int kk = kk0; kk < kk1; ++kk) {
+            mma_ts(tmem + C::col_o(x), tmem + C::col_p(x) + kk * 8, sdesc_sw128(va + kk * 2048, C::kBoxBytes, 1024),
+                   C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+          }
         }
+        __syncwarp();
       };
       auto issue_pv = [&](int x, int st, int acc) { issue_pv_part(x, st, acc, 0, kBN / 16); };
       // K_j sits at ring index 2j, V_j at 2j + 1.
